@@ -1,0 +1,530 @@
+"""Benchmark of the OScaR INT2 KV-cache hot path on GB300.
+
+Headline (one JSON line on rank 0): INT2 decode-attention microseconds per
+step at 128K context for one Llama-3.1-8B-shaped layer (batch 1, 32 query /
+8 KV heads, d = 128; synthetic K/V/q of that shape, seeded), with the packed
+cache resident in HBM and L2 flushed (a 2x-L2 buffer write) before every
+timed step.  Alongside: the roofline of the main split-K kernel (CUDA events
+around its launch), an end-to-end number through host buffers, quantise
+GB/s for the 128K prefill, the in-repo BF16 reference decode and its ratio,
+the 8K..128K context sweep, batch-32 x 32K throughput and a ragged serving
+stream, SM clocks sampled during the measurements, and the CPU oracle timed
+on a bounded sample (single thread, spawned process).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs the same
+workload on its own GPU (replicas: the path has no cross-GPU exchange);
+times are the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "INT2 decode-attn µs/step & HBM GB/s (% of peak) at 128K ctx; quantize GB/s"
+BLOCK_BYTES = 13824
+FALLBACK_HBM_GBS = 6800.0
+CTX = 131072
+HQ, HKV, D = 32, 8, 128
+
+
+# ----------------------------------------------------------------- helpers
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            js = json.load(f)
+        return float(js["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("decode.cu", "common.cuh", "decode_common.cuh", "launch.h"):
+        with open(os.path.join(ROOT, "int2_kv_cache_oscar_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the INT2 decode kernel at 128K from the
+    committed ncu summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "decode_int2_128k.md")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", txt)
+    hsh = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", txt)
+    if m and hsh and hsh.group(1) == kernel_source_hash():
+        return int(m.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the measurements run."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.index)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- GPU arm
+
+class Timer:
+    def __init__(self, torch, flush_bytes):
+        self.torch = torch
+        self.flush = torch.empty(flush_bytes, dtype=torch.uint8, device="cuda")
+
+    def run(self, fn, steps, warmup, flush=True, kernel_events=None):
+        """Mean microseconds of fn() over `steps` timed calls (CUDA events on
+        the current stream, L2 flushed before each call)."""
+        torch = self.torch
+        for _ in range(warmup):
+            if flush:
+                self.flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        pairs, kpairs = [], []
+        for _ in range(steps):
+            if flush:
+                self.flush.zero_()
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            if kernel_events is not None:
+                ks = torch.cuda.Event(enable_timing=True)
+                ke = torch.cuda.Event(enable_timing=True)
+                kernel_events(ks, ke)
+                kpairs.append((ks, ke))
+            s.record()
+            fn()
+            e.record()
+            pairs.append((s, e))
+        torch.cuda.synchronize()
+        if kernel_events is not None:
+            kernel_events(None, None)
+        t = [a.elapsed_time(b) * 1e3 for a, b in pairs]
+        kt = [a.elapsed_time(b) * 1e3 for a, b in kpairs]
+        return statistics.mean(t), (statistics.mean(kt) if kt else None)
+
+
+def build_cache(O_, W, torch, lens, seed_recipe, slots=None, chunk=None, device="cuda", max_len=None):
+    """Generate sequences on the GPU and append them; returns (cache, ks, vs)."""
+    cache = O_.OscarCache(len(lens), HKV, max_len or max(lens))
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed_recipe[0])
+    ks, vs = [], []
+    for i, L in enumerate(lens):
+        k, v = W.make_sequence_kv(L, HKV, seed_recipe[1], gen, device)
+        ks.append(k)
+        vs.append(v)
+        s = i if slots is None else slots[i]
+        step = L if chunk is None else chunk
+        for p0 in range(0, L, step):
+            n = min(step, L - p0)
+            cache.append([s], [0, n], k[p0:p0 + n].contiguous(), v[p0:p0 + n].contiguous())
+    torch.cuda.synchronize()
+    return cache, ks, vs
+
+
+def bf16_cache(torch, ks, vs, max_len):
+    B = len(ks)
+    kc = torch.zeros((B, HKV, max_len, D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    for b in range(B):
+        L = ks[b].shape[0]
+        kc[b, :, :L] = ks[b].transpose(0, 1)
+        vc[b, :, :L] = vs[b].transpose(0, 1)
+    return kc, vc
+
+
+def int2_bytes(lens):
+    return sum(HKV * ((L // 128) * BLOCK_BYTES + (L % 128) * 512) for L in lens)
+
+
+def gpu_arm(args, rank, world):
+    import torch
+
+    from int2_kv_cache_oscar_gb300 import oscar as O_
+    from int2_kv_cache_oscar_gb300 import workloads as W
+
+    dev = torch.cuda.current_device()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    timer = Timer(torch, 2 * l2)
+    peak, peak_kind = load_peaks()
+    K, Wm = args.steps, args.warmup
+    out = {}
+    launches = 0
+
+    with ClockSampler(dev) as clocks:
+        # ---------------- headline: decode at 128K, B = 1
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(2)
+        k, v = W.make_sequence_kv(CTX, HKV, W.LLAMA_RECIPE, gen, "cuda")
+        q = W.make_q(1, HQ, seed=2, device="cuda")
+        cache = O_.OscarCache(1, HKV, CTX)
+
+        def quantize():
+            O_.oscar_cache_reset(cache.handle, 0)
+            cache.append([0], [0, CTX], k, v)
+
+        q_us, _ = timer.run(quantize, K, Wm)
+        quant_read = CTX * HKV * 512
+        quant_write = CTX * HKV * 108
+        quant_gbs = (quant_read + quant_write) / (q_us * 1e-6) / 1e9
+        launches += K * (-(-(CTX // 128) // 900))   # quantise kernels per 128K append
+        outb = torch.empty((1, HQ, D), dtype=torch.bfloat16, device="cuda")
+        ws = cache.workspace(1, HQ)
+
+        def decode():
+            cache.decode([0], q, HQ, outb, ws)
+
+        dec_us, kern_us = timer.run(decode, K, Wm,
+                                    kernel_events=lambda a, b: O_.oscar_set_timing_events(a, b))
+        launches += K * 2
+        O_.oscar_cache_check(cache.handle)
+        alg_bytes = (CTX // 128) * HKV * BLOCK_BYTES
+        step_bytes = alg_bytes + 2 * HQ * D * 2
+        achieved = alg_bytes / (kern_us * 1e-6) / 1e9
+
+        # end to end: pinned host q -> device, decode, device -> pinned host out
+        q_host = q.cpu().pin_memory()
+        o_host = torch.empty((1, HQ, D), dtype=torch.bfloat16).pin_memory()
+        q_dev = torch.empty_like(q)
+
+        def e2e():
+            q_dev.copy_(q_host, non_blocking=True)
+            cache.decode([0], q_dev, HQ, outb, ws)
+            o_host.copy_(outb, non_blocking=True)
+
+        e2e_us, _ = timer.run(e2e, K, Wm)
+        launches += K * 2
+
+        # BF16 reference at 128K
+        kc, vc = bf16_cache(torch, [k], [v], CTX)
+        wsb = torch.empty(O_.oscar_bf16_decode_workspace_bytes(1, HKV, HQ), dtype=torch.uint8,
+                          device="cuda")
+        outr = torch.empty_like(outb)
+
+        def ref_decode():
+            O_.oscar_bf16_decode_attention([0], [CTX], kc, vc, HKV, CTX, q, HQ, 0.0, outr, wsb)
+
+        ref_us, ref_kern = timer.run(ref_decode, K, Wm,
+                                     kernel_events=lambda a, b: O_.oscar_set_timing_events(a, b))
+        launches += K * 2
+        bf16_bytes = CTX * HKV * 512
+        del kc, vc
+        out["bf16_ref"] = {"us_per_step": round(ref_us, 2), "main_kernel_us": round(ref_kern, 2),
+                           "GBps": round(bf16_bytes / (ref_kern * 1e-6) / 1e9, 1),
+                           "frac_of_peak": round(bf16_bytes / (ref_kern * 1e-6) / 1e9 / peak, 3),
+                           "int2_speedup": round(ref_us / dec_us, 2)}
+        del k, v
+        cache.close()
+        del cache
+        torch.cuda.empty_cache()
+
+        # ---------------- context sweep 8K..128K (B = 1), INT2 and BF16
+        sweep = {}
+        if not args.quick:
+            lens = [8192, 16384, 32768, 65536, 131072]
+            for L in lens:
+                c, ks, vs = build_cache(O_, W, torch, [L], (2, W.LLAMA_RECIPE))
+                qq = W.make_q(1, HQ, seed=2, device="cuda")
+                o1 = torch.empty((1, HQ, D), dtype=torch.bfloat16, device="cuda")
+                w1 = c.workspace(1, HQ)
+                t, kt = timer.run(lambda: c.decode([0], qq, HQ, o1, w1), K, Wm,
+                                  kernel_events=lambda a, b: O_.oscar_set_timing_events(a, b))
+                kc, vc = bf16_cache(torch, ks, vs, L)
+                tb, _ = timer.run(lambda: O_.oscar_bf16_decode_attention([0], [L], kc, vc, HKV, L, qq, HQ,
+                                                                         0.0, o1, wsb), K, Wm)
+                launches += 4 * K
+                b = int2_bytes([L])
+                sweep[str(L)] = {"us": round(t, 2), "kernel_us": round(kt, 2),
+                                 "GBps": round(b / (kt * 1e-6) / 1e9, 1),
+                                 "frac": round(b / (kt * 1e-6) / 1e9 / peak, 3),
+                                 "bf16_us": round(tb, 2), "speedup": round(tb / t, 2),
+                                 "cache_bytes": b, "bf16_bytes": L * HKV * 512,
+                                 "mem_ratio": round(L * HKV * 512 / b, 2)}
+                del c, ks, vs, kc, vc
+                torch.cuda.empty_cache()
+        out["sweep"] = sweep
+
+        # ---------------- multi-batch: B = 32 x 32K
+        if not args.quick:
+            B, L = 32, 32768
+            rec = W.multi_batch(B, L).recipe
+            c, ks, vs = build_cache(O_, W, torch, [L] * B, (3, rec))
+            qq = W.make_q(B, HQ, seed=3, device="cuda")
+            o1 = torch.empty((B, HQ, D), dtype=torch.bfloat16, device="cuda")
+            w1 = c.workspace(B, HQ)
+            t, kt = timer.run(lambda: c.decode(list(range(B)), qq, HQ, o1, w1), K, Wm,
+                              kernel_events=lambda a, b: O_.oscar_set_timing_events(a, b))
+            kc, vc = bf16_cache(torch, ks, vs, L)
+            wsb2 = torch.empty(O_.oscar_bf16_decode_workspace_bytes(B, HKV, HQ), dtype=torch.uint8,
+                               device="cuda")
+            tb, _ = timer.run(lambda: O_.oscar_bf16_decode_attention(list(range(B)), [L] * B, kc, vc, HKV, L,
+                                                                     qq, HQ, 0.0, o1, wsb2), K, Wm)
+            launches += 4 * K
+            b = int2_bytes([L] * B)
+            out["multi_batch"] = {"batch": B, "ctx": L, "us": round(t, 2), "tokens_per_s": round(B / (t * 1e-6)),
+                                  "kernel_GBps": round(b / (kt * 1e-6) / 1e9, 1),
+                                  "frac": round(b / (kt * 1e-6) / 1e9 / peak, 3),
+                                  "bf16_us": round(tb, 2), "bf16_tokens_per_s": round(B / (tb * 1e-6)),
+                                  "throughput_ratio": round(tb / t, 2)}
+            del c, ks, vs, kc, vc
+            torch.cuda.empty_cache()
+
+        # ---------------- ragged serving stream: 8 sequences, 4K..128K
+        if not args.quick:
+            lens = W.ragged_lengths(8)
+            c, ks, vs = build_cache(O_, W, torch, lens, (4, W.LLAMA_RECIPE), chunk=4096,
+                                    max_len=max(lens) + 512)
+            gen = torch.Generator(device="cuda")
+            gen.manual_seed(44)
+            nsteps = 64
+            newk = torch.randn((nsteps, 8, HKV, D), generator=gen, device="cuda").to(torch.bfloat16)
+            newv = torch.randn((nsteps, 8, HKV, D), generator=gen, device="cuda").to(torch.bfloat16)
+            qq = W.make_q(8, HQ, seed=4, device="cuda")
+            o1 = torch.empty((8, HQ, D), dtype=torch.bfloat16, device="cuda")
+            w1 = c.workspace(8, HQ)
+            ids = list(range(8))
+            cu = list(range(9))
+            torch.cuda.synchronize()
+            s_ev = torch.cuda.Event(enable_timing=True)
+            e_ev = torch.cuda.Event(enable_timing=True)
+            s_ev.record()
+            for st in range(nsteps):
+                c.append(ids, cu, newk[st], newv[st])
+                c.decode(ids, qq, HQ, o1, w1)
+            e_ev.record()
+            torch.cuda.synchronize()
+            tt = s_ev.elapsed_time(e_ev) * 1e3 / nsteps
+            launches += 3 * nsteps
+            out["ragged_stream"] = {"lens": lens, "steps": nsteps, "us_per_step": round(tt, 2),
+                                    "tokens_per_s": round(8 / (tt * 1e-6))}
+            del c, ks, vs
+            torch.cuda.empty_cache()
+
+    clk = clocks.summary()
+    res = {
+        "dec_us": dec_us, "kern_us": kern_us, "e2e_us": e2e_us, "achieved": achieved, "peak": peak,
+        "peak_kind": peak_kind, "alg_bytes": alg_bytes, "step_bytes": step_bytes, "q_us": q_us,
+        "quant_gbs": quant_gbs, "launches": launches, "clocks": clk, "extra": out,
+    }
+    return res
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def cpu_sample_worker(steps: int):
+    """Runs in a fresh single-threaded process: oracle decode of 1 of the 8
+    KV heads of the 128K workload (4 query heads), timed per step."""
+    import numpy as np
+    import torch
+
+    from int2_kv_cache_oscar_gb300 import workloads as W
+    from oracle import oscar_oracle as OR
+
+    gen = torch.Generator()
+    gen.manual_seed(2)
+    k, v = W.make_sequence_kv(CTX, 1, W.LLAMA_RECIPE, gen)
+    q = W.make_q(1, 4, seed=2)
+    t0 = time.perf_counter()
+    hc = OR.build_head_cache(k[:, 0].double().numpy(), v[:, 0].double().numpy())
+    t_quant = time.perf_counter() - t0
+    qn = q[0].double().numpy()
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        OR.decode_head(qn, hc)
+        times.append(time.perf_counter() - t0)
+    return {"decode_s_per_head": statistics.mean(times), "quant_s_per_head": t_quant}
+
+
+def run_cpu_sample(steps: int):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = ("import json, bench; print('CPUJSON' + json.dumps(bench.cpu_sample_worker(%d)))" % steps)
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
+                       timeout=900)
+    m = re.search(r"CPUJSON(\{.*\})", r.stdout)
+    if not m:
+        raise RuntimeError("CPU oracle sample failed:\n" + r.stdout[-2000:] + r.stderr[-2000:])
+    return json.loads(m.group(1))
+
+
+def cpu_baseline_obj(js, kind="oracle"):
+    us = js["decode_s_per_head"] * HKV * 1e6
+    return {"value": round(us, 1), "unit": "us/step", "cores": 1, "kind": kind,
+            "sample": "oracle decode (float64 numpy) of 1 of the 8 KV heads (4 query heads) over the "
+                      "128K-token cache, scaled x8 to the full step; 1 thread"}
+
+
+# --------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="oscar", choices=["oscar", "reference"])
+    ap.add_argument("--quick", action="store_true", help="headline only (no sweep / batch / stream)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    config = {"workload": "decode-attention over a 131072-token OScaR INT2 cache, one "
+                          "Llama-3.1-8B-shaped layer: batch 1, 32 query / 8 KV heads, head_dim 128, "
+                          "G=128 key groups, 32-channel value groups (seed 2)",
+              "global_batch": world, "seq_len": CTX, "parallelism": f"replicas x{world}",
+              "l2": "flushed (2x L2 write) before every timed step"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        js = run_cpu_sample(max(1, args.steps // 4))
+        cb = cpu_baseline_obj(js)
+        line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "us/step",
+                "n_gpus": args.gpus, "steps": max(1, args.steps // 4), "warmup": 0,
+                "ms_per_step": round(cb["value"] / 1e3, 3), "higher_is_better": False,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": config, "cpu_baseline": cb,
+                "e2e": {"value": cb["value"], "unit": "us/step", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+
+    res = gpu_arm(args, rank, world)
+
+    dec_us, e2e_us = res["dec_us"], res["e2e_us"]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([dec_us, e2e_us, res["kern_us"]], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dec_us, e2e_us, kern = t.tolist()
+        res["kern_us"] = kern
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    cpu = None
+    if not args.no_cpu:
+        try:
+            cpu = cpu_baseline_obj(run_cpu_sample(3))
+        except Exception as e:  # reported, not fatal
+            cpu = {"value": None, "unit": "us/step", "cores": 1, "kind": "oracle", "sample": f"failed: {e}"}
+
+    traffic = profiled_traffic()
+    line = {
+        "metric": METRIC,
+        "value": round(dec_us, 2),
+        "unit": "us/step",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dec_us / 1e3, 5),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32 (fp16 hi/lo tensor-core operands, INT2 codes, bf16 I/O)",
+        "data": "synthetic",
+        "config": config,
+        "roofline": {"bound": "hbm", "achieved": round(res["achieved"], 1), "peak": res["peak"],
+                     "unit": "GB/s", "frac": round(res["achieved"] / res["peak"], 3),
+                     "traffic": traffic, "peak_source": f"hbm_gbs of {res['peak_kind']}",
+                     "kernel": "decode_int2_kernel (split-K main kernel)",
+                     "kernel_us": round(res["kern_us"], 2), "alg_bytes": res["alg_bytes"]},
+        "hbm_GBps_step": round(res["step_bytes"] / (dec_us * 1e-6) / 1e9, 1),
+        "quantize": {"us_128k_prefill": round(res["q_us"], 1), "GBps": round(res["quant_gbs"], 1),
+                     "frac_of_peak": round(res["quant_gbs"] / res["peak"], 3)},
+        "e2e": {"value": round(e2e_us, 2), "unit": "us/step", "h2d_bytes_per_step": HQ * D * 2,
+                "d2h_bytes_per_step": HQ * D * 2},
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+        "cpu_baseline": cpu,
+    }
+    line.update(res["extra"])
+    print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,184 @@
+// Shared constants, arena layout and PTX helpers of the sm_103a OScaR kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace oscar {
+
+constexpr int kHeadDim = 128;        // d
+constexpr int kGroup = 128;          // G: tokens per key group
+constexpr int kVGroup = 32;          // channels per value group
+constexpr int kVGroups = kHeadDim / kVGroup;
+
+// One quantised group of one KV head (see include/oscar.h).
+constexpr int kOffKCodes = 0;
+constexpr int kOffKScale = 4096;
+constexpr int kOffKZero = 4608;
+constexpr int kOffKNorm = 5120;
+constexpr int kOffVCodes = 5632;
+constexpr int kOffVSZ = 9728;
+constexpr int kBlockBytes = 13824;
+
+constexpr int kWindowBytes = 2 * kGroup * kHeadDim * 2;  // K rows then V rows, bf16
+constexpr int kMetaHeader = 256;                          // status words
+
+// Largest GQA group one pass of the INT2 / bf16 decode kernels serves.
+constexpr int kMaxGqa = 4;
+
+// Bounded spin of every mbarrier wait (each try_wait may itself suspend).
+constexpr uint32_t kSpinLimit = 1u << 24;
+constexpr uint32_t kErrTimeout = 1u;
+
+struct ArenaLayout {
+  int64_t meta_bytes;     // header + per (slot, head) s_v maxima, 256-aligned
+  int64_t blocks_off;
+  int64_t windows_off;
+  int64_t total;
+  int32_t max_groups;
+};
+
+__host__ __device__ inline ArenaLayout arena_layout(int32_t max_batch, int32_t hkv, int32_t max_len) {
+  ArenaLayout L;
+  L.max_groups = (max_len + kGroup - 1) / kGroup;
+  int64_t meta = kMetaHeader + (int64_t)max_batch * hkv * 4;
+  L.meta_bytes = (meta + 255) / 256 * 256;
+  L.blocks_off = L.meta_bytes;
+  int64_t blocks = (int64_t)max_batch * hkv * L.max_groups * kBlockBytes;
+  L.windows_off = (L.blocks_off + blocks + 255) / 256 * 256;
+  L.total = L.windows_off + (int64_t)max_batch * hkv * kWindowBytes;
+  return L;
+}
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+                   smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` with a bounded spin.  On timeout, sets the
+// CTA abort flag and the device error word; once the abort flag is set every
+// later wait returns immediately so that the CTA still reaches its barriers
+// and exits.  err_word may be NULL (no device status word).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                  uint32_t* err_word) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+  }
+  *abort_flag = 1;
+  if (err_word != nullptr) atomicOr(err_word, kErrTimeout);
+  return false;
+}
+
+// 1-D bulk copy global -> shared, completing on `bar` (bytes multiple of 16,
+// both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// D += A * B, m16n8k16, A row-major fp16, B column-major fp16, fp32 accumulate.
+__device__ __forceinline__ void mma_f16_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Pack two floats into half2 (lo in bits 0..15), round to nearest even.
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float half_lo_to_float(uint32_t h2) {
+  float f;
+  asm("{\n\t.reg .f16 h;\n\tmov.b32 {h, _}, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(h2));
+  return f;
+}
+
+__device__ __forceinline__ float half_hi_to_float(uint32_t h2) {
+  float f;
+  asm("{\n\t.reg .f16 h;\n\tmov.b32 {_, h}, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(h2));
+  return f;
+}
+
+// Split the pair (x0, x1) into an fp16 "hi" pair and the fp16 "lo" pair of
+// the remainders; return hi when want_lo == 0, lo otherwise.  x - hi is exact
+// in fp32, so hi + lo carries ~22 significant bits.
+__device__ __forceinline__ uint32_t split_half2(float x0, float x1, bool want_lo) {
+  uint32_t hi = pack_half2(x0, x1);
+  float r0 = x0 - half_lo_to_float(hi);
+  float r1 = x1 - half_hi_to_float(hi);
+  uint32_t lo = pack_half2(r0, r1);
+  return want_lo ? lo : hi;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t f32_to_bf16_bits(float x) {
+  uint32_t u = __float_as_uint(x);
+  if ((u & 0x7f800000u) == 0x7f800000u) return (u >> 16) | ((u & 0xffffu) ? 0x40u : 0u);  // inf / nan
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return u >> 16;
+}
+
+// Bit position exponent p of fragment slot i = 2*kk + hf: codes at bits
+// 2i (i <= 4) are read in place; codes at i = 5..7 are read after a 10-bit
+// right shift, i.e. at bits 2(i - 5).  An extracted fp16 is then the
+// subnormal code * 2^(p - 24).
+__host__ __device__ constexpr int frag_p(int i) { return i <= 4 ? 2 * i : 2 * (i - 5); }
+
+// Extract the half2 (two subnormal fp16 codes) of fragment slot i from word w.
+template <int I>
+__device__ __forceinline__ uint32_t frag_extract(uint32_t w) {
+  if constexpr (I <= 4) {
+    return w & (0x00030003u << (2 * I));
+  } else {
+    return (w >> 10) & (0x00030003u << (2 * (I - 5)));
+  }
+}
+
+}  // namespace oscar

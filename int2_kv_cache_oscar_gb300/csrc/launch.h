@@ -1,0 +1,103 @@
+// Host-side launch interface between the C ABI (oscar_api.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace oscar {
+
+// One 128-token group of one sequence that fills during an append (all KV
+// heads run it, grid.y = head).  Tokens 0..n_win-1 of the group come from
+// the window, the rest from input rows in_row, in_row + 1, ...  When
+// tail_count > 0 the same CTA afterwards writes input rows tail_in_row ...
+// into window positions tail_pos ... (the window it has just read).
+struct QuantTask {
+  int32_t slot;
+  int32_t group;
+  int32_t n_win;
+  int32_t in_row;
+  int32_t tail_pos;
+  int32_t tail_count;
+  int32_t tail_in_row;
+  int32_t kind;  // 0 = quantise a group (+ optional tail), 1 = window append only
+};
+
+constexpr int kQuantPlanSmall = 64;
+constexpr int kQuantPlanLarge = 900;
+
+template <int CAP>
+struct QuantPlan {
+  int32_t n_tasks;
+  int32_t hkv;
+  int32_t max_groups;
+  int32_t pad;
+  int64_t blocks_off;
+  int64_t windows_off;
+  QuantTask t[CAP];
+};
+
+cudaError_t launch_quantize_small(const QuantPlan<kQuantPlanSmall>& plan, uint8_t* arena, const uint16_t* k,
+                                  const uint16_t* v, cudaStream_t stream);
+cudaError_t launch_quantize_large(const QuantPlan<kQuantPlanLarge>& plan, uint8_t* arena, const uint16_t* k,
+                                  const uint16_t* v, cudaStream_t stream);
+
+// ------------------------------------------------------------------ decode
+
+// Per-sequence data of one decode launch.  Work units are (sequence, KV head,
+// unit) triples in that order (a unit is one 128-token group of the INT2
+// cache, or one 64-token tile of the bf16 reference cache); sequence b owns
+// units [ubase, ubase + hkv * units_b).
+struct DecodeSeq {
+  int32_t slot;
+  int32_t len;
+  int64_t ubase;  // first unit of this sequence
+  int32_t rank;   // number of earlier sequences with >= 1 unit
+  int32_t pad;
+};
+
+struct DecodeHeader {
+  int32_t n_seqs;
+  int32_t hkv;
+  int32_t gqa;           // query heads per KV head (<= kMaxGqa)
+  int32_t hq;
+  int32_t max_groups;    // INT2: groups per (slot, head); bf16: max_seq_len
+  int32_t n_ctas;        // main-kernel CTAs (N)
+  int32_t bf16_mode;     // 1: bf16 reference cache (64-token units, no window)
+  int32_t pad;
+  int64_t n_units;       // T
+  int64_t blocks_off;
+  int64_t windows_off;
+  float scale_log2;      // softmax_scale * log2(e)
+  int32_t pad2;
+  const uint16_t* q;
+  uint16_t* out;
+  float* partials;
+  uint32_t* err_word;
+};
+
+template <int MAXS>
+struct DecodeParams {
+  DecodeHeader h;
+  DecodeSeq seq[MAXS];
+};
+
+constexpr int kDecodeSeqsSmall = 16;
+constexpr int kDecodeSeqsLarge = 1024;
+
+// Floats of one partial record (o[128], m, l, 2 pad) per query head.
+constexpr int kPartialFloats = 132;
+
+int num_sms(int device);
+int decode_int2_ctas_per_sm();
+int decode_bf16_ctas_per_sm();
+
+template <int MAXS>
+cudaError_t launch_decode_int2(const DecodeParams<MAXS>& p, const uint8_t* arena, cudaStream_t stream,
+                               cudaEvent_t ev_start, cudaEvent_t ev_stop);
+template <int MAXS>
+cudaError_t launch_decode_bf16(const DecodeParams<MAXS>& p, const uint16_t* kc, const uint16_t* vc,
+                               cudaStream_t stream, cudaEvent_t ev_start, cudaEvent_t ev_stop);
+template <int MAXS>
+cudaError_t launch_combine(const DecodeParams<MAXS>& p, const uint8_t* arena, cudaStream_t stream);
+
+}  // namespace oscar

@@ -1,0 +1,532 @@
+// C ABI of the OScaR INT2 KV-cache library: host-side validation, planning
+// and launches.  Every argument is checked before anything is enqueued; on
+// error nothing is enqueued and no host state changes.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <exception>
+#include <string>
+#include <vector>
+
+#include "../../include/oscar.h"
+#include "common.cuh"
+#include "launch.h"
+
+using namespace oscar;
+
+struct oscar_cache {
+  oscar_cache_config cfg;
+  uint8_t* arena;
+  size_t arena_bytes;
+  ArenaLayout layout;
+  std::vector<int32_t> len;  // host mirror of every slot's length
+  int sms;
+};
+
+namespace {
+
+thread_local std::string g_err;
+thread_local cudaEvent_t g_ev_start = nullptr;
+thread_local cudaEvent_t g_ev_stop = nullptr;
+
+oscar_status fail(oscar_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+oscar_status ok() {
+  g_err.clear();
+  return OSCAR_OK;
+}
+
+oscar_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(OSCAR_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Makes cfg.device current for the duration of a call.
+struct DeviceGuard {
+  int prev = -1;
+  bool changed = false;
+  cudaError_t err = cudaSuccess;
+  explicit DeviceGuard(int dev) {
+    err = cudaGetDevice(&prev);
+    if (err == cudaSuccess && prev != dev) {
+      err = cudaSetDevice(dev);
+      changed = err == cudaSuccess;
+    }
+  }
+  ~DeviceGuard() {
+    if (changed) cudaSetDevice(prev);
+  }
+};
+
+oscar_status check_config(const oscar_cache_config* c) {
+  if (!c) return fail(OSCAR_ERR_INVALID_ARG, "config is NULL");
+  if (c->head_dim != kHeadDim) return fail(OSCAR_ERR_UNSUPPORTED, "head_dim must be 128 (got %d)", c->head_dim);
+  if (c->group_size != kGroup) return fail(OSCAR_ERR_UNSUPPORTED, "group_size must be 128 (got %d)", c->group_size);
+  if (c->value_group != kVGroup)
+    return fail(OSCAR_ERR_UNSUPPORTED, "value_group must be 32 (got %d)", c->value_group);
+  if (c->max_batch < 1 || c->num_kv_heads < 1 || c->max_seq_len < 1)
+    return fail(OSCAR_ERR_INVALID_ARG, "max_batch, num_kv_heads and max_seq_len must be >= 1");
+  if (c->device < 0) return fail(OSCAR_ERR_INVALID_ARG, "device must be >= 0");
+  if ((int64_t)c->max_batch * c->num_kv_heads > (1 << 24))
+    return fail(OSCAR_ERR_CAPACITY, "max_batch * num_kv_heads too large");
+  return OSCAR_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+oscar_status check_slots(const oscar_cache* c, int32_t n, const int32_t* ids, std::vector<char>& seen) {
+  seen.assign(c->cfg.max_batch, 0);
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t s = ids[i];
+    if (s < 0 || s >= c->cfg.max_batch) return fail(OSCAR_ERR_INVALID_ARG, "seq_ids[%d] = %d out of range", i, s);
+    if (seen[s]) return fail(OSCAR_ERR_INVALID_ARG, "seq_ids[%d] = %d repeated", i, s);
+    seen[s] = 1;
+  }
+  return OSCAR_OK;
+}
+
+template <int CAP>
+oscar_status run_quant_plan(oscar_cache* c, const std::vector<QuantTask>& tasks, size_t begin, size_t end,
+                            const uint16_t* k, const uint16_t* v, cudaStream_t stream) {
+  QuantPlan<CAP> plan;
+  std::memset(&plan, 0, sizeof(plan));
+  plan.n_tasks = (int32_t)(end - begin);
+  plan.hkv = c->cfg.num_kv_heads;
+  plan.max_groups = c->layout.max_groups;
+  plan.blocks_off = c->layout.blocks_off;
+  plan.windows_off = c->layout.windows_off;
+  for (size_t i = begin; i < end; ++i) plan.t[i - begin] = tasks[i];
+  cudaError_t e;
+  if constexpr (CAP == kQuantPlanSmall)
+    e = launch_quantize_small(plan, c->arena, k, v, stream);
+  else
+    e = launch_quantize_large(plan, c->arena, k, v, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return OSCAR_OK;
+}
+
+size_t partial_bytes(int64_t slots, int gqa) { return (size_t)slots * gqa * kPartialFloats * sizeof(float); }
+
+// Fill the per-sequence table and unit counts of one decode launch.
+template <int MAXS>
+void fill_decode(DecodeParams<MAXS>& P, int32_t n, const int32_t* slots, const int32_t* lens, int hkv,
+                 int bf16_mode, int64_t& rows_nonempty) {
+  int64_t ubase = 0;
+  int32_t rank = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const int len = lens[i];
+    const int units = bf16_mode ? (len + 63) / 64 : len / kGroup;
+    P.seq[i].slot = slots[i];
+    P.seq[i].len = len;
+    P.seq[i].ubase = ubase;
+    P.seq[i].rank = rank;
+    P.seq[i].pad = 0;
+    ubase += (int64_t)hkv * units;
+    if (units > 0) ++rank;
+  }
+  P.h.n_units = ubase;
+  rows_nonempty = (int64_t)rank * hkv;
+}
+
+template <int MAXS>
+oscar_status run_decode(int device, int sms, int ctas_per_sm, int32_t n, const int32_t* slots, const int32_t* lens,
+                        int hkv, int hq, float scale, int bf16_mode, int max_groups, int64_t blocks_off,
+                        int64_t windows_off, const uint8_t* arena, uint32_t* err_word, const uint16_t* kc,
+                        const uint16_t* vc, const void* q, void* out, void* ws, size_t ws_bytes,
+                        cudaStream_t stream) {
+  DecodeParams<MAXS> P;
+  std::memset(&P, 0, sizeof(P));
+  int64_t rows = 0;
+  fill_decode(P, n, slots, lens, hkv, bf16_mode, rows);
+  const int gqa = hq / hkv;
+  const int64_t T = P.h.n_units;
+  const int64_t maxN = (int64_t)sms * ctas_per_sm;
+  const int64_t N = T < maxN ? T : maxN;
+  const size_t need = partial_bytes(N + rows, gqa);
+  if (ws_bytes < need)
+    return fail(OSCAR_ERR_CAPACITY, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+  P.h.n_seqs = n;
+  P.h.hkv = hkv;
+  P.h.gqa = gqa;
+  P.h.hq = hq;
+  P.h.max_groups = max_groups;
+  P.h.n_ctas = (int32_t)N;
+  P.h.bf16_mode = bf16_mode;
+  P.h.blocks_off = blocks_off;
+  P.h.windows_off = windows_off;
+  P.h.scale_log2 = scale * 1.4426950408889634f;
+  P.h.q = static_cast<const uint16_t*>(q);
+  P.h.out = static_cast<uint16_t*>(out);
+  P.h.partials = static_cast<float*>(ws);
+  P.h.err_word = err_word;
+  cudaError_t e;
+  if (bf16_mode)
+    e = launch_decode_bf16(P, kc, vc, stream, g_ev_start, g_ev_stop);
+  else
+    e = launch_decode_int2(P, arena, stream, g_ev_start, g_ev_stop);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  e = launch_combine(P, arena, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  (void)device;
+  return OSCAR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* oscar_last_error(void) { return g_err.c_str(); }
+
+oscar_status oscar_cache_required_bytes(const oscar_cache_config* cfg, size_t* out_bytes) {
+  oscar_status s = check_config(cfg);
+  if (s != OSCAR_OK) return s;
+  if (!out_bytes) return fail(OSCAR_ERR_INVALID_ARG, "out_bytes is NULL");
+  *out_bytes = (size_t)arena_layout(cfg->max_batch, cfg->num_kv_heads, cfg->max_seq_len).total;
+  return ok();
+}
+
+oscar_status oscar_cache_create(const oscar_cache_config* cfg, void* device_arena, size_t arena_bytes,
+                                oscar_cache** out) {
+  try {
+    oscar_status s = check_config(cfg);
+    if (s != OSCAR_OK) return s;
+    if (!out) return fail(OSCAR_ERR_INVALID_ARG, "out is NULL");
+    if (!device_arena) return fail(OSCAR_ERR_INVALID_ARG, "device_arena is NULL");
+    if (!aligned(device_arena, 256)) return fail(OSCAR_ERR_INVALID_ARG, "device_arena must be 256-byte aligned");
+    const ArenaLayout L = arena_layout(cfg->max_batch, cfg->num_kv_heads, cfg->max_seq_len);
+    if (arena_bytes < (size_t)L.total)
+      return fail(OSCAR_ERR_CAPACITY, "arena too small: %zu < %lld bytes", arena_bytes, (long long)L.total);
+    DeviceGuard dg(cfg->device);
+    if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+    int sms = num_sms(cfg->device);
+    if (sms <= 0) return fail(OSCAR_ERR_CUDA, "cannot query the SM count of device %d", cfg->device);
+    cudaError_t e = cudaMemset(device_arena, 0, (size_t)L.meta_bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(arena metadata)");
+    oscar_cache* c = new oscar_cache;
+    c->cfg = *cfg;
+    c->arena = static_cast<uint8_t*>(device_arena);
+    c->arena_bytes = arena_bytes;
+    c->layout = L;
+    c->len.assign(cfg->max_batch, 0);
+    c->sms = sms;
+    *out = c;
+    return ok();
+  } catch (const std::exception& ex) {
+    return fail(OSCAR_ERR_INVALID_ARG, "host allocation failed: %s", ex.what());
+  }
+}
+
+oscar_status oscar_cache_destroy(oscar_cache* cache) {
+  delete cache;
+  return ok();
+}
+
+oscar_status oscar_cache_reset(oscar_cache* c, int32_t seq, void* stream) {
+  if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+  if (seq < -1 || seq >= c->cfg.max_batch) return fail(OSCAR_ERR_INVALID_ARG, "seq %d out of range", seq);
+  DeviceGuard dg(c->cfg.device);
+  if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+  const int hkv = c->cfg.num_kv_heads;
+  uint8_t* meta = c->arena + kMetaHeader;
+  cudaError_t e;
+  if (seq < 0)
+    e = cudaMemsetAsync(meta, 0, (size_t)c->cfg.max_batch * hkv * 4, static_cast<cudaStream_t>(stream));
+  else
+    e = cudaMemsetAsync(meta + (size_t)seq * hkv * 4, 0, (size_t)hkv * 4, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(reset)");
+  if (seq < 0)
+    std::fill(c->len.begin(), c->len.end(), 0);
+  else
+    c->len[seq] = 0;
+  return ok();
+}
+
+oscar_status oscar_cache_length(const oscar_cache* c, int32_t seq, int32_t* out_len) {
+  if (!c || !out_len) return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+  if (seq < 0 || seq >= c->cfg.max_batch) return fail(OSCAR_ERR_INVALID_ARG, "seq %d out of range", seq);
+  *out_len = c->len[seq];
+  return ok();
+}
+
+oscar_status oscar_quantize_append(oscar_cache* c, int32_t n_seqs, const int32_t* seq_ids, const int32_t* cu_new,
+                                   const void* k, const void* v, void* stream) {
+  try {
+    if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+    if (n_seqs < 0) return fail(OSCAR_ERR_INVALID_ARG, "n_seqs < 0");
+    if (n_seqs == 0) return ok();
+    if (!seq_ids || !cu_new) return fail(OSCAR_ERR_INVALID_ARG, "seq_ids / cu_new is NULL");
+    std::vector<char> seen;
+    oscar_status s = check_slots(c, n_seqs, seq_ids, seen);
+    if (s != OSCAR_OK) return s;
+    if (cu_new[0] != 0) return fail(OSCAR_ERR_INVALID_ARG, "cu_new[0] must be 0");
+    for (int32_t i = 0; i < n_seqs; ++i) {
+      if (cu_new[i + 1] < cu_new[i]) return fail(OSCAR_ERR_INVALID_ARG, "cu_new must be non-decreasing");
+      const int64_t nl = (int64_t)c->len[seq_ids[i]] + (cu_new[i + 1] - cu_new[i]);
+      if (nl > c->cfg.max_seq_len)
+        return fail(OSCAR_ERR_CAPACITY, "sequence %d would reach %lld tokens > max_seq_len %d", seq_ids[i],
+                    (long long)nl, c->cfg.max_seq_len);
+    }
+    const int32_t total = cu_new[n_seqs];
+    if (total == 0) return ok();
+    if (!k || !v) return fail(OSCAR_ERR_INVALID_ARG, "k / v is NULL");
+    if (!aligned(k, 16) || !aligned(v, 16)) return fail(OSCAR_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+
+    std::vector<QuantTask> tasks;
+    for (int32_t i = 0; i < n_seqs; ++i) {
+      const int32_t n = cu_new[i + 1] - cu_new[i];
+      if (n == 0) continue;
+      const int32_t slot = seq_ids[i];
+      const int32_t L0 = c->len[slot];
+      const int32_t L1 = L0 + n;
+      const int32_t g_first = L0 / kGroup, g_end = L1 / kGroup;
+      const int32_t tail_start = std::max(L0, g_end * kGroup);
+      const int32_t tail_count = L1 - tail_start;
+      const int32_t tail_row = cu_new[i] + (tail_start - L0);
+      bool tail_done = tail_count == 0;
+      for (int32_t g = g_first; g < g_end; ++g) {
+        QuantTask t{};
+        t.kind = 0;
+        t.slot = slot;
+        t.group = g;
+        t.n_win = (g == g_first) ? L0 - g * kGroup : 0;
+        t.in_row = cu_new[i] + (g * kGroup + t.n_win - L0);
+        t.tail_count = 0;
+        if (g == g_first && t.n_win > 0 && !tail_done) {
+          t.tail_pos = tail_start;
+          t.tail_count = tail_count;
+          t.tail_in_row = tail_row;
+          tail_done = true;
+        }
+        tasks.push_back(t);
+      }
+      if (!tail_done) {
+        QuantTask t{};
+        t.kind = 1;
+        t.slot = slot;
+        t.tail_pos = tail_start;
+        t.tail_count = tail_count;
+        t.tail_in_row = tail_row;
+        tasks.push_back(t);
+      }
+    }
+    DeviceGuard dg(c->cfg.device);
+    if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint16_t* kp = static_cast<const uint16_t*>(k);
+    const uint16_t* vp = static_cast<const uint16_t*>(v);
+    for (size_t b = 0; b < tasks.size();) {
+      const size_t rem = tasks.size() - b;
+      if (rem <= (size_t)kQuantPlanSmall) {
+        s = run_quant_plan<kQuantPlanSmall>(c, tasks, b, tasks.size(), kp, vp, st);
+        b = tasks.size();
+      } else {
+        const size_t e = b + std::min(rem, (size_t)kQuantPlanLarge);
+        s = run_quant_plan<kQuantPlanLarge>(c, tasks, b, e, kp, vp, st);
+        b = e;
+      }
+      if (s != OSCAR_OK) return s;  // earlier chunks may already be enqueued
+    }
+    for (int32_t i = 0; i < n_seqs; ++i) c->len[seq_ids[i]] += cu_new[i + 1] - cu_new[i];
+    return ok();
+  } catch (const std::exception& ex) {
+    return fail(OSCAR_ERR_INVALID_ARG, "host allocation failed: %s", ex.what());
+  }
+}
+
+oscar_status oscar_decode_workspace_bytes(const oscar_cache* c, int32_t n_seqs, int32_t num_q_heads,
+                                          size_t* out_bytes) {
+  if (!c || !out_bytes) return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+  if (n_seqs < 0 || num_q_heads < 1) return fail(OSCAR_ERR_INVALID_ARG, "bad n_seqs / num_q_heads");
+  const int hkv = c->cfg.num_kv_heads;
+  if (num_q_heads % hkv != 0) return fail(OSCAR_ERR_INVALID_ARG, "num_q_heads must be a multiple of Hkv");
+  const int64_t slots = (int64_t)c->sms * decode_int2_ctas_per_sm() + (int64_t)n_seqs * hkv;
+  *out_bytes = partial_bytes(slots, num_q_heads / hkv);
+  return ok();
+}
+
+oscar_status oscar_decode_attention(oscar_cache* c, int32_t n_seqs, const int32_t* seq_ids, const void* q,
+                                    int32_t num_q_heads, float softmax_scale, void* out, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  try {
+    if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+    if (n_seqs < 1) return fail(OSCAR_ERR_INVALID_ARG, "n_seqs must be >= 1");
+    if (n_seqs > kDecodeSeqsLarge) return fail(OSCAR_ERR_CAPACITY, "at most %d sequences per call", kDecodeSeqsLarge);
+    if (!seq_ids || !q || !out || !workspace) return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+    const int hkv = c->cfg.num_kv_heads;
+    if (num_q_heads < hkv || num_q_heads % hkv != 0)
+      return fail(OSCAR_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of Hkv");
+    if (num_q_heads / hkv > kMaxGqa)
+      return fail(OSCAR_ERR_UNSUPPORTED, "at most %d query heads per KV head", kMaxGqa);
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 16))
+      return fail(OSCAR_ERR_INVALID_ARG, "q, out and workspace must be 16-byte aligned");
+    if (!(softmax_scale >= 0.0f) || std::isinf(softmax_scale))
+      return fail(OSCAR_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
+    std::vector<char> seen;
+    oscar_status s = check_slots(c, n_seqs, seq_ids, seen);
+    if (s != OSCAR_OK) return s;
+    std::vector<int32_t> lens(n_seqs);
+    for (int32_t i = 0; i < n_seqs; ++i) {
+      lens[i] = c->len[seq_ids[i]];
+      if (lens[i] < 1) return fail(OSCAR_ERR_INVALID_ARG, "sequence %d is empty", seq_ids[i]);
+    }
+    const float scale = softmax_scale == 0.0f ? 1.0f / std::sqrt((float)kHeadDim) : softmax_scale;
+    DeviceGuard dg(c->cfg.device);
+    if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+    uint32_t* err_word = reinterpret_cast<uint32_t*>(c->arena);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n_seqs <= kDecodeSeqsSmall)
+      s = run_decode<kDecodeSeqsSmall>(c->cfg.device, c->sms, decode_int2_ctas_per_sm(), n_seqs, seq_ids,
+                                       lens.data(), hkv, num_q_heads, scale, 0, c->layout.max_groups,
+                                       c->layout.blocks_off, c->layout.windows_off, c->arena, err_word, nullptr,
+                                       nullptr, q, out, workspace, workspace_bytes, st);
+    else
+      s = run_decode<kDecodeSeqsLarge>(c->cfg.device, c->sms, decode_int2_ctas_per_sm(), n_seqs, seq_ids,
+                                       lens.data(), hkv, num_q_heads, scale, 0, c->layout.max_groups,
+                                       c->layout.blocks_off, c->layout.windows_off, c->arena, err_word, nullptr,
+                                       nullptr, q, out, workspace, workspace_bytes, st);
+    if (s != OSCAR_OK) return s;
+    return ok();
+  } catch (const std::exception& ex) {
+    return fail(OSCAR_ERR_INVALID_ARG, "host allocation failed: %s", ex.what());
+  }
+}
+
+oscar_status oscar_cache_bytes(const oscar_cache* c, int32_t seq, int32_t kind, size_t* out_bytes) {
+  if (!c || !out_bytes) return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+  if (kind == OSCAR_BYTES_ARENA) {
+    *out_bytes = (size_t)c->layout.total;
+    return ok();
+  }
+  if (kind != OSCAR_BYTES_USED && kind != OSCAR_BYTES_BF16_EQUIVALENT)
+    return fail(OSCAR_ERR_INVALID_ARG, "unknown kind %d", kind);
+  if (seq < -1 || seq >= c->cfg.max_batch) return fail(OSCAR_ERR_INVALID_ARG, "seq %d out of range", seq);
+  const int hkv = c->cfg.num_kv_heads;
+  size_t total = 0;
+  for (int32_t s = (seq < 0 ? 0 : seq); s < (seq < 0 ? c->cfg.max_batch : seq + 1); ++s) {
+    const int64_t L = c->len[s];
+    if (kind == OSCAR_BYTES_USED)
+      total += (size_t)hkv * ((L / kGroup) * (int64_t)kBlockBytes + (L % kGroup) * 2 * kHeadDim * 2);
+    else
+      total += (size_t)hkv * L * 2 * kHeadDim * 2;
+  }
+  *out_bytes = total;
+  return ok();
+}
+
+oscar_status oscar_cache_block_offset(const oscar_cache* c, int32_t seq, int32_t kv_head, int32_t group,
+                                      size_t* out_offset) {
+  if (!c || !out_offset) return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+  if (seq < 0 || seq >= c->cfg.max_batch || kv_head < 0 || kv_head >= c->cfg.num_kv_heads || group < 0 ||
+      group >= c->layout.max_groups)
+    return fail(OSCAR_ERR_INVALID_ARG, "index out of range");
+  *out_offset = (size_t)(c->layout.blocks_off +
+                         (((int64_t)seq * c->cfg.num_kv_heads + kv_head) * c->layout.max_groups + group) *
+                             (int64_t)kBlockBytes);
+  return ok();
+}
+
+oscar_status oscar_cache_window_offset(const oscar_cache* c, int32_t seq, int32_t kv_head, size_t* out_offset) {
+  if (!c || !out_offset) return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+  if (seq < 0 || seq >= c->cfg.max_batch || kv_head < 0 || kv_head >= c->cfg.num_kv_heads)
+    return fail(OSCAR_ERR_INVALID_ARG, "index out of range");
+  *out_offset = (size_t)(c->layout.windows_off + ((int64_t)seq * c->cfg.num_kv_heads + kv_head) * kWindowBytes);
+  return ok();
+}
+
+oscar_status oscar_cache_check(oscar_cache* c, void* stream) {
+  if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+  DeviceGuard dg(c->cfg.device);
+  if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  uint32_t word = 0;
+  e = cudaMemcpy(&word, c->arena, 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
+  if (word != 0) {
+    cudaMemset(c->arena, 0, 4);
+    return fail(OSCAR_ERR_DEVICE_TIMEOUT, "a kernel wait timed out (flags 0x%x)", word);
+  }
+  return ok();
+}
+
+oscar_status oscar_bf16_decode_workspace_bytes(int32_t n_seqs, int32_t num_kv_heads, int32_t num_q_heads,
+                                               size_t* out_bytes) {
+  if (!out_bytes || n_seqs < 0 || num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads != 0)
+    return fail(OSCAR_ERR_INVALID_ARG, "bad arguments");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  const int sms = num_sms(dev);
+  if (sms <= 0) return fail(OSCAR_ERR_CUDA, "cannot query the SM count");
+  const int64_t slots = (int64_t)sms * decode_bf16_ctas_per_sm() + (int64_t)n_seqs * num_kv_heads;
+  *out_bytes = partial_bytes(slots, num_q_heads / num_kv_heads);
+  return ok();
+}
+
+oscar_status oscar_bf16_decode_attention(int32_t n_seqs, const int32_t* seq_ids, const int32_t* seq_lens,
+                                         const void* k_cache, const void* v_cache, int32_t num_kv_heads,
+                                         int32_t max_seq_len, const void* q, int32_t num_q_heads,
+                                         float softmax_scale, void* out, void* workspace, size_t workspace_bytes,
+                                         void* stream) {
+  try {
+    if (n_seqs < 1) return fail(OSCAR_ERR_INVALID_ARG, "n_seqs must be >= 1");
+    if (n_seqs > kDecodeSeqsLarge) return fail(OSCAR_ERR_CAPACITY, "at most %d sequences per call", kDecodeSeqsLarge);
+    if (!seq_ids || !seq_lens || !k_cache || !v_cache || !q || !out || !workspace)
+      return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+    if (num_kv_heads < 1 || max_seq_len < 1) return fail(OSCAR_ERR_INVALID_ARG, "bad num_kv_heads / max_seq_len");
+    if (num_q_heads < num_kv_heads || num_q_heads % num_kv_heads != 0)
+      return fail(OSCAR_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of Hkv");
+    if (num_q_heads / num_kv_heads > kMaxGqa)
+      return fail(OSCAR_ERR_UNSUPPORTED, "at most %d query heads per KV head", kMaxGqa);
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 16) ||
+        !aligned(workspace, 16))
+      return fail(OSCAR_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+    if (!(softmax_scale >= 0.0f) || std::isinf(softmax_scale))
+      return fail(OSCAR_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
+    for (int32_t i = 0; i < n_seqs; ++i) {
+      if (seq_ids[i] < 0) return fail(OSCAR_ERR_INVALID_ARG, "seq_ids[%d] < 0", i);
+      if (seq_lens[i] < 1 || seq_lens[i] > max_seq_len)
+        return fail(OSCAR_ERR_INVALID_ARG, "seq_lens[%d] = %d outside [1, max_seq_len]", i, seq_lens[i]);
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    const int sms = num_sms(dev);
+    if (sms <= 0) return fail(OSCAR_ERR_CUDA, "cannot query the SM count");
+    const float scale = softmax_scale == 0.0f ? 1.0f / std::sqrt((float)kHeadDim) : softmax_scale;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint16_t* kc = static_cast<const uint16_t*>(k_cache);
+    const uint16_t* vc = static_cast<const uint16_t*>(v_cache);
+    oscar_status s;
+    if (n_seqs <= kDecodeSeqsSmall)
+      s = run_decode<kDecodeSeqsSmall>(dev, sms, decode_bf16_ctas_per_sm(), n_seqs, seq_ids, seq_lens,
+                                       num_kv_heads, num_q_heads, scale, 1, max_seq_len, 0, 0, nullptr, nullptr, kc,
+                                       vc, q, out, workspace, workspace_bytes, st);
+    else
+      s = run_decode<kDecodeSeqsLarge>(dev, sms, decode_bf16_ctas_per_sm(), n_seqs, seq_ids, seq_lens,
+                                       num_kv_heads, num_q_heads, scale, 1, max_seq_len, 0, 0, nullptr, nullptr, kc,
+                                       vc, q, out, workspace, workspace_bytes, st);
+    if (s != OSCAR_OK) return s;
+    return ok();
+  } catch (const std::exception& ex) {
+    return fail(OSCAR_ERR_INVALID_ARG, "host allocation failed: %s", ex.what());
+  }
+}
+
+oscar_status oscar_set_timing_events(void* start_event, void* stop_event) {
+  if ((start_event == nullptr) != (stop_event == nullptr))
+    return fail(OSCAR_ERR_INVALID_ARG, "pass both events or neither");
+  g_ev_start = static_cast<cudaEvent_t>(start_event);
+  g_ev_stop = static_cast<cudaEvent_t>(stop_event);
+  return ok();
+}
+
+}  // extern "C"

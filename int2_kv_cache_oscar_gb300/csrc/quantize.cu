@@ -1,0 +1,291 @@
+// OScaR compression kernel (sm_103a): quantise every 128-token group that
+// fills during an append, and copy the remaining tokens into the bf16 window.
+//
+// Method ("OScaR", arXiv 2605.19660 Abstract; ai-papers.net summary, section
+// "OScaRの提案手法"): Canalized Rotation (normalised Walsh-Hadamard H_d) of
+// every key, then Omni-Token Scaling (store the token's L2 norm, divide the
+// token by it), then per-channel asymmetric INT2 over the group's 128 tokens.
+// Values: per-token asymmetric INT2 over 32-channel groups (KIVI convention
+// cited in the qiita.com NOVA-KV article).
+//
+// One CTA = one (group, KV head); thread t owns token t of the group.
+//   1. V row of token t: per 32-channel group min/max, s = (max-min)/3, z = min,
+//      codes; codes go to shared memory (transposed), s/z to the block.
+//   2. K row of token t: 128 values in registers; unnormalised fast
+//      Walsh-Hadamard transform (7 butterfly stages, H_d = Hu / sqrt(128));
+//      n_t = sqrt(|Hu k|^2 / 128); k_hat = Hu k / |Hu k| (= H_d k / n_t).
+//   3. Per-channel min/max of k_hat over the 128 tokens (shared memory).
+//   4. Codes of k_hat, packed straight into the fragment-order words.
+//   5. Coalesced 16-byte stores of both code matrices.
+#include "common.cuh"
+#include "launch.h"
+
+namespace oscar {
+namespace {
+
+constexpr int kQThreads = 128;
+constexpr int kKhStride = 132;  // floats per k_hat row in shared memory (padding vs bank conflicts)
+constexpr int kVbStride = 144;  // bytes per value-code row (channel) in shared memory
+
+struct QuantSmem {
+  float kh[kGroup * kKhStride];          // k_hat[t][c]
+  uint8_t vb[kHeadDim * kVbStride];      // value codes [channel][permuted token]
+  uint32_t kw[1024];                     // key code words, fragment order
+  float2 kp[kHeadDim];                   // per-channel (1/s, z)
+  float red[kQThreads / 32];
+};
+
+// Round-half-even code of x against (inv = 1/s, z), clamped to [0, 3]; the
+// magic constant 1.5 * 2^23 leaves rne(v) in the low mantissa bits.
+__device__ __forceinline__ uint32_t int2_code(float x, float inv, float z) {
+  float v = (x - z) * inv;
+  v = fminf(fmaxf(v, 0.0f), 3.0f);
+  return __float_as_uint(v + 12582912.0f) & 3u;
+}
+
+// Position of token/col c inside its 16-byte packing chunk of the byte
+// staging area: chunk (tig, j), byte ((kk * 4) + hf + 2 e).
+__device__ __forceinline__ int vb_perm(int c) {
+  const int ks = c >> 4, j = ks >> 2, kk = ks & 3, hf = (c >> 3) & 1, tig = (c >> 1) & 3, e = c & 1;
+  return ((tig * 2 + j) * 4 + kk) * 4 + hf + 2 * e;
+}
+
+__device__ __forceinline__ void load_row(const uint16_t* src, float (&x)[kHeadDim]) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    uint4 u = __ldg(s + i);
+    x[8 * i + 0] = bf16_lo(u.x);
+    x[8 * i + 1] = bf16_hi(u.x);
+    x[8 * i + 2] = bf16_lo(u.y);
+    x[8 * i + 3] = bf16_hi(u.y);
+    x[8 * i + 4] = bf16_lo(u.z);
+    x[8 * i + 5] = bf16_hi(u.z);
+    x[8 * i + 6] = bf16_lo(u.w);
+    x[8 * i + 7] = bf16_hi(u.w);
+  }
+}
+
+template <int CAP>
+__global__ void __launch_bounds__(kQThreads, 2)
+    quantize_append_kernel(const __grid_constant__ QuantPlan<CAP> plan, uint8_t* __restrict__ arena,
+                           const uint16_t* __restrict__ kin, const uint16_t* __restrict__ vin) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  QuantSmem& S = *reinterpret_cast<QuantSmem*>(smem_raw);
+  const int head = blockIdx.y;
+  const int tid = threadIdx.x;
+  const QuantTask T = plan.t[blockIdx.x];
+  const int hkv = plan.hkv;
+  const int64_t sh = (int64_t)T.slot * hkv + head;
+  uint8_t* win = arena + plan.windows_off + sh * kWindowBytes;
+  uint16_t* win_k = reinterpret_cast<uint16_t*>(win);
+  uint16_t* win_v = win_k + kGroup * kHeadDim;
+
+  if (T.kind == 0) {
+    uint8_t* blk = arena + plan.blocks_off + (sh * plan.max_groups + T.group) * (int64_t)kBlockBytes;
+    const int t = tid;
+    const bool from_win = t < T.n_win;
+    const int64_t row = (int64_t)T.in_row + (t - T.n_win);
+    const uint16_t* ksrc = from_win ? win_k + t * kHeadDim : kin + (row * hkv + head) * kHeadDim;
+    const uint16_t* vsrc = from_win ? win_v + t * kHeadDim : vin + (row * hkv + head) * kHeadDim;
+
+    // ---- values: per-token INT2 over 32-channel groups
+    float smax = 0.0f;
+    {
+      const int pt = vb_perm(t);
+      float sv[kVGroups], zv[kVGroups];
+#pragma unroll
+      for (int gi = 0; gi < kVGroups; ++gi) {
+        float x[kVGroup];
+        const uint4* s4 = reinterpret_cast<const uint4*>(vsrc + gi * kVGroup);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint4 u = __ldg(s4 + i);
+          x[8 * i + 0] = bf16_lo(u.x);
+          x[8 * i + 1] = bf16_hi(u.x);
+          x[8 * i + 2] = bf16_lo(u.y);
+          x[8 * i + 3] = bf16_hi(u.y);
+          x[8 * i + 4] = bf16_lo(u.z);
+          x[8 * i + 5] = bf16_hi(u.z);
+          x[8 * i + 6] = bf16_lo(u.w);
+          x[8 * i + 7] = bf16_hi(u.w);
+        }
+        float mn = x[0], mx = x[0];
+#pragma unroll
+        for (int i = 1; i < kVGroup; ++i) {
+          mn = fminf(mn, x[i]);
+          mx = fmaxf(mx, x[i]);
+        }
+        const float s = (mx - mn) / 3.0f;
+        const float inv = s > 0.0f ? 1.0f / s : 0.0f;
+        sv[gi] = s;
+        zv[gi] = mn;
+        smax = fmaxf(smax, s);
+#pragma unroll
+        for (int i = 0; i < kVGroup; ++i) {
+          S.vb[(gi * kVGroup + i) * kVbStride + pt] = (uint8_t)int2_code(x[i], inv, mn);
+        }
+      }
+      float4* dsz = reinterpret_cast<float4*>(blk + kOffVSZ + 32 * t);
+      dsz[0] = make_float4(sv[0], sv[1], sv[2], sv[3]);
+      dsz[1] = make_float4(zv[0], zv[1], zv[2], zv[3]);
+    }
+
+    // ---- keys: rotation, norm, unit vector
+    float x[kHeadDim];
+    load_row(ksrc, x);
+#pragma unroll
+    for (int h = 1; h < kHeadDim; h <<= 1) {
+#pragma unroll
+      for (int i = 0; i < kHeadDim; i += 2 * h) {
+#pragma unroll
+        for (int j = i; j < i + h; ++j) {
+          const float a = x[j], b = x[j + h];
+          x[j] = a + b;
+          x[j + h] = a - b;
+        }
+      }
+    }
+    float sq[kHeadDim / 2];
+#pragma unroll
+    for (int i = 0; i < kHeadDim / 2; ++i) sq[i] = x[i] * x[i] + x[i + kHeadDim / 2] * x[i + kHeadDim / 2];
+#pragma unroll
+    for (int w = kHeadDim / 4; w >= 1; w >>= 1) {
+#pragma unroll
+      for (int i = 0; i < w; ++i) sq[i] += sq[i + w];
+    }
+    const float ss = sq[0];
+    const float norm = sqrtf(ss * (1.0f / kHeadDim));
+    const float rinv = ss > 0.0f ? 1.0f / sqrtf(ss) : 0.0f;
+#pragma unroll
+    for (int i = 0; i < kHeadDim; ++i) x[i] *= rinv;
+    reinterpret_cast<float*>(blk + kOffKNorm)[t] = norm;
+    {
+      float4* dst = reinterpret_cast<float4*>(&S.kh[t * kKhStride]);
+#pragma unroll
+      for (int i = 0; i < kHeadDim / 4; ++i) dst[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+    }
+    // value-scale maximum of this group -> CTA maximum
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+    if ((tid & 31) == 0) S.red[tid >> 5] = smax;
+    __syncthreads();
+
+    // ---- per-channel key parameters (thread = channel)
+    {
+      const int c = tid;
+      float mn = S.kh[c], mx = mn;
+#pragma unroll 8
+      for (int r = 1; r < kGroup; ++r) {
+        const float v = S.kh[r * kKhStride + c];
+        mn = fminf(mn, v);
+        mx = fmaxf(mx, v);
+      }
+      const float s = (mx - mn) / 3.0f;
+      S.kp[c] = make_float2(s > 0.0f ? 1.0f / s : 0.0f, mn);
+      reinterpret_cast<float*>(blk + kOffKScale)[c] = s;
+      reinterpret_cast<float*>(blk + kOffKZero)[c] = mn;
+    }
+    __syncthreads();
+
+    // ---- key codes of token t, packed into its 8 fragment-order words
+    {
+      const int mt = t >> 4, g = t & 7, r = (t >> 3) & 1;
+#pragma unroll
+      for (int tig = 0; tig < 4; ++tig) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          uint32_t w = 0;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int c = 16 * (4 * j + kk) + 8 * hf + 2 * tig + e;
+                const float2 p = S.kp[c];
+                w |= int2_code(x[c], p.x, p.y) << (16 * e + 4 * kk + 2 * hf);
+              }
+            }
+          }
+          S.kw[((mt * 32 + 4 * g + tig) * 4) + 2 * j + r] = w;
+        }
+      }
+    }
+    __syncthreads();
+
+    // ---- coalesced stores of both code matrices (256 x 16 B each)
+#pragma unroll
+    for (int rep = 0; rep < 2; ++rep) {
+      const int u = tid + rep * kQThreads;
+      reinterpret_cast<uint4*>(blk + kOffKCodes)[u] = reinterpret_cast<const uint4*>(S.kw)[u];
+      const int mt = u >> 5, lane = u & 31, g = lane >> 2, tig = lane & 3;
+      uint32_t wv[4];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int rowc = 16 * mt + g + 8 * r;
+          const uint4 b = *reinterpret_cast<const uint4*>(&S.vb[rowc * kVbStride + (tig * 2 + j) * 16]);
+          const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+          uint32_t w = 0;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t y = (bw[kk] | (bw[kk] >> 6)) & 0x000F000Fu;
+            w |= y << (4 * kk);
+          }
+          wv[2 * j + r] = w;
+        }
+      }
+      reinterpret_cast<uint4*>(blk + kOffVCodes)[u] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    }
+    if (tid == 0) {
+      float m = S.red[0];
+#pragma unroll
+      for (int i = 1; i < kQThreads / 32; ++i) m = fmaxf(m, S.red[i]);
+      atomicMax(reinterpret_cast<unsigned int*>(arena + kMetaHeader) + sh, __float_as_uint(m));
+    }
+    if (T.tail_count <= 0) return;
+    // the window reads above completed before the first __syncthreads
+  }
+
+  // ---- window append: rows tail_in_row.. -> window slots (tail_pos + i) mod 128
+  {
+    const int count = T.tail_count;
+    for (int idx = tid; idx < count * 16; idx += kQThreads) {
+      const int i = idx >> 4, q = idx & 15;
+      const int64_t row = (int64_t)T.tail_in_row + i;
+      const int slot = (T.tail_pos + i) & (kGroup - 1);
+      const uint4* ks = reinterpret_cast<const uint4*>(kin + (row * hkv + head) * kHeadDim);
+      const uint4* vs = reinterpret_cast<const uint4*>(vin + (row * hkv + head) * kHeadDim);
+      reinterpret_cast<uint4*>(win_k + slot * kHeadDim)[q] = __ldg(ks + q);
+      reinterpret_cast<uint4*>(win_v + slot * kHeadDim)[q] = __ldg(vs + q);
+    }
+  }
+}
+
+template <int CAP>
+cudaError_t launch_quantize(const QuantPlan<CAP>& plan, uint8_t* arena, const uint16_t* k, const uint16_t* v,
+                            cudaStream_t stream) {
+  if (plan.n_tasks <= 0) return cudaSuccess;
+  const int smem = (int)sizeof(QuantSmem);
+  cudaError_t e = cudaFuncSetAttribute(quantize_append_kernel<CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(plan.n_tasks, plan.hkv);
+  quantize_append_kernel<CAP><<<grid, kQThreads, smem, stream>>>(plan, arena, k, v);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_small(const QuantPlan<kQuantPlanSmall>& plan, uint8_t* arena, const uint16_t* k,
+                                  const uint16_t* v, cudaStream_t stream) {
+  return launch_quantize(plan, arena, k, v, stream);
+}
+
+cudaError_t launch_quantize_large(const QuantPlan<kQuantPlanLarge>& plan, uint8_t* arena, const uint16_t* k,
+                                  const uint16_t* v, cudaStream_t stream) {
+  return launch_quantize(plan, arena, k, v, stream);
+}
+
+}  // namespace oscar

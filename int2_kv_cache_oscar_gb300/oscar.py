@@ -1,0 +1,260 @@
+"""Thin ctypes binding of liboscar.so (include/oscar.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  Device buffers are torch tensors (PyTorch supplies device memory
+and streams); host integer arrays are Python sequences.  Every function
+raises OscarError when the C call returns a non-zero status.  There is no
+CPU fallback: importing this module fails loudly if the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liboscar.so")
+
+OSCAR_OK = 0
+OSCAR_ERR_INVALID_ARG = 1
+OSCAR_ERR_CAPACITY = 2
+OSCAR_ERR_CUDA = 3
+OSCAR_ERR_UNSUPPORTED = 4
+OSCAR_ERR_DEVICE_TIMEOUT = 5
+
+OSCAR_BYTES_USED = 0
+OSCAR_BYTES_BF16_EQUIVALENT = 1
+OSCAR_BYTES_ARENA = 2
+
+HEAD_DIM = 128
+GROUP = 128
+VALUE_GROUP = 32
+BLOCK_BYTES = 13824
+WINDOW_BYTES = 65536
+
+
+class OscarError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"oscar status {status}: {message}")
+        self.status = status
+
+
+class oscar_cache_config(ctypes.Structure):
+    _fields_ = [("max_batch", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
+                ("group_size", ctypes.c_int32), ("value_group", ctypes.c_int32),
+                ("device", ctypes.c_int32)]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"{_LIB_PATH} is missing: build it with int2_kv_cache_oscar_gb300.build.build()")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P = ctypes.c_void_p
+    I32 = ctypes.c_int32
+    SZ = ctypes.c_size_t
+    I32P = ctypes.POINTER(ctypes.c_int32)
+    sigs = {
+        "oscar_cache_required_bytes": [ctypes.POINTER(oscar_cache_config), ctypes.POINTER(SZ)],
+        "oscar_cache_create": [ctypes.POINTER(oscar_cache_config), P, SZ, ctypes.POINTER(P)],
+        "oscar_cache_destroy": [P],
+        "oscar_cache_reset": [P, I32, P],
+        "oscar_cache_length": [P, I32, I32P],
+        "oscar_quantize_append": [P, I32, I32P, I32P, P, P, P],
+        "oscar_decode_workspace_bytes": [P, I32, I32, ctypes.POINTER(SZ)],
+        "oscar_decode_attention": [P, I32, I32P, P, I32, ctypes.c_float, P, P, SZ, P],
+        "oscar_cache_bytes": [P, I32, I32, ctypes.POINTER(SZ)],
+        "oscar_cache_block_offset": [P, I32, I32, I32, ctypes.POINTER(SZ)],
+        "oscar_cache_window_offset": [P, I32, I32, ctypes.POINTER(SZ)],
+        "oscar_cache_check": [P, P],
+        "oscar_bf16_decode_workspace_bytes": [I32, I32, I32, ctypes.POINTER(SZ)],
+        "oscar_bf16_decode_attention": [I32, I32P, I32P, P, P, I32, I32, P, I32, ctypes.c_float, P, P,
+                                        SZ, P],
+        "oscar_set_timing_events": [P, P],
+    }
+    for name, args in sigs.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = ctypes.c_int
+    lib.oscar_last_error.argtypes = []
+    lib.oscar_last_error.restype = ctypes.c_char_p
+    return lib
+
+
+_lib = _load()
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def raw_library() -> ctypes.CDLL:
+    return _lib
+
+
+def oscar_last_error() -> str:
+    return _lib.oscar_last_error().decode()
+
+
+def _check(status: int):
+    if status != OSCAR_OK:
+        raise OscarError(status, oscar_last_error())
+
+
+def _i32(seq: Sequence[int]):
+    arr = (ctypes.c_int32 * len(seq))(*[int(x) for x in seq])
+    return arr
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def make_config(max_batch: int, num_kv_heads: int, max_seq_len: int, device: int = 0,
+                head_dim: int = HEAD_DIM, group_size: int = GROUP,
+                value_group: int = VALUE_GROUP) -> oscar_cache_config:
+    return oscar_cache_config(max_batch, num_kv_heads, head_dim, max_seq_len, group_size,
+                              value_group, device)
+
+
+def oscar_cache_required_bytes(cfg: oscar_cache_config) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_lib.oscar_cache_required_bytes(ctypes.byref(cfg), ctypes.byref(out)))
+    return out.value
+
+
+def oscar_cache_create(cfg: oscar_cache_config, arena: torch.Tensor) -> ctypes.c_void_p:
+    h = ctypes.c_void_p(0)
+    _check(_lib.oscar_cache_create(ctypes.byref(cfg), _ptr(arena),
+                                   arena.numel() * arena.element_size(), ctypes.byref(h)))
+    return h
+
+
+def oscar_cache_destroy(handle) -> None:
+    _check(_lib.oscar_cache_destroy(handle))
+
+
+def oscar_cache_reset(handle, seq: int = -1, stream=None) -> None:
+    _check(_lib.oscar_cache_reset(handle, seq, _stream(stream)))
+
+
+def oscar_cache_length(handle, seq: int) -> int:
+    out = ctypes.c_int32(0)
+    _check(_lib.oscar_cache_length(handle, seq, ctypes.byref(out)))
+    return out.value
+
+
+def oscar_quantize_append(handle, seq_ids: Sequence[int], cu_new: Sequence[int],
+                          k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
+    _check(_lib.oscar_quantize_append(handle, len(seq_ids), _i32(seq_ids), _i32(cu_new),
+                                      _ptr(k), _ptr(v), _stream(stream)))
+
+
+def oscar_decode_workspace_bytes(handle, n_seqs: int, num_q_heads: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_lib.oscar_decode_workspace_bytes(handle, n_seqs, num_q_heads, ctypes.byref(out)))
+    return out.value
+
+
+def oscar_decode_attention(handle, seq_ids: Sequence[int], q: torch.Tensor, num_q_heads: int,
+                           softmax_scale: float, out: torch.Tensor, workspace: torch.Tensor,
+                           stream=None) -> None:
+    _check(_lib.oscar_decode_attention(handle, len(seq_ids), _i32(seq_ids), _ptr(q), num_q_heads,
+                                       ctypes.c_float(softmax_scale), _ptr(out), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(),
+                                       _stream(stream)))
+
+
+def oscar_cache_bytes(handle, seq: int, kind: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_lib.oscar_cache_bytes(handle, seq, kind, ctypes.byref(out)))
+    return out.value
+
+
+def oscar_cache_block_offset(handle, seq: int, kv_head: int, group: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_lib.oscar_cache_block_offset(handle, seq, kv_head, group, ctypes.byref(out)))
+    return out.value
+
+
+def oscar_cache_window_offset(handle, seq: int, kv_head: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_lib.oscar_cache_window_offset(handle, seq, kv_head, ctypes.byref(out)))
+    return out.value
+
+
+def oscar_cache_check(handle, stream=None) -> None:
+    _check(_lib.oscar_cache_check(handle, _stream(stream)))
+
+
+def oscar_bf16_decode_workspace_bytes(n_seqs: int, num_kv_heads: int, num_q_heads: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_lib.oscar_bf16_decode_workspace_bytes(n_seqs, num_kv_heads, num_q_heads,
+                                                  ctypes.byref(out)))
+    return out.value
+
+
+def oscar_bf16_decode_attention(seq_ids: Sequence[int], seq_lens: Sequence[int],
+                                k_cache: torch.Tensor, v_cache: torch.Tensor, num_kv_heads: int,
+                                max_seq_len: int, q: torch.Tensor, num_q_heads: int,
+                                softmax_scale: float, out: torch.Tensor, workspace: torch.Tensor,
+                                stream=None) -> None:
+    _check(_lib.oscar_bf16_decode_attention(
+        len(seq_ids), _i32(seq_ids), _i32(seq_lens), _ptr(k_cache), _ptr(v_cache), num_kv_heads,
+        max_seq_len, _ptr(q), num_q_heads, ctypes.c_float(softmax_scale), _ptr(out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def oscar_set_timing_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]):
+    s = ctypes.c_void_p(0 if start is None else start.cuda_event)
+    e = ctypes.c_void_p(0 if stop is None else stop.cuda_event)
+    _check(_lib.oscar_set_timing_events(s, e))
+
+
+class OscarCache:
+    """Owns a device arena (a torch uint8 tensor) and the library handle."""
+
+    def __init__(self, max_batch: int, num_kv_heads: int, max_seq_len: int,
+                 device: Optional[torch.device] = None):
+        device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+        self.cfg = make_config(max_batch, num_kv_heads, max_seq_len, device.index or 0)
+        nbytes = oscar_cache_required_bytes(self.cfg)
+        self.arena = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self.handle = oscar_cache_create(self.cfg, self.arena)
+        self.num_kv_heads = num_kv_heads
+        self.max_batch = max_batch
+        self.max_seq_len = max_seq_len
+
+    def close(self):
+        if self.handle is not None and self.handle.value:
+            oscar_cache_destroy(self.handle)
+        self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def length(self, seq: int) -> int:
+        return oscar_cache_length(self.handle, seq)
+
+    def append(self, seq_ids, cu_new, k, v, stream=None):
+        oscar_quantize_append(self.handle, seq_ids, cu_new, k, v, stream)
+
+    def workspace(self, n_seqs: int, num_q_heads: int) -> torch.Tensor:
+        n = oscar_decode_workspace_bytes(self.handle, n_seqs, num_q_heads)
+        return torch.empty(max(n, 16), dtype=torch.uint8, device=self.arena.device)
+
+    def decode(self, seq_ids, q, num_q_heads, out, workspace, softmax_scale=0.0, stream=None):
+        oscar_decode_attention(self.handle, seq_ids, q, num_q_heads, softmax_scale, out, workspace,
+                               stream)

@@ -1,0 +1,82 @@
+"""Reader of the library's device layout, written from the description in
+include/oscar.h (not from the CUDA sources): unpacks a 13,824-byte group
+block into canonical arrays, and packs canonical codes into fragment order
+(used only to check that the two are inverse).
+
+Fragment order of a 128x128 matrix of 2-bit codes X[row][col]: 32-bit word
+w = ((mt*32 + lane)*4 + 2*j + r) holds the 16 codes with
+row = 16*mt + (lane >> 2) + 8*r and col = 16*(4*j + kk) + 8*hf + 2*(lane & 3) + e,
+the code sitting at bits [b, b+1], b = 16*e + 4*kk + 2*hf.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+D = 128
+G = 128
+BLOCK_BYTES = 13824
+OFF_KCODES, OFF_KSCALE, OFF_KZERO, OFF_KNORM, OFF_VCODES, OFF_VSZ = 0, 4096, 4608, 5120, 5632, 9728
+
+
+def _index_tables():
+    rows = np.zeros((1024, 16), np.int64)
+    cols = np.zeros((1024, 16), np.int64)
+    bits = np.zeros((1024, 16), np.int64)
+    for mt in range(8):
+        for lane in range(32):
+            for j in range(2):
+                for r in range(2):
+                    w = (mt * 32 + lane) * 4 + 2 * j + r
+                    n = 0
+                    for kk in range(4):
+                        for hf in range(2):
+                            for e in range(2):
+                                rows[w, n] = 16 * mt + (lane >> 2) + 8 * r
+                                cols[w, n] = 16 * (4 * j + kk) + 8 * hf + 2 * (lane & 3) + e
+                                bits[w, n] = 16 * e + 4 * kk + 2 * hf
+                                n += 1
+    return rows, cols, bits
+
+
+_ROWS, _COLS, _BITS = _index_tables()
+
+
+def unpack_fragment(words: np.ndarray) -> np.ndarray:
+    """uint32 [1024] (little-endian words) -> uint8 codes [128, 128] X[row][col]."""
+    words = np.asarray(words, dtype=np.uint32).reshape(1024)
+    vals = (words[:, None].astype(np.int64) >> _BITS) & 3
+    out = np.zeros((G, D), np.uint8)
+    out[_ROWS, _COLS] = vals
+    return out
+
+
+def pack_fragment(codes: np.ndarray) -> np.ndarray:
+    codes = np.asarray(codes, np.int64)
+    vals = codes[_ROWS, _COLS] << _BITS
+    return np.bitwise_or.reduce(vals, axis=1).astype(np.uint32)
+
+
+def parse_block(raw: np.ndarray) -> dict:
+    """raw: uint8 [13824] -> canonical arrays of one (group, kv head)."""
+    raw = np.ascontiguousarray(np.asarray(raw, np.uint8).reshape(BLOCK_BYTES))
+    kcodes = unpack_fragment(raw[OFF_KCODES:OFF_KCODES + 4096].view("<u4"))        # [token, ch]
+    kscale = raw[OFF_KSCALE:OFF_KSCALE + 512].view("<f4").copy()
+    kzero = raw[OFF_KZERO:OFF_KZERO + 512].view("<f4").copy()
+    knorm = raw[OFF_KNORM:OFF_KNORM + 512].view("<f4").copy()
+    vcodes_t = unpack_fragment(raw[OFF_VCODES:OFF_VCODES + 4096].view("<u4"))      # [ch, token]
+    vsz = raw[OFF_VSZ:OFF_VSZ + 4096].view("<f4").reshape(G, 8)
+    return dict(kcodes=kcodes, kscale=kscale, kzero=kzero, knorm=knorm,
+                vcodes=vcodes_t.T.copy(), vscale=vsz[:, :4].copy(), vzero=vsz[:, 4:].copy())
+
+
+def bf16_bits_to_f64(u16: np.ndarray) -> np.ndarray:
+    u = np.asarray(u16, np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
+def parse_window(raw: np.ndarray, n: int):
+    """raw: uint8 [65536] window of one (slot, head) -> (k [n, d], v [n, d]) float64."""
+    raw = np.ascontiguousarray(np.asarray(raw, np.uint8).reshape(65536))
+    k = bf16_bits_to_f64(raw[:32768].view("<u2").reshape(G, D)[:n])
+    v = bf16_bits_to_f64(raw[32768:].view("<u2").reshape(G, D)[:n])
+    return k, v

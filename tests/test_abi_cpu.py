@@ -1,0 +1,102 @@
+"""C-ABI library: it loads without a GPU, exports every function the header
+declares, and validates arguments on the host (no compute calls here)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "oscar.h")
+
+
+def _declared():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:oscar_status|const char\*)\s+(oscar_\w+)\s*\(", txt, re.M)))
+
+
+@pytest.fixture(scope="module")
+def O():
+    from int2_kv_cache_oscar_gb300 import build
+    if not os.path.exists(build.LIB):
+        build.build()
+    from int2_kv_cache_oscar_gb300 import oscar
+    return oscar
+
+
+def test_header_declares_the_path_calls():
+    names = _declared()
+    for n in ["oscar_cache_create", "oscar_quantize_append", "oscar_decode_attention",
+              "oscar_cache_bytes"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(O):
+    lib = O.raw_library()
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+    out = subprocess.run(["nm", "-D", "--defined-only", O.library_path()], capture_output=True,
+                         text=True).stdout
+    exported = set(re.findall(r" T (oscar_\w+)", out))
+    assert set(_declared()) <= exported
+
+
+def test_required_bytes_layout(O):
+    cfg = O.make_config(3, 8, 1000)
+    n = O.oscar_cache_required_bytes(cfg)
+    meta = -(-(256 + 3 * 8 * 4) // 256) * 256
+    groups = -(-1000 // 128)
+    blocks = 3 * 8 * groups * 13824
+    win_off = -(-(meta + blocks) // 256) * 256
+    assert n == win_off + 3 * 8 * 65536
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("head_dim", 64, 4), ("group_size", 64, 4), ("value_group", 16, 4),
+    ("max_batch", 0, 1), ("num_kv_heads", 0, 1), ("max_seq_len", 0, 1), ("device", -1, 1)])
+def test_bad_configs(O, field, value, status):
+    cfg = O.make_config(2, 2, 256)
+    setattr(cfg, field, value)
+    with pytest.raises(O.OscarError) as e:
+        O.oscar_cache_required_bytes(cfg)
+    assert e.value.status == status
+    assert O.oscar_last_error()
+
+
+def test_null_arguments_rejected_on_host(O):
+    lib = O.raw_library()
+    cfg = O.make_config(1, 1, 128)
+    h = ctypes.c_void_p(0)
+    assert lib.oscar_cache_create(ctypes.byref(cfg), None, 1 << 20, ctypes.byref(h)) == O.OSCAR_ERR_INVALID_ARG
+    assert lib.oscar_cache_create(ctypes.byref(cfg), ctypes.c_void_p(256), 10, ctypes.byref(h)) == \
+        O.OSCAR_ERR_CAPACITY
+    assert lib.oscar_cache_create(ctypes.byref(cfg), ctypes.c_void_p(1000), 1 << 30, ctypes.byref(h)) == \
+        O.OSCAR_ERR_INVALID_ARG          # misaligned arena
+    assert lib.oscar_quantize_append(None, 1, None, None, None, None, None) == O.OSCAR_ERR_INVALID_ARG
+    assert lib.oscar_decode_attention(None, 1, None, None, 4, ctypes.c_float(0), None, None, 0,
+                                      None) == O.OSCAR_ERR_INVALID_ARG
+    sz = ctypes.c_size_t(0)
+    assert lib.oscar_cache_bytes(None, -1, 0, ctypes.byref(sz)) == O.OSCAR_ERR_INVALID_ARG
+    assert lib.oscar_cache_destroy(None) == O.OSCAR_OK
+    assert lib.oscar_set_timing_events(None, None) == O.OSCAR_OK
+    assert lib.oscar_set_timing_events(ctypes.c_void_p(8), None) == O.OSCAR_ERR_INVALID_ARG
+    ids = (ctypes.c_int32 * 1)(0)
+    lens = (ctypes.c_int32 * 1)(0)
+    assert lib.oscar_bf16_decode_attention(1, ids, lens, ctypes.c_void_p(256), ctypes.c_void_p(256), 1,
+                                           128, ctypes.c_void_p(256), 4, ctypes.c_float(0),
+                                           ctypes.c_void_p(256), ctypes.c_void_p(256), 1 << 20,
+                                           None) == O.OSCAR_ERR_INVALID_ARG   # length 0
+
+
+def test_layout_reader_roundtrip():
+    import numpy as np
+    from tests import layout
+    rng = np.random.default_rng(5)
+    codes = rng.integers(0, 4, (128, 128)).astype(np.uint8)
+    words = layout.pack_fragment(codes)
+    assert np.array_equal(layout.unpack_fragment(words), codes)
+    # every (row, col) appears exactly once; 16 codes per word
+    seen = np.zeros((128, 128), int)
+    np.add.at(seen, (layout._ROWS, layout._COLS), 1)
+    assert np.all(seen == 1)
