@@ -134,16 +134,17 @@ __global__ void __launch_bounds__(kQThreads, 2)
     // ---- keys: rotation, norm, unit vector
     float x[kHeadDim];
     load_row(ksrc, x);
+    // stage hb pairs index j (bit hb clear) with j + 2^hb; flat loops so that
+    // every index is a compile-time constant and x stays in registers
 #pragma unroll
-    for (int h = 1; h < kHeadDim; h <<= 1) {
+    for (int hb = 0; hb < 7; ++hb) {
 #pragma unroll
-      for (int i = 0; i < kHeadDim; i += 2 * h) {
-#pragma unroll
-        for (int j = i; j < i + h; ++j) {
-          const float a = x[j], b = x[j + h];
-          x[j] = a + b;
-          x[j + h] = a - b;
-        }
+      for (int n = 0; n < kHeadDim / 2; ++n) {
+        const int h = 1 << hb;
+        const int j = ((n >> hb) << (hb + 1)) | (n & (h - 1));
+        const float a = x[j], b = x[j + h];
+        x[j] = a + b;
+        x[j + h] = a - b;
       }
     }
     float sq[kHeadDim / 2];
