@@ -377,6 +377,37 @@ def gpu_arm(args, rank, world):
     return res
 
 
+def profile_case(args):
+    """Small, self-contained launches for ncu captures (no L2 flush, no
+    bf16 reference, a few hundred MB on the device)."""
+    import torch
+
+    from int2_kv_cache_oscar_gb300 import oscar as O_
+    from int2_kv_cache_oscar_gb300 import workloads as W
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(2)
+    k, v = W.make_sequence_kv(CTX, HKV, W.LLAMA_RECIPE, gen, "cuda")
+    q = W.make_q(1, HQ, seed=2, device="cuda")
+    cache = O_.OscarCache(1, HKV, CTX)
+    if args.profile_quantize:
+        for _ in range(args.steps):
+            O_.oscar_cache_reset(cache.handle, 0)
+            cache.append([0], [0, CTX], k, v)
+        torch.cuda.synchronize()
+        print("profile quantize done")
+        return
+    cache.append([0], [0, CTX], k, v)
+    del k, v
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    out = torch.empty((1, HQ, D), dtype=torch.bfloat16, device="cuda")
+    ws = cache.workspace(1, HQ)
+    for _ in range(args.steps):
+        cache.decode([0], q, HQ, out, ws)
+    O_.oscar_cache_check(cache.handle)
+    print("profile decode done")
+
+
 # ------------------------------------------------------------- CPU oracle
 
 def cpu_sample_worker(steps: int):
@@ -433,6 +464,10 @@ def main():
     ap.add_argument("--impl", default="oscar", choices=["oscar", "reference"])
     ap.add_argument("--quick", action="store_true", help="headline only (no sweep / batch / stream)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--profile-decode", action="store_true",
+                    help="profiling case: build the 128K INT2 cache only and run `steps` decodes")
+    ap.add_argument("--profile-quantize", action="store_true",
+                    help="profiling case: `steps` 128K quantise appends (8 KV heads)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -467,6 +502,9 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     torch.cuda.set_device(local_rank)
+    if args.profile_decode or args.profile_quantize:
+        profile_case(args)
+        return
 
     res = gpu_arm(args, rank, world)
 
