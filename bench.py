@@ -156,6 +156,8 @@ class Timer:
             if kernel_events is not None:
                 ks = torch.cuda.Event(enable_timing=True)
                 ke = torch.cuda.Event(enable_timing=True)
+                ks.record()          # creates the CUDA events (torch creates them lazily)
+                ke.record()
                 kernel_events(ks, ke)
                 kpairs.append((ks, ke))
             s.record()

@@ -134,7 +134,7 @@ def test_decode_bad_args():
     with pytest.raises(O_.OscarError):
         cache.decode([0], q, 32, out, ws)                  # empty sequence
     gen = torch.Generator().manual_seed(2)
-    k, v = W.make_sequence_kv(10, 8, W.LLAMA_RECIPE, gen)
+    k, v = W.make_sequence_kv(200, 8, W.LLAMA_RECIPE, gen)
     U.append_all(cache, [0], [k], [v])
     with pytest.raises(O_.OscarError) as e:
         cache.decode([0], q, 36, out, ws)                  # 36 % 8 != 0
