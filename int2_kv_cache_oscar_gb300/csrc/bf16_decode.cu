@@ -24,6 +24,7 @@ struct Bf16Smem {
   uint8_t v[kStagesB][kTileBytes];
   uint64_t full[kStagesB];
   uint64_t empty[kStagesB];
+  uint32_t issued[kStagesB];   // uses of each stage issued so far (producer -> consumers)
   float ost[kConsumersB][kMaxGqa][kHeadDim];
   float mst[kConsumersB][kMaxGqa];
   float lst[kConsumersB][kMaxGqa];
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(kThreadsB, 2)
     for (int s = 0; s < kStagesB; ++s) {
       mbar_init(&S.full[s], 1);
       mbar_init(&S.empty[s], 1);
+      S.issued[s] = 0;
     }
     S.abort_flag = 0;
     fence_mbar_init();
@@ -94,6 +96,7 @@ __global__ void __launch_bounds__(kThreadsB, 2)
         const int64_t off = (rowbase + (int64_t)g * kTile) * kHeadDim;
         bulk_g2s(S.k[s], kc + off, bytes, &S.full[s]);
         bulk_g2s(S.v[s], vc + off, bytes, &S.full[s]);
+        reinterpret_cast<volatile uint32_t*>(S.issued)[s] = (uint32_t)(k / kStagesB) + 1;
       }
     }
   drain:
@@ -151,7 +154,9 @@ __global__ void __launch_bounds__(kThreadsB, 2)
     for (int64_t kk = k_begin + ((warp - k_begin) % kConsumersB + kConsumersB) % kConsumersB; kk < k_end;
          kk += kConsumersB) {
       const int s = (int)(kk % kStagesB);
-      if (!mbar_wait_bounded(&S.full[s], (uint32_t)((kk / kStagesB) & 1), &S.abort_flag, p.h.err_word)) continue;
+      const uint32_t use = (uint32_t)(kk / kStagesB);
+      if (!wait_issued(&S.issued[s], use, &S.abort_flag, p.h.err_word)) continue;
+      if (!mbar_wait_bounded(&S.full[s], use & 1, &S.abort_flag, p.h.err_word)) continue;
       const int tile = g0 + (int)(kk - k_begin);
       const int rows = min(kTile, len - tile * kTile);
       const uint8_t* ktile = S.k[s];

@@ -101,6 +101,22 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// Wait until the producer has issued use `n` of a ring stage (issued[s] > n).
+// A consumer that waits on the stage's "full" barrier for use n only after
+// this point sees that barrier in phase n or n + 1, never an older phase with
+// the same parity, so the parity test cannot be fooled when several consumer
+// warps share a ring.
+__device__ __forceinline__ bool wait_issued(const volatile uint32_t* issued, uint32_t n, volatile int* abort_flag,
+                                            uint32_t* err_word) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (*issued > n) return true;
+    if (*abort_flag) return false;
+  }
+  *abort_flag = 1;
+  if (err_word != nullptr) atomicOr(err_word, kErrTimeout);
+  return false;
+}
+
 // 1-D bulk copy global -> shared, completing on `bar` (bytes multiple of 16,
 // both addresses 16-byte aligned).
 __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {

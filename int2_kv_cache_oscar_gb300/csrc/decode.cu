@@ -37,6 +37,7 @@ struct DecSmem {
   uint8_t stage[kStages][kBlockBytes];
   uint64_t full[kStages];
   uint64_t empty[kStages];
+  uint32_t issued[kStages];   // uses of each stage issued so far (producer -> consumers)
   float qrot[kMaxGqa][kHeadDim];
   float qmax[kMaxGqa];
   float pbuf[kConsumers][kMaxGqa][kPbStride];
@@ -78,6 +79,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&S.full[s], 1);
       mbar_init(&S.empty[s], 1);
+      S.issued[s] = 0;
     }
     S.abort_flag = 0;
     fence_mbar_init();
@@ -104,6 +106,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         }
         mbar_arrive_expect_tx(&S.full[s], kBlockBytes);
         bulk_g2s(S.stage[s], src, kBlockBytes, &S.full[s]);
+        reinterpret_cast<volatile uint32_t*>(S.issued)[s] = (uint32_t)(k / kStages) + 1;
       }
     }
   drain:
@@ -209,7 +212,9 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     for (int64_t kk = k_begin + ((warp - k_begin) % kConsumers + kConsumers) % kConsumers; kk < k_end;
          kk += kConsumers) {
       const int s = (int)(kk % kStages);
-      if (!mbar_wait_bounded(&S.full[s], (uint32_t)((kk / kStages) & 1), &S.abort_flag, p.h.err_word)) continue;
+      const uint32_t use = (uint32_t)(kk / kStages);
+      if (!wait_issued(&S.issued[s], use, &S.abort_flag, p.h.err_word)) continue;
+      if (!mbar_wait_bounded(&S.full[s], use & 1, &S.abort_flag, p.h.err_word)) continue;
       const uint8_t* blk = S.stage[s];
       const float* ksc = reinterpret_cast<const float*>(blk + kOffKScale);
       const float* kze = reinterpret_cast<const float*>(blk + kOffKZero);
