@@ -8,6 +8,8 @@
 // tokens per step; fp32 dot products reduced with 3 shuffles, online softmax
 // with a lazy rescale (the running max is only raised when a score exceeds it
 // by more than 2^8, so p <= 256), fp32 P.V.
+#include <cstddef>
+
 #include "decode_common.cuh"
 
 namespace oscar {
@@ -20,16 +22,18 @@ constexpr int kTile = 64;
 constexpr int kTileBytes = kTile * kHeadDim * 2;
 
 struct Bf16Smem {
-  uint8_t k[kStagesB][kTileBytes];
-  uint8_t v[kStagesB][kTileBytes];
-  uint64_t full[kStagesB];
-  uint64_t empty[kStagesB];
-  uint32_t issued[kStagesB];   // uses of each stage issued so far (producer -> consumers)
-  float ost[kConsumersB][kMaxGqa][kHeadDim];
+  alignas(128) uint8_t k[kStagesB][kTileBytes];
+  alignas(128) uint8_t v[kStagesB][kTileBytes];
+  alignas(16) float ost[kConsumersB][kMaxGqa][kHeadDim];
   float mst[kConsumersB][kMaxGqa];
   float lst[kConsumersB][kMaxGqa];
+  alignas(8) uint64_t full[kStagesB];
+  uint64_t empty[kStagesB];
+  uint32_t issued[kStagesB];   // uses of each stage issued so far (producer -> consumers)
   int abort_flag;
 };
+static_assert(offsetof(Bf16Smem, v) % 16 == 0, "bulk-copy destinations must be 16-byte aligned");
+static_assert(offsetof(Bf16Smem, full) % 8 == 0, "mbarriers must be 8-byte aligned");
 
 __device__ __forceinline__ void unpack8(const uint4 u, float* x) {
   x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x); x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);

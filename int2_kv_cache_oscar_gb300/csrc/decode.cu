@@ -23,6 +23,8 @@
 //     loaded tile;
 //   * online softmax in the log2 domain; tensor-core accumulators restart at
 //     every group and are added into fp32 registers on the CUDA cores.
+#include <cstddef>
+
 #include "decode_common.cuh"
 
 namespace oscar {
@@ -34,18 +36,23 @@ constexpr int kStages = 6;
 constexpr int kPbStride = kGroup + 8;  // probability rows, padded against bank conflicts
 
 struct DecSmem {
-  uint8_t stage[kStages][kBlockBytes];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint32_t issued[kStages];   // uses of each stage issued so far (producer -> consumers)
-  float qrot[kMaxGqa][kHeadDim];
+  alignas(128) uint8_t stage[kStages][kBlockBytes];
+  alignas(16) float qrot[kMaxGqa][kHeadDim];            // float4 stores
+  alignas(16) float pbuf[kConsumers][kMaxGqa][kPbStride];  // float2 loads
+  alignas(16) float ost[kConsumers][kMaxGqa][kHeadDim];
   float qmax[kMaxGqa];
-  float pbuf[kConsumers][kMaxGqa][kPbStride];
-  float ost[kConsumers][kMaxGqa][kHeadDim];
   float mst[kConsumers][kMaxGqa];
   float lst[kConsumers][kMaxGqa];
+  alignas(8) uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint32_t issued[kStages];   // uses of each stage issued so far (producer -> consumers)
   int abort_flag;
 };
+static_assert(offsetof(DecSmem, qrot) % 16 == 0, "qrot must be 16-byte aligned");
+static_assert(offsetof(DecSmem, pbuf) % 16 == 0, "pbuf must be 16-byte aligned");
+static_assert((kPbStride * 4) % 16 == 0, "pbuf rows must keep 16-byte alignment");
+static_assert(offsetof(DecSmem, full) % 8 == 0, "mbarriers must be 8-byte aligned");
+static_assert(kBlockBytes % 16 == 0, "stages must stay 16-byte aligned");
 
 __device__ __forceinline__ float pow2f(int e) {
   e = max(-126, min(127, e));

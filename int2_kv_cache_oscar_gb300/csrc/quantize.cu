@@ -17,6 +17,8 @@
 //   3. Per-channel min/max of k_hat over the 128 tokens (shared memory).
 //   4. Codes of k_hat, packed straight into the fragment-order words.
 //   5. Coalesced 16-byte stores of both code matrices.
+#include <cstddef>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -28,12 +30,14 @@ constexpr int kKhStride = 132;  // floats per k_hat row in shared memory (paddin
 constexpr int kVbStride = 144;  // bytes per value-code row (channel) in shared memory
 
 struct QuantSmem {
-  float kh[kGroup * kKhStride];          // k_hat[t][c]
-  uint8_t vb[kHeadDim * kVbStride];      // value codes [channel][permuted token]
-  uint32_t kw[1024];                     // key code words, fragment order
-  float2 kp[kHeadDim];                   // per-channel (1/s, z)
+  alignas(16) float kh[kGroup * kKhStride];          // k_hat[t][c]; float4 stores
+  alignas(16) uint8_t vb[kHeadDim * kVbStride];      // value codes [channel][permuted token]; uint4 loads
+  alignas(16) uint32_t kw[1024];                     // key code words, fragment order; uint4 loads
+  alignas(16) float2 kp[kHeadDim];                   // per-channel (1/s, z)
   float red[kQThreads / 32];
 };
+static_assert(offsetof(QuantSmem, vb) % 16 == 0 && offsetof(QuantSmem, kw) % 16 == 0, "alignment");
+static_assert((kKhStride * 4) % 16 == 0 && kVbStride % 16 == 0, "rows must keep 16-byte alignment");
 
 // Round-half-even code of x against (inv = 1/s, z), clamped to [0, 3]; the
 // magic constant 1.5 * 2^23 leaves rne(v) in the low mantissa bits.
