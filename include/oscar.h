@@ -178,6 +178,29 @@ oscar_status oscar_decode_attention(oscar_cache* cache, int32_t n_seqs, const in
                                     void* out, void* workspace, size_t workspace_bytes,
                                     void* stream);
 
+/*
+ * Decode that allocates nothing and takes no workspace.  The OScaR pages have
+ * no counterpart to this call; it exists for callers that cannot allocate
+ * device memory where they decode (code inside a memory pool or arena it does
+ * not own, plugins whose host framework forbids allocation on the serving
+ * path, callers that must keep a fixed device footprint).
+ *   Same arguments and results as oscar_decode_attention, without workspace.
+ *   The split-K partials go to a file-scope device array of 4 MiB that every
+ *   GPU loading this library holds until the process exits.  Calls needing
+ *   more than that (sequences x KV heads plus two rows per SM of partials)
+ *   fail with OSCAR_ERR_CAPACITY and a message; use oscar_decode_attention.
+ *   The first call on a device looks up the array's device address (with
+ *   the cache's device current); make that first call before any CUDA stream
+ *   capture.  No device memory is allocated or freed, and nothing in the
+ *   array needs to start at zero (each call writes every partial it reads).
+ *   Every call shares the one array: calls whose kernels overlap on the GPU
+ *   (different streams, or different threads without ordering) race on it
+ *   and give wrong results.
+ */
+oscar_status oscar_decode_attention_noalloc(oscar_cache* cache, int32_t n_seqs, const int32_t* seq_ids,
+                                            const void* q, int32_t num_q_heads, float softmax_scale,
+                                            void* out, void* stream);
+
 /* Footprint: kind = OSCAR_BYTES_USED / _BF16_EQUIVALENT for slot `seq`
  * (or all slots if seq == -1), or OSCAR_BYTES_ARENA.  Host arithmetic:
  * a full group costs 13,824 B per KV head (108 B per token) versus 65,536 B

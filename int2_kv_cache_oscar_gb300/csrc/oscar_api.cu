@@ -7,6 +7,7 @@
 #include <cstring>
 #include <exception>
 #include <string>
+#include <mutex>
 #include <vector>
 
 #include "../../include/oscar.h"
@@ -519,6 +520,67 @@ oscar_status oscar_bf16_decode_attention(int32_t n_seqs, const int32_t* seq_ids,
   } catch (const std::exception& ex) {
     return fail(OSCAR_ERR_INVALID_ARG, "host allocation failed: %s", ex.what());
   }
+}
+
+// ------------------------------------------------------------------------
+// Decode without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory at the point where they decode:
+// code running inside a memory pool or arena it does not own, plugins whose
+// host framework forbids allocation on the serving path, and callers that
+// must keep a fixed device footprint.  For them the split-K partials live in
+// a fixed file-scope device array instead of a workspace argument.  Every GPU
+// that loads this library holds the array until the process exits.
+constexpr size_t kNoAllocScratchBytes = 4u << 20;  // 4 MiB per device
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on `device` (which must be current).
+// In host code the array's name is only a host-side stand-in; the address
+// that kernels may use is looked up once per device and remembered.
+oscar_status noalloc_scratch(int device, void** out) {
+  if (device < 0 || device >= kNoAllocMaxDevices)
+    return fail(OSCAR_ERR_UNSUPPORTED, "device %d beyond the %d supported", device, kNoAllocMaxDevices);
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[device] == nullptr) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
+    g_noalloc_ptr[device] = ptr;
+  }
+  *out = g_noalloc_ptr[device];
+  return OSCAR_OK;
+}
+}  // namespace
+
+oscar_status oscar_decode_attention_noalloc(oscar_cache* c, int32_t n_seqs, const int32_t* seq_ids, const void* q,
+                                            int32_t num_q_heads, float softmax_scale, void* out, void* stream) {
+  if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+  if (n_seqs < 1) return fail(OSCAR_ERR_INVALID_ARG, "n_seqs must be >= 1");
+  const int hkv = c->cfg.num_kv_heads;
+  if (num_q_heads < hkv || num_q_heads % hkv != 0)
+    return fail(OSCAR_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of Hkv");
+  size_t need = 0;
+  oscar_status s = oscar_decode_workspace_bytes(c, n_seqs, num_q_heads, &need);
+  if (s != OSCAR_OK) return s;
+  if (need > kNoAllocScratchBytes)
+    return fail(OSCAR_ERR_CAPACITY,
+                "decode of %d sequences x %d query heads needs %zu bytes of partials, more than the %zu-byte "
+                "built-in scratch; use oscar_decode_attention with a workspace",
+                n_seqs, num_q_heads, need, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  {
+    DeviceGuard dg(c->cfg.device);
+    if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+    s = noalloc_scratch(c->cfg.device, &scratch);
+    if (s != OSCAR_OK) return s;
+  }
+  return oscar_decode_attention(c, n_seqs, seq_ids, q, num_q_heads, softmax_scale, out, scratch,
+                                kNoAllocScratchBytes, stream);
 }
 
 oscar_status oscar_set_timing_events(void* start_event, void* stop_event) {

@@ -72,6 +72,7 @@ def _load() -> ctypes.CDLL:
         "oscar_bf16_decode_attention": [I32, I32P, I32P, P, P, I32, I32, P, I32, ctypes.c_float, P, P,
                                         SZ, P],
         "oscar_set_timing_events": [P, P],
+        "oscar_decode_attention_noalloc": [P, I32, I32P, P, I32, ctypes.c_float, P, P],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -172,6 +173,14 @@ def oscar_decode_attention(handle, seq_ids: Sequence[int], q: torch.Tensor, num_
                                        ctypes.c_float(softmax_scale), _ptr(out), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(),
                                        _stream(stream)))
+
+
+def oscar_decode_attention_noalloc(handle, seq_ids: Sequence[int], q: torch.Tensor, num_q_heads: int,
+                                   softmax_scale: float, out: torch.Tensor, stream=None) -> None:
+    """Decode without a workspace: the partials go to the library's built-in
+    device scratch (for callers that cannot allocate device memory)."""
+    _check(_lib.oscar_decode_attention_noalloc(handle, len(seq_ids), _i32(seq_ids), _ptr(q), num_q_heads,
+                                               ctypes.c_float(softmax_scale), _ptr(out), _stream(stream)))
 
 
 def oscar_cache_bytes(handle, seq: int, kind: int) -> int:
