@@ -270,7 +270,8 @@ cudaError_t launch_decode_bf16(const DecodeParams<MAXS>& p, const uint16_t* kc, 
                                cudaStream_t stream, cudaEvent_t ev_start, cudaEvent_t ev_stop) {
   if (p.h.n_units <= 0) return cudaSuccess;
   const int smem = (int)sizeof(Bf16Smem);
-  cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel<MAXS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static bool attr_done[64] = {};
+  cudaError_t e = ensure_smem_attr(decode_bf16_kernel<MAXS>, smem, attr_done);
   if (e != cudaSuccess) return e;
   if (ev_start) cudaEventRecord(ev_start, stream);
   decode_bf16_kernel<MAXS><<<p.h.n_ctas, kThreadsB, smem, stream>>>(p, kc, vc);

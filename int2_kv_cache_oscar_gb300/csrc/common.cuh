@@ -50,6 +50,19 @@ __host__ __device__ inline ArenaLayout arena_layout(int32_t max_batch, int32_t h
   return L;
 }
 
+// Raise a kernel's dynamic shared-memory limit once per device (the attribute
+// is per device); later launches skip the driver call.
+template <typename Kernel>
+inline cudaError_t ensure_smem_attr(Kernel kernel, int smem_bytes, bool (&done)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  return e;
+}
+
 // ---------------------------------------------------------------- PTX helpers
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

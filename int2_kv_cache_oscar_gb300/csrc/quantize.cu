@@ -274,7 +274,8 @@ cudaError_t launch_quantize(const QuantPlan<CAP>& plan, uint8_t* arena, const ui
                             cudaStream_t stream) {
   if (plan.n_tasks <= 0) return cudaSuccess;
   const int smem = (int)sizeof(QuantSmem);
-  cudaError_t e = cudaFuncSetAttribute(quantize_append_kernel<CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static bool attr_done[64] = {};
+  cudaError_t e = ensure_smem_attr(quantize_append_kernel<CAP>, smem, attr_done);
   if (e != cudaSuccess) return e;
   dim3 grid(plan.n_tasks, plan.hkv);
   quantize_append_kernel<CAP><<<grid, kQThreads, smem, stream>>>(plan, arena, k, v);
