@@ -7,26 +7,25 @@
 //       = n_t * (sum_c code_tc (q_rot_c s_c) + sum_c q_rot_c z_c) * scale.
 // Output: o = sum_t p_t (code^V_tc s^V_t,gr(c) + z^V_t,gr(c)) / sum_t p_t.
 //
-// Kernel structure (persistent CTAs, 2 per SM; 4 consumer warps + 1 helper):
-//   * helper warp, lane 0: streams whole 13,824-byte group blocks (codes,
-//     scales, zeros, norms of K and V) into a 6-stage shared-memory ring with
-//     1-D bulk copies (cp.async.bulk + mbarrier transaction counts), 5 groups
-//     ahead of the consumers;
-//   * helper warp, all lanes: per segment it rotates the GQA queries (FWHT
-//     over the lanes); per group it builds the B operand of the score
-//     contraction, q_rot * s split into fp16 hi + lo columns and pre-scaled,
-//     plus q_rot . z, into the stage's aux record;
-//   * consumer warp w takes tokens 32w..32w+31 of every group and runs both
-//     contractions with mma.sync m16n8k16: the 2-bit codes are the A operand,
-//     taken straight from the packed words with one AND each (an fp16
-//     subnormal code * 2^(p - 24)); the fp32 factors are the B operand split
-//     into hi + lo fp16 columns (~22 significant bits) pre-scaled by 2^(F - p),
-//     so each product is code * factor * 2^(F - 24); for P.V the hi/lo split
-//     is shared between partner lanes (one shuffle);
-//   * N = 8 columns = 4 query heads x {hi, lo}: all GQA heads share each tile;
-//   * online softmax in the log2 domain per warp; tensor-core accumulators
-//     restart at every group and are added into fp32 registers; every warp
-//     waits on every stage in ring order, so the mbarrier parity test is exact.
+// Kernel structure (persistent CTAs, 2 per SM; 4 consumer warps + 1 producer
+// warp):
+//   * the producer streams whole 13,824-byte group blocks (codes, scales,
+//     zeros, norms of K and V) into a 6-stage shared-memory ring with 1-D
+//     bulk copies (cp.async.bulk + mbarrier transaction counts) and publishes
+//     how many uses of each stage it has issued, so that a consumer waits on
+//     a stage's barrier only for a phase that exists (no parity aliasing);
+//   * each consumer warp takes every 4th group and runs both contractions on
+//     the tensor cores with mma.sync m16n8k16: the 2-bit codes are the A
+//     operand, taken straight from the packed words with one AND each (an
+//     fp16 subnormal code * 2^(p - 24)); the fp32 factors (q_rot * s for
+//     scores, p * s^V for values) are the B operand, split into fp16 hi + lo
+//     columns (~22 significant bits) and pre-scaled by 2^(F - p) so the
+//     product is code * factor * 2^(F - 24); partner lanes (hi column, lo
+//     column of one head) each split half of the pairs and swap halves;
+//   * N = 8 columns = 4 query heads x {hi, lo}: all GQA heads share each
+//     loaded tile; the score k-steps run over 4 independent m-tile chains;
+//   * online softmax in the log2 domain; tensor-core accumulators restart at
+//     every group and are added into fp32 registers on the CUDA cores.
 #include <cstddef>
 
 #include "decode_common.cuh"
@@ -34,37 +33,24 @@
 namespace oscar {
 namespace {
 
-constexpr int kConsumers = 4;                  // consumer warps; warp w takes tokens 32w..32w+31
+constexpr int kConsumers = 4;
 constexpr int kDecThreads = (kConsumers + 1) * 32;
 constexpr int kStages = 6;
-constexpr int kPbStride = 32 + 4;              // probability rows (4 heads x 32 tokens), padded
-
-// Per-stage data the helper warp prepares for the consumers.
-struct GroupAux {
-  uint4 bk[4][32];       // score B fragments: {bk[2i][0], bk[2i][1], bk[2i+1][0], bk[2i+1][1]} per lane
-  float qz[kMaxGqa];     // (H_d q_h) . z of the group, per query head
-  float kq[kMaxGqa];     // 2^(24 - F_h): undoes the operand pre-scaling of head h
-  float fv;              // 2^Fv: pre-scaling of the value-side operand
-  float kv;              // 2^(24 - Fv)
-  float pad[2];
-};
+constexpr int kPbStride = kGroup + 8;  // probability rows, padded against bank conflicts
 
 struct DecSmem {
   alignas(128) uint8_t stage[kStages][kBlockBytes];
-  alignas(16) GroupAux aux[kStages];
-  alignas(16) float qrot[kMaxGqa][kHeadDim];               // helper: rotated queries of the segment
-  alignas(16) float pbuf[kConsumers][kMaxGqa][kPbStride];  // consumer-private probabilities
+  alignas(16) float qrot[kMaxGqa][kHeadDim];              // float4 stores
+  alignas(16) float pbuf[kConsumers][kMaxGqa][kPbStride];  // float2 loads
   alignas(16) float ost[kConsumers][kMaxGqa][kHeadDim];
   float qmax[kMaxGqa];
   float mst[kConsumers][kMaxGqa];
   float lst[kConsumers][kMaxGqa];
   alignas(8) uint64_t full[kStages];
-  uint64_t ready[kStages];
   uint64_t empty[kStages];
+  uint32_t issued[kStages];   // uses of each stage issued so far (producer -> consumers)
   int abort_flag;
 };
-static_assert(offsetof(DecSmem, aux) % 16 == 0, "aux must be 16-byte aligned");
-static_assert(sizeof(GroupAux) % 16 == 0, "aux entries must stay 16-byte aligned");
 static_assert(offsetof(DecSmem, qrot) % 16 == 0, "qrot must be 16-byte aligned");
 static_assert(offsetof(DecSmem, pbuf) % 16 == 0, "pbuf must be 16-byte aligned");
 static_assert((kPbStride * 4) % 16 == 0, "pbuf rows must keep 16-byte alignment");
@@ -84,164 +70,28 @@ __device__ __forceinline__ int range_exponent(float bound) {
   return 15 - e;
 }
 
-template <int I>
-__device__ __forceinline__ void extract4(uint32_t w0, uint32_t w1, uint32_t& a0, uint32_t& a1, uint32_t& a2,
-                                         uint32_t& a3) {
-  a0 = frag_extract<I>(w0);
-  a1 = frag_extract<I>(w1);
-  a2 = frag_extract<I + 1>(w0);
-  a3 = frag_extract<I + 1>(w1);
-}
-
-// A fragment (k-step with ks & 3 == KK) from the two words of rows g, g+8.
+// A fragment of k-step kk (= ks & 3) from the words of rows g and g+8.
 template <int KK>
 __device__ __forceinline__ void frag_a(uint32_t w0, uint32_t w1, uint32_t& a0, uint32_t& a1, uint32_t& a2,
                                        uint32_t& a3) {
-  extract4<2 * KK>(w0, w1, a0, a1, a2, a3);
+  a0 = frag_extract<2 * KK>(w0);
+  a1 = frag_extract<2 * KK>(w1);
+  a2 = frag_extract<2 * KK + 1>(w0);
+  a3 = frag_extract<2 * KK + 1>(w1);
 }
 
-// Consumer work on tokens 32w .. 32w + 31 of one group block.  WQ = w & 1
-// fixes which k-steps (tokens) of the P.V product this warp owns:
-// ks = 2w, 2w + 1, i.e. kk = 2 WQ, 2 WQ + 1 within j = w >> 1.
-struct ConsumerState {
-  float m_run;
-  float l_run;
-  float o_acc[8][2];
-  float zacc[kVGroups];
-};
-
-template <int WQ>
-__device__ __forceinline__ void consume_group(const uint8_t* __restrict__ blk, const GroupAux& aux, int warp,
-                                              int lane, float scale_log2, float* __restrict__ pbw,
-                                              ConsumerState& st) {
-  const int g = lane >> 2, tig = lane & 3;
-  const int hb = g >> 1;
-  const bool want_lo = (g & 1) != 0;
-  const float* knm = reinterpret_cast<const float*>(blk + kOffKNorm);
-  const float* vsz = reinterpret_cast<const float*>(blk + kOffVSZ);
-
-  // ---- scores of tokens 16 mt + g (+8), mt = 2 warp + {0, 1}, head tig
-  uint32_t bk[8][2];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 v = aux.bk[i][lane];
-    bk[2 * i][0] = v.x;
-    bk[2 * i][1] = v.y;
-    bk[2 * i + 1][0] = v.z;
-    bk[2 * i + 1][1] = v.w;
-  }
-  const float qz = aux.qz[tig];
-  const float kq = aux.kq[tig];
-  float sc[4];
-  const uint4* kc = reinterpret_cast<const uint4*>(blk + kOffKCodes);
-#pragma unroll
-  for (int h2 = 0; h2 < 2; ++h2) {
-    const int mt = 2 * warp + h2;
-    const uint4 w = kc[mt * 32 + lane];
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    uint32_t a0, a1, a2, a3;
-    frag_a<0>(w.x, w.y, a0, a1, a2, a3); mma_f16_16816(acc, a0, a1, a2, a3, bk[0][0], bk[0][1]);
-    frag_a<1>(w.x, w.y, a0, a1, a2, a3); mma_f16_16816(acc, a0, a1, a2, a3, bk[1][0], bk[1][1]);
-    frag_a<2>(w.x, w.y, a0, a1, a2, a3); mma_f16_16816(acc, a0, a1, a2, a3, bk[2][0], bk[2][1]);
-    frag_a<3>(w.x, w.y, a0, a1, a2, a3); mma_f16_16816(acc, a0, a1, a2, a3, bk[3][0], bk[3][1]);
-    frag_a<0>(w.z, w.w, a0, a1, a2, a3); mma_f16_16816(acc, a0, a1, a2, a3, bk[4][0], bk[4][1]);
-    frag_a<1>(w.z, w.w, a0, a1, a2, a3); mma_f16_16816(acc, a0, a1, a2, a3, bk[5][0], bk[5][1]);
-    frag_a<2>(w.z, w.w, a0, a1, a2, a3); mma_f16_16816(acc, a0, a1, a2, a3, bk[6][0], bk[6][1]);
-    frag_a<3>(w.z, w.w, a0, a1, a2, a3); mma_f16_16816(acc, a0, a1, a2, a3, bk[7][0], bk[7][1]);
-    const int t0 = 16 * mt + g;
-    sc[2 * h2] = fmaf(acc[0] + acc[1], kq, qz) * knm[t0] * scale_log2;
-    sc[2 * h2 + 1] = fmaf(acc[2] + acc[3], kq, qz) * knm[t0 + 8] * scale_log2;
-  }
-
-  // ---- online softmax over this warp's 32 tokens (head tig)
-  float gm = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-  gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 4));
-  gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 8));
-  gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 16));
-  const float m_new = fmaxf(st.m_run, gm);
-  const float alpha = exp2f(st.m_run - m_new);
-  st.m_run = m_new;
-  float psum = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    sc[i] = exp2f(sc[i] - m_new);
-    psum += sc[i];
-  }
-  st.l_run = fmaf(st.l_run, alpha, psum);
-#pragma unroll
-  for (int gr = 0; gr < kVGroups; ++gr) st.zacc[gr] *= alpha;
-  float* pbt = pbw + tig * kPbStride;
-#pragma unroll
-  for (int h2 = 0; h2 < 2; ++h2) {
-    const int tl = 16 * h2 + g;              // token index within the warp's 32
-    const int t0 = 32 * warp + tl;
-    pbt[tl] = sc[2 * h2];
-    pbt[tl + 8] = sc[2 * h2 + 1];
-    const float4 z0 = *reinterpret_cast<const float4*>(vsz + 8 * t0 + 4);
-    const float4 z1 = *reinterpret_cast<const float4*>(vsz + 8 * (t0 + 8) + 4);
-    st.zacc[0] = fmaf(sc[2 * h2], z0.x, fmaf(sc[2 * h2 + 1], z1.x, st.zacc[0]));
-    st.zacc[1] = fmaf(sc[2 * h2], z0.y, fmaf(sc[2 * h2 + 1], z1.y, st.zacc[1]));
-    st.zacc[2] = fmaf(sc[2 * h2], z0.z, fmaf(sc[2 * h2 + 1], z1.z, st.zacc[2]));
-    st.zacc[3] = fmaf(sc[2 * h2], z0.w, fmaf(sc[2 * h2 + 1], z1.w, st.zacc[3]));
-  }
-  __syncwarp();
-
-  // ---- P.V over this warp's two k-steps: O^T[channel][head x {hi, lo}]
-  float pacc[8][4];
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) pacc[mt][0] = pacc[mt][1] = pacc[mt][2] = pacc[mt][3] = 0.0f;
-  const int jh = warp >> 1;
-  uint2 vw[8];
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt)
-    vw[mt] = *reinterpret_cast<const uint2*>(blk + kOffVCodes + ((mt * 32 + lane) * 4 + 2 * jh) * 4);
-  const float* pbh = pbw + hb * kPbStride;
-#pragma unroll
-  for (int kk2 = 0; kk2 < 2; ++kk2) {
-    constexpr int dummy = 0;
-    (void)dummy;
-    const int kk = 2 * WQ + kk2;               // ks & 3
-    const int tl = 16 * kk2 + 2 * tig + (want_lo ? 8 : 0);   // this lane's two tokens (within the warp's 32)
-    const int t = 32 * warp + tl;
-    // lanes g even hold tokens +0,+1 (b0 half), g odd hold +8,+9 (b1 half); the
-    // partner lane (g xor 1) covers the other half of the same column pair
-    const float fsc = aux.fv * pow2f(-frag_p(2 * kk + (want_lo ? 1 : 0)));
-    const float2 pp = *reinterpret_cast<const float2*>(pbh + tl);
-    const float p0 = pp.x * fsc, p1 = pp.y * fsc;
-    const float4 s0 = *reinterpret_cast<const float4*>(vsz + 8 * t);
-    const float4 s1 = *reinterpret_cast<const float4*>(vsz + 8 * (t + 1));
-    const float sA[4] = {s0.x, s0.y, s0.z, s0.w};
-    const float sB[4] = {s1.x, s1.y, s1.z, s1.w};
-#pragma unroll
-    for (int gr = 0; gr < kVGroups; ++gr) {
-      const float x0 = p0 * sA[gr], x1 = p1 * sB[gr];
-      const uint32_t hi = pack_half2(x0, x1);
-      const uint32_t lo = pack_half2(x0 - half_lo_to_float(hi), x1 - half_hi_to_float(hi));
-      const uint32_t send = want_lo ? hi : lo;
-      const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 4);
-      const uint32_t b0 = want_lo ? recv : hi;
-      const uint32_t b1 = want_lo ? lo : recv;
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int mt = 2 * gr + h2;
-        uint32_t a0, a1, a2, a3;
-        if (WQ == 0) {
-          if (kk2 == 0) frag_a<0>(vw[mt].x, vw[mt].y, a0, a1, a2, a3);
-          else frag_a<1>(vw[mt].x, vw[mt].y, a0, a1, a2, a3);
-        } else {
-          if (kk2 == 0) frag_a<2>(vw[mt].x, vw[mt].y, a0, a1, a2, a3);
-          else frag_a<3>(vw[mt].x, vw[mt].y, a0, a1, a2, a3);
-        }
-        mma_f16_16816(pacc[mt], a0, a1, a2, a3, b0, b1);
-      }
-    }
-  }
-  const float kv = aux.kv;
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    st.o_acc[mt][0] = fmaf(st.o_acc[mt][0], alpha, (pacc[mt][0] + pacc[mt][1]) * kv);
-    st.o_acc[mt][1] = fmaf(st.o_acc[mt][1], alpha, (pacc[mt][2] + pacc[mt][3]) * kv);
-  }
+// Partner-lane split of a B-fragment column pair.  Lanes g = 2h (hi column of
+// head h) and g = 2h + 1 (lo column) need the same fp32 values x for k-rows
+// {2 tig, 2 tig + 1} (register b0) and {2 tig + 8, 2 tig + 9} (register b1).
+// The hi lane computes the b0 pair, the lo lane the b1 pair; each splits its
+// pair into hi + lo fp16 and they swap the half the other one needs.
+__device__ __forceinline__ void split_exchange(float x0, float x1, bool lo_lane, uint32_t& b0, uint32_t& b1) {
+  const uint32_t hi = pack_half2(x0, x1);
+  const uint32_t lo = pack_half2(x0 - half_lo_to_float(hi), x1 - half_hi_to_float(hi));
+  const uint32_t send = lo_lane ? hi : lo;
+  const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 4);
+  b0 = lo_lane ? recv : hi;
+  b1 = lo_lane ? lo : recv;
 }
 
 template <int MAXS>
@@ -256,16 +106,14 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   const int64_t cta = blockIdx.x;
   const int64_t u0 = cta_first_unit(cta, T, N);
   const int64_t u1 = cta_first_unit(cta + 1, T, N);
-  const int64_t nloc = u1 - u0;
   const int hkv = p.h.hkv;
-  const int gqa = p.h.gqa;
   const uint8_t* blocks = arena + p.h.blocks_off;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&S.full[s], 1);
-      mbar_init(&S.ready[s], 32);          // every helper lane arrives after its writes
-      mbar_init(&S.empty[s], kConsumers);
+      mbar_init(&S.empty[s], 1);
+      S.issued[s] = 0;
     }
     S.abort_flag = 0;
     fence_mbar_init();
@@ -273,151 +121,33 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   __syncthreads();
 
   if (warp == kConsumers) {
-    // ============================================================ helper warp
-    const int g = lane >> 2, tig = lane & 3, hb = g >> 1;
-    const bool want_lo = (g & 1) != 0;
-    // lane 0: bulk copy of local unit k into its stage
-    int64_t iss_u = u0;
-    int iss_b = 0, iss_j = 0, iss_g = 0, iss_ng = 1;
-    int64_t iss_k = 0;
-    auto issue_next = [&]() {
-      if (iss_k >= nloc) return;
-      if (iss_k == 0 || iss_g >= iss_ng) locate_unit(p, iss_u, iss_b, iss_j, iss_g, iss_ng);
-      const int s = (int)(iss_k % kStages);
-      if (iss_k >= kStages)
-        mbar_wait_bounded(&S.empty[s], (uint32_t)(((iss_k / kStages) - 1) & 1), &S.abort_flag, p.h.err_word);
-      if (!S.abort_flag) {
-        const uint8_t* src =
-            blocks + (((int64_t)p.seq[iss_b].slot * hkv + iss_j) * p.h.max_groups + iss_g) * kBlockBytes;
-        mbar_arrive_expect_tx(&S.full[s], kBlockBytes);
-        bulk_g2s(S.stage[s], src, kBlockBytes, &S.full[s]);
-      }
-      ++iss_k;
-      ++iss_u;
-      ++iss_g;
-    };
-    if (lane == 0)
-      for (int i = 0; i < kStages - 1; ++i) issue_next();
-
-    float q2[32];
-    float inv2F = 1.0f;
-    float kq_h[kMaxGqa];
-    float fv = 1.0f, kv = 1.0f;
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
     int64_t k = 0;
     int64_t u = u0;
     while (u < u1) {
-      int b, j, g0, ng;
-      locate_unit(p, u, b, j, g0, ng);
+      int b, j, g, ng;
+      locate_unit(p, u, b, j, g, ng);
       const int64_t row_end = p.seq[b].ubase + (int64_t)(j + 1) * ng;
       const int64_t seg_end = row_end < u1 ? row_end : u1;
-      // ---- segment setup: rotate the gqa queries (4 channels per lane)
-      for (int h = 0; h < kMaxGqa; ++h) {
-        float qv[4] = {0.f, 0.f, 0.f, 0.f};
-        if (h < gqa) {
-          const uint2 raw = *reinterpret_cast<const uint2*>(p.h.q + ((int64_t)b * p.h.hq + j * gqa + h) * kHeadDim +
-                                                            4 * lane);
-          qv[0] = bf16_lo(raw.x);
-          qv[1] = bf16_hi(raw.x);
-          qv[2] = bf16_lo(raw.y);
-          qv[3] = bf16_hi(raw.y);
-          const float a = qv[0] + qv[1], bq = qv[0] - qv[1], c = qv[2] + qv[3], d = qv[2] - qv[3];
-          qv[0] = a + c;
-          qv[2] = a - c;
-          qv[1] = bq + d;
-          qv[3] = bq - d;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const bool upper = (lane & o) != 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float other = __shfl_xor_sync(0xffffffffu, qv[i], o);
-              qv[i] = upper ? other - qv[i] : qv[i] + other;
-            }
-          }
-          const float inv_sqrt_d = 0.088388347648318440550f;  // 1/sqrt(128)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) qv[i] *= inv_sqrt_d;
-        }
-        float mx = fmaxf(fmaxf(fabsf(qv[0]), fabsf(qv[1])), fmaxf(fabsf(qv[2]), fabsf(qv[3])));
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        *reinterpret_cast<float4*>(&S.qrot[h][4 * lane]) = make_float4(qv[0], qv[1], qv[2], qv[3]);
-        kq_h[h] = pow2f(24 - range_exponent(mx * (2.0f / 3.0f)));
-        if (h == hb) {
-          const int F = range_exponent(mx * (2.0f / 3.0f));
-          inv2F = pow2f(-F);
-        }
-        if (lane == 0) S.qmax[h] = mx;
-      }
-      __syncwarp();
-      {
-        const int Fb = range_exponent(S.qmax[hb] * (2.0f / 3.0f));
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const int c0 = 16 * ks + 2 * tig;
-          const float f0 = pow2f(Fb - frag_p(2 * (ks & 3)));
-          const float f1 = pow2f(Fb - frag_p(2 * (ks & 3) + 1));
-          q2[4 * ks + 0] = S.qrot[hb][c0] * f0;
-          q2[4 * ks + 1] = S.qrot[hb][c0 + 1] * f0;
-          q2[4 * ks + 2] = S.qrot[hb][c0 + 8] * f1;
-          q2[4 * ks + 3] = S.qrot[hb][c0 + 9] * f1;
-        }
-        const float vmax = __uint_as_float(
-            reinterpret_cast<const uint32_t*>(arena + kMetaHeader)[(int64_t)p.seq[b].slot * hkv + j]);
-        const int Fv = range_exponent(vmax);
-        fv = pow2f(Fv);
-        kv = pow2f(24 - Fv);
-      }
-      // ---- per group: score operands into the stage's aux record
-      for (; u < seg_end; ++u, ++k) {
+      const uint8_t* src = blocks + (((int64_t)p.seq[b].slot * hkv + j) * p.h.max_groups + g) * kBlockBytes;
+      for (; u < seg_end; ++u, ++k, src += kBlockBytes) {
         const int s = (int)(k % kStages);
-        mbar_wait_bounded(&S.full[s], (uint32_t)((k / kStages) & 1), &S.abort_flag, p.h.err_word);
-        const uint8_t* blk = S.stage[s];
-        const float* ksc = reinterpret_cast<const float*>(blk + kOffKScale);
-        const float* kze = reinterpret_cast<const float*>(blk + kOffKZero);
-        GroupAux& ax = S.aux[s];
-        float qzp[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) qzp[i] = 0.0f;
-#pragma unroll
-        for (int ks2 = 0; ks2 < 4; ++ks2) {
-          uint32_t r[4];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int ks = 2 * ks2 + e;
-            const int c0 = 16 * ks + 2 * tig;
-            const float2 s01 = *reinterpret_cast<const float2*>(ksc + c0);
-            const float2 s89 = *reinterpret_cast<const float2*>(ksc + c0 + 8);
-            const float2 z01 = *reinterpret_cast<const float2*>(kze + c0);
-            const float2 z89 = *reinterpret_cast<const float2*>(kze + c0 + 8);
-            r[2 * e] = split_half2(q2[4 * ks] * s01.x, q2[4 * ks + 1] * s01.y, want_lo);
-            r[2 * e + 1] = split_half2(q2[4 * ks + 2] * s89.x, q2[4 * ks + 3] * s89.y, want_lo);
-            const int i0 = 2 * (ks & 3);
-            qzp[i0] = fmaf(q2[4 * ks], z01.x, fmaf(q2[4 * ks + 1], z01.y, qzp[i0]));
-            qzp[i0 + 1] = fmaf(q2[4 * ks + 2], z89.x, fmaf(q2[4 * ks + 3], z89.y, qzp[i0 + 1]));
+        if (k >= kStages) {
+          if (!mbar_wait_bounded(&S.empty[s], (uint32_t)(((k / kStages) - 1) & 1), &S.abort_flag, p.h.err_word)) {
+            goto drain;
           }
-          ax.bk[ks2][lane] = make_uint4(r[0], r[1], r[2], r[3]);
         }
-        float qz = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) qz = fmaf(qzp[i], pow2f(frag_p(i)), qz);
-        qz += __shfl_xor_sync(0xffffffffu, qz, 1);
-        qz += __shfl_xor_sync(0xffffffffu, qz, 2);
-        if ((lane & 7) == 0) ax.qz[hb] = qz * inv2F;   // lanes g = 2 hb, tig = 0
-        if (lane < kMaxGqa) ax.kq[lane] = kq_h[lane < kMaxGqa ? lane : 0];
-        if (lane == 0) {
-          ax.fv = fv;
-          ax.kv = kv;
-        }
-        mbar_arrive(&S.ready[s]);          // release of this lane's aux writes
-        if (lane == 0) issue_next();       // refill: waits until the consumers released unit k - 1
-        __syncwarp();
+        mbar_arrive_expect_tx(&S.full[s], kBlockBytes);
+        bulk_g2s(S.stage[s], src, kBlockBytes, &S.full[s]);
+        reinterpret_cast<volatile uint32_t*>(S.issued)[s] = (uint32_t)(k / kStages) + 1;
       }
     }
-    if (lane == 0 && S.abort_flag) {
+  drain:
+    if (S.abort_flag) {
       // wait (bounded, once more) for the copies that may still be in flight
-      const int64_t first = iss_k > kStages ? iss_k - kStages : 0;
-      for (int64_t kk = first; kk < iss_k; ++kk) {
+      const int64_t first = k > kStages ? k - kStages : 0;
+      for (int64_t kk = first; kk < k; ++kk) {
         const int s = (int)(kk % kStages);
         for (uint32_t i = 0; i < kSpinLimit; ++i)
           if (mbar_try_wait(&S.full[s], (uint32_t)((kk / kStages) & 1))) break;
@@ -426,11 +156,14 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     return;
   }
 
-  // ============================================================== consumers
-  const int g = lane >> 2;
-  const int tig = lane & 3;
+  // -------------------------------------------------------------- consumers
+  const int g = lane >> 2;     // row group of the mma fragments
+  const int tig = lane & 3;    // thread in group
+  const int hb = g >> 1;       // head of this lane's B column
+  const int half = g & 1;      // 0: hi column lane (computes b0 pairs), 1: lo column lane (b1 pairs)
+  const bool lo_lane = half != 0;
+  const int gqa = p.h.gqa;
   const float scale_log2 = p.h.scale_log2;
-  float* pbw = &S.pbuf[warp][0][0];
 
   int64_t k = 0;
   int64_t u = u0;
@@ -439,24 +172,227 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     locate_unit(p, u, b, j, g0, ng);
     const int64_t row_end = p.seq[b].ubase + (int64_t)(j + 1) * ng;
     const int64_t seg_end = row_end < u1 ? row_end : u1;
-    ConsumerState st;
-    st.m_run = -INFINITY;
-    st.l_run = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) st.o_acc[i][0] = st.o_acc[i][1] = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kVGroups; ++i) st.zacc[i] = 0.0f;
+    const int64_t k_begin = k;
+    const int64_t k_end = k + (seg_end - u);
+    const int slot = p.seq[b].slot;
 
-    for (; u < seg_end; ++u, ++k) {
-      const int s = (int)(k % kStages);
-      const uint32_t par = (uint32_t)((k / kStages) & 1);
-      const bool ok = mbar_wait_bounded(&S.ready[s], par, &S.abort_flag, p.h.err_word) &&
-                      mbar_wait_bounded(&S.full[s], par, &S.abort_flag, p.h.err_word);
-      if (ok) {
-        if (warp & 1)
-          consume_group<1>(S.stage[s], S.aux[s], warp, lane, scale_log2, pbw, st);
-        else
-          consume_group<0>(S.stage[s], S.aux[s], warp, lane, scale_log2, pbw, st);
+    // ---- segment setup: rotate the GQA queries (warp w rotates head w)
+    {
+      const int h = warp;
+      float qv[4] = {0.f, 0.f, 0.f, 0.f};
+      if (h < gqa) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(p.h.q + ((int64_t)b * p.h.hq + j * gqa + h) * kHeadDim +
+                                                          4 * lane);
+        qv[0] = bf16_lo(raw.x);
+        qv[1] = bf16_hi(raw.x);
+        qv[2] = bf16_lo(raw.y);
+        qv[3] = bf16_hi(raw.y);
+        // channel c = 4 * lane + i: bits 0,1 in registers, bits 2..6 across lanes
+        const float a = qv[0] + qv[1], bq = qv[0] - qv[1], c = qv[2] + qv[3], d = qv[2] - qv[3];
+        qv[0] = a + c;
+        qv[2] = a - c;
+        qv[1] = bq + d;
+        qv[3] = bq - d;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const bool upper = (lane & o) != 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float other = __shfl_xor_sync(0xffffffffu, qv[i], o);
+            qv[i] = upper ? other - qv[i] : qv[i] + other;
+          }
+        }
+        const float inv_sqrt_d = 0.088388347648318440550f;  // 1/sqrt(128)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qv[i] *= inv_sqrt_d;
+      }
+      float mx = fmaxf(fmaxf(fabsf(qv[0]), fabsf(qv[1])), fmaxf(fabsf(qv[2]), fabsf(qv[3])));
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      *reinterpret_cast<float4*>(&S.qrot[h][4 * lane]) = make_float4(qv[0], qv[1], qv[2], qv[3]);
+      if (lane == 0) S.qmax[h] = mx;
+    }
+    named_bar_sync(1, kConsumers * 32);
+
+    // per-lane constants of this segment
+    const int Fk_b = range_exponent(S.qmax[hb] * (2.0f / 3.0f));     // B-column head hb
+    const int Fk_s = range_exponent(S.qmax[tig] * (2.0f / 3.0f));    // score head tig
+    const float kq = pow2f(24 - Fk_s);
+    const float inv2Fk_b = pow2f(-Fk_b);
+    const float vmax = __uint_as_float(
+        reinterpret_cast<const uint32_t*>(arena + kMetaHeader)[(int64_t)slot * hkv + j]);
+    const int Fv = range_exponent(vmax);
+    const float fv = pow2f(Fv);
+    const float kv = pow2f(24 - Fv);
+    // q2: this lane's 16 query values (its half of each k-step's channel
+    // pairs) times 2^(F - p); zw: the 2^p that maps them back for q_rot . z
+    float q2[16], zw[8];
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int c = 16 * ks + 2 * tig + 8 * half;
+      const int pp = half ? frag_p(2 * (ks & 3) + 1) : frag_p(2 * (ks & 3));
+      const float f = pow2f(Fk_b - pp);
+      q2[2 * ks] = S.qrot[hb][c] * f;
+      q2[2 * ks + 1] = S.qrot[hb][c + 1] * f;
+      zw[ks] = pow2f(pp);
+    }
+
+    float m_run = -INFINITY;   // running max (log2 units) of head tig
+    float l_run = 0.0f;        // partial sum of p over this lane's tokens
+    float o_acc[8][2];         // head tig, channels 16 mt + g + 8 r (times 2^(Fv - 24))
+    float zacc[kVGroups];      // sum_t p_t z^V_t,gr over this lane's tokens
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o_acc[i][0] = o_acc[i][1] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kVGroups; ++i) zacc[i] = 0.0f;
+
+    for (int64_t kk = k_begin + ((warp - k_begin) % kConsumers + kConsumers) % kConsumers; kk < k_end;
+         kk += kConsumers) {
+      const int s = (int)(kk % kStages);
+      const uint32_t use = (uint32_t)(kk / kStages);
+      if (!wait_issued(&S.issued[s], use, &S.abort_flag, p.h.err_word)) continue;
+      if (!mbar_wait_bounded(&S.full[s], use & 1, &S.abort_flag, p.h.err_word)) continue;
+      const uint8_t* blk = S.stage[s];
+      const float* ksc = reinterpret_cast<const float*>(blk + kOffKScale);
+      const float* kze = reinterpret_cast<const float*>(blk + kOffKZero);
+      const float* knm = reinterpret_cast<const float*>(blk + kOffKNorm);
+      const float* vsz = reinterpret_cast<const float*>(blk + kOffVSZ);
+
+      // ---- B fragments of the score contraction, and q_rot . z
+      uint32_t bk[8][2];
+      float qz = 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const int c = 16 * ks + 2 * tig + 8 * half;
+        const float2 s2 = *reinterpret_cast<const float2*>(ksc + c);
+        const float2 z2 = *reinterpret_cast<const float2*>(kze + c);
+        split_exchange(q2[2 * ks] * s2.x, q2[2 * ks + 1] * s2.y, lo_lane, bk[ks][0], bk[ks][1]);
+        qz = fmaf(fmaf(q2[2 * ks], z2.x, q2[2 * ks + 1] * z2.y), zw[ks], qz);
+      }
+      qz += __shfl_xor_sync(0xffffffffu, qz, 1);
+      qz += __shfl_xor_sync(0xffffffffu, qz, 2);
+      qz += __shfl_xor_sync(0xffffffffu, qz, 4);
+      qz *= inv2Fk_b;                                            // q_rot[hb] . z
+      const float qz_s = __shfl_sync(0xffffffffu, qz, 8 * tig);  // q_rot[tig] . z
+
+      // ---- scores: S^T[token][head x {hi, lo}] = codes x B, 8 independent chains
+      float sc[16];
+      {
+        const uint4* kc = reinterpret_cast<const uint4*>(blk + kOffKCodes);
+#pragma unroll
+        for (int mh = 0; mh < 2; ++mh) {
+          uint4 w[4];
+          float acc[4][4];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            w[m] = kc[(4 * mh + m) * 32 + lane];
+            acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.0f;
+          }
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const uint32_t w0 = (ks < 4) ? w[m].x : w[m].z;
+              const uint32_t w1 = (ks < 4) ? w[m].y : w[m].w;
+              uint32_t a0, a1, a2, a3;
+              switch (ks & 3) {
+                case 0: frag_a<0>(w0, w1, a0, a1, a2, a3); break;
+                case 1: frag_a<1>(w0, w1, a0, a1, a2, a3); break;
+                case 2: frag_a<2>(w0, w1, a0, a1, a2, a3); break;
+                default: frag_a<3>(w0, w1, a0, a1, a2, a3); break;
+              }
+              mma_f16_16816(acc[m], a0, a1, a2, a3, bk[ks][0], bk[ks][1]);
+            }
+          }
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const int mt = 4 * mh + m;
+            const int t0 = 16 * mt + g;
+            sc[2 * mt] = fmaf(acc[m][0] + acc[m][1], kq, qz_s) * knm[t0] * scale_log2;
+            sc[2 * mt + 1] = fmaf(acc[m][2] + acc[m][3], kq, qz_s) * knm[t0 + 8] * scale_log2;
+          }
+        }
+      }
+
+      // ---- online softmax (head tig)
+      float gm = sc[0];
+#pragma unroll
+      for (int i = 1; i < 16; ++i) gm = fmaxf(gm, sc[i]);
+      gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 4));
+      gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 8));
+      gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 16));
+      const float m_new = fmaxf(m_run, gm);
+      const float alpha = exp2f(m_run - m_new);
+      m_run = m_new;
+      float psum = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        sc[i] = exp2f(sc[i] - m_new);
+        psum += sc[i];
+      }
+      l_run = fmaf(l_run, alpha, psum);
+#pragma unroll
+      for (int gr = 0; gr < kVGroups; ++gr) zacc[gr] *= alpha;
+      float* pb = S.pbuf[warp][tig];
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const int t0 = 16 * mt + g;
+        pb[t0] = sc[2 * mt];
+        pb[t0 + 8] = sc[2 * mt + 1];
+        const float4 z0 = *reinterpret_cast<const float4*>(vsz + 8 * t0 + 4);
+        const float4 z1 = *reinterpret_cast<const float4*>(vsz + 8 * (t0 + 8) + 4);
+        zacc[0] = fmaf(sc[2 * mt], z0.x, fmaf(sc[2 * mt + 1], z1.x, zacc[0]));
+        zacc[1] = fmaf(sc[2 * mt], z0.y, fmaf(sc[2 * mt + 1], z1.y, zacc[1]));
+        zacc[2] = fmaf(sc[2 * mt], z0.z, fmaf(sc[2 * mt + 1], z1.z, zacc[2]));
+        zacc[3] = fmaf(sc[2 * mt], z0.w, fmaf(sc[2 * mt + 1], z1.w, zacc[3]));
+      }
+      __syncwarp();
+
+      // ---- P.V: O^T[channel][head x {hi, lo}] = codes^V^T x (p * s^V)
+      float pacc[8][4];
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) pacc[mt][0] = pacc[mt][1] = pacc[mt][2] = pacc[mt][3] = 0.0f;
+      const float* pbh = S.pbuf[warp][hb];
+#pragma unroll
+      for (int jh = 0; jh < 2; ++jh) {
+        uint2 vw[8];
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+          vw[mt] = *reinterpret_cast<const uint2*>(blk + kOffVCodes + ((mt * 32 + lane) * 4 + 2 * jh) * 4);
+#pragma unroll
+        for (int kk2 = 0; kk2 < 4; ++kk2) {
+          const int ks = 4 * jh + kk2;
+          const int t = 16 * ks + 2 * tig + 8 * half;   // this lane's two tokens
+          const float fsc = fv * (half ? pow2f(-frag_p(2 * kk2 + 1)) : pow2f(-frag_p(2 * kk2)));
+          const float2 pp = *reinterpret_cast<const float2*>(pbh + t);
+          const float p0 = pp.x * fsc, p1 = pp.y * fsc;
+          const float4 s0 = *reinterpret_cast<const float4*>(vsz + 8 * t);
+          const float4 s1 = *reinterpret_cast<const float4*>(vsz + 8 * (t + 1));
+          const float sA[4] = {s0.x, s0.y, s0.z, s0.w};
+          const float sB[4] = {s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+          for (int gr = 0; gr < kVGroups; ++gr) {
+            uint32_t b0, b1;
+            split_exchange(p0 * sA[gr], p1 * sB[gr], lo_lane, b0, b1);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int mt = 2 * gr + h2;
+              uint32_t a0, a1, a2, a3;
+              switch (kk2) {
+                case 0: frag_a<0>(vw[mt].x, vw[mt].y, a0, a1, a2, a3); break;
+                case 1: frag_a<1>(vw[mt].x, vw[mt].y, a0, a1, a2, a3); break;
+                case 2: frag_a<2>(vw[mt].x, vw[mt].y, a0, a1, a2, a3); break;
+                default: frag_a<3>(vw[mt].x, vw[mt].y, a0, a1, a2, a3); break;
+              }
+              mma_f16_16816(pacc[mt], a0, a1, a2, a3, b0, b1);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o_acc[mt][0] = fmaf(o_acc[mt][0], alpha, pacc[mt][0] + pacc[mt][1]);
+        o_acc[mt][1] = fmaf(o_acc[mt][1], alpha, pacc[mt][2] + pacc[mt][3]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty[s]);
@@ -464,28 +400,28 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 
     // ---- segment end: per-warp state -> shared memory -> CTA merge -> partial
     {
-      float l = st.l_run;
+      float l = l_run;
       l += __shfl_xor_sync(0xffffffffu, l, 4);
       l += __shfl_xor_sync(0xffffffffu, l, 8);
       l += __shfl_xor_sync(0xffffffffu, l, 16);
       float zs[kVGroups];
 #pragma unroll
       for (int gr = 0; gr < kVGroups; ++gr) {
-        float z = st.zacc[gr];
+        float z = zacc[gr];
         z += __shfl_xor_sync(0xffffffffu, z, 4);
         z += __shfl_xor_sync(0xffffffffu, z, 8);
         z += __shfl_xor_sync(0xffffffffu, z, 16);
         zs[gr] = z;
       }
       if (g == 0) {
-        S.mst[warp][tig] = st.m_run;
+        S.mst[warp][tig] = m_run;
         S.lst[warp][tig] = l;
       }
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const float zg = zs[mt >> 1];
-        S.ost[warp][tig][16 * mt + g] = st.o_acc[mt][0] + zg;
-        S.ost[warp][tig][16 * mt + g + 8] = st.o_acc[mt][1] + zg;
+        S.ost[warp][tig][16 * mt + g] = fmaf(o_acc[mt][0], kv, zg);
+        S.ost[warp][tig][16 * mt + g + 8] = fmaf(o_acc[mt][1], kv, zg);
       }
     }
     named_bar_sync(1, kConsumers * 32);
@@ -513,6 +449,8 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       }
     }
     named_bar_sync(1, kConsumers * 32);
+    k = k_end;
+    u = seg_end;
   }
 }
 
