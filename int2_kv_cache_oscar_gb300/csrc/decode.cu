@@ -35,14 +35,17 @@ namespace {
 
 constexpr int kConsumers = 4;
 constexpr int kDecThreads = (kConsumers + 1) * 32;
-constexpr int kStages = 6;
+constexpr int kStages = 4;
+constexpr int kCtasPerSm = 3;
 constexpr int kPbStride = kGroup + 8;  // probability rows, padded against bank conflicts
 
 struct DecSmem {
   alignas(128) uint8_t stage[kStages][kBlockBytes];
   alignas(16) float qrot[kMaxGqa][kHeadDim];              // float4 stores
-  alignas(16) float pbuf[kConsumers][kMaxGqa][kPbStride];  // float2 loads
-  alignas(16) float ost[kConsumers][kMaxGqa][kHeadDim];
+  alignas(16) float4 q2t[4][32];                          // per-lane scaled query values, [i/4][lane]
+  // consumer-private probabilities; at a segment end each warp's region holds
+  // its output rows ([head][channel]) for the CTA merge instead
+  alignas(16) float pbuf[kConsumers][kMaxGqa][kPbStride];
   float qmax[kMaxGqa];
   float mst[kConsumers][kMaxGqa];
   float lst[kConsumers][kMaxGqa];
@@ -51,6 +54,7 @@ struct DecSmem {
   uint32_t issued[kStages];   // uses of each stage issued so far (producer -> consumers)
   int abort_flag;
 };
+static_assert(kPbStride >= kHeadDim, "output rows must fit in the probability rows");
 static_assert(offsetof(DecSmem, qrot) % 16 == 0, "qrot must be 16-byte aligned");
 static_assert(offsetof(DecSmem, pbuf) % 16 == 0, "pbuf must be 16-byte aligned");
 static_assert((kPbStride * 4) % 16 == 0, "pbuf rows must keep 16-byte alignment");
@@ -94,8 +98,16 @@ __device__ __forceinline__ void split_exchange(float x0, float x1, bool lo_lane,
   b1 = lo_lane ? lo : recv;
 }
 
+// 2^x for softmax weights (x <= 0 or small): the hardware approximation,
+// relative error ~2^-22, flushes results below 2^-126 to zero.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <int MAXS>
-__global__ void __launch_bounds__(kDecThreads, 2)
+__global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     decode_int2_kernel(const __grid_constant__ DecodeParams<MAXS> p, const uint8_t* __restrict__ arena) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   DecSmem& S = *reinterpret_cast<DecSmem*>(smem_raw);
@@ -224,18 +236,22 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     const int Fv = range_exponent(vmax);
     const float fv = pow2f(Fv);
     const float kv = pow2f(24 - Fv);
-    // q2: this lane's 16 query values (its half of each k-step's channel
-    // pairs) times 2^(F - p); zw: the 2^p that maps them back for q_rot . z
-    float q2[16], zw[8];
+    // q2 table: this lane's 16 query values (its half of each k-step's
+    // channel pairs) times 2^(F - p); the same for every warp, written by warp 0
+    if (warp == 0) {
+      float q2[16];
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int c = 16 * ks + 2 * tig + 8 * half;
-      const int pp = half ? frag_p(2 * (ks & 3) + 1) : frag_p(2 * (ks & 3));
-      const float f = pow2f(Fk_b - pp);
-      q2[2 * ks] = S.qrot[hb][c] * f;
-      q2[2 * ks + 1] = S.qrot[hb][c + 1] * f;
-      zw[ks] = pow2f(pp);
+      for (int ks = 0; ks < 8; ++ks) {
+        const int c = 16 * ks + 2 * tig + 8 * half;
+        const int pp = half ? frag_p(2 * (ks & 3) + 1) : frag_p(2 * (ks & 3));
+        const float f = pow2f(Fk_b - pp);
+        q2[2 * ks] = S.qrot[hb][c] * f;
+        q2[2 * ks + 1] = S.qrot[hb][c + 1] * f;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) S.q2t[i][lane] = make_float4(q2[4 * i], q2[4 * i + 1], q2[4 * i + 2], q2[4 * i + 3]);
     }
+    named_bar_sync(1, kConsumers * 32);
 
     float m_run = -INFINITY;   // running max (log2 units) of head tig
     float l_run = 0.0f;        // partial sum of p over this lane's tokens
@@ -262,12 +278,19 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       uint32_t bk[8][2];
       float qz = 0.0f;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const int c = 16 * ks + 2 * tig + 8 * half;
-        const float2 s2 = *reinterpret_cast<const float2*>(ksc + c);
-        const float2 z2 = *reinterpret_cast<const float2*>(kze + c);
-        split_exchange(q2[2 * ks] * s2.x, q2[2 * ks + 1] * s2.y, lo_lane, bk[ks][0], bk[ks][1]);
-        qz = fmaf(fmaf(q2[2 * ks], z2.x, q2[2 * ks + 1] * z2.y), zw[ks], qz);
+      for (int i = 0; i < 4; ++i) {
+        const float4 q4 = S.q2t[i][lane];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int ks = 2 * i + e;
+          const float qa = e ? q4.z : q4.x, qb = e ? q4.w : q4.y;
+          const int c = 16 * ks + 2 * tig + 8 * half;
+          const float2 s2 = *reinterpret_cast<const float2*>(ksc + c);
+          const float2 z2 = *reinterpret_cast<const float2*>(kze + c);
+          split_exchange(qa * s2.x, qb * s2.y, lo_lane, bk[ks][0], bk[ks][1]);
+          const float zw = half ? pow2f(frag_p(2 * (ks & 3) + 1)) : pow2f(frag_p(2 * (ks & 3)));
+          qz = fmaf(fmaf(qa, z2.x, qb * z2.y), zw, qz);
+        }
       }
       qz += __shfl_xor_sync(0xffffffffu, qz, 1);
       qz += __shfl_xor_sync(0xffffffffu, qz, 2);
@@ -322,12 +345,12 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 8));
       gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 16));
       const float m_new = fmaxf(m_run, gm);
-      const float alpha = exp2f(m_run - m_new);
+      const float alpha = fast_exp2(m_run - m_new);
       m_run = m_new;
       float psum = 0.0f;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        sc[i] = exp2f(sc[i] - m_new);
+        sc[i] = fast_exp2(sc[i] - m_new);
         psum += sc[i];
       }
       l_run = fmaf(l_run, alpha, psum);
@@ -348,51 +371,54 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       }
       __syncwarp();
 
-      // ---- P.V: O^T[channel][head x {hi, lo}] = codes^V^T x (p * s^V)
-      float pacc[8][4];
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) pacc[mt][0] = pacc[mt][1] = pacc[mt][2] = pacc[mt][3] = 0.0f;
+      // ---- P.V: O^T[channel][head x {hi, lo}] = codes^V^T x (p * s^V), in two
+      // halves of 64 channels (value groups 2 hc, 2 hc + 1) to bound registers
       const float* pbh = S.pbuf[warp][hb];
 #pragma unroll
-      for (int jh = 0; jh < 2; ++jh) {
-        uint2 vw[8];
+      for (int hc = 0; hc < 2; ++hc) {
+        float pacc[4][4];
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt)
-          vw[mt] = *reinterpret_cast<const uint2*>(blk + kOffVCodes + ((mt * 32 + lane) * 4 + 2 * jh) * 4);
+        for (int m = 0; m < 4; ++m) pacc[m][0] = pacc[m][1] = pacc[m][2] = pacc[m][3] = 0.0f;
 #pragma unroll
-        for (int kk2 = 0; kk2 < 4; ++kk2) {
-          const int ks = 4 * jh + kk2;
-          const int t = 16 * ks + 2 * tig + 8 * half;   // this lane's two tokens
-          const float fsc = fv * (half ? pow2f(-frag_p(2 * kk2 + 1)) : pow2f(-frag_p(2 * kk2)));
-          const float2 pp = *reinterpret_cast<const float2*>(pbh + t);
-          const float p0 = pp.x * fsc, p1 = pp.y * fsc;
-          const float4 s0 = *reinterpret_cast<const float4*>(vsz + 8 * t);
-          const float4 s1 = *reinterpret_cast<const float4*>(vsz + 8 * (t + 1));
-          const float sA[4] = {s0.x, s0.y, s0.z, s0.w};
-          const float sB[4] = {s1.x, s1.y, s1.z, s1.w};
+        for (int jh = 0; jh < 2; ++jh) {
+          uint2 vw[4];
 #pragma unroll
-          for (int gr = 0; gr < kVGroups; ++gr) {
-            uint32_t b0, b1;
-            split_exchange(p0 * sA[gr], p1 * sB[gr], lo_lane, b0, b1);
+          for (int m = 0; m < 4; ++m)
+            vw[m] = *reinterpret_cast<const uint2*>(blk + kOffVCodes + (((4 * hc + m) * 32 + lane) * 4 + 2 * jh) * 4);
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              const int mt = 2 * gr + h2;
-              uint32_t a0, a1, a2, a3;
-              switch (kk2) {
-                case 0: frag_a<0>(vw[mt].x, vw[mt].y, a0, a1, a2, a3); break;
-                case 1: frag_a<1>(vw[mt].x, vw[mt].y, a0, a1, a2, a3); break;
-                case 2: frag_a<2>(vw[mt].x, vw[mt].y, a0, a1, a2, a3); break;
-                default: frag_a<3>(vw[mt].x, vw[mt].y, a0, a1, a2, a3); break;
+          for (int kk2 = 0; kk2 < 4; ++kk2) {
+            const int ks = 4 * jh + kk2;
+            const int t = 16 * ks + 2 * tig + 8 * half;   // this lane's two tokens
+            const float fsc = fv * (half ? pow2f(-frag_p(2 * kk2 + 1)) : pow2f(-frag_p(2 * kk2)));
+            const float2 pp = *reinterpret_cast<const float2*>(pbh + t);
+            const float p0 = pp.x * fsc, p1 = pp.y * fsc;
+            const float2 s0 = *reinterpret_cast<const float2*>(vsz + 8 * t + 2 * hc);
+            const float2 s1 = *reinterpret_cast<const float2*>(vsz + 8 * (t + 1) + 2 * hc);
+#pragma unroll
+            for (int g2 = 0; g2 < 2; ++g2) {
+              uint32_t b0, b1;
+              split_exchange(p0 * (g2 ? s0.y : s0.x), p1 * (g2 ? s1.y : s1.x), lo_lane, b0, b1);
+#pragma unroll
+              for (int h2 = 0; h2 < 2; ++h2) {
+                const int m = 2 * g2 + h2;
+                uint32_t a0, a1, a2, a3;
+                switch (kk2) {
+                  case 0: frag_a<0>(vw[m].x, vw[m].y, a0, a1, a2, a3); break;
+                  case 1: frag_a<1>(vw[m].x, vw[m].y, a0, a1, a2, a3); break;
+                  case 2: frag_a<2>(vw[m].x, vw[m].y, a0, a1, a2, a3); break;
+                  default: frag_a<3>(vw[m].x, vw[m].y, a0, a1, a2, a3); break;
+                }
+                mma_f16_16816(pacc[m], a0, a1, a2, a3, b0, b1);
               }
-              mma_f16_16816(pacc[mt], a0, a1, a2, a3, b0, b1);
             }
           }
         }
-      }
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        o_acc[mt][0] = fmaf(o_acc[mt][0], alpha, pacc[mt][0] + pacc[mt][1]);
-        o_acc[mt][1] = fmaf(o_acc[mt][1], alpha, pacc[mt][2] + pacc[mt][3]);
+        for (int m = 0; m < 4; ++m) {
+          const int mt = 4 * hc + m;
+          o_acc[mt][0] = fmaf(o_acc[mt][0], alpha, pacc[m][0] + pacc[m][1]);
+          o_acc[mt][1] = fmaf(o_acc[mt][1], alpha, pacc[m][2] + pacc[m][3]);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty[s]);
@@ -420,8 +446,8 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const float zg = zs[mt >> 1];
-        S.ost[warp][tig][16 * mt + g] = fmaf(o_acc[mt][0], kv, zg);
-        S.ost[warp][tig][16 * mt + g + 8] = fmaf(o_acc[mt][1], kv, zg);
+        S.pbuf[warp][tig][16 * mt + g] = fmaf(o_acc[mt][0], kv, zg);
+        S.pbuf[warp][tig][16 * mt + g + 8] = fmaf(o_acc[mt][1], kv, zg);
       }
     }
     named_bar_sync(1, kConsumers * 32);
@@ -438,7 +464,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         for (int w = 0; w < kConsumers; ++w) {
           const float mw = S.mst[w][h];
           const float f = (mw == -INFINITY) ? 0.0f : exp2f(mw - M);
-          o = fmaf(f, S.ost[w][h][c], o);
+          o = fmaf(f, S.pbuf[w][h][c], o);
           l = fmaf(f, S.lst[w][h], l);
         }
         part[h * kPartialFloats + c] = o;
@@ -455,22 +481,34 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 }
 
 // ---------------------------------------------------------------- combine
-// One CTA per (sequence, KV head), 128 threads.  For each of the gqa query
-// heads: attend to the bf16 window (unrotated q . k: the window holds raw
-// keys), then merge the window state with the row's split-K partials:
-// m* = max m_i, o = sum 2^(m_i - m*) o_i / sum 2^(m_i - m*) l_i, written as
-// bf16.  The partial maxima are read by all threads at once and the weighted
-// sum runs with independent loads per thread (thread = channel), so the
-// merge costs a few memory latencies, not one per partial.
-constexpr int kCombineMaxPartials = 2048;
+// One CTA per (sequence, KV head), 128 threads.  A bulk copy stages the bf16
+// window rows (keys then values) and the row's split-K partial records
+// (contiguous slots) in shared memory; everything after that runs from shared
+// memory:
+//   window: warp h scores query head h against the window tokens (lane =
+//           token, rotated 16-byte chunk order against bank conflicts),
+//           softmax in-warp, then thread = channel sums p_t v_t;
+//   merge:  m* = max(m_window, m_i), o = (sum 2^(m_i - m*) o_i) /
+//           (sum 2^(m_i - m*) l_i), written as bf16.
+constexpr int kCombineThreads = 128;
+constexpr int kCombinePartBytes = 96 * 1024;   // partial records staged per chunk
+constexpr int kCombineSmem = kWindowBytes + kCombinePartBytes;
 
 template <int MAXS>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const __grid_constant__ DecodeParams<MAXS> p, const uint8_t* __restrict__ arena) {
-  __shared__ float wts[kCombineMaxPartials + 1];
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint16_t* wk = reinterpret_cast<uint16_t*>(smem_raw);                 // [128][128] bf16
+  uint16_t* wv = wk + kGroup * kHeadDim;                                // [128][128] bf16
+  float* part = reinterpret_cast<float*>(smem_raw + kWindowBytes);      // partial records
+  __shared__ __align__(16) float qs[kMaxGqa][kHeadDim];
+  __shared__ float pw[kMaxGqa][kGroup];                                 // window probabilities
+  __shared__ float wts[kCombinePartBytes / (kPartialFloats * 4)];
   __shared__ float red[2][4];
   __shared__ float win_m[kMaxGqa], win_l[kMaxGqa];
-  __shared__ __align__(16) float win_o[kMaxGqa][kHeadDim];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+
   const int b = blockIdx.x / p.h.hkv;
   const int j = blockIdx.x % p.h.hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -479,105 +517,168 @@ __global__ void __launch_bounds__(128)
   const int ng = units_of_len(sq.len, p.h.bf16_mode);
   const int wlen = p.h.bf16_mode ? 0 : (sq.len % kGroup);
   const int64_t T = p.h.n_units, N = p.h.n_ctas;
-
-  // ---- window attention: warp h handles query head h (4 channels per lane)
-  for (int h = warp; h < gqa; h += 4) {
-    float M = -INFINITY, L = 0.0f;
-    float o[4] = {0.f, 0.f, 0.f, 0.f};
-    if (wlen > 0) {
-      const int qh = j * gqa + h;
-      const uint2 qr = *reinterpret_cast<const uint2*>(p.h.q + ((int64_t)b * p.h.hq + qh) * kHeadDim + 4 * lane);
-      const float q0 = bf16_lo(qr.x), q1 = bf16_hi(qr.x), q2 = bf16_lo(qr.y), q3 = bf16_hi(qr.y);
-      const uint16_t* wk = reinterpret_cast<const uint16_t*>(
-          arena + p.h.windows_off + ((int64_t)sq.slot * hkv + j) * kWindowBytes);
-      const uint16_t* wv = wk + kGroup * kHeadDim;
-      for (int t = 0; t < wlen; ++t) {
-        const uint2 kr = *reinterpret_cast<const uint2*>(wk + t * kHeadDim + 4 * lane);
-        float d = q0 * bf16_lo(kr.x) + q1 * bf16_hi(kr.x) + q2 * bf16_lo(kr.y) + q3 * bf16_hi(kr.y);
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-        const float s = d * p.h.scale_log2;
-        const float Mn = fmaxf(M, s);
-        const float a = exp2f(M - Mn);
-        const float pt = exp2f(s - Mn);
-        const uint2 vr = *reinterpret_cast<const uint2*>(wv + t * kHeadDim + 4 * lane);
-        o[0] = fmaf(o[0], a, pt * bf16_lo(vr.x));
-        o[1] = fmaf(o[1], a, pt * bf16_hi(vr.x));
-        o[2] = fmaf(o[2], a, pt * bf16_lo(vr.y));
-        o[3] = fmaf(o[3], a, pt * bf16_hi(vr.y));
-        L = fmaf(L, a, pt);
-        M = Mn;
-      }
-    }
-    *reinterpret_cast<float4*>(&win_o[h][4 * lane]) = make_float4(o[0], o[1], o[2], o[3]);
-    if (lane == 0) {
-      win_m[h] = M;
-      win_l[h] = L;
-    }
-  }
-  __syncthreads();
-
-  // ---- merge with the partials of this row
   int64_t first = 0, count = 0, rho = 0;
   if (ng > 0) {
     rho = (int64_t)hkv * sq.rank + j;
     const int64_t U = sq.ubase + (int64_t)j * ng;
     first = cta_of_unit(U, T, N);
     count = cta_of_unit(U + ng - 1, T, N) - first + 1;
-    if (count > kCombineMaxPartials) count = kCombineMaxPartials;  // cannot happen: count <= N
   }
-  for (int h = 0; h < gqa; ++h) {
-    const float* base = p.h.partials + ((first + rho) * gqa + h) * (int64_t)kPartialFloats;
-    const int64_t stride = (int64_t)gqa * kPartialFloats;
-    // maximum over partials and window
-    float mx = (tid == 0) ? win_m[h] : -INFINITY;
-    for (int64_t i = tid; i < count; i += 128) mx = fmaxf(mx, base[i * stride + 128]);
+  const int rec_bytes = gqa * kPartialFloats * 4;          // one slot: gqa records
+  const int per_chunk = kCombinePartBytes / rec_bytes;
+  const int64_t nchunks = (count + per_chunk - 1) / per_chunk;
+
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  for (int i = tid; i < kMaxGqa * kHeadDim / 4; i += kCombineThreads) {
+    const int h = i / (kHeadDim / 4), c4 = i % (kHeadDim / 4);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (h < gqa) {
+      const uint2 r = *reinterpret_cast<const uint2*>(p.h.q + ((int64_t)b * p.h.hq + j * gqa + h) * kHeadDim + 4 * c4);
+      v = make_float4(bf16_lo(r.x), bf16_hi(r.x), bf16_lo(r.y), bf16_hi(r.y));
+    }
+    *reinterpret_cast<float4*>(&qs[h][4 * c4]) = v;
+  }
+  __syncthreads();
+  // stage 0: window rows + first chunk of partials
+  if (tid == 0) {
+    const int64_t n0 = count < per_chunk ? count : per_chunk;
+    const uint32_t wbytes = (uint32_t)wlen * kHeadDim * 2;
+    const uint32_t pbytes = (uint32_t)(n0 * rec_bytes);
+    if (wbytes + pbytes > 0) {
+      mbar_arrive_expect_tx(&bar, 2 * wbytes + pbytes);
+      if (wlen > 0) {
+        const uint8_t* wsrc = arena + p.h.windows_off + ((int64_t)sq.slot * hkv + j) * kWindowBytes;
+        bulk_g2s(wk, wsrc, wbytes, &bar);
+        bulk_g2s(wv, wsrc + kGroup * kHeadDim * 2, wbytes, &bar);
+      }
+      if (pbytes > 0) bulk_g2s(part, p.h.partials + (first + rho) * (int64_t)gqa * kPartialFloats, pbytes, &bar);
+    } else {
+      mbar_arrive(&bar);
+    }
+  }
+  mbar_wait_bounded(&bar, 0, &abort_flag, p.h.err_word);
+
+  // ---- window attention (warp h = query head h; lane = token)
+  if (warp < gqa) {
+    const int h = warp;
+    float sc[4];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int t = lane + 32 * r;
+      float acc = -INFINITY;
+      if (t < wlen) {
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+          const int ch = (i + lane) & 15;                       // rotated 16-byte chunk
+          const uint4 kv4 = *reinterpret_cast<const uint4*>(wk + t * kHeadDim + 8 * ch);
+          const float4 qa = *reinterpret_cast<const float4*>(&qs[h][8 * ch]);
+          const float4 qb = *reinterpret_cast<const float4*>(&qs[h][8 * ch + 4]);
+          a0 = fmaf(qa.x, bf16_lo(kv4.x), a0); a1 = fmaf(qa.y, bf16_hi(kv4.x), a1);
+          a0 = fmaf(qa.z, bf16_lo(kv4.y), a0); a1 = fmaf(qa.w, bf16_hi(kv4.y), a1);
+          a0 = fmaf(qb.x, bf16_lo(kv4.z), a0); a1 = fmaf(qb.y, bf16_hi(kv4.z), a1);
+          a0 = fmaf(qb.z, bf16_lo(kv4.w), a0); a1 = fmaf(qb.w, bf16_hi(kv4.w), a1);
+        }
+        acc = (a0 + a1) * p.h.scale_log2;
+      }
+      sc[r] = acc;
+      mx = fmaxf(mx, acc);
+    }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (lane == 0) red[0][warp] = mx;
-    __syncthreads();
-    const float Mx = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
-    // weights and normaliser
     float lsum = 0.0f;
-    for (int64_t i = tid; i < count; i += 128) {
-      const float mi = base[i * stride + 128];
-      const float w = (mi == -INFINITY) ? 0.0f : exp2f(mi - Mx);
-      wts[i] = w;
-      lsum = fmaf(w, base[i * stride + 129], lsum);
-    }
-    if (tid == 0) {
-      const float w = (win_m[h] == -INFINITY) ? 0.0f : exp2f(win_m[h] - Mx);
-      wts[kCombineMaxPartials] = w;
-      lsum = fmaf(w, win_l[h], lsum);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int t = lane + 32 * r;
+      const float pt = (t < wlen) ? exp2f(sc[r] - mx) : 0.0f;
+      pw[h][t] = pt;
+      lsum += pt;
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-    if (lane == 0) red[1][warp] = lsum;
-    __syncthreads();
-    const float Lt = red[1][0] + red[1][1] + red[1][2] + red[1][3];
-    // weighted sum: thread = channel, independent loads across partials
-    float acc = wts[kCombineMaxPartials] * win_o[h][tid];
-    int64_t i = 0;
-    for (; i + 4 <= count; i += 4) {
-      const float x0 = base[(i + 0) * stride + tid];
-      const float x1 = base[(i + 1) * stride + tid];
-      const float x2 = base[(i + 2) * stride + tid];
-      const float x3 = base[(i + 3) * stride + tid];
-      acc = fmaf(wts[i], x0, acc);
-      acc = fmaf(wts[i + 1], x1, acc);
-      acc = fmaf(wts[i + 2], x2, acc);
-      acc = fmaf(wts[i + 3], x3, acc);
+    if (lane == 0) {
+      win_m[h] = (wlen > 0) ? mx : -INFINITY;
+      win_l[h] = lsum;
     }
-    for (; i < count; ++i) acc = fmaf(wts[i], base[i * stride + tid], acc);
-    const float ov = acc / Lt;
+  }
+  __syncthreads();
+  float wo[kMaxGqa];                                 // thread = channel: window sum p_t v_t
+#pragma unroll
+  for (int h = 0; h < kMaxGqa; ++h) wo[h] = 0.0f;
+  for (int t = 0; t < wlen; ++t) {
+    const float v = __uint_as_float((uint32_t)wv[t * kHeadDim + tid] << 16);
+#pragma unroll
+    for (int h = 0; h < kMaxGqa; ++h) wo[h] = fmaf(pw[h][t], v, wo[h]);
+  }
+
+  // ---- merge: window state + partial records, chunk by chunk
+  float Mh[kMaxGqa], Lh[kMaxGqa], Oh[kMaxGqa];
+#pragma unroll
+  for (int h = 0; h < kMaxGqa; ++h) {
+    Mh[h] = (h < gqa) ? win_m[h] : -INFINITY;
+    Lh[h] = (h < gqa) ? win_l[h] : 0.0f;
+    Oh[h] = wo[h];
+  }
+  for (int64_t ck = 0; ck < nchunks; ++ck) {
+    const int64_t c0 = ck * per_chunk;
+    const int n = (int)((count - c0) < per_chunk ? (count - c0) : per_chunk);
+    if (ck > 0) {
+      __syncthreads();                               // everyone done with the previous chunk
+      if (tid == 0) {
+        mbar_arrive_expect_tx(&bar, (uint32_t)(n * rec_bytes));
+        bulk_g2s(part, p.h.partials + (first + rho + c0) * (int64_t)gqa * kPartialFloats, (uint32_t)(n * rec_bytes),
+                 &bar);
+      }
+      mbar_wait_bounded(&bar, (uint32_t)(ck & 1), &abort_flag, p.h.err_word);
+    }
+#pragma unroll
+    for (int h = 0; h < kMaxGqa; ++h) {
+      if (h >= gqa) break;
+      float mx = -INFINITY;
+      for (int i = tid; i < n; i += kCombineThreads) mx = fmaxf(mx, part[(i * gqa + h) * kPartialFloats + 128]);
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      if (lane == 0) red[0][warp] = mx;
+      __syncthreads();
+      const float Mc = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
+      const float Mn = fmaxf(Mh[h], Mc);
+      float lsum = 0.0f;
+      for (int i = tid; i < n; i += kCombineThreads) {
+        const float mi = part[(i * gqa + h) * kPartialFloats + 128];
+        const float w = (mi == -INFINITY) ? 0.0f : exp2f(mi - Mn);
+        wts[i] = w;
+        lsum = fmaf(w, part[(i * gqa + h) * kPartialFloats + 129], lsum);
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+      if (lane == 0) red[1][warp] = lsum;
+      __syncthreads();
+      const float Lc = red[1][0] + red[1][1] + red[1][2] + red[1][3];
+      const float a = (Mh[h] == -INFINITY) ? 0.0f : exp2f(Mh[h] - Mn);
+      float acc = Oh[h] * a;
+      for (int i = 0; i < n; ++i) acc = fmaf(wts[i], part[(i * gqa + h) * kPartialFloats + tid], acc);
+      Oh[h] = acc;
+      Lh[h] = Lh[h] * a + Lc;
+      Mh[h] = Mn;
+      __syncthreads();                               // wts / red reused
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < kMaxGqa; ++h) {
+    if (h >= gqa) break;
+    const float ov = Oh[h] / Lh[h];
     p.h.out[((int64_t)b * p.h.hq + j * gqa + h) * kHeadDim + tid] = (uint16_t)f32_to_bf16_bits(ov);
-    __syncthreads();   // wts / red reused by the next head
   }
 }
 
 }  // namespace
 
-int decode_int2_ctas_per_sm() { return 2; }
+int decode_int2_ctas_per_sm() { return kCtasPerSm; }
 
 int num_sms(int device) {
   int n = 0;
@@ -602,7 +703,10 @@ cudaError_t launch_decode_int2(const DecodeParams<MAXS>& p, const uint8_t* arena
 
 template <int MAXS>
 cudaError_t launch_combine(const DecodeParams<MAXS>& p, const uint8_t* arena, cudaStream_t stream) {
-  combine_kernel<MAXS><<<p.h.n_seqs * p.h.hkv, 128, 0, stream>>>(p, arena);
+  static bool attr_done[64] = {};
+  cudaError_t e = ensure_smem_attr(combine_kernel<MAXS>, kCombineSmem, attr_done);
+  if (e != cudaSuccess) return e;
+  combine_kernel<MAXS><<<p.h.n_seqs * p.h.hkv, kCombineThreads, kCombineSmem, stream>>>(p, arena);
   return cudaGetLastError();
 }
 
