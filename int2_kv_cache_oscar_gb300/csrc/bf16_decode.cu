@@ -258,7 +258,8 @@ __global__ void __launch_bounds__(kThreadsB, 2)
     named_bar_sync(1, kConsumersB * 32);
     k = k_end;
     u = seg_end;
-  }
+  }  // this CTA's partials are written: let the dependent combine launch
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 }  // namespace

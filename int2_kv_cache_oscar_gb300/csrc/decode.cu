@@ -35,8 +35,8 @@ namespace {
 
 constexpr int kConsumers = 4;
 constexpr int kDecThreads = (kConsumers + 1) * 32;
-constexpr int kStages = 4;
-constexpr int kCtasPerSm = 3;
+constexpr int kStages = 7;
+constexpr int kCtasPerSm = 2;
 constexpr int kPbStride = kGroup + 8;  // probability rows, padded against bank conflicts
 
 struct DecSmem {
@@ -477,22 +477,28 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     named_bar_sync(1, kConsumers * 32);
     k = k_end;
     u = seg_end;
-  }
+  }  // this CTA's partials are written: let the dependent combine launch
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- combine
-// One CTA per (sequence, KV head), 128 threads.  A bulk copy stages the bf16
-// window rows (keys then values) and the row's split-K partial records
-// (contiguous slots) in shared memory; everything after that runs from shared
-// memory:
-//   window: warp h scores query head h against the window tokens (lane =
-//           token, rotated 16-byte chunk order against bank conflicts),
-//           softmax in-warp, then thread = channel sums p_t v_t;
+// One CTA per (sequence, KV head), 128 threads per query head (thread = one
+// (head, channel) output).  It is launched as a programmatic dependent of the
+// main kernel: the setup overlaps the main kernel's tail and griddepcontrol.wait
+// guards every read of its partials.  A bulk copy stages the bf16 window rows
+// (keys then values) and the row's split-K partial records (contiguous slots)
+// in shared memory; everything after that runs from shared memory:
+//   window: the 4 warps of head h score 32 window tokens each (lane = token,
+//           rotated 16-byte chunk order against bank conflicts); thread
+//           (h, c) then sums p_t v_t;
 //   merge:  m* = max(m_window, m_i), o = (sum 2^(m_i - m*) o_i) /
 //           (sum 2^(m_i - m*) l_i), written as bf16.
-constexpr int kCombineThreads = 128;
+constexpr int kCombineThreads = 128 * kMaxGqa;
 constexpr int kCombinePartBytes = 96 * 1024;   // partial records staged per chunk
 constexpr int kCombineSmem = kWindowBytes + kCombinePartBytes;
+constexpr int kCombineMaxChunk = kCombinePartBytes / (kPartialFloats * 4);
+
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 template <int MAXS>
 __global__ void __launch_bounds__(kCombineThreads)
@@ -503,17 +509,22 @@ __global__ void __launch_bounds__(kCombineThreads)
   float* part = reinterpret_cast<float*>(smem_raw + kWindowBytes);      // partial records
   __shared__ __align__(16) float qs[kMaxGqa][kHeadDim];
   __shared__ float pw[kMaxGqa][kGroup];                                 // window probabilities
-  __shared__ float wts[kCombinePartBytes / (kPartialFloats * 4)];
-  __shared__ float red[2][4];
+  __shared__ float wts[kMaxGqa][kCombineMaxChunk];
+  __shared__ float red[kMaxGqa][2][4];
   __shared__ float win_m[kMaxGqa], win_l[kMaxGqa];
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
 
   const int b = blockIdx.x / p.h.hkv;
   const int j = blockIdx.x % p.h.hkv;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x;
+  const int h = tid >> 7;            // query head within the group
+  const int c = tid & 127;           // channel
+  const int wih = c >> 5;            // warp within the head
+  const int lane = tid & 31;
   const DecodeSeq sq = p.seq[b];
   const int hkv = p.h.hkv, gqa = p.h.gqa;
+  const bool active = h < gqa;
   const int ng = units_of_len(sq.len, p.h.bf16_mode);
   const int wlen = p.h.bf16_mode ? 0 : (sq.len % kGroup);
   const int64_t T = p.h.n_units, N = p.h.n_ctas;
@@ -533,16 +544,10 @@ __global__ void __launch_bounds__(kCombineThreads)
     abort_flag = 0;
     fence_mbar_init();
   }
-  for (int i = tid; i < kMaxGqa * kHeadDim / 4; i += kCombineThreads) {
-    const int h = i / (kHeadDim / 4), c4 = i % (kHeadDim / 4);
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (h < gqa) {
-      const uint2 r = *reinterpret_cast<const uint2*>(p.h.q + ((int64_t)b * p.h.hq + j * gqa + h) * kHeadDim + 4 * c4);
-      v = make_float4(bf16_lo(r.x), bf16_hi(r.x), bf16_lo(r.y), bf16_hi(r.y));
-    }
-    *reinterpret_cast<float4*>(&qs[h][4 * c4]) = v;
-  }
+  qs[h][c] = active ? __uint_as_float((uint32_t)p.h.q[((int64_t)b * p.h.hq + j * gqa + h) * kHeadDim + c] << 16)
+                    : 0.0f;
   __syncthreads();
+  grid_dependency_wait();            // the main kernel's partials are complete and visible
   // stage 0: window rows + first chunk of partials
   if (tid == 0) {
     const int64_t n0 = count < per_chunk ? count : per_chunk;
@@ -562,68 +567,59 @@ __global__ void __launch_bounds__(kCombineThreads)
   }
   mbar_wait_bounded(&bar, 0, &abort_flag, p.h.err_word);
 
-  // ---- window attention (warp h = query head h; lane = token)
-  if (warp < gqa) {
-    const int h = warp;
-    float sc[4];
-    float mx = -INFINITY;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int t = lane + 32 * r;
-      float acc = -INFINITY;
-      if (t < wlen) {
-        float a0 = 0.f, a1 = 0.f;
+  // ---- window attention: warp wih of head h scores tokens 32 wih + lane
+  float mxw = -INFINITY;
+  float scw = -INFINITY;
+  if (active) {
+    const int t = 32 * wih + lane;
+    if (t < wlen) {
+      float a0 = 0.f, a1 = 0.f;
 #pragma unroll 4
-        for (int i = 0; i < 16; ++i) {
-          const int ch = (i + lane) & 15;                       // rotated 16-byte chunk
-          const uint4 kv4 = *reinterpret_cast<const uint4*>(wk + t * kHeadDim + 8 * ch);
-          const float4 qa = *reinterpret_cast<const float4*>(&qs[h][8 * ch]);
-          const float4 qb = *reinterpret_cast<const float4*>(&qs[h][8 * ch + 4]);
-          a0 = fmaf(qa.x, bf16_lo(kv4.x), a0); a1 = fmaf(qa.y, bf16_hi(kv4.x), a1);
-          a0 = fmaf(qa.z, bf16_lo(kv4.y), a0); a1 = fmaf(qa.w, bf16_hi(kv4.y), a1);
-          a0 = fmaf(qb.x, bf16_lo(kv4.z), a0); a1 = fmaf(qb.y, bf16_hi(kv4.z), a1);
-          a0 = fmaf(qb.z, bf16_lo(kv4.w), a0); a1 = fmaf(qb.w, bf16_hi(kv4.w), a1);
-        }
-        acc = (a0 + a1) * p.h.scale_log2;
+      for (int i = 0; i < 16; ++i) {
+        const int ch = (i + lane) & 15;                       // rotated 16-byte chunk
+        const uint4 kv4 = *reinterpret_cast<const uint4*>(wk + t * kHeadDim + 8 * ch);
+        const float4 qa = *reinterpret_cast<const float4*>(&qs[h][8 * ch]);
+        const float4 qb = *reinterpret_cast<const float4*>(&qs[h][8 * ch + 4]);
+        a0 = fmaf(qa.x, bf16_lo(kv4.x), a0); a1 = fmaf(qa.y, bf16_hi(kv4.x), a1);
+        a0 = fmaf(qa.z, bf16_lo(kv4.y), a0); a1 = fmaf(qa.w, bf16_hi(kv4.y), a1);
+        a0 = fmaf(qb.x, bf16_lo(kv4.z), a0); a1 = fmaf(qb.y, bf16_hi(kv4.z), a1);
+        a0 = fmaf(qb.z, bf16_lo(kv4.w), a0); a1 = fmaf(qb.w, bf16_hi(kv4.w), a1);
       }
-      sc[r] = acc;
-      mx = fmaxf(mx, acc);
+      scw = (a0 + a1) * p.h.scale_log2;
     }
+    mxw = scw;
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    float lsum = 0.0f;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int t = lane + 32 * r;
-      const float pt = (t < wlen) ? exp2f(sc[r] - mx) : 0.0f;
-      pw[h][t] = pt;
-      lsum += pt;
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-    if (lane == 0) {
-      win_m[h] = (wlen > 0) ? mx : -INFINITY;
-      win_l[h] = lsum;
-    }
+    for (int off = 16; off >= 1; off >>= 1) mxw = fmaxf(mxw, __shfl_xor_sync(0xffffffffu, mxw, off));
+    if (lane == 0) red[h][0][wih] = mxw;
   }
   __syncthreads();
-  float wo[kMaxGqa];                                 // thread = channel: window sum p_t v_t
+  if (active) {
+    const float M = fmaxf(fmaxf(red[h][0][0], red[h][0][1]), fmaxf(red[h][0][2], red[h][0][3]));
+    const int t = 32 * wih + lane;
+    const float pt = (t < wlen) ? exp2f(scw - M) : 0.0f;
+    pw[h][t] = pt;
+    float ls = pt;
 #pragma unroll
-  for (int h = 0; h < kMaxGqa; ++h) wo[h] = 0.0f;
-  for (int t = 0; t < wlen; ++t) {
-    const float v = __uint_as_float((uint32_t)wv[t * kHeadDim + tid] << 16);
-#pragma unroll
-    for (int h = 0; h < kMaxGqa; ++h) wo[h] = fmaf(pw[h][t], v, wo[h]);
+    for (int off = 16; off >= 1; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
+    if (lane == 0) red[h][1][wih] = ls;
+    if (c == 0) win_m[h] = (wlen > 0) ? M : -INFINITY;
+  }
+  __syncthreads();
+  float Mh = -INFINITY, Lh = 0.0f, Oh = 0.0f;
+  if (active) {
+    Mh = win_m[h];
+    Lh = red[h][1][0] + red[h][1][1] + red[h][1][2] + red[h][1][3];
+    float o0 = 0.f, o1 = 0.f;
+    int t = 0;
+    for (; t + 2 <= wlen; t += 2) {
+      o0 = fmaf(pw[h][t], __uint_as_float((uint32_t)wv[t * kHeadDim + c] << 16), o0);
+      o1 = fmaf(pw[h][t + 1], __uint_as_float((uint32_t)wv[(t + 1) * kHeadDim + c] << 16), o1);
+    }
+    if (t < wlen) o0 = fmaf(pw[h][t], __uint_as_float((uint32_t)wv[t * kHeadDim + c] << 16), o0);
+    Oh = o0 + o1;
   }
 
-  // ---- merge: window state + partial records, chunk by chunk
-  float Mh[kMaxGqa], Lh[kMaxGqa], Oh[kMaxGqa];
-#pragma unroll
-  for (int h = 0; h < kMaxGqa; ++h) {
-    Mh[h] = (h < gqa) ? win_m[h] : -INFINITY;
-    Lh[h] = (h < gqa) ? win_l[h] : 0.0f;
-    Oh[h] = wo[h];
-  }
+  // ---- merge: window state + partial records, chunk by chunk (heads in parallel)
   for (int64_t ck = 0; ck < nchunks; ++ck) {
     const int64_t c0 = ck * per_chunk;
     const int n = (int)((count - c0) < per_chunk ? (count - c0) : per_chunk);
@@ -636,43 +632,50 @@ __global__ void __launch_bounds__(kCombineThreads)
       }
       mbar_wait_bounded(&bar, (uint32_t)(ck & 1), &abort_flag, p.h.err_word);
     }
+    float mx = -INFINITY;
+    if (active)
+      for (int i = c; i < n; i += 128) mx = fmaxf(mx, part[(i * gqa + h) * kPartialFloats + 128]);
 #pragma unroll
-    for (int h = 0; h < kMaxGqa; ++h) {
-      if (h >= gqa) break;
-      float mx = -INFINITY;
-      for (int i = tid; i < n; i += kCombineThreads) mx = fmaxf(mx, part[(i * gqa + h) * kPartialFloats + 128]);
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      if (lane == 0) red[0][warp] = mx;
-      __syncthreads();
-      const float Mc = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
-      const float Mn = fmaxf(Mh[h], Mc);
-      float lsum = 0.0f;
-      for (int i = tid; i < n; i += kCombineThreads) {
+    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (active && lane == 0) red[h][0][wih] = mx;
+    __syncthreads();
+    float Mn = Mh;
+    if (active) {
+      const float Mc = fmaxf(fmaxf(red[h][0][0], red[h][0][1]), fmaxf(red[h][0][2], red[h][0][3]));
+      Mn = fmaxf(Mh, Mc);
+    }
+    float lsum = 0.0f;
+    if (active)
+      for (int i = c; i < n; i += 128) {
         const float mi = part[(i * gqa + h) * kPartialFloats + 128];
         const float w = (mi == -INFINITY) ? 0.0f : exp2f(mi - Mn);
-        wts[i] = w;
+        wts[h][i] = w;
         lsum = fmaf(w, part[(i * gqa + h) * kPartialFloats + 129], lsum);
       }
 #pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-      if (lane == 0) red[1][warp] = lsum;
-      __syncthreads();
-      const float Lc = red[1][0] + red[1][1] + red[1][2] + red[1][3];
-      const float a = (Mh[h] == -INFINITY) ? 0.0f : exp2f(Mh[h] - Mn);
-      float acc = Oh[h] * a;
-      for (int i = 0; i < n; ++i) acc = fmaf(wts[i], part[(i * gqa + h) * kPartialFloats + tid], acc);
-      Oh[h] = acc;
-      Lh[h] = Lh[h] * a + Lc;
-      Mh[h] = Mn;
-      __syncthreads();                               // wts / red reused
+    for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+    if (active && lane == 0) red[h][1][wih] = lsum;
+    __syncthreads();
+    if (active) {
+      const float Lc = red[h][1][0] + red[h][1][1] + red[h][1][2] + red[h][1][3];
+      const float a = (Mh == -INFINITY) ? 0.0f : exp2f(Mh - Mn);
+      float acc0 = Oh * a, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+      int i = 0;
+      for (; i + 4 <= n; i += 4) {
+        acc0 = fmaf(wts[h][i], part[((i + 0) * gqa + h) * kPartialFloats + c], acc0);
+        acc1 = fmaf(wts[h][i + 1], part[((i + 1) * gqa + h) * kPartialFloats + c], acc1);
+        acc2 = fmaf(wts[h][i + 2], part[((i + 2) * gqa + h) * kPartialFloats + c], acc2);
+        acc3 = fmaf(wts[h][i + 3], part[((i + 3) * gqa + h) * kPartialFloats + c], acc3);
+      }
+      for (; i < n; ++i) acc0 = fmaf(wts[h][i], part[(i * gqa + h) * kPartialFloats + c], acc0);
+      Oh = (acc0 + acc1) + (acc2 + acc3);
+      Lh = Lh * a + Lc;
+      Mh = Mn;
     }
   }
-#pragma unroll
-  for (int h = 0; h < kMaxGqa; ++h) {
-    if (h >= gqa) break;
-    const float ov = Oh[h] / Lh[h];
-    p.h.out[((int64_t)b * p.h.hq + j * gqa + h) * kHeadDim + tid] = (uint16_t)f32_to_bf16_bits(ov);
+  if (active) {
+    const float ov = Oh / Lh;
+    p.h.out[((int64_t)b * p.h.hq + j * gqa + h) * kHeadDim + c] = (uint16_t)f32_to_bf16_bits(ov);
   }
 }
 
@@ -706,7 +709,19 @@ cudaError_t launch_combine(const DecodeParams<MAXS>& p, const uint8_t* arena, cu
   static bool attr_done[64] = {};
   cudaError_t e = ensure_smem_attr(combine_kernel<MAXS>, kCombineSmem, attr_done);
   if (e != cudaSuccess) return e;
-  combine_kernel<MAXS><<<p.h.n_seqs * p.h.hkv, kCombineThreads, kCombineSmem, stream>>>(p, arena);
+  // programmatic dependent launch: may start while the main kernel drains
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.h.n_seqs * p.h.hkv);
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = kCombineSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, combine_kernel<MAXS>, p, arena);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
