@@ -131,6 +131,23 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise max of per-rank timings over all ranks (replicas: the job
+    takes as long as its slowest rank).  Identity when not distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def replica_throughput(us_per_step: float, world: int, batch: int = 1) -> float:
+    """Whole-job decode tokens/s when every rank runs an independent replica."""
+    return world * batch / (us_per_step * 1e-6)
+
+
 # ------------------------------------------------------------- GPU arm
 
 class Timer:
@@ -512,11 +529,7 @@ def main():
 
     dec_us, e2e_us = res["dec_us"], res["e2e_us"]
     if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([dec_us, e2e_us, res["kern_us"]], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dec_us, e2e_us, kern = t.tolist()
-        res["kern_us"] = kern
+        dec_us, e2e_us, res["kern_us"] = max_over_ranks([dec_us, e2e_us, res["kern_us"]], device="cuda")
     if rank != 0:
         if world > 1:
             dist.barrier()
@@ -555,6 +568,7 @@ def main():
                      "frac_of_peak": round(res["quant_gbs"] / res["peak"], 3)},
         "e2e": {"value": round(e2e_us, 2), "unit": "us/step", "h2d_bytes_per_step": HQ * D * 2,
                 "d2h_bytes_per_step": HQ * D * 2},
+        "tokens_per_s": round(replica_throughput(dec_us, world)),
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
         "cpu_baseline": cpu,
