@@ -8,13 +8,15 @@
 // Values: per-token asymmetric INT2 over 32-channel groups (KIVI convention
 // cited in the qiita.com NOVA-KV article).
 //
-// One CTA = one (group, KV head); thread t owns token t of the group.
-//   1. V row of token t: per 32-channel group min/max, s = (max-min)/3, z = min,
-//      codes; codes go to shared memory (transposed), s/z to the block.
-//   2. K row of token t: 128 values in registers; unnormalised fast
-//      Walsh-Hadamard transform (7 butterfly stages, H_d = Hu / sqrt(128));
+// One CTA = one (group, KV head), 256 threads; the thread pair (2t, 2t+1)
+// owns token t, each thread 64 of its channels.
+//   1. V: per 32-channel group min/max, s = (max-min)/3, z = min, codes; codes
+//      go to shared memory (transposed), s/z to the block.
+//   2. K: unnormalised fast Walsh-Hadamard transform, H_d = Hu / sqrt(128):
+//      6 butterfly stages in registers, the 7th across the thread pair;
 //      n_t = sqrt(|Hu k|^2 / 128); k_hat = Hu k / |Hu k| (= H_d k / n_t).
-//   3. Per-channel min/max of k_hat over the 128 tokens (shared memory).
+//   3. Per-channel min/max of k_hat over the 128 tokens (shared memory,
+//      16-token slices, then 8 slices).
 //   4. Codes of k_hat, packed straight into the fragment-order words.
 //   5. Coalesced 16-byte stores of both code matrices.
 #include <cstddef>
@@ -25,13 +27,15 @@
 namespace oscar {
 namespace {
 
-constexpr int kQThreads = 128;
-constexpr int kKhStride = 132;  // floats per k_hat row in shared memory (padding vs bank conflicts)
-constexpr int kVbStride = 144;  // bytes per value-code row (channel) in shared memory
+constexpr int kQThreads = 256;   // two threads per token: channels [0, 64) and [64, 128)
+constexpr int kKhStride = 132;   // floats per k_hat row in shared memory (padding vs bank conflicts)
+constexpr int kVbStride = 144;   // bytes per value-code row (channel) in shared memory
 
 struct QuantSmem {
-  alignas(16) float kh[kGroup * kKhStride];          // k_hat[t][c]; float4 stores
+  alignas(16) float kh[kGroup * kKhStride];          // k_hat[t][c]; float4 stores / loads
   alignas(16) uint8_t vb[kHeadDim * kVbStride];      // value codes [channel][permuted token]; uint4 loads
+  alignas(16) float4 rmin[8][kHeadDim / 4];          // per 16-token slice: channel minima
+  alignas(16) float4 rmax[8][kHeadDim / 4];          // per 16-token slice: channel maxima
   alignas(16) uint32_t kw[1024];                     // key code words, fragment order; uint4 loads
   alignas(16) float2 kp[kHeadDim];                   // per-channel (1/s, z)
   float red[kQThreads / 32];
@@ -39,11 +43,12 @@ struct QuantSmem {
 static_assert(offsetof(QuantSmem, vb) % 16 == 0 && offsetof(QuantSmem, kw) % 16 == 0, "alignment");
 static_assert((kKhStride * 4) % 16 == 0 && kVbStride % 16 == 0, "rows must keep 16-byte alignment");
 
-// Round-half-even code of x against (inv = 1/s, z), clamped to [0, 3]; the
-// magic constant 1.5 * 2^23 leaves rne(v) in the low mantissa bits.
+// Round-half-even code of x against (inv = 1/s, z): v = fl32(fl32(x - z) * inv);
+// x >= z and x <= max keep v in [0, 3] (s == 0 gives inv = 0, v = 0), so no
+// clamp is needed; the magic constant 1.5 * 2^23 leaves rne(v) in the low
+// mantissa bits.
 __device__ __forceinline__ uint32_t int2_code(float x, float inv, float z) {
-  float v = (x - z) * inv;
-  v = fminf(fmaxf(v, 0.0f), 3.0f);
+  const float v = (x - z) * inv;
   return __float_as_uint(v + 12582912.0f) & 3u;
 }
 
@@ -54,11 +59,11 @@ __device__ __forceinline__ int vb_perm(int c) {
   return ((tig * 2 + j) * 4 + kk) * 4 + hf + 2 * e;
 }
 
-__device__ __forceinline__ void load_row(const uint16_t* src, float (&x)[kHeadDim]) {
+__device__ __forceinline__ void load64(const uint16_t* src, float (&x)[64]) {
   const uint4* s = reinterpret_cast<const uint4*>(src);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    uint4 u = __ldg(s + i);
+  for (int i = 0; i < 8; ++i) {
+    const uint4 u = __ldg(s + i);
     x[8 * i + 0] = bf16_lo(u.x);
     x[8 * i + 1] = bf16_hi(u.x);
     x[8 * i + 2] = bf16_lo(u.y);
@@ -87,63 +92,50 @@ __global__ void __launch_bounds__(kQThreads, 2)
 
   if (T.kind == 0) {
     uint8_t* blk = arena + plan.blocks_off + (sh * plan.max_groups + T.group) * (int64_t)kBlockBytes;
-    const int t = tid;
+    const int t = tid >> 1;          // token of the group
+    const int half = tid & 1;        // channels [64 half, 64 half + 64)
     const bool from_win = t < T.n_win;
     const int64_t row = (int64_t)T.in_row + (t - T.n_win);
-    const uint16_t* ksrc = from_win ? win_k + t * kHeadDim : kin + (row * hkv + head) * kHeadDim;
-    const uint16_t* vsrc = from_win ? win_v + t * kHeadDim : vin + (row * hkv + head) * kHeadDim;
+    const uint16_t* ksrc = (from_win ? win_k + t * kHeadDim : kin + (row * hkv + head) * kHeadDim) + 64 * half;
+    const uint16_t* vsrc = (from_win ? win_v + t * kHeadDim : vin + (row * hkv + head) * kHeadDim) + 64 * half;
 
-    // ---- values: per-token INT2 over 32-channel groups
+    // ---- values: per-token INT2 over this thread's two 32-channel groups
     float smax = 0.0f;
     {
+      float x[64];
+      load64(vsrc, x);
       const int pt = vb_perm(t);
-      float sv[kVGroups], zv[kVGroups];
+      float sv[2], zv[2];
 #pragma unroll
-      for (int gi = 0; gi < kVGroups; ++gi) {
-        float x[kVGroup];
-        const uint4* s4 = reinterpret_cast<const uint4*>(vsrc + gi * kVGroup);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint4 u = __ldg(s4 + i);
-          x[8 * i + 0] = bf16_lo(u.x);
-          x[8 * i + 1] = bf16_hi(u.x);
-          x[8 * i + 2] = bf16_lo(u.y);
-          x[8 * i + 3] = bf16_hi(u.y);
-          x[8 * i + 4] = bf16_lo(u.z);
-          x[8 * i + 5] = bf16_hi(u.z);
-          x[8 * i + 6] = bf16_lo(u.w);
-          x[8 * i + 7] = bf16_hi(u.w);
-        }
-        float mn = x[0], mx = x[0];
+      for (int g2 = 0; g2 < 2; ++g2) {
+        float mn = x[32 * g2], mx = x[32 * g2];
 #pragma unroll
         for (int i = 1; i < kVGroup; ++i) {
-          mn = fminf(mn, x[i]);
-          mx = fmaxf(mx, x[i]);
+          mn = fminf(mn, x[32 * g2 + i]);
+          mx = fmaxf(mx, x[32 * g2 + i]);
         }
-        const float s = (mx - mn) / 3.0f;
-        const float inv = s > 0.0f ? 1.0f / s : 0.0f;
-        sv[gi] = s;
-        zv[gi] = mn;
-        smax = fmaxf(smax, s);
+        const float sc = (mx - mn) / 3.0f;
+        const float inv = sc > 0.0f ? 1.0f / sc : 0.0f;
+        sv[g2] = sc;
+        zv[g2] = mn;
+        smax = fmaxf(smax, sc);
+        const int gi = 2 * half + g2;
 #pragma unroll
-        for (int i = 0; i < kVGroup; ++i) {
-          S.vb[(gi * kVGroup + i) * kVbStride + pt] = (uint8_t)int2_code(x[i], inv, mn);
-        }
+        for (int i = 0; i < kVGroup; ++i)
+          S.vb[(gi * kVGroup + i) * kVbStride + pt] = (uint8_t)int2_code(x[32 * g2 + i], inv, mn);
       }
-      float4* dsz = reinterpret_cast<float4*>(blk + kOffVSZ + 32 * t);
-      dsz[0] = make_float4(sv[0], sv[1], sv[2], sv[3]);
-      dsz[1] = make_float4(zv[0], zv[1], zv[2], zv[3]);
+      *reinterpret_cast<float2*>(blk + kOffVSZ + 32 * t + 8 * half) = make_float2(sv[0], sv[1]);
+      *reinterpret_cast<float2*>(blk + kOffVSZ + 32 * t + 16 + 8 * half) = make_float2(zv[0], zv[1]);
     }
 
-    // ---- keys: rotation, norm, unit vector
-    float x[kHeadDim];
-    load_row(ksrc, x);
-    // stage hb pairs index j (bit hb clear) with j + 2^hb; flat loops so that
-    // every index is a compile-time constant and x stays in registers
+    // ---- keys: rotation (6 butterfly stages in registers + 1 across the
+    // thread pair), norm, unit vector
+    float x[64];
+    load64(ksrc, x);
 #pragma unroll
-    for (int hb = 0; hb < 7; ++hb) {
+    for (int hb = 0; hb < 6; ++hb) {
 #pragma unroll
-      for (int n = 0; n < kHeadDim / 2; ++n) {
+      for (int n = 0; n < 32; ++n) {
         const int h = 1 << hb;
         const int j = ((n >> hb) << (hb + 1)) | (n & (h - 1));
         const float a = x[j], b = x[j + h];
@@ -151,78 +143,93 @@ __global__ void __launch_bounds__(kQThreads, 2)
         x[j + h] = a - b;
       }
     }
-    float sq[kHeadDim / 2];
 #pragma unroll
-    for (int i = 0; i < kHeadDim / 2; ++i) sq[i] = x[i] * x[i] + x[i + kHeadDim / 2] * x[i + kHeadDim / 2];
+    for (int i = 0; i < 64; ++i) {
+      const float y = __shfl_xor_sync(0xffffffffu, x[i], 1);   // the partner's channel i + 64 or i - 64
+      x[i] = half ? y - x[i] : x[i] + y;
+    }
+    float sq[32];
 #pragma unroll
-    for (int w = kHeadDim / 4; w >= 1; w >>= 1) {
+    for (int i = 0; i < 32; ++i) sq[i] = x[i] * x[i] + x[i + 32] * x[i + 32];
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
 #pragma unroll
       for (int i = 0; i < w; ++i) sq[i] += sq[i + w];
     }
-    const float ss = sq[0];
+    const float ss = sq[0] + __shfl_xor_sync(0xffffffffu, sq[0], 1);
     const float norm = sqrtf(ss * (1.0f / kHeadDim));
     const float rinv = ss > 0.0f ? 1.0f / sqrtf(ss) : 0.0f;
 #pragma unroll
-    for (int i = 0; i < kHeadDim; ++i) x[i] *= rinv;
-    reinterpret_cast<float*>(blk + kOffKNorm)[t] = norm;
+    for (int i = 0; i < 64; ++i) x[i] *= rinv;
+    if (half == 0) reinterpret_cast<float*>(blk + kOffKNorm)[t] = norm;
     {
-      float4* dst = reinterpret_cast<float4*>(&S.kh[t * kKhStride]);
+      float4* dst = reinterpret_cast<float4*>(&S.kh[t * kKhStride + 64 * half]);
 #pragma unroll
-      for (int i = 0; i < kHeadDim / 4; ++i) dst[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+      for (int i = 0; i < 16; ++i) dst[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
     }
-    // value-scale maximum of this group -> CTA maximum
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
     if ((tid & 31) == 0) S.red[tid >> 5] = smax;
     __syncthreads();
 
-    // ---- per-channel key parameters (thread = channel)
+    // ---- per-channel key parameters: 16-token slices of 4 channels, then 8 slices
     {
-      const int c = tid;
-      float mn = S.kh[c], mx = mn;
-#pragma unroll 8
-      for (int r = 1; r < kGroup; ++r) {
-        const float v = S.kh[r * kKhStride + c];
-        mn = fminf(mn, v);
-        mx = fmaxf(mx, v);
+      const int cq = tid & 31, ts = tid >> 5;
+      float4 mn = *reinterpret_cast<const float4*>(&S.kh[(16 * ts) * kKhStride + 4 * cq]);
+      float4 mx = mn;
+#pragma unroll
+      for (int r = 1; r < 16; ++r) {
+        const float4 v = *reinterpret_cast<const float4*>(&S.kh[(16 * ts + r) * kKhStride + 4 * cq]);
+        mn.x = fminf(mn.x, v.x); mn.y = fminf(mn.y, v.y); mn.z = fminf(mn.z, v.z); mn.w = fminf(mn.w, v.w);
+        mx.x = fmaxf(mx.x, v.x); mx.y = fmaxf(mx.y, v.y); mx.z = fmaxf(mx.z, v.z); mx.w = fmaxf(mx.w, v.w);
       }
-      const float s = (mx - mn) / 3.0f;
-      S.kp[c] = make_float2(s > 0.0f ? 1.0f / s : 0.0f, mn);
-      reinterpret_cast<float*>(blk + kOffKScale)[c] = s;
+      S.rmin[ts][cq] = mn;
+      S.rmax[ts][cq] = mx;
+    }
+    __syncthreads();
+    if (tid < kHeadDim) {
+      const int c = tid;
+      const float* rmn = reinterpret_cast<const float*>(S.rmin);
+      const float* rmx = reinterpret_cast<const float*>(S.rmax);
+      float mn = rmn[c], mx = rmx[c];
+#pragma unroll
+      for (int ts = 1; ts < 8; ++ts) {
+        mn = fminf(mn, rmn[ts * kHeadDim + c]);
+        mx = fmaxf(mx, rmx[ts * kHeadDim + c]);
+      }
+      const float sc = (mx - mn) / 3.0f;
+      S.kp[c] = make_float2(sc > 0.0f ? 1.0f / sc : 0.0f, mn);
+      reinterpret_cast<float*>(blk + kOffKScale)[c] = sc;
       reinterpret_cast<float*>(blk + kOffKZero)[c] = mn;
     }
     __syncthreads();
 
-    // ---- key codes of token t, packed into its 8 fragment-order words
+    // ---- key codes of token t, channels of half: the 4 fragment words with j = half
     {
       const int mt = t >> 4, g = t & 7, r = (t >> 3) & 1;
 #pragma unroll
       for (int tig = 0; tig < 4; ++tig) {
+        uint32_t w = 0;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          uint32_t w = 0;
+        for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
+          for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int c = 16 * (4 * j + kk) + 8 * hf + 2 * tig + e;
-                const float2 p = S.kp[c];
-                w |= int2_code(x[c], p.x, p.y) << (16 * e + 4 * kk + 2 * hf);
-              }
+            for (int e = 0; e < 2; ++e) {
+              const int i = 16 * kk + 8 * hf + 2 * tig + e;    // channel 64 half + i
+              const float2 pq = S.kp[64 * half + i];
+              w |= int2_code(x[i], pq.x, pq.y) << (16 * e + 4 * kk + 2 * hf);
             }
           }
-          S.kw[((mt * 32 + 4 * g + tig) * 4) + 2 * j + r] = w;
         }
+        S.kw[((mt * 32 + 4 * g + tig) * 4) + 2 * half + r] = w;
       }
     }
     __syncthreads();
 
     // ---- coalesced stores of both code matrices (256 x 16 B each)
-#pragma unroll
-    for (int rep = 0; rep < 2; ++rep) {
-      const int u = tid + rep * kQThreads;
+    {
+      const int u = tid;
       reinterpret_cast<uint4*>(blk + kOffKCodes)[u] = reinterpret_cast<const uint4*>(S.kw)[u];
       const int mt = u >> 5, lane = u & 31, g = lane >> 2, tig = lane & 3;
       uint32_t wv[4];
