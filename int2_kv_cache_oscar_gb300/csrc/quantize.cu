@@ -30,27 +30,44 @@ namespace {
 constexpr int kQThreads = 256;   // two threads per token: channels [0, 64) and [64, 128)
 constexpr int kKhStride = 132;   // floats per k_hat row in shared memory (padding vs bank conflicts)
 constexpr int kVbStride = 144;   // bytes per value-code row (channel) in shared memory
+constexpr int kKrawOffset = 128 * kKhStride * 4 - 128 * 256;   // raw K rows at the end of the k_hat buffer
 
 struct QuantSmem {
   alignas(16) float kh[kGroup * kKhStride];          // k_hat[t][c]; float4 stores / loads
-  alignas(16) uint8_t vb[kHeadDim * kVbStride];      // value codes [channel][permuted token]; uint4 loads
+  alignas(16) uint8_t vb[kHeadDim * kVbStride + 16];  // value codes [channel][permuted token]; uint4 loads
   alignas(16) float4 rmin[8][kHeadDim / 4];          // per 16-token slice: channel minima
   alignas(16) float4 rmax[8][kHeadDim / 4];          // per 16-token slice: channel maxima
   alignas(16) uint32_t kw[1024];                     // key code words, fragment order; uint4 loads
-  alignas(16) float2 kp[kHeadDim];                   // per-channel (1/s, z)
+  alignas(16) float2 kp[kHeadDim + 4];               // per-channel (1/s, z), see kp_index
   float red[kQThreads / 32];
 };
 static_assert(offsetof(QuantSmem, vb) % 16 == 0 && offsetof(QuantSmem, kw) % 16 == 0, "alignment");
 static_assert((kKhStride * 4) % 16 == 0 && kVbStride % 16 == 0, "rows must keep 16-byte alignment");
 
-// Round-half-even code of x against (inv = 1/s, z): v = fl32(fl32(x - z) * inv);
+// Round-half-even code of x against (inv = 1/s, z): v = fl32(fl32(x - z) * inv)
+// (the product is rounded before the integer rounding, as the decision rule
+// specifies);
 // x >= z and x <= max keep v in [0, 3] (s == 0 gives inv = 0, v = 0), so no
 // clamp is needed; the magic constant 1.5 * 2^23 leaves rne(v) in the low
 // mantissa bits.
 __device__ __forceinline__ uint32_t int2_code(float x, float inv, float z) {
-  const float v = (x - z) * inv;
+  const float v = __fmul_rn(x - z, inv);   // rounded product; never contracted into the add
   return __float_as_uint(v + 12582912.0f) & 3u;
 }
+
+// Byte offset of value-code row (channel) c: rows of the upper 64 channels are
+// shifted by 16 bytes so that the two threads of a token (one per channel
+// half) store into different banks.
+__device__ __forceinline__ int vb_row(int c) { return c * kVbStride + ((c >> 6) << 4); }
+
+// Index of channel c in the (1/s, z) table: the upper half is shifted by 4
+// entries (32 bytes) for the same reason.
+__device__ __forceinline__ int kp_index(int c) { return c + ((c >> 6) << 2); }
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Position of token/col c inside its 16-byte packing chunk of the byte
 // staging area: chunk (tig, j), byte ((kk * 4) + hf + 2 e).
@@ -99,6 +116,13 @@ __global__ void __launch_bounds__(kQThreads, 2)
     const uint16_t* ksrc = (from_win ? win_k + t * kHeadDim : kin + (row * hkv + head) * kHeadDim) + 64 * half;
     const uint16_t* vsrc = (from_win ? win_v + t * kHeadDim : vin + (row * hkv + head) * kHeadDim) + 64 * half;
 
+    // raw K rows (bf16, 256 B each) -> upper half of the k_hat buffer, in
+    // flight while the values are processed
+    uint8_t* kraw = reinterpret_cast<uint8_t*>(S.kh) + kKrawOffset;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cp_async16(kraw + t * 256 + 128 * half + 16 * i, ksrc + 8 * i);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+
     // ---- values: per-token INT2 over this thread's two 32-channel groups
     float smax = 0.0f;
     {
@@ -122,7 +146,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
         const int gi = 2 * half + g2;
 #pragma unroll
         for (int i = 0; i < kVGroup; ++i)
-          S.vb[(gi * kVGroup + i) * kVbStride + pt] = (uint8_t)int2_code(x[32 * g2 + i], inv, mn);
+          S.vb[vb_row(gi * kVGroup + i) + pt] = (uint8_t)int2_code(x[32 * g2 + i], inv, mn);
       }
       *reinterpret_cast<float2*>(blk + kOffVSZ + 32 * t + 8 * half) = make_float2(sv[0], sv[1]);
       *reinterpret_cast<float2*>(blk + kOffVSZ + 32 * t + 16 + 8 * half) = make_float2(zv[0], zv[1]);
@@ -131,7 +155,24 @@ __global__ void __launch_bounds__(kQThreads, 2)
     // ---- keys: rotation (6 butterfly stages in registers + 1 across the
     // thread pair), norm, unit vector
     float x[64];
-    load64(ksrc, x);
+    cp_async_wait_all();
+    __syncthreads();                   // every thread's raw K row is in shared memory
+    {
+      const uint4* s4 = reinterpret_cast<const uint4*>(kraw + t * 256 + 128 * half);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 u = s4[i];
+        x[8 * i + 0] = bf16_lo(u.x);
+        x[8 * i + 1] = bf16_hi(u.x);
+        x[8 * i + 2] = bf16_lo(u.y);
+        x[8 * i + 3] = bf16_hi(u.y);
+        x[8 * i + 4] = bf16_lo(u.z);
+        x[8 * i + 5] = bf16_hi(u.z);
+        x[8 * i + 6] = bf16_lo(u.w);
+        x[8 * i + 7] = bf16_hi(u.w);
+      }
+    }
+    __syncthreads();                   // raw rows read before k_hat rows overwrite them
 #pragma unroll
     for (int hb = 0; hb < 6; ++hb) {
 #pragma unroll
@@ -198,7 +239,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
         mx = fmaxf(mx, rmx[ts * kHeadDim + c]);
       }
       const float sc = (mx - mn) / 3.0f;
-      S.kp[c] = make_float2(sc > 0.0f ? 1.0f / sc : 0.0f, mn);
+      S.kp[kp_index(c)] = make_float2(sc > 0.0f ? 1.0f / sc : 0.0f, mn);
       reinterpret_cast<float*>(blk + kOffKScale)[c] = sc;
       reinterpret_cast<float*>(blk + kOffKZero)[c] = mn;
     }
@@ -217,7 +258,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const int i = 16 * kk + 8 * hf + 2 * tig + e;    // channel 64 half + i
-              const float2 pq = S.kp[64 * half + i];
+              const float2 pq = S.kp[kp_index(64 * half + i)];
               w |= int2_code(x[i], pq.x, pq.y) << (16 * e + 4 * kk + 2 * hf);
             }
           }
@@ -238,7 +279,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const int rowc = 16 * mt + g + 8 * r;
-          const uint4 b = *reinterpret_cast<const uint4*>(&S.vb[rowc * kVbStride + (tig * 2 + j) * 16]);
+          const uint4 b = *reinterpret_cast<const uint4*>(&S.vb[vb_row(rowc) + (tig * 2 + j) * 16]);
           const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
           uint32_t w = 0;
 #pragma unroll
