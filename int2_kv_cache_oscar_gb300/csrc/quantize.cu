@@ -117,10 +117,12 @@ __global__ void __launch_bounds__(kQThreads, 2)
     const uint16_t* vsrc = (from_win ? win_v + t * kHeadDim : vin + (row * hkv + head) * kHeadDim) + 64 * half;
 
     // raw K rows (bf16, 256 B each) -> upper half of the k_hat buffer, in
-    // flight while the values are processed
+    // flight while the values are processed; chunk i of a thread's 128 bytes
+    // is stored at slot (i + t) mod 8 so that a warp's 16-byte accesses
+    // spread over all bank groups
     uint8_t* kraw = reinterpret_cast<uint8_t*>(S.kh) + kKrawOffset;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) cp_async16(kraw + t * 256 + 128 * half + 16 * i, ksrc + 8 * i);
+    for (int i = 0; i < 8; ++i) cp_async16(kraw + t * 256 + 128 * half + 16 * ((i + t) & 7), ksrc + 8 * i);
     asm volatile("cp.async.commit_group;" ::: "memory");
 
     // ---- values: per-token INT2 over this thread's two 32-channel groups
@@ -161,7 +163,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
       const uint4* s4 = reinterpret_cast<const uint4*>(kraw + t * 256 + 128 * half);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const uint4 u = s4[i];
+        const uint4 u = s4[(i + t) & 7];   // 16-byte chunks rotated by token: 8 bank groups per warp
         x[8 * i + 0] = bf16_lo(u.x);
         x[8 * i + 1] = bf16_hi(u.x);
         x[8 * i + 2] = bf16_lo(u.y);
