@@ -3,12 +3,17 @@
 // It stands in for the pages' comparator, BF16 FlashDecoding-v2 (ai-papers.net
 // summary, section "実験結果"), to give the INT2/BF16 speed ratio on this GPU.
 //
-// Producer warp: 1-D bulk copies of 64-token K and V tiles (16 KB each) into
-// a 3-stage ring.  Consumer warp: 8 lanes per token (16 channels each), 4
-// tokens per step; fp32 dot products reduced with 3 shuffles, online softmax
-// with a lazy rescale (the running max is only raised when a score exceeds it
-// by more than 2^8, so p <= 256), fp32 P.V.
+//   * producer warp: 2-D TMA (cp.async.bulk.tensor, 128-byte swizzle) of
+//     64-token K and V tiles, two 64x64 boxes each, into a 3-stage ring;
+//   * consumer warp (every 4th tile): scores S^T = K q^T on the tensor cores
+//     (mma.sync m16n8k16 bf16, A = K via ldmatrix, B = q, 4 of 8 columns
+//     used), online softmax in fp32 (log2 domain), then O^T = V^T P^T with
+//     A = V^T via ldmatrix.trans and B = P split into bf16 hi + lo columns
+//     (4 heads x {hi, lo} = 8 columns); accumulators restart every tile and
+//     are added into fp32 registers.
 #include <cstddef>
+
+#include <cudaTypedefs.h>
 
 #include "decode_common.cuh"
 
@@ -19,11 +24,13 @@ constexpr int kConsumersB = 4;
 constexpr int kThreadsB = (kConsumersB + 1) * 32;
 constexpr int kStagesB = 3;
 constexpr int kTile = 64;
-constexpr int kTileBytes = kTile * kHeadDim * 2;
+constexpr int kBoxBytes = 64 * 128;            // 64 rows x 64 bf16 channels
+constexpr int kStageBytesB = 4 * kBoxBytes;    // K box 0, K box 1, V box 0, V box 1
+constexpr int kPbStrideB = kTile + 4;
 
 struct Bf16Smem {
-  alignas(128) uint8_t k[kStagesB][kTileBytes];
-  alignas(128) uint8_t v[kStagesB][kTileBytes];
+  alignas(1024) uint8_t stage[kStagesB][kStageBytesB];
+  alignas(16) float pbuf[kConsumersB][kMaxGqa][kPbStrideB];
   alignas(16) float ost[kConsumersB][kMaxGqa][kHeadDim];
   float mst[kConsumersB][kMaxGqa];
   float lst[kConsumersB][kMaxGqa];
@@ -32,30 +39,68 @@ struct Bf16Smem {
   uint32_t issued[kStagesB];   // uses of each stage issued so far (producer -> consumers)
   int abort_flag;
 };
-static_assert(offsetof(Bf16Smem, v) % 16 == 0, "bulk-copy destinations must be 16-byte aligned");
+static_assert(kStageBytesB % 1024 == 0, "128-byte-swizzled boxes need 1024-byte alignment");
 static_assert(offsetof(Bf16Smem, full) % 8 == 0, "mbarriers must be 8-byte aligned");
 
-__device__ __forceinline__ void unpack8(const uint4 u, float* x) {
-  x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x); x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
-  x[4] = bf16_lo(u.z); x[5] = bf16_hi(u.z); x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
 }
 
-// 16 bf16 of one row chunk; lanes with sw = 1 read the upper 16 bytes first so
-// that the 8 lanes of a token hit 8 distinct bank groups.
-__device__ __forceinline__ void load16(const uint8_t* src, int sw, float* x) {
-  const uint4* r = reinterpret_cast<const uint4*>(src);
-  const uint4 c0 = r[sw], c1 = r[sw ^ 1];
-  const uint4 lo = sw ? c1 : c0, hi = sw ? c0 : c1;
-  unpack8(lo, &x[0]);
-  unpack8(hi, &x[8]);
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Byte offset of row r, 16-byte chunk ch inside a 128-byte-swizzled 64x128 B box.
+__device__ __forceinline__ uint32_t swz(int r, int ch) { return (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4)); }
+
+// Partner-lane bf16 hi/lo split (see the INT2 kernel): lanes g = 2h (hi
+// column) and g = 2h + 1 (lo column) each split one pair and swap halves.
+__device__ __forceinline__ void split_exchange_bf16(float x0, float x1, bool lo_lane, uint32_t& b0, uint32_t& b1) {
+  const uint32_t hi = pack_bf16x2(x0, x1);
+  const float r0 = x0 - __uint_as_float(hi << 16);
+  const float r1 = x1 - __uint_as_float(hi & 0xffff0000u);
+  const uint32_t lo = pack_bf16x2(r0, r1);
+  const uint32_t send = lo_lane ? hi : lo;
+  const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 4);
+  b0 = lo_lane ? recv : hi;
+  b1 = lo_lane ? lo : recv;
 }
 
 template <int MAXS>
 __global__ void __launch_bounds__(kThreadsB, 2)
-    decode_bf16_kernel(const __grid_constant__ DecodeParams<MAXS> p, const uint16_t* __restrict__ kc,
-                       const uint16_t* __restrict__ vc) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  Bf16Smem& S = *reinterpret_cast<Bf16Smem*>(smem_raw);
+    decode_bf16_kernel(const __grid_constant__ DecodeParams<MAXS> p, const __grid_constant__ CUtensorMap tmk,
+                       const __grid_constant__ CUtensorMap tmv) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the dynamic window is only guaranteed 16-byte aligned: round up to 1024
+  Bf16Smem& S = *reinterpret_cast<Bf16Smem*>(
+      smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t T = p.h.n_units;
@@ -78,13 +123,13 @@ __global__ void __launch_bounds__(kThreadsB, 2)
   __syncthreads();
 
   if (warp == kConsumersB) {
+    // ------------------------------------------------------------ producer
     if (lane != 0) return;
     int64_t k = 0;
     int64_t u = u0;
     while (u < u1) {
       int b, j, g, ng;
       locate_unit(p, u, b, j, g, ng);
-      const int len = p.seq[b].len;
       const int64_t row_end = p.seq[b].ubase + (int64_t)(j + 1) * ng;
       const int64_t seg_end = row_end < u1 ? row_end : u1;
       const int64_t rowbase = ((int64_t)p.seq[b].slot * hkv + j) * max_len;
@@ -94,12 +139,12 @@ __global__ void __launch_bounds__(kThreadsB, 2)
           if (!mbar_wait_bounded(&S.empty[s], (uint32_t)(((k / kStagesB) - 1) & 1), &S.abort_flag, p.h.err_word))
             goto drain;
         }
-        const int rows = min(kTile, len - g * kTile);
-        const uint32_t bytes = (uint32_t)rows * kHeadDim * 2;
-        mbar_arrive_expect_tx(&S.full[s], 2 * bytes);
-        const int64_t off = (rowbase + (int64_t)g * kTile) * kHeadDim;
-        bulk_g2s(S.k[s], kc + off, bytes, &S.full[s]);
-        bulk_g2s(S.v[s], vc + off, bytes, &S.full[s]);
+        const int r0 = (int)(rowbase + (int64_t)g * kTile);
+        mbar_arrive_expect_tx(&S.full[s], kStageBytesB);
+        tma_load_2d(S.stage[s] + 0 * kBoxBytes, &tmk, 0, r0, &S.full[s]);
+        tma_load_2d(S.stage[s] + 1 * kBoxBytes, &tmk, 64, r0, &S.full[s]);
+        tma_load_2d(S.stage[s] + 2 * kBoxBytes, &tmv, 0, r0, &S.full[s]);
+        tma_load_2d(S.stage[s] + 3 * kBoxBytes, &tmv, 64, r0, &S.full[s]);
         reinterpret_cast<volatile uint32_t*>(S.issued)[s] = (uint32_t)(k / kStagesB) + 1;
       }
     }
@@ -115,10 +160,14 @@ __global__ void __launch_bounds__(kThreadsB, 2)
     return;
   }
 
-  const int ts = lane >> 3;   // token slot 0..3
-  const int cq = lane & 7;    // channels 16 cq .. 16 cq + 15
-  const int sw = (cq >> 2) & 1;  // read order of the two 16-byte halves (bank spread)
+  // -------------------------------------------------------------- consumers
+  const int g = lane >> 2, tig = lane & 3;
+  const int hb = g >> 1;
+  const int half = g & 1;
+  const bool lo_lane = half != 0;
   const int gqa = p.h.gqa;
+  const float scale_log2 = p.h.scale_log2;
+  float* pbw = &S.pbuf[warp][0][0];
 
   int64_t k = 0;
   int64_t u = u0;
@@ -131,29 +180,22 @@ __global__ void __launch_bounds__(kThreadsB, 2)
     const int64_t k_begin = k;
     const int64_t k_end = k + (seg_end - u);
 
-    float qf[kMaxGqa][16];
+    // B operand of the score contraction: column n = g is query head g (zero beyond gqa)
+    uint32_t qb[8][2];
+    {
+      const uint16_t* qrow = p.h.q + ((int64_t)b * p.h.hq + j * gqa + (g < gqa ? g : 0)) * kHeadDim;
 #pragma unroll
-    for (int h = 0; h < kMaxGqa; ++h) {
-      if (h < gqa) {
-        const uint4* q4 = reinterpret_cast<const uint4*>(p.h.q + ((int64_t)b * p.h.hq + j * gqa + h) * kHeadDim +
-                                                         16 * cq);
-        unpack8(q4[0], &qf[h][0]);
-        unpack8(q4[1], &qf[h][8]);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) qf[h][i] *= p.h.scale_log2;
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) qf[h][i] = 0.0f;
+      for (int ks = 0; ks < 8; ++ks) {
+        const int c = 16 * ks + 2 * tig;
+        qb[ks][0] = g < gqa ? *reinterpret_cast<const uint32_t*>(qrow + c) : 0u;
+        qb[ks][1] = g < gqa ? *reinterpret_cast<const uint32_t*>(qrow + c + 8) : 0u;
       }
     }
-    float m[kMaxGqa], l[kMaxGqa], o[kMaxGqa][16];
+    float m_run[2] = {-INFINITY, -INFINITY};   // heads 2 tig, 2 tig + 1
+    float l_run[2] = {0.0f, 0.0f};
+    float o_acc[8][2];                         // head tig, channels 16 mt + g (+8)
 #pragma unroll
-    for (int h = 0; h < kMaxGqa; ++h) {
-      m[h] = -INFINITY;
-      l[h] = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) o[h][i] = 0.0f;
-    }
+    for (int i = 0; i < 8; ++i) o_acc[i][0] = o_acc[i][1] = 0.0f;
 
     for (int64_t kk = k_begin + ((warp - k_begin) % kConsumersB + kConsumersB) % kConsumersB; kk < k_end;
          kk += kConsumersB) {
@@ -163,73 +205,131 @@ __global__ void __launch_bounds__(kThreadsB, 2)
       if (!mbar_wait_bounded(&S.full[s], use & 1, &S.abort_flag, p.h.err_word)) continue;
       const int tile = g0 + (int)(kk - k_begin);
       const int rows = min(kTile, len - tile * kTile);
-      const uint8_t* ktile = S.k[s];
-      const uint8_t* vtile = S.v[s];
-      for (int it = 0; it < kTile / 4; ++it) {
-        const int t = 4 * it + ts;
-        if (4 * it >= rows) break;                 // warp-uniform
-        const bool valid = t < rows;
-        const int tr = valid ? t : rows - 1;
-        float kx[16];
-        load16(ktile + tr * 256 + 32 * cq, sw, kx);
-        float sc[kMaxGqa];
-#pragma unroll
-        for (int h = 0; h < kMaxGqa; ++h) {
-          float d = 0.0f;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) d = fmaf(qf[h][i], kx[i], d);
-          d += __shfl_xor_sync(0xffffffffu, d, 1);
-          d += __shfl_xor_sync(0xffffffffu, d, 2);
-          d += __shfl_xor_sync(0xffffffffu, d, 4);
-          sc[h] = d;
+      uint8_t* st = S.stage[s];
+      if (rows < kTile) {
+        // rows past the sequence end hold whatever the cache has there: zero them
+        for (int idx = lane; idx < (kTile - rows) * 4 * 8; idx += 32) {
+          const int r = rows + idx / 32, box = (idx / 8) & 3, q = idx & 7;
+          reinterpret_cast<uint4*>(st + box * kBoxBytes + r * 128)[q] = make_uint4(0, 0, 0, 0);
         }
-        if (valid) {
-          float vx[16];
-          load16(vtile + tr * 256 + 32 * cq, sw, vx);
+        __syncwarp();
+      }
+      const uint32_t kbase = smem_u32(st);
+      const uint32_t vbase = kbase + 2 * kBoxBytes;
+
+      // ---- scores S^T[token][head]
+      float sc[4][4];
 #pragma unroll
-          for (int h = 0; h < kMaxGqa; ++h) {
-            if (sc[h] > m[h] + 8.0f) {
-              const float a = exp2f(m[h] - sc[h]);
-              m[h] = sc[h];
-              l[h] *= a;
+      for (int mt = 0; mt < 4; ++mt) sc[mt][0] = sc[mt][1] = sc[mt][2] = sc[mt][3] = 0.0f;
 #pragma unroll
-              for (int i = 0; i < 16; ++i) o[h][i] *= a;
-            }
-            const float pt = exp2f(sc[h] - m[h]);
-            l[h] += pt;
+      for (int ks = 0; ks < 8; ++ks) {
+        const int box = ks >> 2;
+        const int ch = 2 * (ks & 3) + (lane >> 4);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) o[h][i] = fmaf(pt, vx[i], o[h][i]);
+        for (int mt = 0; mt < 4; ++mt) {
+          const int r = 16 * mt + (lane & 7) + ((lane >> 3) & 1) * 8;
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(kbase + box * kBoxBytes + swz(r, ch), a0, a1, a2, a3);
+          mma_bf16_16816(sc[mt], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+        }
+      }
+      // ---- online softmax for heads 2 tig + e (rows past the end masked)
+      float gm[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int t = 16 * mt + g + 8 * r;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float v = (t < rows) ? sc[mt][2 * r + e] * scale_log2 : -INFINITY;
+            sc[mt][2 * r + e] = v;
+            gm[e] = fmaxf(gm[e], v);
           }
         }
       }
+      float alpha[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        gm[e] = fmaxf(gm[e], __shfl_xor_sync(0xffffffffu, gm[e], 4));
+        gm[e] = fmaxf(gm[e], __shfl_xor_sync(0xffffffffu, gm[e], 8));
+        gm[e] = fmaxf(gm[e], __shfl_xor_sync(0xffffffffu, gm[e], 16));
+        const float m_new = fmaxf(m_run[e], gm[e]);
+        alpha[e] = exp2f(m_run[e] - m_new);
+        m_run[e] = m_new;
+        float ps = 0.0f;
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const float pv = exp2f(sc[mt][2 * r + e] - m_new);
+            sc[mt][2 * r + e] = pv;
+            ps += pv;
+          }
+        }
+        l_run[e] = fmaf(l_run[e], alpha[e], ps);
+      }
+      if (tig < 2) {
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+          for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) pbw[(2 * tig + e) * kPbStrideB + 16 * mt + g + 8 * r] = sc[mt][2 * r + e];
+      }
+      __syncwarp();
+      // alpha of head tig (the O rows this lane owns) from lane tig >> 1
+      const float al0 = __shfl_sync(0xffffffffu, alpha[0], tig >> 1);
+      const float al1 = __shfl_sync(0xffffffffu, alpha[1], tig >> 1);
+      const float alpha_o = (tig & 1) ? al1 : al0;
+
+      // ---- O^T[channel][head x {hi, lo}] = V^T x P^T
+      float pacc[8][4];
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) pacc[mt][0] = pacc[mt][1] = pacc[mt][2] = pacc[mt][3] = 0.0f;
+      const float* pbh = pbw + hb * kPbStrideB;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const int t = 16 * ks + 2 * tig + 8 * half;
+        const float2 pp = *reinterpret_cast<const float2*>(pbh + t);
+        uint32_t b0, b1;
+        split_exchange_bf16(pp.x, pp.y, lo_lane, b0, b1);
+        const int r = 16 * ks + (lane & 7) + ((lane >> 4) & 1) * 8;   // token row
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          const int box = mt >> 2;
+          const int ch = 2 * (mt & 3) + ((lane >> 3) & 1);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(vbase + box * kBoxBytes + swz(r, ch), a0, a1, a2, a3);
+          mma_bf16_16816(pacc[mt], a0, a1, a2, a3, b0, b1);
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o_acc[mt][0] = fmaf(o_acc[mt][0], alpha_o, pacc[mt][0] + pacc[mt][1]);
+        o_acc[mt][1] = fmaf(o_acc[mt][1], alpha_o, pacc[mt][2] + pacc[mt][3]);
+      }
+      if (rows < kTile) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty[s]);
     }
 
-    // ---- merge the 4 token slots of the warp, then the CTA
+    // ---- segment end: per-warp state -> shared memory -> CTA merge -> partial
 #pragma unroll
-    for (int h = 0; h < kMaxGqa; ++h) {
-      float M = fmaxf(m[h], __shfl_xor_sync(0xffffffffu, m[h], 8));
-      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 16));
-      const float a = (m[h] == -INFINITY) ? 0.0f : exp2f(m[h] - M);
-      float lh = l[h] * a;
-      lh += __shfl_xor_sync(0xffffffffu, lh, 8);
-      lh += __shfl_xor_sync(0xffffffffu, lh, 16);
+    for (int e = 0; e < 2; ++e) {
+      float l = l_run[e];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      if (g == 0 && tig < 2) {
+        S.mst[warp][2 * tig + e] = m_run[e];
+        S.lst[warp][2 * tig + e] = l;
+      }
+    }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float x = o[h][i] * a;
-        x += __shfl_xor_sync(0xffffffffu, x, 8);
-        x += __shfl_xor_sync(0xffffffffu, x, 16);
-        o[h][i] = x;
-      }
-      if (ts == 0) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) S.ost[warp][h][16 * cq + i] = o[h][i];
-      }
-      if (lane == 0) {
-        S.mst[warp][h] = M;
-        S.lst[warp][h] = lh;
-      }
+    for (int mt = 0; mt < 8; ++mt) {
+      S.ost[warp][tig][16 * mt + g] = o_acc[mt][0];
+      S.ost[warp][tig][16 * mt + g + 8] = o_acc[mt][1];
     }
     named_bar_sync(1, kConsumersB * 32);
     {
@@ -258,8 +358,31 @@ __global__ void __launch_bounds__(kThreadsB, 2)
     named_bar_sync(1, kConsumersB * 32);
     k = k_end;
     u = seg_end;
-  }  // this CTA's partials are written: let the dependent combine launch
+  }
+  // this CTA's partials are written: let the dependent combine launch
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// 2-D tensor map over rows of 128 bf16 channels: box = 64 channels x 64 rows,
+// 128-byte swizzle.
+bool encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (encode == nullptr) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[2] = {kHeadDim, rows};
+  const cuuint64_t strides[1] = {kHeadDim * 2};
+  const cuuint32_t box[2] = {64, kTile};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -270,12 +393,17 @@ template <int MAXS>
 cudaError_t launch_decode_bf16(const DecodeParams<MAXS>& p, const uint16_t* kc, const uint16_t* vc,
                                cudaStream_t stream, cudaEvent_t ev_start, cudaEvent_t ev_stop) {
   if (p.h.n_units <= 0) return cudaSuccess;
-  const int smem = (int)sizeof(Bf16Smem);
+  int max_slot = 0;
+  for (int i = 0; i < p.h.n_seqs; ++i) max_slot = p.seq[i].slot > max_slot ? p.seq[i].slot : max_slot;
+  const uint64_t rows = (uint64_t)(max_slot + 1) * p.h.hkv * p.h.max_groups;
+  CUtensorMap tmk, tmv;
+  if (!encode_rows_map(&tmk, kc, rows) || !encode_rows_map(&tmv, vc, rows)) return cudaErrorInvalidValue;
+  const int smem = (int)sizeof(Bf16Smem) + 1024;   // + slack for the 1024-byte alignment of the stages
   static bool attr_done[64] = {};
   cudaError_t e = ensure_smem_attr(decode_bf16_kernel<MAXS>, smem, attr_done);
   if (e != cudaSuccess) return e;
   if (ev_start) cudaEventRecord(ev_start, stream);
-  decode_bf16_kernel<MAXS><<<p.h.n_ctas, kThreadsB, smem, stream>>>(p, kc, vc);
+  decode_bf16_kernel<MAXS><<<p.h.n_ctas, kThreadsB, smem, stream>>>(p, tmk, tmv);
   e = cudaGetLastError();
   if (ev_stop) cudaEventRecord(ev_stop, stream);
   return e;
