@@ -84,6 +84,16 @@ __device__ __forceinline__ void frag_a(uint32_t w0, uint32_t w1, uint32_t& a0, u
   a3 = frag_extract<2 * KK + 1>(w1);
 }
 
+__device__ __forceinline__ void frag_a_dyn(int kk, uint32_t w0, uint32_t w1, uint32_t& a0, uint32_t& a1,
+                                           uint32_t& a2, uint32_t& a3) {
+  switch (kk) {
+    case 0: frag_a<0>(w0, w1, a0, a1, a2, a3); break;
+    case 1: frag_a<1>(w0, w1, a0, a1, a2, a3); break;
+    case 2: frag_a<2>(w0, w1, a0, a1, a2, a3); break;
+    default: frag_a<3>(w0, w1, a0, a1, a2, a3); break;
+  }
+}
+
 // Partner-lane split of a B-fragment column pair.  Lanes g = 2h (hi column of
 // head h) and g = 2h + 1 (lo column) need the same fp32 values x for k-rows
 // {2 tig, 2 tig + 1} (register b0) and {2 tig + 8, 2 tig + 9} (register b1).
@@ -91,7 +101,8 @@ __device__ __forceinline__ void frag_a(uint32_t w0, uint32_t w1, uint32_t& a0, u
 // pair into hi + lo fp16 and they swap the half the other one needs.
 __device__ __forceinline__ void split_exchange(float x0, float x1, bool lo_lane, uint32_t& b0, uint32_t& b1) {
   const uint32_t hi = pack_half2(x0, x1);
-  const uint32_t lo = pack_half2(x0 - half_lo_to_float(hi), x1 - half_hi_to_float(hi));
+  const float2 r = __fadd2_rn(make_float2(x0, x1), make_float2(-half_lo_to_float(hi), -half_hi_to_float(hi)));
+  const uint32_t lo = pack_half2(r.x, r.y);
   const uint32_t send = lo_lane ? hi : lo;
   const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 4);
   b0 = lo_lane ? recv : hi;
@@ -188,8 +199,8 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     const int64_t k_end = k + (seg_end - u);
     const int slot = p.seq[b].slot;
 
-    // ---- segment setup: rotate the GQA queries (warp w rotates head w)
-    {
+    // ---- segment setup: rotate the GQA queries (warp h < 4 rotates head h)
+    if (warp < kMaxGqa) {
       const int h = warp;
       float qv[4] = {0.f, 0.f, 0.f, 0.f};
       if (h < gqa) {
@@ -229,7 +240,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     // per-lane constants of this segment
     const int Fk_b = range_exponent(S.qmax[hb] * (2.0f / 3.0f));     // B-column head hb
     const int Fk_s = range_exponent(S.qmax[tig] * (2.0f / 3.0f));    // score head tig
-    const float kq = pow2f(24 - Fk_s);
+    const float kqs = pow2f(24 - Fk_s) * scale_log2;
     const float inv2Fk_b = pow2f(-Fk_b);
     const float vmax = __uint_as_float(
         reinterpret_cast<const uint32_t*>(arena + kMetaHeader)[(int64_t)slot * hkv + j]);
@@ -253,12 +264,22 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     }
     named_bar_sync(1, kConsumers * 32);
 
+    // bit-position weights of this lane's k-rows: 2^p for the score zero term,
+    // 2^(Fv - p) for the value factors
+    float zwk[4], fsc[4];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const int pp = half ? frag_p(2 * kk + 1) : frag_p(2 * kk);
+      zwk[kk] = pow2f(pp);
+      fsc[kk] = fv * pow2f(-pp);
+    }
+
     float m_run = -INFINITY;   // running max (log2 units) of head tig
     float l_run = 0.0f;        // partial sum of p over this lane's tokens
-    float o_acc[8][2];         // head tig, channels 16 mt + g + 8 r (times 2^(Fv - 24))
+    float2 o_acc[8];           // head tig, channels 16 mt + g (.x) and + 8 (.y), times 2^(Fv - 24)
     float zacc[kVGroups];      // sum_t p_t z^V_t,gr over this lane's tokens
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o_acc[i][0] = o_acc[i][1] = 0.0f;
+    for (int i = 0; i < 8; ++i) o_acc[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int i = 0; i < kVGroups; ++i) zacc[i] = 0.0f;
 
@@ -276,32 +297,38 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
 
       // ---- B fragments of the score contraction, and q_rot . z
       uint32_t bk[8][2];
-      float qz = 0.0f;
+      float2 qzc[4];   // per k-step class (ks & 3): sum of q2 * z over this lane's channel pairs
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qzc[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float4 q4 = S.q2t[i][lane];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int ks = 2 * i + e;
-          const float qa = e ? q4.z : q4.x, qb = e ? q4.w : q4.y;
+          const float2 qq = e ? make_float2(q4.z, q4.w) : make_float2(q4.x, q4.y);
           const int c = 16 * ks + 2 * tig + 8 * half;
           const float2 s2 = *reinterpret_cast<const float2*>(ksc + c);
           const float2 z2 = *reinterpret_cast<const float2*>(kze + c);
-          split_exchange(qa * s2.x, qb * s2.y, lo_lane, bk[ks][0], bk[ks][1]);
-          const float zw = half ? pow2f(frag_p(2 * (ks & 3) + 1)) : pow2f(frag_p(2 * (ks & 3)));
-          qz = fmaf(fmaf(qa, z2.x, qb * z2.y), zw, qz);
+          const float2 x = __fmul2_rn(qq, s2);
+          split_exchange(x.x, x.y, lo_lane, bk[ks][0], bk[ks][1]);
+          qzc[ks & 3] = __ffma2_rn(qq, z2, qzc[ks & 3]);
         }
       }
+      float qz = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qz = fmaf(qzc[i].x + qzc[i].y, zwk[i], qz);
       qz += __shfl_xor_sync(0xffffffffu, qz, 1);
       qz += __shfl_xor_sync(0xffffffffu, qz, 2);
       qz += __shfl_xor_sync(0xffffffffu, qz, 4);
-      qz *= inv2Fk_b;                                            // q_rot[hb] . z
-      const float qz_s = __shfl_sync(0xffffffffu, qz, 8 * tig);  // q_rot[tig] . z
+      qz *= inv2Fk_b;                                                          // q_rot[hb] . z
+      const float qzs = __shfl_sync(0xffffffffu, qz, 8 * tig) * scale_log2;   // head tig, log2 units
 
       // ---- scores: S^T[token][head x {hi, lo}] = codes x B, 8 independent chains
-      float sc[16];
+      float2 sc[8];   // tokens 16 mt + g (.x) and + 8 (.y), head tig
       {
         const uint4* kc = reinterpret_cast<const uint4*>(blk + kOffKCodes);
+        const float2 kq2 = make_float2(kqs, kqs), qz2 = make_float2(qzs, qzs);
 #pragma unroll
         for (int mh = 0; mh < 2; ++mh) {
           uint4 w[4];
@@ -318,12 +345,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
               const uint32_t w0 = (ks < 4) ? w[m].x : w[m].z;
               const uint32_t w1 = (ks < 4) ? w[m].y : w[m].w;
               uint32_t a0, a1, a2, a3;
-              switch (ks & 3) {
-                case 0: frag_a<0>(w0, w1, a0, a1, a2, a3); break;
-                case 1: frag_a<1>(w0, w1, a0, a1, a2, a3); break;
-                case 2: frag_a<2>(w0, w1, a0, a1, a2, a3); break;
-                default: frag_a<3>(w0, w1, a0, a1, a2, a3); break;
-              }
+              frag_a_dyn(ks & 3, w0, w1, a0, a1, a2, a3);
               mma_f16_16816(acc[m], a0, a1, a2, a3, bk[ks][0], bk[ks][1]);
             }
           }
@@ -331,94 +353,87 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
           for (int m = 0; m < 4; ++m) {
             const int mt = 4 * mh + m;
             const int t0 = 16 * mt + g;
-            sc[2 * mt] = fmaf(acc[m][0] + acc[m][1], kq, qz_s) * knm[t0] * scale_log2;
-            sc[2 * mt + 1] = fmaf(acc[m][2] + acc[m][3], kq, qz_s) * knm[t0 + 8] * scale_log2;
+            const float2 a = make_float2(acc[m][0] + acc[m][1], acc[m][2] + acc[m][3]);
+            sc[mt] = __fmul2_rn(__ffma2_rn(a, kq2, qz2), make_float2(knm[t0], knm[t0 + 8]));
           }
         }
       }
 
       // ---- online softmax (head tig)
-      float gm = sc[0];
+      float gm = fmaxf(sc[0].x, sc[0].y);
 #pragma unroll
-      for (int i = 1; i < 16; ++i) gm = fmaxf(gm, sc[i]);
+      for (int i = 1; i < 8; ++i) gm = fmaxf(gm, fmaxf(sc[i].x, sc[i].y));
       gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 4));
       gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 8));
       gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 16));
       const float m_new = fmaxf(m_run, gm);
       const float alpha = fast_exp2(m_run - m_new);
       m_run = m_new;
-      float psum = 0.0f;
+      const float2 neg_m = make_float2(-m_new, -m_new);
+      float2 psum = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        sc[i] = fast_exp2(sc[i] - m_new);
-        psum += sc[i];
+      for (int i = 0; i < 8; ++i) {
+        const float2 d = __fadd2_rn(sc[i], neg_m);
+        sc[i] = make_float2(fast_exp2(d.x), fast_exp2(d.y));
+        psum = __fadd2_rn(psum, sc[i]);
       }
-      l_run = fmaf(l_run, alpha, psum);
+      l_run = fmaf(l_run, alpha, psum.x + psum.y);
 #pragma unroll
       for (int gr = 0; gr < kVGroups; ++gr) zacc[gr] *= alpha;
       float* pb = S.pbuf[warp][tig];
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const int t0 = 16 * mt + g;
-        pb[t0] = sc[2 * mt];
-        pb[t0 + 8] = sc[2 * mt + 1];
+        pb[t0] = sc[mt].x;
+        pb[t0 + 8] = sc[mt].y;
         const float4 z0 = *reinterpret_cast<const float4*>(vsz + 8 * t0 + 4);
         const float4 z1 = *reinterpret_cast<const float4*>(vsz + 8 * (t0 + 8) + 4);
-        zacc[0] = fmaf(sc[2 * mt], z0.x, fmaf(sc[2 * mt + 1], z1.x, zacc[0]));
-        zacc[1] = fmaf(sc[2 * mt], z0.y, fmaf(sc[2 * mt + 1], z1.y, zacc[1]));
-        zacc[2] = fmaf(sc[2 * mt], z0.z, fmaf(sc[2 * mt + 1], z1.z, zacc[2]));
-        zacc[3] = fmaf(sc[2 * mt], z0.w, fmaf(sc[2 * mt + 1], z1.w, zacc[3]));
+        zacc[0] = fmaf(sc[mt].x, z0.x, fmaf(sc[mt].y, z1.x, zacc[0]));
+        zacc[1] = fmaf(sc[mt].x, z0.y, fmaf(sc[mt].y, z1.y, zacc[1]));
+        zacc[2] = fmaf(sc[mt].x, z0.z, fmaf(sc[mt].y, z1.z, zacc[2]));
+        zacc[3] = fmaf(sc[mt].x, z0.w, fmaf(sc[mt].y, z1.w, zacc[3]));
       }
       __syncwarp();
 
-      // ---- P.V: O^T[channel][head x {hi, lo}] = codes^V^T x (p * s^V), in two
-      // halves of 64 channels (value groups 2 hc, 2 hc + 1) to bound registers
-      const float* pbh = S.pbuf[warp][hb];
+      // ---- P.V: O^T[channel][head x {hi, lo}] = codes^V^T x (p * s^V); each
+      // k-step's factors are built once and feed all 8 channel m-tiles
+      {
+        const float* pbh = S.pbuf[warp][hb];
+        float pacc[8][4];
 #pragma unroll
-      for (int hc = 0; hc < 2; ++hc) {
-        float pacc[4][4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) pacc[m][0] = pacc[m][1] = pacc[m][2] = pacc[m][3] = 0.0f;
+        for (int mt = 0; mt < 8; ++mt) pacc[mt][0] = pacc[mt][1] = pacc[mt][2] = pacc[mt][3] = 0.0f;
 #pragma unroll
         for (int jh = 0; jh < 2; ++jh) {
-          uint2 vw[4];
+          uint2 vw[8];
 #pragma unroll
-          for (int m = 0; m < 4; ++m)
-            vw[m] = *reinterpret_cast<const uint2*>(blk + kOffVCodes + (((4 * hc + m) * 32 + lane) * 4 + 2 * jh) * 4);
+          for (int mt = 0; mt < 8; ++mt)
+            vw[mt] = *reinterpret_cast<const uint2*>(blk + kOffVCodes + ((mt * 32 + lane) * 4 + 2 * jh) * 4);
 #pragma unroll
           for (int kk2 = 0; kk2 < 4; ++kk2) {
-            const int ks = 4 * jh + kk2;
-            const int t = 16 * ks + 2 * tig + 8 * half;   // this lane's two tokens
-            const float fsc = fv * (half ? pow2f(-frag_p(2 * kk2 + 1)) : pow2f(-frag_p(2 * kk2)));
-            const float2 pp = *reinterpret_cast<const float2*>(pbh + t);
-            const float p0 = pp.x * fsc, p1 = pp.y * fsc;
-            const float2 s0 = *reinterpret_cast<const float2*>(vsz + 8 * t + 2 * hc);
-            const float2 s1 = *reinterpret_cast<const float2*>(vsz + 8 * (t + 1) + 2 * hc);
+            const int t = 16 * (4 * jh + kk2) + 2 * tig + 8 * half;   // this lane's two tokens
+            const float2 pr = __fmul2_rn(*reinterpret_cast<const float2*>(pbh + t), make_float2(fsc[kk2], fsc[kk2]));
+            const float4 s0 = *reinterpret_cast<const float4*>(vsz + 8 * t);
+            const float4 s1 = *reinterpret_cast<const float4*>(vsz + 8 * (t + 1));
 #pragma unroll
-            for (int g2 = 0; g2 < 2; ++g2) {
+            for (int gr = 0; gr < kVGroups; ++gr) {
+              const float sa = gr == 0 ? s0.x : gr == 1 ? s0.y : gr == 2 ? s0.z : s0.w;
+              const float sb = gr == 0 ? s1.x : gr == 1 ? s1.y : gr == 2 ? s1.z : s1.w;
               uint32_t b0, b1;
-              split_exchange(p0 * (g2 ? s0.y : s0.x), p1 * (g2 ? s1.y : s1.x), lo_lane, b0, b1);
+              split_exchange(pr.x * sa, pr.y * sb, lo_lane, b0, b1);
 #pragma unroll
               for (int h2 = 0; h2 < 2; ++h2) {
-                const int m = 2 * g2 + h2;
+                const int mt = 2 * gr + h2;
                 uint32_t a0, a1, a2, a3;
-                switch (kk2) {
-                  case 0: frag_a<0>(vw[m].x, vw[m].y, a0, a1, a2, a3); break;
-                  case 1: frag_a<1>(vw[m].x, vw[m].y, a0, a1, a2, a3); break;
-                  case 2: frag_a<2>(vw[m].x, vw[m].y, a0, a1, a2, a3); break;
-                  default: frag_a<3>(vw[m].x, vw[m].y, a0, a1, a2, a3); break;
-                }
-                mma_f16_16816(pacc[m], a0, a1, a2, a3, b0, b1);
+                frag_a_dyn(kk2, vw[mt].x, vw[mt].y, a0, a1, a2, a3);
+                mma_f16_16816(pacc[mt], a0, a1, a2, a3, b0, b1);
               }
             }
           }
         }
+        const float2 al2 = make_float2(alpha, alpha);
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const int mt = 4 * hc + m;
-          o_acc[mt][0] = fmaf(o_acc[mt][0], alpha, pacc[m][0] + pacc[m][1]);
-          o_acc[mt][1] = fmaf(o_acc[mt][1], alpha, pacc[m][2] + pacc[m][3]);
-        }
+        for (int mt = 0; mt < 8; ++mt)
+          o_acc[mt] = __ffma2_rn(o_acc[mt], al2, make_float2(pacc[mt][0] + pacc[mt][1], pacc[mt][2] + pacc[mt][3]));
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty[s]);
@@ -446,16 +461,17 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const float zg = zs[mt >> 1];
-        S.pbuf[warp][tig][16 * mt + g] = fmaf(o_acc[mt][0], kv, zg);
-        S.pbuf[warp][tig][16 * mt + g + 8] = fmaf(o_acc[mt][1], kv, zg);
+        S.pbuf[warp][tig][16 * mt + g] = fmaf(o_acc[mt].x, kv, zg);
+        S.pbuf[warp][tig][16 * mt + g + 8] = fmaf(o_acc[mt].y, kv, zg);
       }
     }
     named_bar_sync(1, kConsumers * 32);
     {
-      const int c = threadIdx.x;  // 0..127: channel
       const int64_t rho = (int64_t)hkv * p.seq[b].rank + j;
       float* part = p.h.partials + (cta + rho) * (int64_t)gqa * kPartialFloats;
-      for (int h = 0; h < gqa; ++h) {
+      for (int idx = threadIdx.x; idx < gqa * kHeadDim; idx += kConsumers * 32) {
+        const int h = idx >> 7;
+        const int c = idx & (kHeadDim - 1);
         float M = S.mst[0][h];
 #pragma unroll
         for (int w = 1; w < kConsumers; ++w) M = fmaxf(M, S.mst[w][h]);
@@ -511,7 +527,7 @@ __global__ void __launch_bounds__(kCombineThreads)
   __shared__ float pw[kMaxGqa][kGroup];                                 // window probabilities
   __shared__ float wts[kMaxGqa][kCombineMaxChunk];
   __shared__ float red[kMaxGqa][2][4];
-  __shared__ float win_m[kMaxGqa], win_l[kMaxGqa];
+  __shared__ float win_m[kMaxGqa];
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
 
