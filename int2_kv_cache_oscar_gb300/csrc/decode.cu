@@ -52,6 +52,7 @@ struct DecSmem {
   alignas(8) uint64_t full[kStages];
   uint64_t empty[kStages];
   uint32_t issued[kStages];   // uses of each stage issued so far (producer -> consumers)
+  uint64_t qready;            // consumers have requested their first queries (-> producer)
   int abort_flag;
 };
 static_assert(kPbStride >= kHeadDim, "output rows must fit in the probability rows");
@@ -138,6 +139,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       mbar_init(&S.empty[s], 1);
       S.issued[s] = 0;
     }
+    mbar_init(&S.qready, kConsumers);
     S.abort_flag = 0;
     fence_mbar_init();
   }
@@ -148,6 +150,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     if (lane != 0) return;
     int64_t k = 0;
     int64_t u = u0;
+    if (!mbar_wait_bounded(&S.qready, 0, &S.abort_flag, p.h.err_word)) goto drain;
     while (u < u1) {
       int b, j, g, ng;
       locate_unit(p, u, b, j, g, ng);
@@ -188,8 +191,34 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
   const int gqa = p.h.gqa;
   const float scale_log2 = p.h.scale_log2;
 
+  // The query rows and value-scale maxima of this CTA's first two segments
+  // are requested before the producer's first bulk copy (it waits on qready):
+  // requested after it they would queue behind every CTA's initial ring fill.
+  uint2 qpre0 = make_uint2(0u, 0u), qpre1 = make_uint2(0u, 0u);
+  uint32_t vpre0 = 0u, vpre1 = 0u;
+  {
+    int64_t uu = u0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      if (uu < u1) {
+        int b, j, gg, ng;
+        locate_unit(p, uu, b, j, gg, ng);
+        uint2 qr = make_uint2(0u, 0u);
+        if (warp < gqa)
+          qr = *reinterpret_cast<const uint2*>(p.h.q + ((int64_t)b * p.h.hq + j * gqa + warp) * kHeadDim + 4 * lane);
+        const uint32_t vr = reinterpret_cast<const uint32_t*>(arena + kMetaHeader)[(int64_t)p.seq[b].slot * hkv + j];
+        if (i == 0) { qpre0 = qr; vpre0 = vr; } else { qpre1 = qr; vpre1 = vr; }
+        const int64_t row_end = p.seq[b].ubase + (int64_t)(j + 1) * ng;
+        uu = row_end < u1 ? row_end : u1;
+      }
+    }
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&S.qready);
+
   int64_t k = 0;
   int64_t u = u0;
+  int seg_idx = 0;
   while (u < u1) {
     int b, j, g0, ng;
     locate_unit(p, u, b, j, g0, ng);
@@ -204,8 +233,10 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       const int h = warp;
       float qv[4] = {0.f, 0.f, 0.f, 0.f};
       if (h < gqa) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(p.h.q + ((int64_t)b * p.h.hq + j * gqa + h) * kHeadDim +
-                                                          4 * lane);
+        const uint2 raw = seg_idx == 0   ? qpre0
+                          : seg_idx == 1 ? qpre1
+                                         : *reinterpret_cast<const uint2*>(
+                                               p.h.q + ((int64_t)b * p.h.hq + j * gqa + h) * kHeadDim + 4 * lane);
         qv[0] = bf16_lo(raw.x);
         qv[1] = bf16_hi(raw.x);
         qv[2] = bf16_lo(raw.y);
@@ -243,7 +274,9 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     const float kqs = pow2f(24 - Fk_s) * scale_log2;
     const float inv2Fk_b = pow2f(-Fk_b);
     const float vmax = __uint_as_float(
-        reinterpret_cast<const uint32_t*>(arena + kMetaHeader)[(int64_t)slot * hkv + j]);
+        seg_idx == 0   ? vpre0
+        : seg_idx == 1 ? vpre1
+                       : reinterpret_cast<const uint32_t*>(arena + kMetaHeader)[(int64_t)slot * hkv + j]);
     const int Fv = range_exponent(vmax);
     const float fv = pow2f(Fv);
     const float kv = pow2f(24 - Fv);
@@ -493,6 +526,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     named_bar_sync(1, kConsumers * 32);
     k = k_end;
     u = seg_end;
+    ++seg_idx;
   }  // this CTA's partials are written: let the dependent combine launch
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

@@ -10,15 +10,19 @@
 //
 // One CTA = one (group, KV head), 256 threads; the thread pair (2t, 2t+1)
 // owns token t, each thread 64 of its channels.
-//   1. V: per 32-channel group min/max, s = (max-min)/3, z = min, codes; codes
-//      go to shared memory (transposed), s/z to the block.
+//   1. V: per 32-channel group min/max (on packed bf16 pairs: exact), s =
+//      (max-min)/3, z = min, codes; codes go to shared memory (transposed),
+//      s/z to the block.
 //   2. K: unnormalised fast Walsh-Hadamard transform, H_d = Hu / sqrt(128):
-//      6 butterfly stages in registers, the 7th across the thread pair;
+//      6 butterfly stages in registers (packed f32x2), the 7th across the
+//      thread pair through the token's shared-memory row;
 //      n_t = sqrt(|Hu k|^2 / 128); k_hat = Hu k / |Hu k| (= H_d k / n_t).
 //   3. Per-channel min/max of k_hat over the 128 tokens (shared memory,
 //      16-token slices, then 8 slices).
 //   4. Codes of k_hat, packed straight into the fragment-order words.
 //   5. Coalesced 16-byte stores of both code matrices.
+// Every code decision is fl32(fl32(x - z) * fl32(1/s)) rounded half to even;
+// the packed f32x2 operations round each lane exactly like the scalar ones.
 #include <cstddef>
 
 #include "common.cuh"
@@ -28,41 +32,55 @@ namespace oscar {
 namespace {
 
 constexpr int kQThreads = 256;   // two threads per token: channels [0, 64) and [64, 128)
-constexpr int kKhStride = 132;   // floats per k_hat row in shared memory (padding vs bank conflicts)
+constexpr int kKhStride = 136;   // floats per k_hat row: channels [0, 64) at 0, [64, 128) at 68
 constexpr int kVbStride = 144;   // bytes per value-code row (channel) in shared memory
 constexpr int kKrawOffset = 128 * kKhStride * 4 - 128 * 256;   // raw K rows at the end of the k_hat buffer
+constexpr float kMagic = 12582912.0f;                          // 1.5 * 2^23
+constexpr uint32_t kMagicBits = 0x4B400000u;
 
 struct QuantSmem {
-  alignas(16) float kh[kGroup * kKhStride];          // k_hat[t][c]; float4 stores / loads
+  alignas(16) float kh[kGroup * kKhStride];          // k_hat[t][kh_col(c)]; float4 stores / loads
   alignas(16) uint8_t vb[kHeadDim * kVbStride + 16];  // value codes [channel][permuted token]; uint4 loads
   alignas(16) float4 rmin[8][kHeadDim / 4];          // per 16-token slice: channel minima
   alignas(16) float4 rmax[8][kHeadDim / 4];          // per 16-token slice: channel maxima
   alignas(16) uint32_t kw[1024];                     // key code words, fragment order; uint4 loads
-  alignas(16) float2 kp[kHeadDim + 4];               // per-channel (1/s, z), see kp_index
+  alignas(16) float4 kq[kHeadDim / 2 + 1];           // per channel pair (1/s, 1/s', -z, -z'), see kq_index
   float red[kQThreads / 32];
 };
 static_assert(offsetof(QuantSmem, vb) % 16 == 0 && offsetof(QuantSmem, kw) % 16 == 0, "alignment");
+static_assert(offsetof(QuantSmem, kq) % 16 == 0, "alignment");
 static_assert((kKhStride * 4) % 16 == 0 && kVbStride % 16 == 0, "rows must keep 16-byte alignment");
+static_assert(kKrawOffset % 16 == 0 && kKrawOffset >= 0, "raw key rows must be 16-byte aligned");
 
-// Round-half-even code of x against (inv = 1/s, z): v = fl32(fl32(x - z) * inv)
-// (the product is rounded before the integer rounding, as the decision rule
-// specifies);
-// x >= z and x <= max keep v in [0, 3] (s == 0 gives inv = 0, v = 0), so no
-// clamp is needed; the magic constant 1.5 * 2^23 leaves rne(v) in the low
-// mantissa bits.
-__device__ __forceinline__ uint32_t int2_code(float x, float inv, float z) {
-  const float v = __fmul_rn(x - z, inv);   // rounded product; never contracted into the add
-  return __float_as_uint(v + 12582912.0f) & 3u;
+// Column of channel c in a k_hat row: the upper 64 channels are shifted by 16
+// bytes, so that the two threads of a token write different banks and a
+// warp's 16-byte row accesses are conflict-free.
+__device__ __forceinline__ int kh_col(int c) { return c + ((c >> 6) << 2); }
+
+// Entry of channel pair (c, c + 1) in the key-parameter table; the upper half
+// is shifted by one entry (16 bytes) for the same reason.
+__device__ __forceinline__ int kq_index(int c) { return (c >> 1) + (c >> 6); }
+
+// Rounded code decision of a pair against (1/s, -z): the float bits of
+// fl32(fl32(x - z) * inv) + 1.5 * 2^23, i.e. 0x4B400000 + code.  x >= z and
+// x <= max keep the product in [0, 3] (s == 0 gives inv = 0, code 0), so no
+// clamp is needed and the code is the low byte.  Every step is rounded, so an
+// exact tie k + 1/2 goes to the even code: the difference is one packed add
+// (a packed add cannot absorb the product before it, see the k_hat scaling),
+// the product and the magic add are scalar __fmul_rn / __fadd_rn, which are
+// never fused into a multiply-add.  A packed multiply is not used here: the
+// compiler may fuse it with a following packed add even when both carry an
+// explicit rounding mode, which moves ties to the unrounded product's side.
+__device__ __forceinline__ uint2 code_bits2(float2 x, float2 inv, float2 negz) {
+  const float2 d = __fadd2_rn(x, negz);
+  const float vx = __fmul_rn(d.x, inv.x), vy = __fmul_rn(d.y, inv.y);
+  return make_uint2(__float_as_uint(__fadd_rn(vx, kMagic)), __float_as_uint(__fadd_rn(vy, kMagic)));
 }
 
 // Byte offset of value-code row (channel) c: rows of the upper 64 channels are
 // shifted by 16 bytes so that the two threads of a token (one per channel
 // half) store into different banks.
 __device__ __forceinline__ int vb_row(int c) { return c * kVbStride + ((c >> 6) << 4); }
-
-// Index of channel c in the (1/s, z) table: the upper half is shifted by 4
-// entries (32 bytes) for the same reason.
-__device__ __forceinline__ int kp_index(int c) { return c + ((c >> 6) << 2); }
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
@@ -76,20 +94,28 @@ __device__ __forceinline__ int vb_perm(int c) {
   return ((tig * 2 + j) * 4 + kk) * 4 + hf + 2 * e;
 }
 
-__device__ __forceinline__ void load64(const uint16_t* src, float (&x)[64]) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint4 u = __ldg(s + i);
-    x[8 * i + 0] = bf16_lo(u.x);
-    x[8 * i + 1] = bf16_hi(u.x);
-    x[8 * i + 2] = bf16_lo(u.y);
-    x[8 * i + 3] = bf16_hi(u.y);
-    x[8 * i + 4] = bf16_lo(u.z);
-    x[8 * i + 5] = bf16_hi(u.z);
-    x[8 * i + 6] = bf16_lo(u.w);
-    x[8 * i + 7] = bf16_hi(u.w);
-  }
+__device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) { return make_float2(bf16_lo(u), bf16_hi(u)); }
+
+// Sum of (0x4B400000 << shift) over the shifts of one key-code word
+// (16 e + 4 kk + 2 hf), modulo 2^32: the float bits' constant part,
+// subtracted once per word.
+__host__ __device__ constexpr uint32_t key_word_magic() {
+  uint32_t m = 0;
+  for (int kk = 0; kk < 4; ++kk)
+    for (int hf = 0; hf < 2; ++hf)
+      for (int e = 0; e < 2; ++e) m += kMagicBits << (16 * e + 4 * kk + 2 * hf);
+  return m;
 }
 
 template <int CAP>
@@ -116,7 +142,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
     const uint16_t* ksrc = (from_win ? win_k + t * kHeadDim : kin + (row * hkv + head) * kHeadDim) + 64 * half;
     const uint16_t* vsrc = (from_win ? win_v + t * kHeadDim : vin + (row * hkv + head) * kHeadDim) + 64 * half;
 
-    // raw K rows (bf16, 256 B each) -> upper half of the k_hat buffer, in
+    // raw K rows (bf16, 256 B each) -> upper part of the k_hat buffer, in
     // flight while the values are processed; chunk i of a thread's 128 bytes
     // is stored at slot (i + t) mod 8 so that a warp's 16-byte accesses
     // spread over all bank groups
@@ -128,27 +154,45 @@ __global__ void __launch_bounds__(kQThreads, 2)
     // ---- values: per-token INT2 over this thread's two 32-channel groups
     float smax = 0.0f;
     {
-      float x[64];
-      load64(vsrc, x);
+      uint4 vr[8];
+      const uint4* vs4 = reinterpret_cast<const uint4*>(vsrc);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) vr[i] = __ldg(vs4 + i);
       const int pt = vb_perm(t);
       float sv[2], zv[2];
 #pragma unroll
       for (int g2 = 0; g2 < 2; ++g2) {
-        float mn = x[32 * g2], mx = x[32 * g2];
+        const uint4* w4 = vr + 4 * g2;
+        uint32_t mn2 = w4[0].x, mx2 = w4[0].x;
 #pragma unroll
-        for (int i = 1; i < kVGroup; ++i) {
-          mn = fminf(mn, x[32 * g2 + i]);
-          mx = fmaxf(mx, x[32 * g2 + i]);
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t ws[4] = {w4[i].x, w4[i].y, w4[i].z, w4[i].w};
+#pragma unroll
+          for (int e = (i == 0 ? 1 : 0); e < 4; ++e) {
+            mn2 = bf16x2_min(mn2, ws[e]);
+            mx2 = bf16x2_max(mx2, ws[e]);
+          }
         }
+        const float mn = fminf(bf16_lo(mn2), bf16_hi(mn2));
+        const float mx = fmaxf(bf16_lo(mx2), bf16_hi(mx2));
         const float sc = (mx - mn) / 3.0f;
         const float inv = sc > 0.0f ? 1.0f / sc : 0.0f;
         sv[g2] = sc;
         zv[g2] = mn;
         smax = fmaxf(smax, sc);
         const int gi = 2 * half + g2;
+        const float2 inv2 = make_float2(inv, inv), negz2 = make_float2(-mn, -mn);
 #pragma unroll
-        for (int i = 0; i < kVGroup; ++i)
-          S.vb[vb_row(gi * kVGroup + i) + pt] = (uint8_t)int2_code(x[32 * g2 + i], inv, mn);
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t ws[4] = {w4[i].x, w4[i].y, w4[i].z, w4[i].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = gi * kVGroup + 8 * i + 2 * e;
+            const uint2 cb = code_bits2(bf16x2_to_float2(ws[e]), inv2, negz2);
+            S.vb[vb_row(c) + pt] = (uint8_t)cb.x;       // low byte = code
+            S.vb[vb_row(c + 1) + pt] = (uint8_t)cb.y;
+          }
+        }
       }
       *reinterpret_cast<float2*>(blk + kOffVSZ + 32 * t + 8 * half) = make_float2(sv[0], sv[1]);
       *reinterpret_cast<float2*>(blk + kOffVSZ + 32 * t + 16 + 8 * half) = make_float2(zv[0], zv[1]);
@@ -156,7 +200,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
 
     // ---- keys: rotation (6 butterfly stages in registers + 1 across the
     // thread pair), norm, unit vector
-    float x[64];
+    float2 x[32];                      // channels 64 half + 2i, + 2i + 1
     cp_async_wait_all();
     __syncthreads();                   // every thread's raw K row is in shared memory
     {
@@ -164,51 +208,65 @@ __global__ void __launch_bounds__(kQThreads, 2)
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const uint4 u = s4[(i + t) & 7];   // 16-byte chunks rotated by token: 8 bank groups per warp
-        x[8 * i + 0] = bf16_lo(u.x);
-        x[8 * i + 1] = bf16_hi(u.x);
-        x[8 * i + 2] = bf16_lo(u.y);
-        x[8 * i + 3] = bf16_hi(u.y);
-        x[8 * i + 4] = bf16_lo(u.z);
-        x[8 * i + 5] = bf16_hi(u.z);
-        x[8 * i + 6] = bf16_lo(u.w);
-        x[8 * i + 7] = bf16_hi(u.w);
+        x[4 * i + 0] = bf16x2_to_float2(u.x);
+        x[4 * i + 1] = bf16x2_to_float2(u.y);
+        x[4 * i + 2] = bf16x2_to_float2(u.z);
+        x[4 * i + 3] = bf16x2_to_float2(u.w);
       }
     }
     __syncthreads();                   // raw rows read before k_hat rows overwrite them
+    // stage h = 1: within each pair
 #pragma unroll
-    for (int hb = 0; hb < 6; ++hb) {
+    for (int i = 0; i < 32; ++i) x[i] = make_float2(x[i].x + x[i].y, x[i].x - x[i].y);
+    // stages h = 2 .. 32: pairs (i, i + h/2) of float2
 #pragma unroll
-      for (int n = 0; n < 32; ++n) {
+    for (int hb = 0; hb < 5; ++hb) {
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
         const int h = 1 << hb;
         const int j = ((n >> hb) << (hb + 1)) | (n & (h - 1));
-        const float a = x[j], b = x[j + h];
-        x[j] = a + b;
-        x[j + h] = a - b;
+        const float2 a = x[j], b = x[j + h];
+        x[j] = __fadd2_rn(a, b);
+        x[j + h] = __fadd2_rn(a, make_float2(-b.x, -b.y));
       }
     }
+    // stage h = 64 across the thread pair, through this token's k_hat row
+    float* krow = &S.kh[t * kKhStride];
+    {
+      float4* mine = reinterpret_cast<float4*>(krow + 68 * half);
 #pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      const float y = __shfl_xor_sync(0xffffffffu, x[i], 1);   // the partner's channel i + 64 or i - 64
-      x[i] = half ? y - x[i] : x[i] + y;
+      for (int i = 0; i < 16; ++i) mine[i] = make_float4(x[2 * i].x, x[2 * i].y, x[2 * i + 1].x, x[2 * i + 1].y);
+      __syncwarp();
+      const float4* other = reinterpret_cast<const float4*>(krow + 68 * (half ^ 1));
+      const float2 sgn = half ? make_float2(-1.0f, -1.0f) : make_float2(1.0f, 1.0f);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float4 y = other[i];
+        x[2 * i] = __ffma2_rn(x[2 * i], sgn, make_float2(y.x, y.y));          // a + b, or a - b
+        x[2 * i + 1] = __ffma2_rn(x[2 * i + 1], sgn, make_float2(y.z, y.w));
+      }
     }
-    float sq[32];
+    float2 sq2 = make_float2(0.0f, 0.0f), sq2b = make_float2(0.0f, 0.0f);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) sq[i] = x[i] * x[i] + x[i + 32] * x[i + 32];
-#pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) {
-#pragma unroll
-      for (int i = 0; i < w; ++i) sq[i] += sq[i + w];
+    for (int i = 0; i < 32; i += 2) {
+      sq2 = __ffma2_rn(x[i], x[i], sq2);
+      sq2b = __ffma2_rn(x[i + 1], x[i + 1], sq2b);
     }
-    const float ss = sq[0] + __shfl_xor_sync(0xffffffffu, sq[0], 1);
+    const float sq = (sq2.x + sq2.y) + (sq2b.x + sq2b.y);
+    const float ss = sq + __shfl_xor_sync(0xffffffffu, sq, 1);
     const float norm = sqrtf(ss * (1.0f / kHeadDim));
     const float rinv = ss > 0.0f ? 1.0f / sqrtf(ss) : 0.0f;
+    // scalar rounded products: the k_hat in registers (code decisions) is the
+    // k_hat stored below (parameters), and its packed subtraction in
+    // code_bits2 cannot be fused with this multiply
 #pragma unroll
-    for (int i = 0; i < 64; ++i) x[i] *= rinv;
+    for (int i = 0; i < 32; ++i) x[i] = make_float2(__fmul_rn(x[i].x, rinv), __fmul_rn(x[i].y, rinv));
     if (half == 0) reinterpret_cast<float*>(blk + kOffKNorm)[t] = norm;
+    __syncwarp();                      // the partner has read this thread's pre-stage values
     {
-      float4* dst = reinterpret_cast<float4*>(&S.kh[t * kKhStride + 64 * half]);
+      float4* dst = reinterpret_cast<float4*>(krow + 68 * half);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) dst[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+      for (int i = 0; i < 16; ++i) dst[i] = make_float4(x[2 * i].x, x[2 * i].y, x[2 * i + 1].x, x[2 * i + 1].y);
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
@@ -218,11 +276,12 @@ __global__ void __launch_bounds__(kQThreads, 2)
     // ---- per-channel key parameters: 16-token slices of 4 channels, then 8 slices
     {
       const int cq = tid & 31, ts = tid >> 5;
-      float4 mn = *reinterpret_cast<const float4*>(&S.kh[(16 * ts) * kKhStride + 4 * cq]);
+      const int col = kh_col(4 * cq);
+      float4 mn = *reinterpret_cast<const float4*>(&S.kh[(16 * ts) * kKhStride + col]);
       float4 mx = mn;
 #pragma unroll
       for (int r = 1; r < 16; ++r) {
-        const float4 v = *reinterpret_cast<const float4*>(&S.kh[(16 * ts + r) * kKhStride + 4 * cq]);
+        const float4 v = *reinterpret_cast<const float4*>(&S.kh[(16 * ts + r) * kKhStride + col]);
         mn.x = fminf(mn.x, v.x); mn.y = fminf(mn.y, v.y); mn.z = fminf(mn.z, v.z); mn.w = fminf(mn.w, v.w);
         mx.x = fmaxf(mx.x, v.x); mx.y = fmaxf(mx.y, v.y); mx.z = fmaxf(mx.z, v.z); mx.w = fmaxf(mx.w, v.w);
       }
@@ -241,7 +300,9 @@ __global__ void __launch_bounds__(kQThreads, 2)
         mx = fmaxf(mx, rmx[ts * kHeadDim + c]);
       }
       const float sc = (mx - mn) / 3.0f;
-      S.kp[kp_index(c)] = make_float2(sc > 0.0f ? 1.0f / sc : 0.0f, mn);
+      float* kqf = reinterpret_cast<float*>(&S.kq[kq_index(c)]);
+      kqf[c & 1] = sc > 0.0f ? 1.0f / sc : 0.0f;
+      kqf[2 + (c & 1)] = -mn;
       reinterpret_cast<float*>(blk + kOffKScale)[c] = sc;
       reinterpret_cast<float*>(blk + kOffKZero)[c] = mn;
     }
@@ -252,17 +313,16 @@ __global__ void __launch_bounds__(kQThreads, 2)
       const int mt = t >> 4, g = t & 7, r = (t >> 3) & 1;
 #pragma unroll
       for (int tig = 0; tig < 4; ++tig) {
-        uint32_t w = 0;
+        uint32_t w = 0u - key_word_magic();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int i = 16 * kk + 8 * hf + 2 * tig + e;    // channel 64 half + i
-              const float2 pq = S.kp[kp_index(64 * half + i)];
-              w |= int2_code(x[i], pq.x, pq.y) << (16 * e + 4 * kk + 2 * hf);
-            }
+            const int i = 16 * kk + 8 * hf + 2 * tig;          // channels 64 half + i, + i + 1 (e = 0, 1)
+            const float4 pq = S.kq[kq_index(64 * half + i)];
+            const uint2 cb = code_bits2(x[i >> 1], make_float2(pq.x, pq.y), make_float2(pq.z, pq.w));
+            w += cb.x << (4 * kk + 2 * hf);
+            w += cb.y << (16 + 4 * kk + 2 * hf);
           }
         }
         S.kw[((mt * 32 + 4 * g + tig) * 4) + 2 * half + r] = w;
