@@ -11,11 +11,12 @@
 // One CTA = one (group, KV head), 256 threads; the thread pair (2t, 2t+1)
 // owns token t, each thread 64 of its channels.
 //   1. V: per 32-channel group min/max (on packed bf16 pairs: exact), s =
-//      (max-min)/3, z = min, codes; codes go to shared memory (transposed),
-//      s/z to the block.
+//      (max-min)/3, z = min, codes; codes go to shared memory (transposed,
+//      four channels per byte), s/z to the block.  The key row is already
+//      being loaded into registers.
 //   2. K: unnormalised fast Walsh-Hadamard transform, H_d = Hu / sqrt(128):
 //      6 butterfly stages in registers (packed f32x2), the 7th across the
-//      thread pair through the token's shared-memory row;
+//      thread pair with shuffles;
 //      n_t = sqrt(|Hu k|^2 / 128); k_hat = Hu k / |Hu k| (= H_d k / n_t).
 //   3. Per-channel min/max of k_hat over the 128 tokens (shared memory,
 //      16-token slices, then 8 slices).
@@ -33,14 +34,14 @@ namespace {
 
 constexpr int kQThreads = 256;   // two threads per token: channels [0, 64) and [64, 128)
 constexpr int kKhStride = 136;   // floats per k_hat row: channels [0, 64) at 0, [64, 128) at 68
-constexpr int kVbStride = 144;   // bytes per value-code row (channel) in shared memory
-constexpr int kKrawOffset = 128 * kKhStride * 4 - 128 * 256;   // raw K rows at the end of the k_hat buffer
+constexpr int kVbStride = 144;   // bytes per value-code row (4 channels) in shared memory
+constexpr int kVbRows = kHeadDim / 4;
 constexpr float kMagic = 12582912.0f;                          // 1.5 * 2^23
 constexpr uint32_t kMagicBits = 0x4B400000u;
 
 struct QuantSmem {
   alignas(16) float kh[kGroup * kKhStride];          // k_hat[t][kh_col(c)]; float4 stores / loads
-  alignas(16) uint8_t vb[kHeadDim * kVbStride + 16];  // value codes [channel][permuted token]; uint4 loads
+  alignas(16) uint8_t vb[kVbRows * kVbStride + 16];  // value codes [channel / 4][permuted token]; uint4 loads
   alignas(16) float4 rmin[8][kHeadDim / 4];          // per 16-token slice: channel minima
   alignas(16) float4 rmax[8][kHeadDim / 4];          // per 16-token slice: channel maxima
   alignas(16) uint32_t kw[1024];                     // key code words, fragment order; uint4 loads
@@ -50,7 +51,6 @@ struct QuantSmem {
 static_assert(offsetof(QuantSmem, vb) % 16 == 0 && offsetof(QuantSmem, kw) % 16 == 0, "alignment");
 static_assert(offsetof(QuantSmem, kq) % 16 == 0, "alignment");
 static_assert((kKhStride * 4) % 16 == 0 && kVbStride % 16 == 0, "rows must keep 16-byte alignment");
-static_assert(kKrawOffset % 16 == 0 && kKrawOffset >= 0, "raw key rows must be 16-byte aligned");
 
 // Column of channel c in a k_hat row: the upper 64 channels are shifted by 16
 // bytes, so that the two threads of a token write different banks and a
@@ -77,15 +77,11 @@ __device__ __forceinline__ uint2 code_bits2(float2 x, float2 inv, float2 negz) {
   return make_uint2(__float_as_uint(__fadd_rn(vx, kMagic)), __float_as_uint(__fadd_rn(vy, kMagic)));
 }
 
-// Byte offset of value-code row (channel) c: rows of the upper 64 channels are
+// Byte offset of value-code row q (channels 4q .. 4q + 3, code of channel
+// 4q + i in bits 2i, 2i + 1 of each byte): rows of the upper 64 channels are
 // shifted by 16 bytes so that the two threads of a token (one per channel
 // half) store into different banks.
-__device__ __forceinline__ int vb_row(int c) { return c * kVbStride + ((c >> 6) << 4); }
-
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ int vb_row(int q) { return q * kVbStride + ((q >> 4) << 4); }
 
 // Position of token/col c inside its 16-byte packing chunk of the byte
 // staging area: chunk (tig, j), byte ((kk * 4) + hf + 2 e).
@@ -142,14 +138,13 @@ __global__ void __launch_bounds__(kQThreads, 2)
     const uint16_t* ksrc = (from_win ? win_k + t * kHeadDim : kin + (row * hkv + head) * kHeadDim) + 64 * half;
     const uint16_t* vsrc = (from_win ? win_v + t * kHeadDim : vin + (row * hkv + head) * kHeadDim) + 64 * half;
 
-    // raw K rows (bf16, 256 B each) -> upper part of the k_hat buffer, in
-    // flight while the values are processed; chunk i of a thread's 128 bytes
-    // is stored at slot (i + t) mod 8 so that a warp's 16-byte accesses
-    // spread over all bank groups
-    uint8_t* kraw = reinterpret_cast<uint8_t*>(S.kh) + kKrawOffset;
+    // this thread's half key row (64 bf16), in flight while the values are processed
+    uint4 kr[8];
+    {
+      const uint4* ks4 = reinterpret_cast<const uint4*>(ksrc);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) cp_async16(kraw + t * 256 + 128 * half + 16 * ((i + t) & 7), ksrc + 8 * i);
-    asm volatile("cp.async.commit_group;" ::: "memory");
+      for (int i = 0; i < 8; ++i) kr[i] = __ldg(ks4 + i);
+    }
 
     // ---- values: per-token INT2 over this thread's two 32-channel groups
     float smax = 0.0f;
@@ -186,11 +181,12 @@ __global__ void __launch_bounds__(kQThreads, 2)
         for (int i = 0; i < 4; ++i) {
           const uint32_t ws[4] = {w4[i].x, w4[i].y, w4[i].z, w4[i].w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = gi * kVGroup + 8 * i + 2 * e;
-            const uint2 cb = code_bits2(bf16x2_to_float2(ws[e]), inv2, negz2);
-            S.vb[vb_row(c) + pt] = (uint8_t)cb.x;       // low byte = code
-            S.vb[vb_row(c + 1) + pt] = (uint8_t)cb.y;
+          for (int qq = 0; qq < 2; ++qq) {   // channels gi*32 + 8i + 4qq .. + 3
+            const uint2 c01 = code_bits2(bf16x2_to_float2(ws[2 * qq]), inv2, negz2);
+            const uint2 c23 = code_bits2(bf16x2_to_float2(ws[2 * qq + 1]), inv2, negz2);
+            // low bytes are the codes (the float bits' constant part has a zero low byte)
+            const uint32_t b = (c01.x & 0xffu) | ((c01.y & 0xffu) << 2) | ((c23.x & 0xffu) << 4) | ((c23.y & 0xffu) << 6);
+            S.vb[vb_row(gi * 8 + 2 * i + qq) + pt] = (uint8_t)b;
           }
         }
       }
@@ -201,20 +197,13 @@ __global__ void __launch_bounds__(kQThreads, 2)
     // ---- keys: rotation (6 butterfly stages in registers + 1 across the
     // thread pair), norm, unit vector
     float2 x[32];                      // channels 64 half + 2i, + 2i + 1
-    cp_async_wait_all();
-    __syncthreads();                   // every thread's raw K row is in shared memory
-    {
-      const uint4* s4 = reinterpret_cast<const uint4*>(kraw + t * 256 + 128 * half);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint4 u = s4[(i + t) & 7];   // 16-byte chunks rotated by token: 8 bank groups per warp
-        x[4 * i + 0] = bf16x2_to_float2(u.x);
-        x[4 * i + 1] = bf16x2_to_float2(u.y);
-        x[4 * i + 2] = bf16x2_to_float2(u.z);
-        x[4 * i + 3] = bf16x2_to_float2(u.w);
-      }
+    for (int i = 0; i < 8; ++i) {
+      x[4 * i + 0] = bf16x2_to_float2(kr[i].x);
+      x[4 * i + 1] = bf16x2_to_float2(kr[i].y);
+      x[4 * i + 2] = bf16x2_to_float2(kr[i].z);
+      x[4 * i + 3] = bf16x2_to_float2(kr[i].w);
     }
-    __syncthreads();                   // raw rows read before k_hat rows overwrite them
     // stage h = 1: within each pair
 #pragma unroll
     for (int i = 0; i < 32; ++i) x[i] = make_float2(x[i].x + x[i].y, x[i].x - x[i].y);
@@ -230,22 +219,16 @@ __global__ void __launch_bounds__(kQThreads, 2)
         x[j + h] = __fadd2_rn(a, make_float2(-b.x, -b.y));
       }
     }
-    // stage h = 64 across the thread pair, through this token's k_hat row
-    float* krow = &S.kh[t * kKhStride];
+    // stage h = 64 across the thread pair (the partner holds channel c +- 64)
     {
-      float4* mine = reinterpret_cast<float4*>(krow + 68 * half);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) mine[i] = make_float4(x[2 * i].x, x[2 * i].y, x[2 * i + 1].x, x[2 * i + 1].y);
-      __syncwarp();
-      const float4* other = reinterpret_cast<const float4*>(krow + 68 * (half ^ 1));
       const float2 sgn = half ? make_float2(-1.0f, -1.0f) : make_float2(1.0f, 1.0f);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float4 y = other[i];
-        x[2 * i] = __ffma2_rn(x[2 * i], sgn, make_float2(y.x, y.y));          // a + b, or a - b
-        x[2 * i + 1] = __ffma2_rn(x[2 * i + 1], sgn, make_float2(y.z, y.w));
+      for (int i = 0; i < 32; ++i) {
+        const float2 y = make_float2(__shfl_xor_sync(0xffffffffu, x[i].x, 1), __shfl_xor_sync(0xffffffffu, x[i].y, 1));
+        x[i] = __ffma2_rn(x[i], sgn, y);   // a + b, or a - b
       }
     }
+    float* krow = &S.kh[t * kKhStride];
     float2 sq2 = make_float2(0.0f, 0.0f), sq2b = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
@@ -262,7 +245,6 @@ __global__ void __launch_bounds__(kQThreads, 2)
 #pragma unroll
     for (int i = 0; i < 32; ++i) x[i] = make_float2(__fmul_rn(x[i].x, rinv), __fmul_rn(x[i].y, rinv));
     if (half == 0) reinterpret_cast<float*>(blk + kOffKNorm)[t] = norm;
-    __syncwarp();                      // the partner has read this thread's pre-stage values
     {
       float4* dst = reinterpret_cast<float4*>(krow + 68 * half);
 #pragma unroll
@@ -341,12 +323,14 @@ __global__ void __launch_bounds__(kQThreads, 2)
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const int rowc = 16 * mt + g + 8 * r;
-          const uint4 b = *reinterpret_cast<const uint4*>(&S.vb[vb_row(rowc) + (tig * 2 + j) * 16]);
+          const int sh = 2 * (rowc & 3);                 // this channel's bits in each byte
+          const uint4 b = *reinterpret_cast<const uint4*>(&S.vb[vb_row(rowc >> 2) + (tig * 2 + j) * 16]);
           const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
           uint32_t w = 0;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t y = (bw[kk] | (bw[kk] >> 6)) & 0x000F000Fu;
+            const uint32_t cw = (bw[kk] >> sh) & 0x03030303u;
+            const uint32_t y = (cw | (cw >> 6)) & 0x000F000Fu;
             w |= y << (4 * kk);
           }
           wv[2 * j + r] = w;
