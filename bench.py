@@ -397,8 +397,9 @@ def gpu_arm(args, rank, world):
 
 
 def profile_case(args):
-    """Small, self-contained launches for ncu captures (no L2 flush, no
-    bf16 reference, a few hundred MB on the device)."""
+    """Small, self-contained launches for ncu captures (no L2 flush, a few
+    hundred MB on the device): the INT2 decode, the 128K quantise, or the
+    BF16 reference decode."""
     import torch
 
     from int2_kv_cache_oscar_gb300 import oscar as O_
@@ -408,6 +409,17 @@ def profile_case(args):
     k, v = W.make_sequence_kv(CTX, HKV, W.LLAMA_RECIPE, gen, "cuda")
     q = W.make_q(1, HQ, seed=2, device="cuda")
     cache = O_.OscarCache(1, HKV, CTX)
+    if args.profile_bf16:
+        kc, vc = bf16_cache(torch, [k], [v], CTX)
+        del k, v
+        torch.cuda.synchronize()
+        out = torch.empty((1, HQ, D), dtype=torch.bfloat16, device="cuda")
+        wsb = torch.empty(O_.oscar_bf16_decode_workspace_bytes(1, HKV, HQ), dtype=torch.uint8, device="cuda")
+        for _ in range(args.steps):
+            O_.oscar_bf16_decode_attention([0], [CTX], kc, vc, HKV, CTX, q, HQ, 0.0, out, wsb)
+        torch.cuda.synchronize()
+        print("profile bf16 done")
+        return
     if args.profile_quantize:
         for _ in range(args.steps):
             O_.oscar_cache_reset(cache.handle, 0)
@@ -485,6 +497,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--profile-decode", action="store_true",
                     help="profiling case: build the 128K INT2 cache only and run `steps` decodes")
+    ap.add_argument("--profile-bf16", action="store_true",
+                    help="small self-contained BF16 reference decode launches for ncu")
     ap.add_argument("--profile-quantize", action="store_true",
                     help="profiling case: `steps` 128K quantise appends (8 KV heads)")
     args = ap.parse_args()
@@ -521,7 +535,7 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     torch.cuda.set_device(local_rank)
-    if args.profile_decode or args.profile_quantize:
+    if args.profile_decode or args.profile_quantize or args.profile_bf16:
         profile_case(args)
         return
 
