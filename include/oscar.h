@@ -179,6 +179,28 @@ oscar_status oscar_decode_attention(oscar_cache* cache, int32_t n_seqs, const in
                                     void* stream);
 
 /*
+ * One decode step fused: append one token to each of `n_seqs` sequences,
+ * then decode, with the same result as oscar_quantize_append (one row per
+ * sequence) followed by oscar_decode_attention.  The ai-papers.net OScaR
+ * summary, section "まとめと今後の展望", notes that the quantisation
+ * overhead weighs relatively more at short context; this call removes one
+ * launch from most decode steps.
+ *   k_new, v_new  device bf16 [n_seqs, Hkv, 128], the new token of each
+ *                 sequence (16-byte aligned)
+ *   other arguments as for oscar_decode_attention.
+ * When no sequence's new length is a multiple of 128 (127 steps in 128),
+ * the step is one decode launch: the combine kernel attends the new token as
+ * the last window row straight from k_new / v_new and stores it into the
+ * window.  When a group closes, the quantiser runs first (two launches), so
+ * the group is attended quantised.  All arguments are validated before
+ * anything is enqueued; on error nothing changes.
+ */
+oscar_status oscar_append_decode(oscar_cache* cache, int32_t n_seqs, const int32_t* seq_ids,
+                                 const void* k_new, const void* v_new, const void* q,
+                                 int32_t num_q_heads, float softmax_scale, void* out,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Decode that allocates nothing and takes no workspace.  The OScaR pages have
  * no counterpart to this call; it exists for callers that cannot allocate
  * device memory where they decode (code inside a memory pool or arena it does

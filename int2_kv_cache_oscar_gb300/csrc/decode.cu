@@ -577,6 +577,10 @@ __global__ void __launch_bounds__(kCombineThreads)
   const bool active = h < gqa;
   const int ng = units_of_len(sq.len, p.h.bf16_mode);
   const int wlen = p.h.bf16_mode ? 0 : (sq.len % kGroup);
+  // fused append: the newest window row comes from the input (the host only
+  // fuses when no group closes, so wlen >= 1); the others from the arena
+  const bool fused = p.h.k_new != nullptr;
+  const int wstored = fused ? wlen - 1 : wlen;
   const int64_t T = p.h.n_units, N = p.h.n_ctas;
   int64_t first = 0, count = 0, rho = 0;
   if (ng > 0) {
@@ -596,16 +600,30 @@ __global__ void __launch_bounds__(kCombineThreads)
   }
   qs[h][c] = active ? __uint_as_float((uint32_t)p.h.q[((int64_t)b * p.h.hq + j * gqa + h) * kHeadDim + c] << 16)
                     : 0.0f;
+  if (fused && tid < 32) {
+    // the new token: 16 x 16 bytes of K (tid < 16) and of V, into shared row
+    // wlen - 1 and into the arena window slot it occupies from now on (the
+    // main kernel never reads windows; the bulk copy below reads rows < wlen - 1)
+    const int part = tid >> 4, chunk = tid & 15;
+    const uint16_t* src = (part ? p.h.v_new : p.h.k_new) + ((int64_t)b * hkv + j) * kHeadDim + 8 * chunk;
+    const uint4 val = *reinterpret_cast<const uint4*>(src);
+    uint16_t* srow = (part ? wv : wk) + (wlen - 1) * kHeadDim;
+    *reinterpret_cast<uint4*>(srow + 8 * chunk) = val;
+    uint16_t* arow = reinterpret_cast<uint16_t*>(const_cast<uint8_t*>(arena) + p.h.windows_off +
+                                                 ((int64_t)sq.slot * hkv + j) * kWindowBytes) +
+                     part * kGroup * kHeadDim + (wlen - 1) * kHeadDim;
+    *reinterpret_cast<uint4*>(arow + 8 * chunk) = val;
+  }
   __syncthreads();
   grid_dependency_wait();            // the main kernel's partials are complete and visible
   // stage 0: window rows + first chunk of partials
   if (tid == 0) {
     const int64_t n0 = count < per_chunk ? count : per_chunk;
-    const uint32_t wbytes = (uint32_t)wlen * kHeadDim * 2;
+    const uint32_t wbytes = (uint32_t)wstored * kHeadDim * 2;
     const uint32_t pbytes = (uint32_t)(n0 * rec_bytes);
     if (wbytes + pbytes > 0) {
       mbar_arrive_expect_tx(&bar, 2 * wbytes + pbytes);
-      if (wlen > 0) {
+      if (wstored > 0) {
         const uint8_t* wsrc = arena + p.h.windows_off + ((int64_t)sq.slot * hkv + j) * kWindowBytes;
         bulk_g2s(wk, wsrc, wbytes, &bar);
         bulk_g2s(wv, wsrc + kGroup * kHeadDim * 2, wbytes, &bar);

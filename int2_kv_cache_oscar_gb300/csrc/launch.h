@@ -73,6 +73,11 @@ struct DecodeHeader {
   uint16_t* out;
   float* partials;
   uint32_t* err_word;
+  // fused append: when set, each (sequence, KV head) row's newest window
+  // token (window row len mod 128 - 1) is taken from these [n_seqs, hkv, d]
+  // bf16 rows instead of the arena, and stored into the arena window
+  const uint16_t* k_new;
+  const uint16_t* v_new;
 };
 
 template <int MAXS>

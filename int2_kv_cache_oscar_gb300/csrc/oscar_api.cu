@@ -142,7 +142,7 @@ oscar_status run_decode(int device, int sms, int ctas_per_sm, int32_t n, const i
                         int hkv, int hq, float scale, int bf16_mode, int max_groups, int64_t blocks_off,
                         int64_t windows_off, const uint8_t* arena, uint32_t* err_word, const uint16_t* kc,
                         const uint16_t* vc, const void* q, void* out, void* ws, size_t ws_bytes,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, const void* k_new = nullptr, const void* v_new = nullptr) {
   DecodeParams<MAXS> P;
   std::memset(&P, 0, sizeof(P));
   int64_t rows = 0;
@@ -168,6 +168,8 @@ oscar_status run_decode(int device, int sms, int ctas_per_sm, int32_t n, const i
   P.h.out = static_cast<uint16_t*>(out);
   P.h.partials = static_cast<float*>(ws);
   P.h.err_word = err_word;
+  P.h.k_new = static_cast<const uint16_t*>(k_new);
+  P.h.v_new = static_cast<const uint16_t*>(v_new);
   cudaError_t e;
   if (bf16_mode)
     e = launch_decode_bf16(P, kc, vc, stream, g_ev_start, g_ev_stop);
@@ -394,6 +396,73 @@ oscar_status oscar_decode_attention(oscar_cache* c, int32_t n_seqs, const int32_
                                        c->layout.blocks_off, c->layout.windows_off, c->arena, err_word, nullptr,
                                        nullptr, q, out, workspace, workspace_bytes, st);
     if (s != OSCAR_OK) return s;
+    return ok();
+  } catch (const std::exception& ex) {
+    return fail(OSCAR_ERR_INVALID_ARG, "host allocation failed: %s", ex.what());
+  }
+}
+
+oscar_status oscar_append_decode(oscar_cache* c, int32_t n_seqs, const int32_t* seq_ids, const void* k_new,
+                                 const void* v_new, const void* q, int32_t num_q_heads, float softmax_scale, void* out,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  try {
+    // every argument is checked before anything is enqueued
+    if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+    if (n_seqs < 1) return fail(OSCAR_ERR_INVALID_ARG, "n_seqs must be >= 1");
+    if (n_seqs > kDecodeSeqsLarge) return fail(OSCAR_ERR_CAPACITY, "at most %d sequences per call", kDecodeSeqsLarge);
+    if (!seq_ids || !k_new || !v_new || !q || !out || !workspace) return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+    const int hkv = c->cfg.num_kv_heads;
+    if (num_q_heads < hkv || num_q_heads % hkv != 0)
+      return fail(OSCAR_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of Hkv");
+    if (num_q_heads / hkv > kMaxGqa)
+      return fail(OSCAR_ERR_UNSUPPORTED, "at most %d query heads per KV head", kMaxGqa);
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 16))
+      return fail(OSCAR_ERR_INVALID_ARG, "k_new, v_new, q, out and workspace must be 16-byte aligned");
+    if (!(softmax_scale >= 0.0f) || std::isinf(softmax_scale))
+      return fail(OSCAR_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
+    std::vector<char> seen;
+    oscar_status s = check_slots(c, n_seqs, seq_ids, seen);
+    if (s != OSCAR_OK) return s;
+    size_t need = 0;
+    s = oscar_decode_workspace_bytes(c, n_seqs, num_q_heads, &need);
+    if (s != OSCAR_OK) return s;
+    if (workspace_bytes < need)
+      return fail(OSCAR_ERR_CAPACITY, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+    bool closes = false;
+    std::vector<int32_t> lens(n_seqs);
+    for (int32_t i = 0; i < n_seqs; ++i) {
+      lens[i] = c->len[seq_ids[i]] + 1;
+      if (lens[i] > c->cfg.max_seq_len)
+        return fail(OSCAR_ERR_CAPACITY, "sequence %d would reach %d tokens > max_seq_len %d", seq_ids[i], lens[i],
+                    c->cfg.max_seq_len);
+      if (lens[i] % kGroup == 0) closes = true;
+    }
+    if (closes) {
+      // a group closes: it is attended quantised, so the quantiser runs first
+      std::vector<int32_t> cu(n_seqs + 1);
+      for (int32_t i = 0; i <= n_seqs; ++i) cu[i] = i;
+      s = oscar_quantize_append(c, n_seqs, seq_ids, cu.data(), k_new, v_new, stream);
+      if (s != OSCAR_OK) return s;
+      return oscar_decode_attention(c, n_seqs, seq_ids, q, num_q_heads, softmax_scale, out, workspace,
+                                    workspace_bytes, stream);
+    }
+    const float scale = softmax_scale == 0.0f ? 1.0f / std::sqrt((float)kHeadDim) : softmax_scale;
+    DeviceGuard dg(c->cfg.device);
+    if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+    uint32_t* err_word = reinterpret_cast<uint32_t*>(c->arena);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n_seqs <= kDecodeSeqsSmall)
+      s = run_decode<kDecodeSeqsSmall>(c->cfg.device, c->sms, decode_int2_ctas_per_sm(), n_seqs, seq_ids,
+                                       lens.data(), hkv, num_q_heads, scale, 0, c->layout.max_groups,
+                                       c->layout.blocks_off, c->layout.windows_off, c->arena, err_word, nullptr,
+                                       nullptr, q, out, workspace, workspace_bytes, st, k_new, v_new);
+    else
+      s = run_decode<kDecodeSeqsLarge>(c->cfg.device, c->sms, decode_int2_ctas_per_sm(), n_seqs, seq_ids,
+                                       lens.data(), hkv, num_q_heads, scale, 0, c->layout.max_groups,
+                                       c->layout.blocks_off, c->layout.windows_off, c->arena, err_word, nullptr,
+                                       nullptr, q, out, workspace, workspace_bytes, st, k_new, v_new);
+    if (s != OSCAR_OK) return s;
+    for (int32_t i = 0; i < n_seqs; ++i) c->len[seq_ids[i]] = lens[i];
     return ok();
   } catch (const std::exception& ex) {
     return fail(OSCAR_ERR_INVALID_ARG, "host allocation failed: %s", ex.what());

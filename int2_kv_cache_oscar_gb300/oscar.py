@@ -73,6 +73,7 @@ def _load() -> ctypes.CDLL:
                                         SZ, P],
         "oscar_set_timing_events": [P, P],
         "oscar_decode_attention_noalloc": [P, I32, I32P, P, I32, ctypes.c_float, P, P],
+        "oscar_append_decode": [P, I32, I32P, P, P, P, I32, ctypes.c_float, P, P, SZ, P],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -183,6 +184,16 @@ def oscar_decode_attention_noalloc(handle, seq_ids: Sequence[int], q: torch.Tens
                                                ctypes.c_float(softmax_scale), _ptr(out), _stream(stream)))
 
 
+def oscar_append_decode(handle, seq_ids: Sequence[int], k_new: torch.Tensor, v_new: torch.Tensor,
+                        q: torch.Tensor, num_q_heads: int, softmax_scale: float, out: torch.Tensor,
+                        workspace: torch.Tensor, stream=None) -> None:
+    """Append one token per sequence and decode, in one call (one launch when
+    no group closes)."""
+    _check(_lib.oscar_append_decode(handle, len(seq_ids), _i32(seq_ids), _ptr(k_new), _ptr(v_new), _ptr(q),
+                                    num_q_heads, ctypes.c_float(softmax_scale), _ptr(out), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
 def oscar_cache_bytes(handle, seq: int, kind: int) -> int:
     out = ctypes.c_size_t(0)
     _check(_lib.oscar_cache_bytes(handle, seq, kind, ctypes.byref(out)))
@@ -267,3 +278,8 @@ class OscarCache:
     def decode(self, seq_ids, q, num_q_heads, out, workspace, softmax_scale=0.0, stream=None):
         oscar_decode_attention(self.handle, seq_ids, q, num_q_heads, softmax_scale, out, workspace,
                                stream)
+
+    def append_decode(self, seq_ids, k_new, v_new, q, num_q_heads, out, workspace, softmax_scale=0.0,
+                      stream=None):
+        oscar_append_decode(self.handle, seq_ids, k_new, v_new, q, num_q_heads, softmax_scale, out, workspace,
+                            stream)
