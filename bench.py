@@ -157,13 +157,25 @@ class Timer:
 
     def run(self, fn, steps, warmup, flush=True, kernel_events=None):
         """Mean microseconds of fn() over `steps` timed calls (CUDA events on
-        the current stream, L2 flushed before each call)."""
+        the current stream, L2 flushed before each call).  With
+        kernel_events, a second pass of `steps` calls also times the main
+        kernel alone with events the library records around its launch; the
+        step time comes from the first pass, where no such events sit
+        between the step's kernels."""
         torch = self.torch
         for _ in range(warmup):
             if flush:
                 self.flush.zero_()
             fn()
         torch.cuda.synchronize()
+        t, _ = self._pass(fn, steps, flush, None)
+        kt = None
+        if kernel_events is not None:
+            _, kt = self._pass(fn, steps, flush, kernel_events)
+        return t, kt
+
+    def _pass(self, fn, steps, flush, kernel_events):
+        torch = self.torch
         pairs, kpairs = [], []
         for _ in range(steps):
             if flush:
@@ -263,7 +275,7 @@ def gpu_arm(args, rank, world):
 
         dec_us, kern_us = timer.run(decode, K, Wm,
                                     kernel_events=lambda a, b: O_.oscar_set_timing_events(a, b))
-        launches += K * 2
+        launches += K * 4                                  # two timed passes of main + combine
         O_.oscar_cache_check(cache.handle)
         alg_bytes = (CTX // 128) * HKV * BLOCK_BYTES
         step_bytes = alg_bytes + 2 * HQ * D * 2
@@ -293,7 +305,7 @@ def gpu_arm(args, rank, world):
 
         ref_us, ref_kern = timer.run(ref_decode, K, Wm,
                                      kernel_events=lambda a, b: O_.oscar_set_timing_events(a, b))
-        launches += K * 2
+        launches += K * 4
         bf16_bytes = CTX * HKV * 512
         del kc, vc
         out["bf16_ref"] = {"us_per_step": round(ref_us, 2), "main_kernel_us": round(ref_kern, 2),
@@ -319,7 +331,7 @@ def gpu_arm(args, rank, world):
                 kc, vc = bf16_cache(torch, ks, vs, L)
                 tb, _ = timer.run(lambda: O_.oscar_bf16_decode_attention([0], [L], kc, vc, HKV, L, qq, HQ,
                                                                          0.0, o1, wsb), K, Wm)
-                launches += 4 * K
+                launches += 6 * K                          # INT2: two passes; BF16: one
                 b = int2_bytes([L])
                 sweep[str(L)] = {"us": round(t, 2), "kernel_us": round(kt, 2),
                                  "GBps": round(b / (kt * 1e-6) / 1e9, 1),
@@ -346,7 +358,7 @@ def gpu_arm(args, rank, world):
                                device="cuda")
             tb, _ = timer.run(lambda: O_.oscar_bf16_decode_attention(list(range(B)), [L] * B, kc, vc, HKV, L,
                                                                      qq, HQ, 0.0, o1, wsb2), K, Wm)
-            launches += 4 * K
+            launches += 6 * K
             b = int2_bytes([L] * B)
             out["multi_batch"] = {"batch": B, "ctx": L, "us": round(t, 2), "tokens_per_s": round(B / (t * 1e-6)),
                                   "kernel_GBps": round(b / (kt * 1e-6) / 1e9, 1),
