@@ -52,6 +52,15 @@ def load_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def read_peak_tflops():
+    """Measured dense bf16 tensor throughput (burst), else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f).get("bf16_tflops", 1900.0))
+    return 1900.0
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     for name in ("decode.cu", "common.cuh", "decode_common.cuh", "launch.h"):
@@ -366,6 +375,27 @@ def gpu_arm(args, rank, world):
                                   "bf16_us": round(tb, 2), "bf16_tokens_per_s": round(B / (tb * 1e-6)),
                                   "throughput_ratio": round(tb / t, 2)}
             del c, ks, vs, kc, vc
+            torch.cuda.empty_cache()
+
+        # ---------------- chunked prefill: 512 queries against a 32K-token history
+        if not args.quick:
+            L, C = 32768, 512
+            c, ks, vs = build_cache(O_, W, torch, [L], (5, W.LLAMA_RECIPE))
+            genp = torch.Generator(device="cuda")
+            genp.manual_seed(55)
+            qc = torch.randn((C, HQ, D), generator=genp, device="cuda").to(torch.bfloat16)
+            oc = torch.empty_like(qc)
+            lc = torch.empty((C, HQ), dtype=torch.float32, device="cuda")
+            tp, _ = timer.run(lambda: O_.oscar_prefill_attention(c.handle, 0, qc, HQ, 0.0, oc, lc), K, Wm)
+            launches += K
+            flops = 4.0 * C * HQ * L * D                    # q.k and p.v, 2 flops per multiply-add
+            tf = flops / (tp * 1e-6) / 1e12
+            bf16_peak = read_peak_tflops()
+            out["prefill"] = {"chunk": C, "ctx": L, "us": round(tp, 1), "tflops": round(tf, 1),
+                              "bound": "tensor", "peak_tflops": bf16_peak,
+                              "frac_of_bf16_peak": round(tf / bf16_peak, 3) if bf16_peak else None,
+                              "note": "fp16 hi+lo operands: 2 mma per product term"}
+            del c, ks, vs, qc, oc, lc
             torch.cuda.empty_cache()
 
         # ---------------- ragged serving stream: 8 sequences, 4K..128K

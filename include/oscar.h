@@ -201,6 +201,24 @@ oscar_status oscar_append_decode(oscar_cache* cache, int32_t n_seqs, const int32
                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Chunked-prefill attention over the cache: each of the n_q queries of a new
+ * chunk of sequence `seq` attends to every token already in its cache
+ * (quantised groups and window; no mask, the cache precedes the chunk), with
+ * the decode path's scores and values (OScaR abstract; ai-papers.net
+ * "OScaRの提案手法").  Call it before appending the chunk; the chunk's own
+ * causal attention is merged in by the caller with lse.
+ *   q            device bf16 [n_q, num_q_heads, 128], 16-byte aligned
+ *   out          device bf16 [n_q, num_q_heads, 128], 16-byte aligned
+ *   lse          device fp32 [n_q, num_q_heads] or NULL: ln sum_t exp(s_t)
+ *                per row (natural log, scores times softmax_scale)
+ *   softmax_scale  0 means 1 / sqrt(128)
+ * Any GQA ratio.  Needs no workspace.  The sequence must be non-empty.
+ */
+oscar_status oscar_prefill_attention(oscar_cache* cache, int32_t seq, int32_t n_q, const void* q,
+                                     int32_t num_q_heads, float softmax_scale, void* out, float* lse,
+                                     void* stream);
+
+/*
  * Decode that allocates nothing and takes no workspace.  The OScaR pages have
  * no counterpart to this call; it exists for callers that cannot allocate
  * device memory where they decode (code inside a memory pool or arena it does

@@ -92,6 +92,31 @@ constexpr int kDecodeSeqsLarge = 1024;
 // Floats of one partial record (o[128], m, l, 2 pad) per query head.
 constexpr int kPartialFloats = 132;
 
+// ----------------------------------------------------------------- prefill
+
+// One chunked-prefill attention launch: n_q queries of one sequence against
+// every token in its cache.  Rows are (query, head) pairs, query-major.
+struct PrefillParams {
+  int32_t slot;
+  int32_t hkv;
+  int32_t gqa;
+  int32_t hq;
+  int32_t rows;          // n_q * gqa (per KV head)
+  int32_t ng;            // full groups in the cache
+  int32_t wlen;          // window tokens
+  int32_t max_groups;
+  int64_t blocks_off;
+  int64_t windows_off;
+  float scale_log2;      // softmax_scale * log2(e)
+  int32_t pad;
+  const uint16_t* q;     // [n_q, hq, d] bf16
+  uint16_t* out;         // [n_q, hq, d] bf16
+  float* lse;            // [n_q, hq] fp32 natural-log log-sum-exp, or NULL
+  uint32_t* err_word;
+};
+
+cudaError_t launch_prefill(const PrefillParams& p, const uint8_t* arena, cudaStream_t stream);
+
 int num_sms(int device);
 int decode_int2_ctas_per_sm();
 int decode_bf16_ctas_per_sm();

@@ -469,6 +469,48 @@ oscar_status oscar_append_decode(oscar_cache* c, int32_t n_seqs, const int32_t* 
   }
 }
 
+oscar_status oscar_prefill_attention(oscar_cache* c, int32_t seq, int32_t n_q, const void* q, int32_t num_q_heads,
+                                     float softmax_scale, void* out, float* lse, void* stream) {
+  if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+  if (seq < 0 || seq >= c->cfg.max_batch) return fail(OSCAR_ERR_INVALID_ARG, "seq %d out of range", seq);
+  if (n_q < 1) return fail(OSCAR_ERR_INVALID_ARG, "n_q must be >= 1");
+  if (!q || !out) return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+  const int hkv = c->cfg.num_kv_heads;
+  if (num_q_heads < hkv || num_q_heads % hkv != 0)
+    return fail(OSCAR_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of Hkv");
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(lse, 4))
+    return fail(OSCAR_ERR_INVALID_ARG, "q and out must be 16-byte aligned, lse 4-byte aligned");
+  if (!(softmax_scale >= 0.0f) || std::isinf(softmax_scale))
+    return fail(OSCAR_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
+  const int L = c->len[seq];
+  if (L < 1) return fail(OSCAR_ERR_INVALID_ARG, "sequence %d is empty", seq);
+  const int64_t rows = (int64_t)n_q * (num_q_heads / hkv);
+  if (rows > (int64_t)INT32_MAX / 2) return fail(OSCAR_ERR_CAPACITY, "too many query rows");
+  PrefillParams P;
+  std::memset(&P, 0, sizeof(P));
+  P.slot = seq;
+  P.hkv = hkv;
+  P.gqa = num_q_heads / hkv;
+  P.hq = num_q_heads;
+  P.rows = (int32_t)rows;
+  P.ng = L / kGroup;
+  P.wlen = L % kGroup;
+  P.max_groups = c->layout.max_groups;
+  P.blocks_off = c->layout.blocks_off;
+  P.windows_off = c->layout.windows_off;
+  const float scale = softmax_scale == 0.0f ? 1.0f / std::sqrt((float)kHeadDim) : softmax_scale;
+  P.scale_log2 = scale * 1.4426950408889634f;
+  P.q = static_cast<const uint16_t*>(q);
+  P.out = static_cast<uint16_t*>(out);
+  P.lse = lse;
+  P.err_word = reinterpret_cast<uint32_t*>(c->arena);
+  DeviceGuard dg(c->cfg.device);
+  if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+  cudaError_t e = launch_prefill(P, c->arena, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return ok();
+}
+
 oscar_status oscar_cache_bytes(const oscar_cache* c, int32_t seq, int32_t kind, size_t* out_bytes) {
   if (!c || !out_bytes) return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
   if (kind == OSCAR_BYTES_ARENA) {

@@ -74,6 +74,7 @@ def _load() -> ctypes.CDLL:
         "oscar_set_timing_events": [P, P],
         "oscar_decode_attention_noalloc": [P, I32, I32P, P, I32, ctypes.c_float, P, P],
         "oscar_append_decode": [P, I32, I32P, P, P, P, I32, ctypes.c_float, P, P, SZ, P],
+        "oscar_prefill_attention": [P, I32, I32, P, I32, ctypes.c_float, P, P, P],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -192,6 +193,15 @@ def oscar_append_decode(handle, seq_ids: Sequence[int], k_new: torch.Tensor, v_n
     _check(_lib.oscar_append_decode(handle, len(seq_ids), _i32(seq_ids), _ptr(k_new), _ptr(v_new), _ptr(q),
                                     num_q_heads, ctypes.c_float(softmax_scale), _ptr(out), _ptr(workspace),
                                     workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def oscar_prefill_attention(handle, seq: int, q: torch.Tensor, num_q_heads: int, softmax_scale: float,
+                            out: torch.Tensor, lse: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Attention of a chunk's queries q [n_q, num_q_heads, 128] over the
+    sequence's cached tokens; out gets the rows, lse (fp32 [n_q, heads]) their
+    log-sum-exp."""
+    _check(_lib.oscar_prefill_attention(handle, seq, q.shape[0], _ptr(q), num_q_heads,
+                                        ctypes.c_float(softmax_scale), _ptr(out), _ptr(lse), _stream(stream)))
 
 
 def oscar_cache_bytes(handle, seq: int, kind: int) -> int:

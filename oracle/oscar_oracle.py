@@ -294,6 +294,31 @@ def decode_attention(q: np.ndarray, caches: Sequence[Sequence[HeadCache]],
     return out
 
 
+def history_attention(q: np.ndarray, cache: HeadCache, softmax_scale: Optional[float] = None):
+    """Chunked-prefill attention of query rows q [R, d] (the chunk's queries of
+    the query heads sharing one KV head) over every token already in the
+    cache: quantised groups and window, no mask (the cache precedes the
+    chunk).  Returns (o [R, d], lse [R]) with lse = ln sum_t exp(s_t), so that
+    the chunk's own causal part can be merged in (merge_attention)."""
+    if cache.length == 0:
+        raise ValueError("attention over an empty cache")
+    s = decode_scores(q, cache, softmax_scale)              # [T, R]
+    m = s.max(axis=0)
+    e = np.exp(s - m[None, :])
+    l = e.sum(axis=0)
+    o = (e / l[None, :]).T @ decode_values(cache)
+    return o, m + np.log(l)
+
+
+def merge_attention(o1: np.ndarray, lse1: np.ndarray, o2: np.ndarray, lse2: np.ndarray):
+    """Attention over the union of two disjoint key sets from the parts'
+    outputs and log-sum-exps (the log-sum-exp merge of split-K decoding)."""
+    mx = np.maximum(lse1, lse2)
+    w1, w2 = np.exp(lse1 - mx), np.exp(lse2 - mx)
+    o = (w1[:, None] * o1 + w2[:, None] * o2) / (w1 + w2)[:, None]
+    return o, mx + np.log(w1 + w2)
+
+
 def attention_exact(q: np.ndarray, k: np.ndarray, v: np.ndarray,
                     softmax_scale: Optional[float] = None) -> np.ndarray:
     """Unquantised single-query attention of q [Hg, d] over k, v [L, d]."""

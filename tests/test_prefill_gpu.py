@@ -1,0 +1,81 @@
+"""GPU parity of oscar_prefill_attention (a chunk's queries against every token
+already in the cache).
+
+Gate, per (query, head) row, against the oracle's history_attention over the
+SAME cache read back from the GPU: the output within 2e-3 + half a bf16 ulp
+(the decode rule), the log-sum-exp within 1e-3 (score errors of the hi + lo
+products are ~1e-6 relative; ex2.approx adds ~2^-22).
+"""
+import numpy as np
+import pytest
+import torch
+
+from int2_kv_cache_oscar_gb300 import workloads as W
+from oracle import oscar_oracle as O
+from tests import gpu_util as U
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+LSE_TOL = 1e-3
+
+
+def _run(L, hkv, hq, n_q, seed, scale=0.0):
+    O_ = U.lib()
+    gen = torch.Generator().manual_seed(seed)
+    k, v = W.make_sequence_kv(L, hkv, W.LLAMA_RECIPE, gen)
+    cache = O_.OscarCache(1, hkv, L + 128)
+    U.append_all(cache, [0], [k], [v])
+    q = torch.randn((n_q, hq, 128), generator=gen).to(torch.bfloat16)
+    out = torch.empty((n_q, hq, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((n_q, hq), dtype=torch.float32, device="cuda")
+    O_.oscar_prefill_attention(cache.handle, 0, q.cuda(), hq, scale, out, lse)
+    torch.cuda.synchronize()
+    O_.oscar_cache_check(cache.handle)
+    arena = U.read_arena(cache)
+    got, gl, qn = U.f64(out), lse.cpu().numpy().astype(np.float64), U.f64(q)
+    gqa = hq // hkv
+    worst = worst_lse = 0.0
+    for j in range(hkv):
+        head = U.gpu_head(cache, arena, 0, j)
+        rows = qn[:, j * gqa:(j + 1) * gqa].reshape(-1, 128)      # query-major rows
+        o_ref, l_ref = O.history_attention(rows, head, None if scale == 0.0 else scale)
+        o_gpu = got[:, j * gqa:(j + 1) * gqa].reshape(-1, 128)
+        l_gpu = gl[:, j * gqa:(j + 1) * gqa].reshape(-1)
+        worst = max(worst, P.assert_decode(o_gpu, o_ref, f"L={L} head {j}"))
+        e = float(np.abs(l_gpu - l_ref).max())
+        assert e <= LSE_TOL, f"L={L} head {j}: lse error {e:.2e}"
+        worst_lse = max(worst_lse, e)
+    print(f"prefill L={L} hkv={hkv} hq={hq} n_q={n_q}: max|o err|={worst:.2e} max|lse err|={worst_lse:.2e}")
+
+
+@pytest.mark.parametrize("L", [8192 + 100, 1024, 100, 129, 1])
+def test_prefill_history_lengths(L):
+    _run(L, hkv=2, hq=8, n_q=37, seed=61 + L % 7)
+
+
+@pytest.mark.parametrize("gqa", [1, 2, 4])
+def test_prefill_gqa(gqa):
+    _run(2048 + 17, hkv=2, hq=2 * gqa, n_q=20, seed=70 + gqa)
+
+
+def test_prefill_scale_and_single_query():
+    _run(4096 + 5, hkv=1, hq=4, n_q=1, seed=80, scale=0.05)
+
+
+def test_prefill_bad_args():
+    O_ = U.lib()
+    cache = O_.OscarCache(2, 2, 256)
+    q = torch.zeros((3, 8, 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(q)
+    with pytest.raises(O_.OscarError) as e:
+        O_.oscar_prefill_attention(cache.handle, 0, q, 8, 0.0, out)     # empty sequence
+    assert e.value.status == O_.OSCAR_ERR_INVALID_ARG
+    k = torch.zeros((10, 2, 128), dtype=torch.bfloat16, device="cuda")
+    cache.append([0], [0, 10], k, k)
+    with pytest.raises(O_.OscarError) as e:
+        O_.oscar_prefill_attention(cache.handle, 0, q, 7, 0.0, out)     # heads not a multiple of Hkv
+    assert e.value.status == O_.OSCAR_ERR_INVALID_ARG
+    with pytest.raises(O_.OscarError) as e:
+        O_.oscar_prefill_attention(cache.handle, 5, q, 8, 0.0, out)     # slot out of range
+    assert e.value.status == O_.OSCAR_ERR_INVALID_ARG
