@@ -10,10 +10,13 @@
 // With many queries the contraction is a matrix product, so the rows go on
 // the mma M dimension (FlashAttention-2 style; the decode kernel instead puts
 // the 4 heads of one query on N):
-//   * a CTA takes 64 (query, head) rows of one KV head (4 consumer warps x 16
-//     rows) and streams every group block of that head through a
-//     shared-memory ring (1-D bulk copies, one producer lane, all 4 warps
-//     consume every stage);
+//   * a CTA takes 128 (query, head) rows of one KV head (8 warps x 16 rows,
+//     two per SM sub-partition) and streams every group block of that head
+//     through a shared-memory ring of 1-D bulk copies; every warp reads every
+//     stage, and the last warp to release a stage issues its refill (no
+//     producer warp: 8 warps keep 255 registers each);
+//   * a group is taken in two 64-token halves, one online-softmax step each
+//     (32 score registers per lane);
 //   * scores, m16n8k16 f16: A = the rows' rotated queries times the group's
 //     key scales, fp16 hi + lo (~22 bits), pre-scaled by 2^(F_row - p); B =
 //     the packed key codes: a fragment-order word of token row t is exactly
@@ -34,8 +37,8 @@
 namespace oscar {
 namespace {
 
-constexpr int kPfConsumers = 4;
-constexpr int kPfThreads = (kPfConsumers + 1) * 32;
+constexpr int kPfConsumers = 8;
+constexpr int kPfThreads = kPfConsumers * 32;     // no producer warp: the last reader refills a stage
 constexpr int kPfRows = 16 * kPfConsumers;   // (query, head) rows per CTA
 constexpr int kPfStages = 6;
 constexpr int kQrStride = 136;               // floats per staged rotated query row (16-byte rows, spread banks)
@@ -47,9 +50,9 @@ struct PfSmem {
   alignas(16) uint32_t qb[kPfRows][kQbStride];           // raw query rows, bf16 pairs
   float fexp[kPfRows];                                   // 2^(24 - F_row)
   alignas(8) uint64_t full[kPfStages];
-  uint64_t empty[kPfStages];
   uint64_t wbar;
-  uint32_t issued[kPfStages];
+  uint32_t released[kPfStages];   // warps done with a stage, summed over its uses
+  uint32_t nissued[kPfStages];    // copies issued into a stage
   int abort_flag;
 };
 static_assert(offsetof(PfSmem, qr) % 16 == 0 && offsetof(PfSmem, qb) % 16 == 0, "alignment");
@@ -114,15 +117,16 @@ __device__ __forceinline__ void pf_b_dyn(int kk, uint32_t w, uint32_t& b0, uint3
   }
 }
 
-// Online-softmax step of the lane's two rows over 32 new log2-domain scores
+// Online-softmax step of the lane's two rows over new log2-domain scores
 // sc[nt][0..1] (row g) and sc[nt][2..3] (row g + 8) of nt_used tiles: the
 // scores become probabilities, the running maxima and sums are updated, and
 // the factor that rescales the state accumulated so far is returned per row.
-__device__ __forceinline__ void pf_softmax(float (&sc)[16][4], int nt_used, float (&m_run)[2], float (&l_run)[2],
+template <int NT>
+__device__ __forceinline__ void pf_softmax(float (&sc)[NT][4], int nt_used, float (&m_run)[2], float (&l_run)[2],
                                            float (&alpha)[2]) {
   float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-  for (int nt = 0; nt < 16; ++nt) {
+  for (int nt = 0; nt < NT; ++nt) {
     if (nt < nt_used) {
       mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
       mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
@@ -141,7 +145,7 @@ __device__ __forceinline__ void pf_softmax(float (&sc)[16][4], int nt_used, floa
   m_run[1] = mn1;
   float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
-  for (int nt = 0; nt < 16; ++nt) {
+  for (int nt = 0; nt < NT; ++nt) {
     if (nt < nt_used) {
       sc[nt][0] = pf_exp2(sc[nt][0] - base0);
       sc[nt][1] = pf_exp2(sc[nt][1] - base0);
@@ -170,39 +174,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPfStages; ++s) {
       mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], kPfConsumers);
-      S.issued[s] = 0;
+      S.released[s] = 0;
+      S.nissued[s] = 0;
     }
     mbar_init(&S.wbar, 1);
     S.abort_flag = 0;
     fence_mbar_init();
+    for (int k = 0; k < ng && k < kPfStages; ++k) {
+      mbar_arrive_expect_tx(&S.full[k], kBlockBytes);
+      bulk_g2s(S.stage[k], blocks + (int64_t)k * kBlockBytes, kBlockBytes, &S.full[k]);
+      S.nissued[k] = 1;
+    }
   }
   __syncthreads();
-
-  if (warp == kPfConsumers) {
-    // ------------------------------------------------------------ producer
-    if (lane != 0) return;
-    int k = 0;
-    for (; k < ng; ++k) {
-      const int s = k % kPfStages;
-      if (k >= kPfStages) {
-        if (!mbar_wait_bounded(&S.empty[s], (uint32_t)(((k / kPfStages) - 1) & 1), &S.abort_flag, p.err_word))
-          break;
-      }
-      mbar_arrive_expect_tx(&S.full[s], kBlockBytes);
-      bulk_g2s(S.stage[s], blocks + (int64_t)k * kBlockBytes, kBlockBytes, &S.full[s]);
-      reinterpret_cast<volatile uint32_t*>(S.issued)[s] = (uint32_t)(k / kPfStages) + 1;
-    }
-    if (S.abort_flag) {
-      const int first = k > kPfStages ? k - kPfStages : 0;
-      for (int kk = first; kk < k; ++kk) {
-        const int s = kk % kPfStages;
-        for (uint32_t i = 0; i < kSpinLimit; ++i)
-          if (mbar_try_wait(&S.full[s], (uint32_t)((kk / kPfStages) & 1))) break;
-      }
-    }
-    return;
-  }
 
   // -------------------------------------------------------------- consumers
   const int g = lane >> 2, tig = lane & 3;
@@ -285,7 +269,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   for (int k = 0; k < ng; ++k) {
     const int s = k % kPfStages;
     const uint32_t use = (uint32_t)(k / kPfStages);
-    if (!wait_issued(&S.issued[s], use, &S.abort_flag, p.err_word)) break;
+    // every warp reads every use of a stage, and a refill waits for all of
+    // them, so no warp can be two uses ahead: the parity test cannot alias
     if (!mbar_wait_bounded(&S.full[s], use & 1, &S.abort_flag, p.err_word)) break;
     const uint8_t* blk = S.stage[s];
     const float* ksc = reinterpret_cast<const float*>(blk + kOffKScale);
@@ -295,118 +280,123 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint4* kc = reinterpret_cast<const uint4*>(blk + kOffKCodes);
     const uint4* vc = reinterpret_cast<const uint4*>(blk + kOffVCodes);
 
-    // ---- scores: acc[nt] = tokens 8 nt + 2 tig + {0, 1} of rows g, g + 8
-    float sc[16][4];
+    float qz0 = 0.0f, qz1 = 0.0f;   // q_rot . z of the lane's rows (times 2^F), from the first half
+    float qzt0 = 0.0f, qzt1 = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.0f;
-    float qz0 = 0.0f, qz1 = 0.0f;
+    for (int hh = 0; hh < 2; ++hh) {
+      // ---- scores of tokens 64 hh .. 64 hh + 63: sc[ntl] = tokens 64 hh + 8 ntl + 2 tig + {0, 1}
+      float sc[8][4];
 #pragma unroll
-    for (int jh = 0; jh < 2; ++jh) {
-      uint32_t kw[16];   // word (j = jh, r) of m-tile mt: tile nt = 2 mt + r
+      for (int i = 0; i < 8; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.0f;
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const uint4 w4 = kc[mt * 32 + lane];
-        kw[2 * mt] = jh ? w4.z : w4.x;
-        kw[2 * mt + 1] = jh ? w4.w : w4.y;
-      }
+      for (int jh = 0; jh < 2; ++jh) {
+        uint32_t kw[8];   // word (j = jh, r) of token m-tile 4 hh + mtl: tile ntl = 2 mtl + r
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const int ks = 4 * jh + kk;
-        const int c0 = 16 * ks + 2 * tig, c1 = c0 + 8;
-        const float2 x00 = *reinterpret_cast<const float2*>(q0row + c0);
-        const float2 x01 = *reinterpret_cast<const float2*>(q0row + c1);
-        const float2 x10 = *reinterpret_cast<const float2*>(q1row + c0);
-        const float2 x11 = *reinterpret_cast<const float2*>(q1row + c1);
-        const float2 s0 = *reinterpret_cast<const float2*>(ksc + c0);
-        const float2 s1 = *reinterpret_cast<const float2*>(ksc + c1);
-        const float2 z0 = *reinterpret_cast<const float2*>(kze + c0);
-        const float2 z1 = *reinterpret_cast<const float2*>(kze + c1);
-        qz0 = fmaf(fmaf(x00.x, z0.x, x00.y * z0.y), zw[kk][0], qz0);
-        qz0 = fmaf(fmaf(x01.x, z1.x, x01.y * z1.y), zw[kk][1], qz0);
-        qz1 = fmaf(fmaf(x10.x, z0.x, x10.y * z0.y), zw[kk][0], qz1);
-        qz1 = fmaf(fmaf(x11.x, z1.x, x11.y * z1.y), zw[kk][1], qz1);
-        uint32_t ah[4], al[4];
-        split_f16(x00.x * s0.x, x00.y * s0.y, ah[0], al[0]);
-        split_f16(x10.x * s0.x, x10.y * s0.y, ah[1], al[1]);
-        split_f16(x01.x * s1.x, x01.y * s1.y, ah[2], al[2]);
-        split_f16(x11.x * s1.x, x11.y * s1.y, ah[3], al[3]);
+        for (int mtl = 0; mtl < 4; ++mtl) {
+          const uint4 w4 = kc[(4 * hh + mtl) * 32 + lane];
+          kw[2 * mtl] = jh ? w4.z : w4.x;
+          kw[2 * mtl + 1] = jh ? w4.w : w4.y;
+        }
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-          uint32_t b0, b1;
-          pf_b_dyn(kk, kw[nt], b0, b1);
-          mma_f16_16816(sc[nt], ah[0], ah[1], ah[2], ah[3], b0, b1);
-          mma_f16_16816(sc[nt], al[0], al[1], al[2], al[3], b0, b1);
+        for (int kk = 0; kk < 4; ++kk) {
+          const int ks = 4 * jh + kk;
+          const int c0 = 16 * ks + 2 * tig, c1 = c0 + 8;
+          const float2 x00 = *reinterpret_cast<const float2*>(q0row + c0);
+          const float2 x01 = *reinterpret_cast<const float2*>(q0row + c1);
+          const float2 x10 = *reinterpret_cast<const float2*>(q1row + c0);
+          const float2 x11 = *reinterpret_cast<const float2*>(q1row + c1);
+          const float2 s0 = *reinterpret_cast<const float2*>(ksc + c0);
+          const float2 s1 = *reinterpret_cast<const float2*>(ksc + c1);
+          if (hh == 0) {
+            const float2 z0 = *reinterpret_cast<const float2*>(kze + c0);
+            const float2 z1 = *reinterpret_cast<const float2*>(kze + c1);
+            qz0 = fmaf(fmaf(x00.x, z0.x, x00.y * z0.y), zw[kk][0], qz0);
+            qz0 = fmaf(fmaf(x01.x, z1.x, x01.y * z1.y), zw[kk][1], qz0);
+            qz1 = fmaf(fmaf(x10.x, z0.x, x10.y * z0.y), zw[kk][0], qz1);
+            qz1 = fmaf(fmaf(x11.x, z1.x, x11.y * z1.y), zw[kk][1], qz1);
+          }
+          uint32_t ah[4], al[4];
+          split_f16(x00.x * s0.x, x00.y * s0.y, ah[0], al[0]);
+          split_f16(x10.x * s0.x, x10.y * s0.y, ah[1], al[1]);
+          split_f16(x01.x * s1.x, x01.y * s1.y, ah[2], al[2]);
+          split_f16(x11.x * s1.x, x11.y * s1.y, ah[3], al[3]);
+#pragma unroll
+          for (int ntl = 0; ntl < 8; ++ntl) {
+            uint32_t b0, b1;
+            pf_b_dyn(kk, kw[ntl], b0, b1);
+            mma_f16_16816(sc[ntl], ah[0], ah[1], ah[2], ah[3], b0, b1);
+            mma_f16_16816(sc[ntl], al[0], al[1], al[2], al[3], b0, b1);
+          }
         }
       }
-    }
-    qz0 += __shfl_xor_sync(0xffffffffu, qz0, 1);
-    qz0 += __shfl_xor_sync(0xffffffffu, qz0, 2);
-    qz1 += __shfl_xor_sync(0xffffffffu, qz1, 1);
-    qz1 += __shfl_xor_sync(0xffffffffu, qz1, 2);
-    // qr = q_rot 2^(F - p) and zw = 2^p: qz * 2^-F = q_rot . z; fexp = 2^(24 - F)
-    const float qzt0 = qz0 * fe0 * (1.0f / 16777216.0f), qzt1 = qz1 * fe1 * (1.0f / 16777216.0f);
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      const float2 n2 = *reinterpret_cast<const float2*>(knm + 8 * nt + 2 * tig);
-      sc[nt][0] = fmaf(sc[nt][0], fe0, qzt0) * n2.x * p.scale_log2;
-      sc[nt][1] = fmaf(sc[nt][1], fe0, qzt0) * n2.y * p.scale_log2;
-      sc[nt][2] = fmaf(sc[nt][2], fe1, qzt1) * n2.x * p.scale_log2;
-      sc[nt][3] = fmaf(sc[nt][3], fe1, qzt1) * n2.y * p.scale_log2;
-    }
-
-    // ---- online softmax, rescale the state
-    float alpha[2];
-    pf_softmax(sc, 16, m_run, l_run, alpha);
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      oacc[nt][0] *= alpha[0];
-      oacc[nt][1] *= alpha[0];
-      oacc[nt][2] *= alpha[1];
-      oacc[nt][3] *= alpha[1];
-    }
-#pragma unroll
-    for (int gv = 0; gv < kVGroups; ++gv) {
-      zacc[0][gv] *= alpha[0];
-      zacc[1][gv] *= alpha[1];
-    }
-    // value zeros: sum_t p_t z^V_t,gv over the lane's 32 tokens
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = 8 * nt + 2 * tig + e;
-        const float4 z4 = *reinterpret_cast<const float4*>(vsz + 8 * t + 4);
-        zacc[0][0] = fmaf(sc[nt][e], z4.x, zacc[0][0]);
-        zacc[0][1] = fmaf(sc[nt][e], z4.y, zacc[0][1]);
-        zacc[0][2] = fmaf(sc[nt][e], z4.z, zacc[0][2]);
-        zacc[0][3] = fmaf(sc[nt][e], z4.w, zacc[0][3]);
-        zacc[1][0] = fmaf(sc[nt][2 + e], z4.x, zacc[1][0]);
-        zacc[1][1] = fmaf(sc[nt][2 + e], z4.y, zacc[1][1]);
-        zacc[1][2] = fmaf(sc[nt][2 + e], z4.z, zacc[1][2]);
-        zacc[1][3] = fmaf(sc[nt][2 + e], z4.w, zacc[1][3]);
+      if (hh == 0) {
+        qz0 += __shfl_xor_sync(0xffffffffu, qz0, 1);
+        qz0 += __shfl_xor_sync(0xffffffffu, qz0, 2);
+        qz1 += __shfl_xor_sync(0xffffffffu, qz1, 1);
+        qz1 += __shfl_xor_sync(0xffffffffu, qz1, 2);
+        // qr = q_rot 2^(F - p) and zw = 2^p: qz * 2^-F = q_rot . z; fexp = 2^(24 - F)
+        qzt0 = qz0 * fe0 * (1.0f / 16777216.0f);
+        qzt1 = qz1 * fe1 * (1.0f / 16777216.0f);
       }
-    }
-
-    // ---- P.V: k-step ks = tokens 16 ks .. 16 ks + 15 (score tiles 2 ks, 2 ks + 1)
 #pragma unroll
-    for (int jh = 0; jh < 2; ++jh) {
-      uint32_t vw[16];   // word (j = jh, r) of channel m-tile mt: channel tile nt = 2 mt + r
+      for (int ntl = 0; ntl < 8; ++ntl) {
+        const float2 n2 = *reinterpret_cast<const float2*>(knm + 64 * hh + 8 * ntl + 2 * tig);
+        sc[ntl][0] = fmaf(sc[ntl][0], fe0, qzt0) * n2.x * p.scale_log2;
+        sc[ntl][1] = fmaf(sc[ntl][1], fe0, qzt0) * n2.y * p.scale_log2;
+        sc[ntl][2] = fmaf(sc[ntl][2], fe1, qzt1) * n2.x * p.scale_log2;
+        sc[ntl][3] = fmaf(sc[ntl][3], fe1, qzt1) * n2.y * p.scale_log2;
+      }
+
+      // ---- online softmax, rescale the state
+      float alpha[2];
+      pf_softmax<8>(sc, 8, m_run, l_run, alpha);
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        oacc[nt][0] *= alpha[0];
+        oacc[nt][1] *= alpha[0];
+        oacc[nt][2] *= alpha[1];
+        oacc[nt][3] *= alpha[1];
+      }
+#pragma unroll
+      for (int gv = 0; gv < kVGroups; ++gv) {
+        zacc[0][gv] *= alpha[0];
+        zacc[1][gv] *= alpha[1];
+      }
+      // value zeros: sum_t p_t z^V_t,gv over the lane's 16 tokens of this half
+#pragma unroll
+      for (int ntl = 0; ntl < 8; ++ntl) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int t = 64 * hh + 8 * ntl + 2 * tig + e;
+          const float4 z4 = *reinterpret_cast<const float4*>(vsz + 8 * t + 4);
+          zacc[0][0] = fmaf(sc[ntl][e], z4.x, zacc[0][0]);
+          zacc[0][1] = fmaf(sc[ntl][e], z4.y, zacc[0][1]);
+          zacc[0][2] = fmaf(sc[ntl][e], z4.z, zacc[0][2]);
+          zacc[0][3] = fmaf(sc[ntl][e], z4.w, zacc[0][3]);
+          zacc[1][0] = fmaf(sc[ntl][2 + e], z4.x, zacc[1][0]);
+          zacc[1][1] = fmaf(sc[ntl][2 + e], z4.y, zacc[1][1]);
+          zacc[1][2] = fmaf(sc[ntl][2 + e], z4.z, zacc[1][2]);
+          zacc[1][3] = fmaf(sc[ntl][2 + e], z4.w, zacc[1][3]);
+        }
+      }
+
+      // ---- P.V over this half: k-steps ks = 4 hh + kk (score tiles 2 kk, 2 kk + 1)
+      uint32_t vw[16];   // word (j = hh, r) of channel m-tile mt: channel tile nt = 2 mt + r
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const uint4 w4 = vc[mt * 32 + lane];
-        vw[2 * mt] = jh ? w4.z : w4.x;
-        vw[2 * mt + 1] = jh ? w4.w : w4.y;
+        vw[2 * mt] = hh ? w4.z : w4.x;
+        vw[2 * mt + 1] = hh ? w4.w : w4.y;
       }
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        const int ks = 4 * jh + kk;
-        const int t0 = 16 * ks + 2 * tig, t1 = t0 + 8;
+        const int t0 = 64 * hh + 16 * kk + 2 * tig, t1 = t0 + 8;
         const float4 sa = *reinterpret_cast<const float4*>(vsz + 8 * t0);
         const float4 sb = *reinterpret_cast<const float4*>(vsz + 8 * (t0 + 1));
         const float4 sc4 = *reinterpret_cast<const float4*>(vsz + 8 * t1);
         const float4 sd = *reinterpret_cast<const float4*>(vsz + 8 * (t1 + 1));
-        const float* p00 = sc[2 * ks];       // tokens t0, t0+1: rows g (0, 1), g + 8 (2, 3)
-        const float* p01 = sc[2 * ks + 1];   // tokens t1, t1+1
+        const float* p00 = sc[2 * kk];       // tokens t0, t0+1: rows g (0, 1), g + 8 (2, 3)
+        const float* p01 = sc[2 * kk + 1];   // tokens t1, t1+1
         const float f0 = fsc[kk][0], f1 = fsc[kk][1];
 #pragma unroll
         for (int gv = 0; gv < kVGroups; ++gv) {
@@ -431,13 +421,36 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty[s]);
+    if (lane == 0) {
+      __threadfence_block();                                   // this warp's reads of the stage are done
+      const uint32_t before = atomicAdd(&S.released[s], 1u);
+      if (before == (use + 1) * kPfConsumers - 1 && k + kPfStages < ng) {
+        __threadfence_block();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic reads before the async write
+        mbar_arrive_expect_tx(&S.full[s], kBlockBytes);
+        bulk_g2s(S.stage[s], blocks + (int64_t)(k + kPfStages) * kBlockBytes, kBlockBytes, &S.full[s]);
+        S.nissued[s] = use + 2;
+      }
+    }
+  }
+  // every warp leaves the group loop here, so all see the same abort state
+  named_bar_sync(1, kPfConsumers * 32);
+  if (S.abort_flag) {
+    // a wait gave up: before the CTA exits, wait (bounded) for copies still in flight
+    if (threadIdx.x == 0) {
+      for (int s = 0; s < kPfStages; ++s) {
+        const uint32_t n = *reinterpret_cast<volatile uint32_t*>(&S.nissued[s]);
+        if (n == 0) continue;
+        for (uint32_t i = 0; i < kSpinLimit; ++i)
+          if (mbar_try_wait(&S.full[s], (n - 1) & 1)) break;
+      }
+    }
+    return;
   }
 
   // ---- the window (bf16 rows after the last group), on bf16 tensor cores
   const int wlen = p.wlen;
-  if (wlen > 0) {
-    named_bar_sync(1, kPfConsumers * 32);   // every warp is done with the ring
+  if (wlen > 0) {   // every warp is done with the ring (barrier above)
     uint16_t* wk = reinterpret_cast<uint16_t*>(S.stage[0]);
     uint16_t* wv = wk + kGroup * kHeadDim;
     if (threadIdx.x == 0) {
@@ -485,7 +498,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       }
       float alpha[2];
-      pf_softmax(sc, nt_used, m_run, l_run, alpha);
+      pf_softmax<16>(sc, nt_used, m_run, l_run, alpha);
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
         oacc[nt][0] *= alpha[0];
