@@ -111,11 +111,23 @@ def omni_token_scaling(r: np.ndarray):
 # article; OScaR abstract: INT2 per-channel paradigm)
 # ---------------------------------------------------------------------------
 
-def int2_params(x_min: np.ndarray, x_max: np.ndarray):
-    """Scale and zero of an asymmetric 4-level quantiser, stored as float32."""
+def store_meta(x: np.ndarray, meta_bits: int = 32) -> np.ndarray:
+    """Stored metadata: float32, or (meta_bits = 16) that float32 rounded to
+    float16, nearest even; returned as float32 (exact either way)."""
+    x32 = np.asarray(x).astype(np.float32)
+    if meta_bits == 16:
+        return x32.astype(np.float16).astype(np.float32)
+    if meta_bits != 32:
+        raise ValueError("meta_bits must be 32 or 16")
+    return x32
+
+
+def int2_params(x_min: np.ndarray, x_max: np.ndarray, meta_bits: int = 32):
+    """Scale and zero of an asymmetric 4-level quantiser as stored: float32,
+    or float16 in the 16-bit metadata layout (the float32 value rounded)."""
     s32 = ((x_max - x_min) / MAX_CODE).astype(np.float32)
     z32 = np.asarray(x_min).astype(np.float32)
-    return s32, z32
+    return store_meta(s32, meta_bits), store_meta(z32, meta_bits)
 
 
 def int2_codes(x: np.ndarray, s32: np.ndarray, z32: np.ndarray):
@@ -157,26 +169,27 @@ class ValueGroup:
     pre: np.ndarray     # float64 [..., G, d]
 
 
-def quantize_key_group(k: np.ndarray) -> KeyGroup:
+def quantize_key_group(k: np.ndarray, meta_bits: int = 32) -> KeyGroup:
     """OScaR key path for one group of tokens (axis -2) of bf16-valued keys.
 
     Steps in the pages' order: Canalized Rotation, then Omni-Token Scaling,
-    then per-channel asymmetric INT2 over the group's tokens.
+    then per-channel asymmetric INT2 over the group's tokens.  The codes are
+    decided against the stored (possibly float16) scale and zero.
     """
     k = np.asarray(k, dtype=np.float64)
     r = canalized_rotation(k)
     n, k_hat = omni_token_scaling(r)
-    s32, z32 = int2_params(k_hat.min(axis=-2), k_hat.max(axis=-2))
+    s32, z32 = int2_params(k_hat.min(axis=-2), k_hat.max(axis=-2), meta_bits)
     codes, pre = int2_codes(k_hat, s32[..., None, :], z32[..., None, :])
-    return KeyGroup(codes, s32, z32, n.astype(np.float32), pre)
+    return KeyGroup(codes, s32, z32, store_meta(n, meta_bits), pre)
 
 
-def quantize_value_group(v: np.ndarray) -> ValueGroup:
+def quantize_value_group(v: np.ndarray, meta_bits: int = 32) -> ValueGroup:
     """Per-token asymmetric INT2 of values over groups of 32 channels."""
     v = np.asarray(v, dtype=np.float64)
     d = v.shape[-1]
     vg = v.reshape(v.shape[:-1] + (d // VALUE_GROUP, VALUE_GROUP))
-    s32, z32 = int2_params(vg.min(axis=-1), vg.max(axis=-1))
+    s32, z32 = int2_params(vg.min(axis=-1), vg.max(axis=-1), meta_bits)
     codes, pre = int2_codes(vg, s32[..., None], z32[..., None])
     return ValueGroup(codes.reshape(v.shape), s32, z32, pre.reshape(v.shape))
 
@@ -214,9 +227,10 @@ class HeadCache:
         return self.num_groups * KEY_GROUP + self.window_k.shape[0]
 
 
-def build_head_cache(k: np.ndarray, v: np.ndarray) -> HeadCache:
+def build_head_cache(k: np.ndarray, v: np.ndarray, meta_bits: int = 32) -> HeadCache:
     """Quantise every full group of positions [128 g, 128 g + 128) of one head
-    (k, v: [L, d]) and keep the remaining L mod 128 tokens as the window."""
+    (k, v: [L, d]) and keep the remaining L mod 128 tokens as the window.
+    meta_bits = 16 stores scales, zeros and norms as float16."""
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     L, d = k.shape
@@ -224,8 +238,8 @@ def build_head_cache(k: np.ndarray, v: np.ndarray) -> HeadCache:
     cut = ng * KEY_GROUP
     keys = values = None
     if ng > 0:
-        keys = quantize_key_group(k[:cut].reshape(ng, KEY_GROUP, d))
-        values = quantize_value_group(v[:cut].reshape(ng, KEY_GROUP, d))
+        keys = quantize_key_group(k[:cut].reshape(ng, KEY_GROUP, d), meta_bits)
+        values = quantize_value_group(v[:cut].reshape(ng, KEY_GROUP, d), meta_bits)
     return HeadCache(keys, values, k[cut:].copy(), v[cut:].copy())
 
 
