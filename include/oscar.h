@@ -71,6 +71,10 @@ typedef struct oscar_cache_config {
   int32_t group_size;    /* must be 128 (G)                                  */
   int32_t value_group;   /* must be 32 (Gv)                                  */
   int32_t device;        /* CUDA device ordinal of the arena                 */
+  int32_t meta_bits;     /* 32 (default; 0 also means 32): float32 scales,   */
+                         /* zeros and norms, 13,824-byte blocks; 16: float16 */
+                         /* (rounded to nearest even; codes decided against  */
+                         /* the rounded values), 11,008-byte blocks          */
 } oscar_cache_config;
 
 /* Kinds for oscar_cache_bytes. */
@@ -88,15 +92,16 @@ enum {
  *   [256, M)                       per (slot, kv head): float32 bit pattern of
  *                                  the largest value scale s_v quantised so
  *                                  far (4 bytes each), M = 256-aligned end
- *   blocks  (base = M)             one 13,824-byte block per
+ *   blocks  (base = M)             one block of B bytes per
  *                                  (slot, kv head, group g):
- *                                  base + ((slot*Hkv + head)*max_groups + g)*13824,
- *                                  max_groups = ceil(max_seq_len / 128)
+ *                                  base + ((slot*Hkv + head)*max_groups + g)*B,
+ *                                  max_groups = ceil(max_seq_len / 128),
+ *                                  B = 13,824 (meta_bits 32) or 11,008 (16)
  *   windows (after the blocks,     65,536 bytes per (slot, kv head): 128 bf16
  *            256-aligned)          key rows (slot p mod 128) then 128 bf16
  *                                  value rows, 256 bytes per row
  *
- * One group block (the unit the decode kernel streams):
+ * One group block (the unit the decode kernel streams), meta_bits 32:
  *   +0      K codes, 4,096 B, "fragment order" of the 128x128 matrix
  *           X[row = token][col = channel]
  *   +4096   K scale s_c, float32 [128] (per channel)
@@ -105,6 +110,10 @@ enum {
  *   +5632   V codes, 4,096 B, fragment order of X[row = channel][col = token]
  *   +9728   V scale/zero: per token t (32 B): s[t][0..3] then z[t][0..3]
  *           (float32), one pair per 32-channel group
+ * meta_bits 16: the same sections with float16 metadata:
+ *   +0 K codes, +4096 K scale, +4352 K zero, +4608 K norm (float16 [128]
+ *   each), +4864 V codes, +8960 V scale/zero (per token 16 B: s[t][0..3]
+ *   then z[t][0..3], float16); 11,008 bytes, 86 per token and head.
  *
  * Fragment order of a 128x128 matrix of 2-bit codes X[row][col]: 32-bit word
  * number  w = ((mt*32 + lane)*4 + 2*j + r)  holds the 16 codes with

@@ -20,6 +20,27 @@ constexpr int kOffVCodes = 5632;
 constexpr int kOffVSZ = 9728;
 constexpr int kBlockBytes = 13824;
 
+// The same block with float16 metadata (scales, zeros, norms).
+constexpr int kOff16KScale = 4096;
+constexpr int kOff16KZero = 4352;
+constexpr int kOff16KNorm = 4608;
+constexpr int kOff16VCodes = 4864;
+constexpr int kOff16VSZ = 8960;
+constexpr int kBlockBytes16 = 11008;
+
+// Block layout by metadata width: section offsets, block size, bytes per
+// metadata element.
+template <bool M16>
+struct Blk {
+  static constexpr int kKScale = M16 ? kOff16KScale : kOffKScale;
+  static constexpr int kKZero = M16 ? kOff16KZero : kOffKZero;
+  static constexpr int kKNorm = M16 ? kOff16KNorm : kOffKNorm;
+  static constexpr int kVCodes = M16 ? kOff16VCodes : kOffVCodes;
+  static constexpr int kVSZ = M16 ? kOff16VSZ : kOffVSZ;
+  static constexpr int kBytes = M16 ? kBlockBytes16 : kBlockBytes;
+  static constexpr int kMeta = M16 ? 2 : 4;
+};
+
 constexpr int kWindowBytes = 2 * kGroup * kHeadDim * 2;  // K rows then V rows, bf16
 constexpr int kMetaHeader = 256;                          // status words
 
@@ -38,13 +59,14 @@ struct ArenaLayout {
   int32_t max_groups;
 };
 
-__host__ __device__ inline ArenaLayout arena_layout(int32_t max_batch, int32_t hkv, int32_t max_len) {
+__host__ __device__ inline ArenaLayout arena_layout(int32_t max_batch, int32_t hkv, int32_t max_len,
+                                                    int32_t block_bytes = kBlockBytes) {
   ArenaLayout L;
   L.max_groups = (max_len + kGroup - 1) / kGroup;
   int64_t meta = kMetaHeader + (int64_t)max_batch * hkv * 4;
   L.meta_bytes = (meta + 255) / 256 * 256;
   L.blocks_off = L.meta_bytes;
-  int64_t blocks = (int64_t)max_batch * hkv * L.max_groups * kBlockBytes;
+  int64_t blocks = (int64_t)max_batch * hkv * L.max_groups * block_bytes;
   L.windows_off = (L.blocks_off + blocks + 255) / 256 * 256;
   L.total = L.windows_off + (int64_t)max_batch * hkv * kWindowBytes;
   return L;
@@ -209,5 +231,36 @@ __device__ __forceinline__ uint32_t frag_extract(uint32_t w) {
     return (w >> 10) & (0x00030003u << (2 * (I - 5)));
   }
 }
+
+// Metadata of a staged block as float: float32 sections, or float16 ones
+// (converted exactly).
+template <bool M16>
+struct Meta {
+  // elements i, i + 1 of a per-channel or per-token array
+  __device__ static float2 two(const uint8_t* a, int i) {
+    if constexpr (M16) {
+      const uint32_t h = *reinterpret_cast<const uint32_t*>(a + 2 * i);
+      return make_float2(half_lo_to_float(h), half_hi_to_float(h));
+    } else {
+      return *reinterpret_cast<const float2*>(a + 4 * i);
+    }
+  }
+  __device__ static float one(const uint8_t* a, int i) {
+    if constexpr (M16) {
+      return half_lo_to_float(*reinterpret_cast<const uint16_t*>(a + 2 * i));
+    } else {
+      return reinterpret_cast<const float*>(a)[i];
+    }
+  }
+  // value scales (which = 0) or zeros (which = 1) of token t, groups 0..3
+  __device__ static float4 vsz4(const uint8_t* vsz, int t, int which) {
+    if constexpr (M16) {
+      const uint2 h = *reinterpret_cast<const uint2*>(vsz + 16 * t + 8 * which);
+      return make_float4(half_lo_to_float(h.x), half_hi_to_float(h.x), half_lo_to_float(h.y), half_hi_to_float(h.y));
+    } else {
+      return *reinterpret_cast<const float4*>(vsz + 32 * t + 16 * which);
+    }
+  }
+};
 
 }  // namespace oscar

@@ -35,12 +35,21 @@ namespace {
 
 constexpr int kConsumers = 4;
 constexpr int kDecThreads = (kConsumers + 1) * 32;
-constexpr int kStages = 7;
 constexpr int kCtasPerSm = 2;
 constexpr int kPbStride = kGroup + 8;  // probability rows, padded against bank conflicts
 
-struct DecSmem {
-  alignas(128) uint8_t stage[kStages][kBlockBytes];
+// Ring geometry by metadata width: 7 stages of 13,824 B, or 8 of 11,008 B
+// (float16 metadata), two CTAs per SM either way.
+template <bool M16>
+struct Ring {
+  static constexpr int kStages = M16 ? 8 : 7;
+  static constexpr int kStageBytes = Blk<M16>::kBytes;
+};
+
+template <bool M16>
+struct DecSmemT {
+  static constexpr int kStages = Ring<M16>::kStages;
+  alignas(128) uint8_t stage[kStages][Ring<M16>::kStageBytes];
   alignas(16) float qrot[kMaxGqa][kHeadDim];              // float4 stores
   alignas(16) float4 q2t[4][32];                          // per-lane scaled query values, [i/4][lane]
   // consumer-private probabilities; at a segment end each warp's region holds
@@ -56,11 +65,18 @@ struct DecSmem {
   int abort_flag;
 };
 static_assert(kPbStride >= kHeadDim, "output rows must fit in the probability rows");
-static_assert(offsetof(DecSmem, qrot) % 16 == 0, "qrot must be 16-byte aligned");
-static_assert(offsetof(DecSmem, pbuf) % 16 == 0, "pbuf must be 16-byte aligned");
 static_assert((kPbStride * 4) % 16 == 0, "pbuf rows must keep 16-byte alignment");
-static_assert(offsetof(DecSmem, full) % 8 == 0, "mbarriers must be 8-byte aligned");
-static_assert(kBlockBytes % 16 == 0, "stages must stay 16-byte aligned");
+static_assert(offsetof(DecSmemT<false>, qrot) % 16 == 0 && offsetof(DecSmemT<true>, qrot) % 16 == 0,
+              "qrot must be 16-byte aligned");
+static_assert(offsetof(DecSmemT<false>, pbuf) % 16 == 0 && offsetof(DecSmemT<true>, pbuf) % 16 == 0,
+              "pbuf must be 16-byte aligned");
+static_assert(offsetof(DecSmemT<false>, full) % 8 == 0 && offsetof(DecSmemT<true>, full) % 8 == 0,
+              "mbarriers must be 8-byte aligned");
+static_assert(kBlockBytes % 128 == 0 && kBlockBytes16 % 128 == 0, "stages must stay 128-byte aligned");
+static_assert(kCtasPerSm * (sizeof(DecSmemT<false>) + 1024) <= 233472 &&
+                  kCtasPerSm * (sizeof(DecSmemT<true>) + 1024) <= 233472,
+              "two CTAs per SM");
+
 
 __device__ __forceinline__ float pow2f(int e) {
   e = max(-126, min(127, e));
@@ -118,9 +134,14 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-template <int MAXS>
+template <int MAXS, bool M16>
 __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     decode_int2_kernel(const __grid_constant__ DecodeParams<MAXS> p, const uint8_t* __restrict__ arena) {
+  using DecSmem = DecSmemT<M16>;
+  using B = Blk<M16>;
+  using MR = Meta<M16>;
+  constexpr int kStages = DecSmem::kStages;
+  constexpr int kStageBytes = B::kBytes;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   DecSmem& S = *reinterpret_cast<DecSmem*>(smem_raw);
   const int warp = threadIdx.x >> 5;
@@ -156,16 +177,16 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       locate_unit(p, u, b, j, g, ng);
       const int64_t row_end = p.seq[b].ubase + (int64_t)(j + 1) * ng;
       const int64_t seg_end = row_end < u1 ? row_end : u1;
-      const uint8_t* src = blocks + (((int64_t)p.seq[b].slot * hkv + j) * p.h.max_groups + g) * kBlockBytes;
-      for (; u < seg_end; ++u, ++k, src += kBlockBytes) {
+      const uint8_t* src = blocks + (((int64_t)p.seq[b].slot * hkv + j) * p.h.max_groups + g) * kStageBytes;
+      for (; u < seg_end; ++u, ++k, src += kStageBytes) {
         const int s = (int)(k % kStages);
         if (k >= kStages) {
           if (!mbar_wait_bounded(&S.empty[s], (uint32_t)(((k / kStages) - 1) & 1), &S.abort_flag, p.h.err_word)) {
             goto drain;
           }
         }
-        mbar_arrive_expect_tx(&S.full[s], kBlockBytes);
-        bulk_g2s(S.stage[s], src, kBlockBytes, &S.full[s]);
+        mbar_arrive_expect_tx(&S.full[s], kStageBytes);
+        bulk_g2s(S.stage[s], src, kStageBytes, &S.full[s]);
         reinterpret_cast<volatile uint32_t*>(S.issued)[s] = (uint32_t)(k / kStages) + 1;
       }
     }
@@ -323,10 +344,10 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       if (!wait_issued(&S.issued[s], use, &S.abort_flag, p.h.err_word)) continue;
       if (!mbar_wait_bounded(&S.full[s], use & 1, &S.abort_flag, p.h.err_word)) continue;
       const uint8_t* blk = S.stage[s];
-      const float* ksc = reinterpret_cast<const float*>(blk + kOffKScale);
-      const float* kze = reinterpret_cast<const float*>(blk + kOffKZero);
-      const float* knm = reinterpret_cast<const float*>(blk + kOffKNorm);
-      const float* vsz = reinterpret_cast<const float*>(blk + kOffVSZ);
+      const uint8_t* ksc = blk + B::kKScale;
+      const uint8_t* kze = blk + B::kKZero;
+      const uint8_t* knm = blk + B::kKNorm;
+      const uint8_t* vsz = blk + B::kVSZ;
 
       // ---- B fragments of the score contraction, and q_rot . z
       uint32_t bk[8][2];
@@ -341,8 +362,8 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
           const int ks = 2 * i + e;
           const float2 qq = e ? make_float2(q4.z, q4.w) : make_float2(q4.x, q4.y);
           const int c = 16 * ks + 2 * tig + 8 * half;
-          const float2 s2 = *reinterpret_cast<const float2*>(ksc + c);
-          const float2 z2 = *reinterpret_cast<const float2*>(kze + c);
+          const float2 s2 = MR::two(ksc, c);
+          const float2 z2 = MR::two(kze, c);
           const float2 x = __fmul2_rn(qq, s2);
           split_exchange(x.x, x.y, lo_lane, bk[ks][0], bk[ks][1]);
           qzc[ks & 3] = __ffma2_rn(qq, z2, qzc[ks & 3]);
@@ -387,7 +408,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
             const int mt = 4 * mh + m;
             const int t0 = 16 * mt + g;
             const float2 a = make_float2(acc[m][0] + acc[m][1], acc[m][2] + acc[m][3]);
-            sc[mt] = __fmul2_rn(__ffma2_rn(a, kq2, qz2), make_float2(knm[t0], knm[t0 + 8]));
+            sc[mt] = __fmul2_rn(__ffma2_rn(a, kq2, qz2), make_float2(MR::one(knm, t0), MR::one(knm, t0 + 8)));
           }
         }
       }
@@ -419,8 +440,8 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
         const int t0 = 16 * mt + g;
         pb[t0] = sc[mt].x;
         pb[t0 + 8] = sc[mt].y;
-        const float4 z0 = *reinterpret_cast<const float4*>(vsz + 8 * t0 + 4);
-        const float4 z1 = *reinterpret_cast<const float4*>(vsz + 8 * (t0 + 8) + 4);
+        const float4 z0 = MR::vsz4(vsz, t0, 1);
+        const float4 z1 = MR::vsz4(vsz, t0 + 8, 1);
         zacc[0] = fmaf(sc[mt].x, z0.x, fmaf(sc[mt].y, z1.x, zacc[0]));
         zacc[1] = fmaf(sc[mt].x, z0.y, fmaf(sc[mt].y, z1.y, zacc[1]));
         zacc[2] = fmaf(sc[mt].x, z0.z, fmaf(sc[mt].y, z1.z, zacc[2]));
@@ -440,13 +461,13 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
           uint2 vw[8];
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt)
-            vw[mt] = *reinterpret_cast<const uint2*>(blk + kOffVCodes + ((mt * 32 + lane) * 4 + 2 * jh) * 4);
+            vw[mt] = *reinterpret_cast<const uint2*>(blk + B::kVCodes + ((mt * 32 + lane) * 4 + 2 * jh) * 4);
 #pragma unroll
           for (int kk2 = 0; kk2 < 4; ++kk2) {
             const int t = 16 * (4 * jh + kk2) + 2 * tig + 8 * half;   // this lane's two tokens
             const float2 pr = __fmul2_rn(*reinterpret_cast<const float2*>(pbh + t), make_float2(fsc[kk2], fsc[kk2]));
-            const float4 s0 = *reinterpret_cast<const float4*>(vsz + 8 * t);
-            const float4 s1 = *reinterpret_cast<const float4*>(vsz + 8 * (t + 1));
+            const float4 s0 = MR::vsz4(vsz, t, 0);
+            const float4 s1 = MR::vsz4(vsz, t + 1, 0);
 #pragma unroll
             for (int gr = 0; gr < kVGroups; ++gr) {
               const float sa = gr == 0 ? s0.x : gr == 1 ? s0.y : gr == 2 ? s0.z : s0.w;
@@ -757,19 +778,26 @@ int num_sms(int device) {
   return n;
 }
 
-template <int MAXS>
-cudaError_t launch_decode_int2(const DecodeParams<MAXS>& p, const uint8_t* arena, cudaStream_t stream,
-                               cudaEvent_t ev_start, cudaEvent_t ev_stop) {
+template <int MAXS, bool M16>
+cudaError_t launch_decode_int2_t(const DecodeParams<MAXS>& p, const uint8_t* arena, cudaStream_t stream,
+                                 cudaEvent_t ev_start, cudaEvent_t ev_stop) {
   if (p.h.n_units <= 0) return cudaSuccess;
-  const int smem = (int)sizeof(DecSmem);
+  const int smem = (int)sizeof(DecSmemT<M16>);
   static bool attr_done[64] = {};
-  cudaError_t e = ensure_smem_attr(decode_int2_kernel<MAXS>, smem, attr_done);
+  cudaError_t e = ensure_smem_attr(decode_int2_kernel<MAXS, M16>, smem, attr_done);
   if (e != cudaSuccess) return e;
   if (ev_start) cudaEventRecord(ev_start, stream);
-  decode_int2_kernel<MAXS><<<p.h.n_ctas, kDecThreads, smem, stream>>>(p, arena);
+  decode_int2_kernel<MAXS, M16><<<p.h.n_ctas, kDecThreads, smem, stream>>>(p, arena);
   e = cudaGetLastError();
   if (ev_stop) cudaEventRecord(ev_stop, stream);
   return e;
+}
+
+template <int MAXS>
+cudaError_t launch_decode_int2(const DecodeParams<MAXS>& p, const uint8_t* arena, bool meta16, cudaStream_t stream,
+                               cudaEvent_t ev_start, cudaEvent_t ev_stop) {
+  return meta16 ? launch_decode_int2_t<MAXS, true>(p, arena, stream, ev_start, ev_stop)
+                : launch_decode_int2_t<MAXS, false>(p, arena, stream, ev_start, ev_stop);
 }
 
 template <int MAXS>
@@ -794,9 +822,9 @@ cudaError_t launch_combine(const DecodeParams<MAXS>& p, const uint8_t* arena, cu
 }
 
 template cudaError_t launch_decode_int2<kDecodeSeqsSmall>(const DecodeParams<kDecodeSeqsSmall>&, const uint8_t*,
-                                                          cudaStream_t, cudaEvent_t, cudaEvent_t);
+                                                          bool, cudaStream_t, cudaEvent_t, cudaEvent_t);
 template cudaError_t launch_decode_int2<kDecodeSeqsLarge>(const DecodeParams<kDecodeSeqsLarge>&, const uint8_t*,
-                                                          cudaStream_t, cudaEvent_t, cudaEvent_t);
+                                                          bool, cudaStream_t, cudaEvent_t, cudaEvent_t);
 template cudaError_t launch_combine<kDecodeSeqsSmall>(const DecodeParams<kDecodeSeqsSmall>&, const uint8_t*,
                                                       cudaStream_t);
 template cudaError_t launch_combine<kDecodeSeqsLarge>(const DecodeParams<kDecodeSeqsLarge>&, const uint8_t*,

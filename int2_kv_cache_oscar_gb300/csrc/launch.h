@@ -36,10 +36,11 @@ struct QuantPlan {
   QuantTask t[CAP];
 };
 
+// meta16: the float16-metadata block layout (see include/oscar.h)
 cudaError_t launch_quantize_small(const QuantPlan<kQuantPlanSmall>& plan, uint8_t* arena, const uint16_t* k,
-                                  const uint16_t* v, cudaStream_t stream);
+                                  const uint16_t* v, bool meta16, cudaStream_t stream);
 cudaError_t launch_quantize_large(const QuantPlan<kQuantPlanLarge>& plan, uint8_t* arena, const uint16_t* k,
-                                  const uint16_t* v, cudaStream_t stream);
+                                  const uint16_t* v, bool meta16, cudaStream_t stream);
 
 // ------------------------------------------------------------------ decode
 
@@ -115,14 +116,14 @@ struct PrefillParams {
   uint32_t* err_word;
 };
 
-cudaError_t launch_prefill(const PrefillParams& p, const uint8_t* arena, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillParams& p, const uint8_t* arena, bool meta16, cudaStream_t stream);
 
 int num_sms(int device);
 int decode_int2_ctas_per_sm();
 int decode_bf16_ctas_per_sm();
 
 template <int MAXS>
-cudaError_t launch_decode_int2(const DecodeParams<MAXS>& p, const uint8_t* arena, cudaStream_t stream,
+cudaError_t launch_decode_int2(const DecodeParams<MAXS>& p, const uint8_t* arena, bool meta16, cudaStream_t stream,
                                cudaEvent_t ev_start, cudaEvent_t ev_stop);
 template <int MAXS>
 cudaError_t launch_decode_bf16(const DecodeParams<MAXS>& p, const uint16_t* kc, const uint16_t* vc,

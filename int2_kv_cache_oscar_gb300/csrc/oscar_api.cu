@@ -18,6 +18,8 @@ using namespace oscar;
 
 struct oscar_cache {
   oscar_cache_config cfg;
+  bool meta16;               // float16 metadata layout
+  int block_bytes;
   uint8_t* arena;
   size_t arena_bytes;
   ArenaLayout layout;
@@ -76,6 +78,8 @@ oscar_status check_config(const oscar_cache_config* c) {
   if (c->max_batch < 1 || c->num_kv_heads < 1 || c->max_seq_len < 1)
     return fail(OSCAR_ERR_INVALID_ARG, "max_batch, num_kv_heads and max_seq_len must be >= 1");
   if (c->device < 0) return fail(OSCAR_ERR_INVALID_ARG, "device must be >= 0");
+  if (c->meta_bits != 0 && c->meta_bits != 32 && c->meta_bits != 16)
+    return fail(OSCAR_ERR_UNSUPPORTED, "meta_bits must be 32 or 16 (got %d)", c->meta_bits);
   if ((int64_t)c->max_batch * c->num_kv_heads > (1 << 24))
     return fail(OSCAR_ERR_CAPACITY, "max_batch * num_kv_heads too large");
   return OSCAR_OK;
@@ -107,9 +111,9 @@ oscar_status run_quant_plan(oscar_cache* c, const std::vector<QuantTask>& tasks,
   for (size_t i = begin; i < end; ++i) plan.t[i - begin] = tasks[i];
   cudaError_t e;
   if constexpr (CAP == kQuantPlanSmall)
-    e = launch_quantize_small(plan, c->arena, k, v, stream);
+    e = launch_quantize_small(plan, c->arena, k, v, c->meta16, stream);
   else
-    e = launch_quantize_large(plan, c->arena, k, v, stream);
+    e = launch_quantize_large(plan, c->arena, k, v, c->meta16, stream);
   if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
   return OSCAR_OK;
 }
@@ -142,7 +146,8 @@ oscar_status run_decode(int device, int sms, int ctas_per_sm, int32_t n, const i
                         int hkv, int hq, float scale, int bf16_mode, int max_groups, int64_t blocks_off,
                         int64_t windows_off, const uint8_t* arena, uint32_t* err_word, const uint16_t* kc,
                         const uint16_t* vc, const void* q, void* out, void* ws, size_t ws_bytes,
-                        cudaStream_t stream, const void* k_new = nullptr, const void* v_new = nullptr) {
+                        cudaStream_t stream, const void* k_new = nullptr, const void* v_new = nullptr,
+                        bool meta16 = false) {
   DecodeParams<MAXS> P;
   std::memset(&P, 0, sizeof(P));
   int64_t rows = 0;
@@ -174,7 +179,7 @@ oscar_status run_decode(int device, int sms, int ctas_per_sm, int32_t n, const i
   if (bf16_mode)
     e = launch_decode_bf16(P, kc, vc, stream, g_ev_start, g_ev_stop);
   else
-    e = launch_decode_int2(P, arena, stream, g_ev_start, g_ev_stop);
+    e = launch_decode_int2(P, arena, meta16, stream, g_ev_start, g_ev_stop);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   e = launch_combine(P, arena, stream);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
@@ -192,7 +197,8 @@ oscar_status oscar_cache_required_bytes(const oscar_cache_config* cfg, size_t* o
   oscar_status s = check_config(cfg);
   if (s != OSCAR_OK) return s;
   if (!out_bytes) return fail(OSCAR_ERR_INVALID_ARG, "out_bytes is NULL");
-  *out_bytes = (size_t)arena_layout(cfg->max_batch, cfg->num_kv_heads, cfg->max_seq_len).total;
+  *out_bytes = (size_t)arena_layout(cfg->max_batch, cfg->num_kv_heads, cfg->max_seq_len,
+                                    cfg->meta_bits == 16 ? kBlockBytes16 : kBlockBytes).total;
   return ok();
 }
 
@@ -204,7 +210,9 @@ oscar_status oscar_cache_create(const oscar_cache_config* cfg, void* device_aren
     if (!out) return fail(OSCAR_ERR_INVALID_ARG, "out is NULL");
     if (!device_arena) return fail(OSCAR_ERR_INVALID_ARG, "device_arena is NULL");
     if (!aligned(device_arena, 256)) return fail(OSCAR_ERR_INVALID_ARG, "device_arena must be 256-byte aligned");
-    const ArenaLayout L = arena_layout(cfg->max_batch, cfg->num_kv_heads, cfg->max_seq_len);
+    const bool meta16 = cfg->meta_bits == 16;
+    const ArenaLayout L = arena_layout(cfg->max_batch, cfg->num_kv_heads, cfg->max_seq_len,
+                                       meta16 ? kBlockBytes16 : kBlockBytes);
     if (arena_bytes < (size_t)L.total)
       return fail(OSCAR_ERR_CAPACITY, "arena too small: %zu < %lld bytes", arena_bytes, (long long)L.total);
     DeviceGuard dg(cfg->device);
@@ -215,6 +223,8 @@ oscar_status oscar_cache_create(const oscar_cache_config* cfg, void* device_aren
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(arena metadata)");
     oscar_cache* c = new oscar_cache;
     c->cfg = *cfg;
+    c->meta16 = meta16;
+    c->block_bytes = meta16 ? kBlockBytes16 : kBlockBytes;
     c->arena = static_cast<uint8_t*>(device_arena);
     c->arena_bytes = arena_bytes;
     c->layout = L;
@@ -389,12 +399,14 @@ oscar_status oscar_decode_attention(oscar_cache* c, int32_t n_seqs, const int32_
       s = run_decode<kDecodeSeqsSmall>(c->cfg.device, c->sms, decode_int2_ctas_per_sm(), n_seqs, seq_ids,
                                        lens.data(), hkv, num_q_heads, scale, 0, c->layout.max_groups,
                                        c->layout.blocks_off, c->layout.windows_off, c->arena, err_word, nullptr,
-                                       nullptr, q, out, workspace, workspace_bytes, st);
+                                       nullptr, q, out, workspace, workspace_bytes, st, nullptr, nullptr,
+                                       c->meta16);
     else
       s = run_decode<kDecodeSeqsLarge>(c->cfg.device, c->sms, decode_int2_ctas_per_sm(), n_seqs, seq_ids,
                                        lens.data(), hkv, num_q_heads, scale, 0, c->layout.max_groups,
                                        c->layout.blocks_off, c->layout.windows_off, c->arena, err_word, nullptr,
-                                       nullptr, q, out, workspace, workspace_bytes, st);
+                                       nullptr, q, out, workspace, workspace_bytes, st, nullptr, nullptr,
+                                       c->meta16);
     if (s != OSCAR_OK) return s;
     return ok();
   } catch (const std::exception& ex) {
@@ -455,12 +467,14 @@ oscar_status oscar_append_decode(oscar_cache* c, int32_t n_seqs, const int32_t* 
       s = run_decode<kDecodeSeqsSmall>(c->cfg.device, c->sms, decode_int2_ctas_per_sm(), n_seqs, seq_ids,
                                        lens.data(), hkv, num_q_heads, scale, 0, c->layout.max_groups,
                                        c->layout.blocks_off, c->layout.windows_off, c->arena, err_word, nullptr,
-                                       nullptr, q, out, workspace, workspace_bytes, st, k_new, v_new);
+                                       nullptr, q, out, workspace, workspace_bytes, st, k_new, v_new,
+                                       c->meta16);
     else
       s = run_decode<kDecodeSeqsLarge>(c->cfg.device, c->sms, decode_int2_ctas_per_sm(), n_seqs, seq_ids,
                                        lens.data(), hkv, num_q_heads, scale, 0, c->layout.max_groups,
                                        c->layout.blocks_off, c->layout.windows_off, c->arena, err_word, nullptr,
-                                       nullptr, q, out, workspace, workspace_bytes, st, k_new, v_new);
+                                       nullptr, q, out, workspace, workspace_bytes, st, k_new, v_new,
+                                       c->meta16);
     if (s != OSCAR_OK) return s;
     for (int32_t i = 0; i < n_seqs; ++i) c->len[seq_ids[i]] = lens[i];
     return ok();
@@ -506,7 +520,7 @@ oscar_status oscar_prefill_attention(oscar_cache* c, int32_t seq, int32_t n_q, c
   P.err_word = reinterpret_cast<uint32_t*>(c->arena);
   DeviceGuard dg(c->cfg.device);
   if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
-  cudaError_t e = launch_prefill(P, c->arena, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_prefill(P, c->arena, c->meta16, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return ok();
 }
@@ -525,7 +539,7 @@ oscar_status oscar_cache_bytes(const oscar_cache* c, int32_t seq, int32_t kind, 
   for (int32_t s = (seq < 0 ? 0 : seq); s < (seq < 0 ? c->cfg.max_batch : seq + 1); ++s) {
     const int64_t L = c->len[s];
     if (kind == OSCAR_BYTES_USED)
-      total += (size_t)hkv * ((L / kGroup) * (int64_t)kBlockBytes + (L % kGroup) * 2 * kHeadDim * 2);
+      total += (size_t)hkv * ((L / kGroup) * (int64_t)c->block_bytes + (L % kGroup) * 2 * kHeadDim * 2);
     else
       total += (size_t)hkv * L * 2 * kHeadDim * 2;
   }
@@ -541,7 +555,7 @@ oscar_status oscar_cache_block_offset(const oscar_cache* c, int32_t seq, int32_t
     return fail(OSCAR_ERR_INVALID_ARG, "index out of range");
   *out_offset = (size_t)(c->layout.blocks_off +
                          (((int64_t)seq * c->cfg.num_kv_heads + kv_head) * c->layout.max_groups + group) *
-                             (int64_t)kBlockBytes);
+                             (int64_t)c->block_bytes);
   return ok();
 }
 

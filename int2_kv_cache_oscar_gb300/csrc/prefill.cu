@@ -161,15 +161,18 @@ __device__ __forceinline__ void pf_softmax(float (&sc)[NT][4], int nt_used, floa
   l_run[1] = fmaf(l_run[1], alpha[1], s1);
 }
 
+template <bool M16>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_int2_kernel(const __grid_constant__ PrefillParams p, const uint8_t* __restrict__ arena) {
+  using B = Blk<M16>;           // ring stages keep 13,824-byte slots; a block copy is B::kBytes
+  using MR = Meta<M16>;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   PfSmem& S = *reinterpret_cast<PfSmem*>(smem_raw);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int j = blockIdx.y;                 // KV head
   const int ng = p.ng;
-  const uint8_t* blocks = arena + p.blocks_off + ((int64_t)p.slot * p.hkv + j) * p.max_groups * (int64_t)kBlockBytes;
+  const uint8_t* blocks = arena + p.blocks_off + ((int64_t)p.slot * p.hkv + j) * p.max_groups * (int64_t)B::kBytes;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPfStages; ++s) {
@@ -181,8 +184,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     S.abort_flag = 0;
     fence_mbar_init();
     for (int k = 0; k < ng && k < kPfStages; ++k) {
-      mbar_arrive_expect_tx(&S.full[k], kBlockBytes);
-      bulk_g2s(S.stage[k], blocks + (int64_t)k * kBlockBytes, kBlockBytes, &S.full[k]);
+      mbar_arrive_expect_tx(&S.full[k], B::kBytes);
+      bulk_g2s(S.stage[k], blocks + (int64_t)k * B::kBytes, B::kBytes, &S.full[k]);
       S.nissued[k] = 1;
     }
   }
@@ -273,12 +276,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // them, so no warp can be two uses ahead: the parity test cannot alias
     if (!mbar_wait_bounded(&S.full[s], use & 1, &S.abort_flag, p.err_word)) break;
     const uint8_t* blk = S.stage[s];
-    const float* ksc = reinterpret_cast<const float*>(blk + kOffKScale);
-    const float* kze = reinterpret_cast<const float*>(blk + kOffKZero);
-    const float* knm = reinterpret_cast<const float*>(blk + kOffKNorm);
-    const float* vsz = reinterpret_cast<const float*>(blk + kOffVSZ);
+    const uint8_t* ksc = blk + B::kKScale;
+    const uint8_t* kze = blk + B::kKZero;
+    const uint8_t* knm = blk + B::kKNorm;
+    const uint8_t* vsz = blk + B::kVSZ;
     const uint4* kc = reinterpret_cast<const uint4*>(blk + kOffKCodes);
-    const uint4* vc = reinterpret_cast<const uint4*>(blk + kOffVCodes);
+    const uint4* vc = reinterpret_cast<const uint4*>(blk + B::kVCodes);
 
     float qz0 = 0.0f, qz1 = 0.0f;   // q_rot . z of the lane's rows (times 2^F), from the first half
     float qzt0 = 0.0f, qzt1 = 0.0f;
@@ -305,11 +308,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const float2 x01 = *reinterpret_cast<const float2*>(q0row + c1);
           const float2 x10 = *reinterpret_cast<const float2*>(q1row + c0);
           const float2 x11 = *reinterpret_cast<const float2*>(q1row + c1);
-          const float2 s0 = *reinterpret_cast<const float2*>(ksc + c0);
-          const float2 s1 = *reinterpret_cast<const float2*>(ksc + c1);
+          const float2 s0 = MR::two(ksc, c0);
+          const float2 s1 = MR::two(ksc, c1);
           if (hh == 0) {
-            const float2 z0 = *reinterpret_cast<const float2*>(kze + c0);
-            const float2 z1 = *reinterpret_cast<const float2*>(kze + c1);
+            const float2 z0 = MR::two(kze, c0);
+            const float2 z1 = MR::two(kze, c1);
             qz0 = fmaf(fmaf(x00.x, z0.x, x00.y * z0.y), zw[kk][0], qz0);
             qz0 = fmaf(fmaf(x01.x, z1.x, x01.y * z1.y), zw[kk][1], qz0);
             qz1 = fmaf(fmaf(x10.x, z0.x, x10.y * z0.y), zw[kk][0], qz1);
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
 #pragma unroll
       for (int ntl = 0; ntl < 8; ++ntl) {
-        const float2 n2 = *reinterpret_cast<const float2*>(knm + 64 * hh + 8 * ntl + 2 * tig);
+        const float2 n2 = MR::two(knm, 64 * hh + 8 * ntl + 2 * tig);
         sc[ntl][0] = fmaf(sc[ntl][0], fe0, qzt0) * n2.x * p.scale_log2;
         sc[ntl][1] = fmaf(sc[ntl][1], fe0, qzt0) * n2.y * p.scale_log2;
         sc[ntl][2] = fmaf(sc[ntl][2], fe1, qzt1) * n2.x * p.scale_log2;
@@ -368,7 +371,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int t = 64 * hh + 8 * ntl + 2 * tig + e;
-          const float4 z4 = *reinterpret_cast<const float4*>(vsz + 8 * t + 4);
+          const float4 z4 = MR::vsz4(vsz, t, 1);
           zacc[0][0] = fmaf(sc[ntl][e], z4.x, zacc[0][0]);
           zacc[0][1] = fmaf(sc[ntl][e], z4.y, zacc[0][1]);
           zacc[0][2] = fmaf(sc[ntl][e], z4.z, zacc[0][2]);
@@ -391,10 +394,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const int t0 = 64 * hh + 16 * kk + 2 * tig, t1 = t0 + 8;
-        const float4 sa = *reinterpret_cast<const float4*>(vsz + 8 * t0);
-        const float4 sb = *reinterpret_cast<const float4*>(vsz + 8 * (t0 + 1));
-        const float4 sc4 = *reinterpret_cast<const float4*>(vsz + 8 * t1);
-        const float4 sd = *reinterpret_cast<const float4*>(vsz + 8 * (t1 + 1));
+        const float4 sa = MR::vsz4(vsz, t0, 0);
+        const float4 sb = MR::vsz4(vsz, t0 + 1, 0);
+        const float4 sc4 = MR::vsz4(vsz, t1, 0);
+        const float4 sd = MR::vsz4(vsz, t1 + 1, 0);
         const float* p00 = sc[2 * kk];       // tokens t0, t0+1: rows g (0, 1), g + 8 (2, 3)
         const float* p01 = sc[2 * kk + 1];   // tokens t1, t1+1
         const float f0 = fsc[kk][0], f1 = fsc[kk][1];
@@ -427,8 +430,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (before == (use + 1) * kPfConsumers - 1 && k + kPfStages < ng) {
         __threadfence_block();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic reads before the async write
-        mbar_arrive_expect_tx(&S.full[s], kBlockBytes);
-        bulk_g2s(S.stage[s], blocks + (int64_t)(k + kPfStages) * kBlockBytes, kBlockBytes, &S.full[s]);
+        mbar_arrive_expect_tx(&S.full[s], B::kBytes);
+        bulk_g2s(S.stage[s], blocks + (int64_t)(k + kPfStages) * B::kBytes, B::kBytes, &S.full[s]);
         S.nissued[s] = use + 2;
       }
     }
@@ -576,15 +579,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillParams& p, const uint8_t* arena, cudaStream_t stream) {
-  if (p.rows <= 0) return cudaSuccess;
+namespace {
+template <bool M16>
+cudaError_t launch_prefill_t(const PrefillParams& p, const uint8_t* arena, cudaStream_t stream) {
   static bool attr_done[64] = {};
   const int smem = (int)sizeof(PfSmem);
-  cudaError_t e = ensure_smem_attr(prefill_int2_kernel, smem, attr_done);
+  cudaError_t e = ensure_smem_attr(prefill_int2_kernel<M16>, smem, attr_done);
   if (e != cudaSuccess) return e;
   const dim3 grid((p.rows + kPfRows - 1) / kPfRows, p.hkv);
-  prefill_int2_kernel<<<grid, kPfThreads, smem, stream>>>(p, arena);
+  prefill_int2_kernel<M16><<<grid, kPfThreads, smem, stream>>>(p, arena);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillParams& p, const uint8_t* arena, bool meta16, cudaStream_t stream) {
+  if (p.rows <= 0) return cudaSuccess;
+  return meta16 ? launch_prefill_t<true>(p, arena, stream) : launch_prefill_t<false>(p, arena, stream);
 }
 
 }  // namespace oscar

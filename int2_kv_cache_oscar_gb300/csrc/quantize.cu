@@ -26,6 +26,8 @@
 // the packed f32x2 operations round each lane exactly like the scalar ones.
 #include <cstddef>
 
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -77,6 +79,17 @@ __device__ __forceinline__ uint2 code_bits2(float2 x, float2 inv, float2 negz) {
   return make_uint2(__float_as_uint(__fadd_rn(vx, kMagic)), __float_as_uint(__fadd_rn(vy, kMagic)));
 }
 
+// Code 0..3 from the float bits of a decision, clamped: in the float16
+// metadata layout the rounded zero and scale can move a value by up to
+// |z| 2^-12 / s outside [0, 3] (the method's rule clamps).
+__device__ __forceinline__ uint32_t clamped_code(uint32_t bits) {
+  const int c = (int)(bits - kMagicBits);
+  return (uint32_t)min(max(c, 0), 3);
+}
+
+// The float16 that the 16-bit metadata layout stores for x (nearest even).
+__device__ __forceinline__ float to_half_value(float x) { return __half2float(__float2half_rn(x)); }
+
 // Byte offset of value-code row q (channels 4q .. 4q + 3, code of channel
 // 4q + i in bits 2i, 2i + 1 of each byte): rows of the upper 64 channels are
 // shifted by 16 bytes so that the two threads of a token (one per channel
@@ -114,7 +127,7 @@ __host__ __device__ constexpr uint32_t key_word_magic() {
   return m;
 }
 
-template <int CAP>
+template <int CAP, bool M16>
 __global__ void __launch_bounds__(kQThreads, 2)
     quantize_append_kernel(const __grid_constant__ QuantPlan<CAP> plan, uint8_t* __restrict__ arena,
                            const uint16_t* __restrict__ kin, const uint16_t* __restrict__ vin) {
@@ -130,7 +143,8 @@ __global__ void __launch_bounds__(kQThreads, 2)
   uint16_t* win_v = win_k + kGroup * kHeadDim;
 
   if (T.kind == 0) {
-    uint8_t* blk = arena + plan.blocks_off + (sh * plan.max_groups + T.group) * (int64_t)kBlockBytes;
+    using B = Blk<M16>;
+    uint8_t* blk = arena + plan.blocks_off + (sh * plan.max_groups + T.group) * (int64_t)B::kBytes;
     const int t = tid >> 1;          // token of the group
     const int half = tid & 1;        // channels [64 half, 64 half + 64)
     const bool from_win = t < T.n_win;
@@ -170,13 +184,18 @@ __global__ void __launch_bounds__(kQThreads, 2)
         }
         const float mn = fminf(bf16_lo(mn2), bf16_hi(mn2));
         const float mx = fmaxf(bf16_lo(mx2), bf16_hi(mx2));
-        const float sc = (mx - mn) / 3.0f;
+        float sc = (mx - mn) / 3.0f;
+        float zq = mn;
+        if constexpr (M16) {     // decide against the stored (rounded) parameters
+          sc = to_half_value(sc);
+          zq = to_half_value(mn);
+        }
         const float inv = sc > 0.0f ? 1.0f / sc : 0.0f;
         sv[g2] = sc;
-        zv[g2] = mn;
+        zv[g2] = zq;
         smax = fmaxf(smax, sc);
         const int gi = 2 * half + g2;
-        const float2 inv2 = make_float2(inv, inv), negz2 = make_float2(-mn, -mn);
+        const float2 inv2 = make_float2(inv, inv), negz2 = make_float2(-zq, -zq);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const uint32_t ws[4] = {w4[i].x, w4[i].y, w4[i].z, w4[i].w};
@@ -184,14 +203,25 @@ __global__ void __launch_bounds__(kQThreads, 2)
           for (int qq = 0; qq < 2; ++qq) {   // channels gi*32 + 8i + 4qq .. + 3
             const uint2 c01 = code_bits2(bf16x2_to_float2(ws[2 * qq]), inv2, negz2);
             const uint2 c23 = code_bits2(bf16x2_to_float2(ws[2 * qq + 1]), inv2, negz2);
-            // low bytes are the codes (the float bits' constant part has a zero low byte)
-            const uint32_t b = (c01.x & 0xffu) | ((c01.y & 0xffu) << 2) | ((c23.x & 0xffu) << 4) | ((c23.y & 0xffu) << 6);
+            uint32_t b;
+            if constexpr (M16) {
+              b = clamped_code(c01.x) | (clamped_code(c01.y) << 2) | (clamped_code(c23.x) << 4) |
+                  (clamped_code(c23.y) << 6);
+            } else {
+              // low bytes are the codes (the float bits' constant part has a zero low byte)
+              b = (c01.x & 0xffu) | ((c01.y & 0xffu) << 2) | ((c23.x & 0xffu) << 4) | ((c23.y & 0xffu) << 6);
+            }
             S.vb[vb_row(gi * 8 + 2 * i + qq) + pt] = (uint8_t)b;
           }
         }
       }
-      *reinterpret_cast<float2*>(blk + kOffVSZ + 32 * t + 8 * half) = make_float2(sv[0], sv[1]);
-      *reinterpret_cast<float2*>(blk + kOffVSZ + 32 * t + 16 + 8 * half) = make_float2(zv[0], zv[1]);
+      if constexpr (M16) {   // per token 16 B: s[0..3] then z[0..3], float16 (exact: already rounded)
+        *reinterpret_cast<uint32_t*>(blk + B::kVSZ + 16 * t + 4 * half) = pack_half2(sv[0], sv[1]);
+        *reinterpret_cast<uint32_t*>(blk + B::kVSZ + 16 * t + 8 + 4 * half) = pack_half2(zv[0], zv[1]);
+      } else {
+        *reinterpret_cast<float2*>(blk + kOffVSZ + 32 * t + 8 * half) = make_float2(sv[0], sv[1]);
+        *reinterpret_cast<float2*>(blk + kOffVSZ + 32 * t + 16 + 8 * half) = make_float2(zv[0], zv[1]);
+      }
     }
 
     // ---- keys: rotation (6 butterfly stages in registers + 1 across the
@@ -244,7 +274,12 @@ __global__ void __launch_bounds__(kQThreads, 2)
     // code_bits2 cannot be fused with this multiply
 #pragma unroll
     for (int i = 0; i < 32; ++i) x[i] = make_float2(__fmul_rn(x[i].x, rinv), __fmul_rn(x[i].y, rinv));
-    if (half == 0) reinterpret_cast<float*>(blk + kOffKNorm)[t] = norm;
+    if (half == 0) {
+      if constexpr (M16)
+        reinterpret_cast<__half*>(blk + B::kKNorm)[t] = __float2half_rn(norm);
+      else
+        reinterpret_cast<float*>(blk + kOffKNorm)[t] = norm;
+    }
     {
       float4* dst = reinterpret_cast<float4*>(krow + 68 * half);
 #pragma unroll
@@ -281,12 +316,21 @@ __global__ void __launch_bounds__(kQThreads, 2)
         mn = fminf(mn, rmn[ts * kHeadDim + c]);
         mx = fmaxf(mx, rmx[ts * kHeadDim + c]);
       }
-      const float sc = (mx - mn) / 3.0f;
+      float sc = (mx - mn) / 3.0f;
+      if constexpr (M16) {     // decide against the stored (rounded) parameters
+        sc = to_half_value(sc);
+        mn = to_half_value(mn);
+      }
       float* kqf = reinterpret_cast<float*>(&S.kq[kq_index(c)]);
       kqf[c & 1] = sc > 0.0f ? 1.0f / sc : 0.0f;
       kqf[2 + (c & 1)] = -mn;
-      reinterpret_cast<float*>(blk + kOffKScale)[c] = sc;
-      reinterpret_cast<float*>(blk + kOffKZero)[c] = mn;
+      if constexpr (M16) {
+        reinterpret_cast<__half*>(blk + B::kKScale)[c] = __float2half_rn(sc);
+        reinterpret_cast<__half*>(blk + B::kKZero)[c] = __float2half_rn(mn);
+      } else {
+        reinterpret_cast<float*>(blk + kOffKScale)[c] = sc;
+        reinterpret_cast<float*>(blk + kOffKZero)[c] = mn;
+      }
     }
     __syncthreads();
 
@@ -295,7 +339,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
       const int mt = t >> 4, g = t & 7, r = (t >> 3) & 1;
 #pragma unroll
       for (int tig = 0; tig < 4; ++tig) {
-        uint32_t w = 0u - key_word_magic();
+        uint32_t w = M16 ? 0u : 0u - key_word_magic();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
@@ -303,8 +347,13 @@ __global__ void __launch_bounds__(kQThreads, 2)
             const int i = 16 * kk + 8 * hf + 2 * tig;          // channels 64 half + i, + i + 1 (e = 0, 1)
             const float4 pq = S.kq[kq_index(64 * half + i)];
             const uint2 cb = code_bits2(x[i >> 1], make_float2(pq.x, pq.y), make_float2(pq.z, pq.w));
-            w += cb.x << (4 * kk + 2 * hf);
-            w += cb.y << (16 + 4 * kk + 2 * hf);
+            if constexpr (M16) {
+              w |= clamped_code(cb.x) << (4 * kk + 2 * hf);
+              w |= clamped_code(cb.y) << (16 + 4 * kk + 2 * hf);
+            } else {
+              w += cb.x << (4 * kk + 2 * hf);
+              w += cb.y << (16 + 4 * kk + 2 * hf);
+            }
           }
         }
         S.kw[((mt * 32 + 4 * g + tig) * 4) + 2 * half + r] = w;
@@ -336,7 +385,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
           wv[2 * j + r] = w;
         }
       }
-      reinterpret_cast<uint4*>(blk + kOffVCodes)[u] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      reinterpret_cast<uint4*>(blk + B::kVCodes)[u] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
     }
     if (tid == 0) {
       float m = S.red[0];
@@ -363,29 +412,31 @@ __global__ void __launch_bounds__(kQThreads, 2)
   }
 }
 
-template <int CAP>
+template <int CAP, bool M16>
 cudaError_t launch_quantize(const QuantPlan<CAP>& plan, uint8_t* arena, const uint16_t* k, const uint16_t* v,
                             cudaStream_t stream) {
   if (plan.n_tasks <= 0) return cudaSuccess;
   const int smem = (int)sizeof(QuantSmem);
   static bool attr_done[64] = {};
-  cudaError_t e = ensure_smem_attr(quantize_append_kernel<CAP>, smem, attr_done);
+  cudaError_t e = ensure_smem_attr(quantize_append_kernel<CAP, M16>, smem, attr_done);
   if (e != cudaSuccess) return e;
   dim3 grid(plan.n_tasks, plan.hkv);
-  quantize_append_kernel<CAP><<<grid, kQThreads, smem, stream>>>(plan, arena, k, v);
+  quantize_append_kernel<CAP, M16><<<grid, kQThreads, smem, stream>>>(plan, arena, k, v);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_quantize_small(const QuantPlan<kQuantPlanSmall>& plan, uint8_t* arena, const uint16_t* k,
-                                  const uint16_t* v, cudaStream_t stream) {
-  return launch_quantize(plan, arena, k, v, stream);
+                                  const uint16_t* v, bool meta16, cudaStream_t stream) {
+  return meta16 ? launch_quantize<kQuantPlanSmall, true>(plan, arena, k, v, stream)
+                : launch_quantize<kQuantPlanSmall, false>(plan, arena, k, v, stream);
 }
 
 cudaError_t launch_quantize_large(const QuantPlan<kQuantPlanLarge>& plan, uint8_t* arena, const uint16_t* k,
-                                  const uint16_t* v, cudaStream_t stream) {
-  return launch_quantize(plan, arena, k, v, stream);
+                                  const uint16_t* v, bool meta16, cudaStream_t stream) {
+  return meta16 ? launch_quantize<kQuantPlanLarge, true>(plan, arena, k, v, stream)
+                : launch_quantize<kQuantPlanLarge, false>(plan, arena, k, v, stream);
 }
 
 }  // namespace oscar

@@ -31,6 +31,7 @@ HEAD_DIM = 128
 GROUP = 128
 VALUE_GROUP = 32
 BLOCK_BYTES = 13824
+BLOCK_BYTES_META16 = 11008
 WINDOW_BYTES = 65536
 
 
@@ -44,7 +45,7 @@ class oscar_cache_config(ctypes.Structure):
     _fields_ = [("max_batch", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
                 ("group_size", ctypes.c_int32), ("value_group", ctypes.c_int32),
-                ("device", ctypes.c_int32)]
+                ("device", ctypes.c_int32), ("meta_bits", ctypes.c_int32)]
 
 
 def _load() -> ctypes.CDLL:
@@ -124,9 +125,9 @@ def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
 
 def make_config(max_batch: int, num_kv_heads: int, max_seq_len: int, device: int = 0,
                 head_dim: int = HEAD_DIM, group_size: int = GROUP,
-                value_group: int = VALUE_GROUP) -> oscar_cache_config:
+                value_group: int = VALUE_GROUP, meta_bits: int = 32) -> oscar_cache_config:
     return oscar_cache_config(max_batch, num_kv_heads, head_dim, max_seq_len, group_size,
-                              value_group, device)
+                              value_group, device, meta_bits)
 
 
 def oscar_cache_required_bytes(cfg: oscar_cache_config) -> int:
@@ -254,9 +255,10 @@ class OscarCache:
     """Owns a device arena (a torch uint8 tensor) and the library handle."""
 
     def __init__(self, max_batch: int, num_kv_heads: int, max_seq_len: int,
-                 device: Optional[torch.device] = None):
+                 device: Optional[torch.device] = None, meta_bits: int = 32):
         device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
-        self.cfg = make_config(max_batch, num_kv_heads, max_seq_len, device.index or 0)
+        self.cfg = make_config(max_batch, num_kv_heads, max_seq_len, device.index or 0, meta_bits=meta_bits)
+        self.meta_bits = meta_bits
         nbytes = oscar_cache_required_bytes(self.cfg)
         self.arena = torch.empty(nbytes, dtype=torch.uint8, device=device)
         self.handle = oscar_cache_create(self.cfg, self.arena)

@@ -58,7 +58,8 @@ def gpu_head(cache, arena: np.ndarray, slot: int, head: int) -> O.HeadCache:
         parts = []
         for g in range(ng):
             off = O_.oscar_cache_block_offset(cache.handle, slot, head, g)
-            parts.append(layout.parse_block(arena[off:off + layout.BLOCK_BYTES]))
+            mb = getattr(cache, "meta_bits", 32)
+            parts.append(layout.parse_block(arena[off:off + layout.block_bytes(mb)], mb))
         st = {k: np.stack([p[k] for p in parts]) for k in parts[0]}
         keys = O.KeyGroup(st["kcodes"], st["kscale"], st["kzero"], st["knorm"], None)
         values = O.ValueGroup(st["vcodes"], st["vscale"], st["vzero"], None)
@@ -67,8 +68,8 @@ def gpu_head(cache, arena: np.ndarray, slot: int, head: int) -> O.HeadCache:
     return O.HeadCache(keys, values, wk, wv)
 
 
-def oracle_head(k: torch.Tensor, v: torch.Tensor, head: int) -> O.HeadCache:
-    return O.build_head_cache(f64(k[:, head]), f64(v[:, head]))
+def oracle_head(k: torch.Tensor, v: torch.Tensor, head: int, meta_bits: int = 32) -> O.HeadCache:
+    return O.build_head_cache(f64(k[:, head]), f64(v[:, head]), meta_bits)
 
 
 def live_bytes(cache, arena: np.ndarray, slot: int) -> np.ndarray:
@@ -82,7 +83,7 @@ def live_bytes(cache, arena: np.ndarray, slot: int) -> np.ndarray:
     for h in range(hkv):
         for g in range(ng):
             off = O_.oscar_cache_block_offset(cache.handle, slot, h, g)
-            parts.append(arena[off:off + layout.BLOCK_BYTES])
+            parts.append(arena[off:off + layout.block_bytes(getattr(cache, "meta_bits", 32))])
         off = O_.oscar_cache_window_offset(cache.handle, slot, h)
         parts.append(arena[off:off + w * 256])
         parts.append(arena[off + 32768:off + 32768 + w * 256])

@@ -16,6 +16,13 @@ D = 128
 G = 128
 BLOCK_BYTES = 13824
 OFF_KCODES, OFF_KSCALE, OFF_KZERO, OFF_KNORM, OFF_VCODES, OFF_VSZ = 0, 4096, 4608, 5120, 5632, 9728
+# the same block with float16 metadata (meta_bits = 16)
+BLOCK_BYTES16 = 11008
+OFF16_KSCALE, OFF16_KZERO, OFF16_KNORM, OFF16_VCODES, OFF16_VSZ = 4096, 4352, 4608, 4864, 8960
+
+
+def block_bytes(meta_bits: int = 32) -> int:
+    return BLOCK_BYTES16 if meta_bits == 16 else BLOCK_BYTES
 
 
 def _index_tables():
@@ -56,8 +63,18 @@ def pack_fragment(codes: np.ndarray) -> np.ndarray:
     return np.bitwise_or.reduce(vals, axis=1).astype(np.uint32)
 
 
-def parse_block(raw: np.ndarray) -> dict:
-    """raw: uint8 [13824] -> canonical arrays of one (group, kv head)."""
+def parse_block(raw: np.ndarray, meta_bits: int = 32) -> dict:
+    """raw: uint8 [13824] (or [11008] with float16 metadata) -> canonical
+    arrays of one (group, kv head); metadata returned as float32."""
+    if meta_bits == 16:
+        raw = np.ascontiguousarray(np.asarray(raw, np.uint8).reshape(BLOCK_BYTES16))
+        kcodes = unpack_fragment(raw[OFF_KCODES:OFF_KCODES + 4096].view("<u4"))
+        f16 = lambda a, n: raw[a:a + 2 * n].view("<f2").astype(np.float32)
+        vcodes_t = unpack_fragment(raw[OFF16_VCODES:OFF16_VCODES + 4096].view("<u4"))
+        vsz = raw[OFF16_VSZ:OFF16_VSZ + 2048].view("<f2").astype(np.float32).reshape(G, 8)
+        return dict(kcodes=kcodes, kscale=f16(OFF16_KSCALE, 128), kzero=f16(OFF16_KZERO, 128),
+                    knorm=f16(OFF16_KNORM, 128), vcodes=vcodes_t.T.copy(), vscale=vsz[:, :4].copy(),
+                    vzero=vsz[:, 4:].copy())
     raw = np.ascontiguousarray(np.asarray(raw, np.uint8).reshape(BLOCK_BYTES))
     kcodes = unpack_fragment(raw[OFF_KCODES:OFF_KCODES + 4096].view("<u4"))        # [token, ch]
     kscale = raw[OFF_KSCALE:OFF_KSCALE + 512].view("<f4").copy()

@@ -42,19 +42,23 @@ def test_every_declared_symbol_is_exported(O):
     assert set(_declared()) <= exported
 
 
-def test_required_bytes_layout(O):
-    cfg = O.make_config(3, 8, 1000)
+@pytest.mark.parametrize("meta_bits,block", [(32, 13824), (0, 13824), (16, 11008)])
+def test_required_bytes_layout(O, meta_bits, block):
+    cfg = O.make_config(3, 8, 1000, meta_bits=meta_bits)
     n = O.oscar_cache_required_bytes(cfg)
     meta = -(-(256 + 3 * 8 * 4) // 256) * 256
     groups = -(-1000 // 128)
-    blocks = 3 * 8 * groups * 13824
+    blocks = 3 * 8 * groups * block
     win_off = -(-(meta + blocks) // 256) * 256
     assert n == win_off + 3 * 8 * 65536
+    # 128 tokens x (32 + 32 code bytes + metadata) per block: 108 or 86 bytes a token
+    assert block == 128 * (108 if block == 13824 else 86)
 
 
 @pytest.mark.parametrize("field,value,status", [
     ("head_dim", 64, 4), ("group_size", 64, 4), ("value_group", 16, 4),
-    ("max_batch", 0, 1), ("num_kv_heads", 0, 1), ("max_seq_len", 0, 1), ("device", -1, 1)])
+    ("max_batch", 0, 1), ("num_kv_heads", 0, 1), ("max_seq_len", 0, 1), ("device", -1, 1),
+    ("meta_bits", 8, 4), ("meta_bits", 64, 4)])
 def test_bad_configs(O, field, value, status):
     cfg = O.make_config(2, 2, 256)
     setattr(cfg, field, value)
@@ -100,3 +104,28 @@ def test_layout_reader_roundtrip():
     seen = np.zeros((128, 128), int)
     np.add.at(seen, (layout._ROWS, layout._COLS), 1)
     assert np.all(seen == 1)
+
+
+def test_layout_reader_fp16_block():
+    """The float16-metadata block reader against a block assembled by hand
+    from the header's offsets."""
+    import numpy as np
+    from tests import layout
+    rng = np.random.default_rng(6)
+    kc = rng.integers(0, 4, (128, 128)).astype(np.uint8)
+    vc = rng.integers(0, 4, (128, 128)).astype(np.uint8)
+    ks, kz, kn = (rng.standard_normal(128).astype(np.float16) for _ in range(3))
+    vs = rng.standard_normal((128, 4)).astype(np.float16)
+    vz = rng.standard_normal((128, 4)).astype(np.float16)
+    raw = np.zeros(11008, np.uint8)
+    raw[0:4096] = layout.pack_fragment(kc).view(np.uint8)
+    raw[4096:4352] = ks.view(np.uint8)
+    raw[4352:4608] = kz.view(np.uint8)
+    raw[4608:4864] = kn.view(np.uint8)
+    raw[4864:8960] = layout.pack_fragment(vc.T).view(np.uint8)
+    raw[8960:11008] = np.concatenate([vs, vz], axis=1).reshape(-1).view(np.uint8)
+    b = layout.parse_block(raw, 16)
+    assert np.array_equal(b["kcodes"], kc) and np.array_equal(b["vcodes"], vc)
+    assert np.array_equal(b["kscale"], ks.astype(np.float32)) and np.array_equal(b["knorm"], kn.astype(np.float32))
+    assert np.array_equal(b["kzero"], kz.astype(np.float32))
+    assert np.array_equal(b["vscale"], vs.astype(np.float32)) and np.array_equal(b["vzero"], vz.astype(np.float32))
