@@ -210,9 +210,10 @@ class Timer:
         return statistics.mean(t), (statistics.mean(kt) if kt else None)
 
 
-def build_cache(O_, W, torch, lens, seed_recipe, slots=None, chunk=None, device="cuda", max_len=None):
+def build_cache(O_, W, torch, lens, seed_recipe, slots=None, chunk=None, device="cuda", max_len=None,
+                meta_bits=32):
     """Generate sequences on the GPU and append them; returns (cache, ks, vs)."""
-    cache = O_.OscarCache(len(lens), HKV, max_len or max(lens))
+    cache = O_.OscarCache(len(lens), HKV, max_len or max(lens), meta_bits=meta_bits)
     gen = torch.Generator(device=device)
     gen.manual_seed(seed_recipe[0])
     ks, vs = [], []
@@ -321,6 +322,30 @@ def gpu_arm(args, rank, world):
                            "GBps": round(bf16_bytes / (ref_kern * 1e-6) / 1e9, 1),
                            "frac_of_peak": round(bf16_bytes / (ref_kern * 1e-6) / 1e9 / peak, 3),
                            "int2_speedup": round(ref_us / dec_us, 2)}
+
+        # 16-bit metadata layout (86 B per token and KV head) on the same 128K sequence
+        c16 = O_.OscarCache(1, HKV, CTX, meta_bits=16)
+
+        def quantize16():
+            O_.oscar_cache_reset(c16.handle, 0)
+            c16.append([0], [0, CTX], k, v)
+
+        q16_us, _ = timer.run(quantize16, K, Wm)
+        launches += K * (-(-(CTX // 128) // 900))
+        ws16 = c16.workspace(1, HQ)
+        d16_us, k16_us = timer.run(lambda: c16.decode([0], q, HQ, outb, ws16), K, Wm,
+                                   kernel_events=lambda a, b: O_.oscar_set_timing_events(a, b))
+        launches += K * 4
+        O_.oscar_cache_check(c16.handle)
+        b16 = (CTX // 128) * HKV * O_.BLOCK_BYTES_META16
+        out["meta16"] = {"us_per_step": round(d16_us, 2), "main_kernel_us": round(k16_us, 2),
+                         "GBps": round(b16 / (k16_us * 1e-6) / 1e9, 1),
+                         "frac_of_peak": round(b16 / (k16_us * 1e-6) / 1e9 / peak, 3),
+                         "cache_bytes": b16, "bytes_per_token_head": O_.BLOCK_BYTES_META16 / 128,
+                         "step_speedup_vs_fp32_meta": round(dec_us / d16_us, 3),
+                         "quantize_us": round(q16_us, 1)}
+        c16.close()
+        del c16, ws16
         del k, v
         cache.close()
         del cache
@@ -456,17 +481,33 @@ def gpu_arm(args, rank, world):
 
 def profile_case(args):
     """Small, self-contained launches for ncu captures (no L2 flush, a few
-    hundred MB on the device): the INT2 decode, the 128K quantise, or the
-    BF16 reference decode."""
+    hundred MB on the device): the INT2 decode, the 128K quantise, the BF16
+    reference decode or the chunked prefill (512 queries over 32K tokens);
+    --meta16 selects the 16-bit metadata layout."""
     import torch
 
     from int2_kv_cache_oscar_gb300 import oscar as O_
     from int2_kv_cache_oscar_gb300 import workloads as W
+    meta_bits = 16 if args.meta16 else 32
+    if args.profile_prefill:
+        L, C = 32768, 512
+        c, _, _ = build_cache(O_, W, torch, [L], (5, W.LLAMA_RECIPE), meta_bits=meta_bits)
+        genp = torch.Generator(device="cuda")
+        genp.manual_seed(55)
+        qc = torch.randn((C, HQ, D), generator=genp, device="cuda").to(torch.bfloat16)
+        oc = torch.empty_like(qc)
+        lc = torch.empty((C, HQ), dtype=torch.float32, device="cuda")
+        for _ in range(args.steps):
+            O_.oscar_prefill_attention(c.handle, 0, qc, HQ, 0.0, oc, lc)
+        torch.cuda.synchronize()
+        O_.oscar_cache_check(c.handle)
+        print("profile prefill done")
+        return
     gen = torch.Generator(device="cuda")
     gen.manual_seed(2)
     k, v = W.make_sequence_kv(CTX, HKV, W.LLAMA_RECIPE, gen, "cuda")
     q = W.make_q(1, HQ, seed=2, device="cuda")
-    cache = O_.OscarCache(1, HKV, CTX)
+    cache = O_.OscarCache(1, HKV, CTX, meta_bits=meta_bits)
     if args.profile_bf16:
         kc, vc = bf16_cache(torch, [k], [v], CTX)
         del k, v
@@ -559,6 +600,10 @@ def main():
                     help="small self-contained BF16 reference decode launches for ncu")
     ap.add_argument("--profile-quantize", action="store_true",
                     help="profiling case: `steps` 128K quantise appends (8 KV heads)")
+    ap.add_argument("--profile-prefill", action="store_true",
+                    help="profiling case: `steps` chunked-prefill calls, 512 queries over 32K tokens")
+    ap.add_argument("--meta16", action="store_true",
+                    help="profiling cases use the 16-bit metadata layout")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -593,7 +638,7 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     torch.cuda.set_device(local_rank)
-    if args.profile_decode or args.profile_quantize or args.profile_bf16:
+    if args.profile_decode or args.profile_quantize or args.profile_bf16 or args.profile_prefill:
         profile_case(args)
         return
 
