@@ -171,16 +171,24 @@ oscar_status oscar_decode_workspace_bytes(const oscar_cache* cache, int32_t n_se
  * Single-query decode attention over the packed cache (split-K flash
  * decoding, GQA, ragged batch).
  *   seq_ids      host int32 [n_seqs]; every slot must have length >= 1
- *   q            device bf16 [n_seqs, num_q_heads, 128] (unrotated queries)
+ *   q            bf16 [n_seqs, num_q_heads, 128] (unrotated queries), 16-byte
+ *                aligned, in device memory or page-locked host memory
  *   num_q_heads  multiple of Hkv with num_q_heads / Hkv <= 4
  *   softmax_scale  0 means 1 / sqrt(128)
- *   out          device bf16 [n_seqs, num_q_heads, 128]
+ *   out          bf16 [n_seqs, num_q_heads, 128], 16-byte aligned, in device
+ *                memory or page-locked host memory
  *   workspace    device scratch of >= oscar_decode_workspace_bytes bytes,
  *                16-byte aligned; contents need not be initialised
  * For a quantised token t with norm n_t the score is
  *   s_t = n_t * (H_d q) . (code_t * s + z) * softmax_scale,
  * for a window token s_t = q . k_t * softmax_scale; out = softmax(s) . v_hat.
  * Attends to exactly the tokens in the cache (append the current token first).
+ * Host buffers: q and out may be page-locked host memory (cudaHostAlloc,
+ * cudaHostRegister, torch pin_memory); the kernels then read q and write out
+ * in place through the device mapping (over NVLink-C2C on Grace systems), so
+ * a decode step from host inputs to host outputs needs no staging copies.
+ * Pageable host memory and device memory of another device fail with
+ * OSCAR_ERR_INVALID_ARG before anything is enqueued.
  */
 oscar_status oscar_decode_attention(oscar_cache* cache, int32_t n_seqs, const int32_t* seq_ids,
                                     const void* q, int32_t num_q_heads, float softmax_scale,
@@ -194,9 +202,10 @@ oscar_status oscar_decode_attention(oscar_cache* cache, int32_t n_seqs, const in
  * summary, section "まとめと今後の展望", notes that the quantisation
  * overhead weighs relatively more at short context; this call removes one
  * launch from most decode steps.
- *   k_new, v_new  device bf16 [n_seqs, Hkv, 128], the new token of each
- *                 sequence (16-byte aligned)
- *   other arguments as for oscar_decode_attention.
+ *   k_new, v_new  bf16 [n_seqs, Hkv, 128], the new token of each sequence
+ *                 (16-byte aligned; device or page-locked host memory)
+ *   other arguments as for oscar_decode_attention (q and out may be host
+ *   buffers in the same way).
  * When no sequence's new length is a multiple of 128 (127 steps in 128),
  * the step is one decode launch: the combine kernel attends the new token as
  * the last window row straight from k_new / v_new and stores it into the

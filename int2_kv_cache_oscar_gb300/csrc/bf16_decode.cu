@@ -121,6 +121,11 @@ __global__ void __launch_bounds__(kThreadsB, 2)
     fence_mbar_init();
   }
   __syncthreads();
+  // Every CTA of this grid is resident from the start (persistent grid), so
+  // the dependent combine may be scheduled now: its CTAs take SMs as these
+  // exit and stage what does not depend on the partials; its
+  // griddepcontrol.wait still waits for this whole grid to complete.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == kConsumersB) {
     // ------------------------------------------------------------ producer
@@ -359,8 +364,6 @@ __global__ void __launch_bounds__(kThreadsB, 2)
     k = k_end;
     u = seg_end;
   }
-  // this CTA's partials are written: let the dependent combine launch
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // 2-D tensor map over rows of 128 bf16 channels: box = 64 channels x 64 rows,

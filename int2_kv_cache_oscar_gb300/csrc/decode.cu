@@ -165,6 +165,11 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     fence_mbar_init();
   }
   __syncthreads();
+  // Every CTA of this grid is resident from the start (persistent grid), so
+  // the dependent combine may be scheduled now: its CTAs take SMs as these
+  // exit and attend to the window meanwhile; its griddepcontrol.wait still
+  // waits for this whole grid to complete before reading the partials.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == kConsumers) {
     // ------------------------------------------------------------ producer
@@ -548,17 +553,18 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     k = k_end;
     u = seg_end;
     ++seg_idx;
-  }  // this CTA's partials are written: let the dependent combine launch
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  }
 }
 
 // ---------------------------------------------------------------- combine
 // One CTA per (sequence, KV head), 128 threads per query head (thread = one
 // (head, channel) output).  It is launched as a programmatic dependent of the
-// main kernel: the setup overlaps the main kernel's tail and griddepcontrol.wait
-// guards every read of its partials.  A bulk copy stages the bf16 window rows
-// (keys then values) and the row's split-K partial records (contiguous slots)
-// in shared memory; everything after that runs from shared memory:
+// main kernel, which allows that at its start: combine CTAs take SMs as main
+// CTAs exit and attend to the window (which the main kernel never reads) while
+// the rest of the main grid drains; griddepcontrol.wait then guards every read
+// of the partials.  Bulk copies stage the bf16 window rows (keys then values)
+// and then the row's split-K partial records (contiguous slots) in shared
+// memory; everything after that runs from shared memory:
 //   window: the 4 warps of head h score 32 window tokens each (lane = token,
 //           rotated 16-byte chunk order against bank conflicts); thread
 //           (h, c) then sums p_t v_t;
@@ -636,20 +642,14 @@ __global__ void __launch_bounds__(kCombineThreads)
     *reinterpret_cast<uint4*>(arow + 8 * chunk) = val;
   }
   __syncthreads();
-  grid_dependency_wait();            // the main kernel's partials are complete and visible
-  // stage 0: window rows + first chunk of partials
+  // phase 0 of the barrier: the stored window rows
   if (tid == 0) {
-    const int64_t n0 = count < per_chunk ? count : per_chunk;
     const uint32_t wbytes = (uint32_t)wstored * kHeadDim * 2;
-    const uint32_t pbytes = (uint32_t)(n0 * rec_bytes);
-    if (wbytes + pbytes > 0) {
-      mbar_arrive_expect_tx(&bar, 2 * wbytes + pbytes);
-      if (wstored > 0) {
-        const uint8_t* wsrc = arena + p.h.windows_off + ((int64_t)sq.slot * hkv + j) * kWindowBytes;
-        bulk_g2s(wk, wsrc, wbytes, &bar);
-        bulk_g2s(wv, wsrc + kGroup * kHeadDim * 2, wbytes, &bar);
-      }
-      if (pbytes > 0) bulk_g2s(part, p.h.partials + (first + rho) * (int64_t)gqa * kPartialFloats, pbytes, &bar);
+    if (wbytes > 0) {
+      mbar_arrive_expect_tx(&bar, 2 * wbytes);
+      const uint8_t* wsrc = arena + p.h.windows_off + ((int64_t)sq.slot * hkv + j) * kWindowBytes;
+      bulk_g2s(wk, wsrc, wbytes, &bar);
+      bulk_g2s(wv, wsrc + kGroup * kHeadDim * 2, wbytes, &bar);
     } else {
       mbar_arrive(&bar);
     }
@@ -708,19 +708,19 @@ __global__ void __launch_bounds__(kCombineThreads)
     Oh = o0 + o1;
   }
 
-  // ---- merge: window state + partial records, chunk by chunk (heads in parallel)
+  // ---- merge: window state + partial records, chunk by chunk (heads in parallel);
+  // chunk ck arrives on phase ck + 1 of the barrier
+  grid_dependency_wait();            // the main kernel's partials are complete and visible
   for (int64_t ck = 0; ck < nchunks; ++ck) {
     const int64_t c0 = ck * per_chunk;
     const int n = (int)((count - c0) < per_chunk ? (count - c0) : per_chunk);
-    if (ck > 0) {
-      __syncthreads();                               // everyone done with the previous chunk
-      if (tid == 0) {
-        mbar_arrive_expect_tx(&bar, (uint32_t)(n * rec_bytes));
-        bulk_g2s(part, p.h.partials + (first + rho + c0) * (int64_t)gqa * kPartialFloats, (uint32_t)(n * rec_bytes),
-                 &bar);
-      }
-      mbar_wait_bounded(&bar, (uint32_t)(ck & 1), &abort_flag, p.h.err_word);
+    if (ck > 0) __syncthreads();                     // everyone done with the previous chunk
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&bar, (uint32_t)(n * rec_bytes));
+      bulk_g2s(part, p.h.partials + (first + rho + c0) * (int64_t)gqa * kPartialFloats, (uint32_t)(n * rec_bytes),
+               &bar);
     }
+    mbar_wait_bounded(&bar, (uint32_t)((ck + 1) & 1), &abort_flag, p.h.err_word);
     float mx = -INFINITY;
     if (active)
       for (int i = c; i < n; i += 128) mx = fmaxf(mx, part[(i * gqa + h) * kPartialFloats + 128]);

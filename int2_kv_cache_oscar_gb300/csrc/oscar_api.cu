@@ -87,6 +87,45 @@ oscar_status check_config(const oscar_cache_config* c) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// The address the kernels use for a caller buffer, with the cache's device
+// current: device or managed memory of that device as it is; page-locked host
+// memory (cudaHostAlloc, cudaHostRegister) through its device mapping, which
+// the kernels then read or write in place (over NVLink-C2C on Grace systems)
+// instead of the caller staging copies.  Pageable host memory is refused.
+oscar_status device_view(const void* ptr, const char* name, int device, const void** out) {
+  cudaPointerAttributes a;
+  const cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(OSCAR_ERR_INVALID_ARG, "%s: not an address known to CUDA (%s)", name, cudaGetErrorString(e));
+  }
+  switch (a.type) {
+    case cudaMemoryTypeDevice:
+      if (a.device != device)
+        return fail(OSCAR_ERR_INVALID_ARG, "%s is on device %d, the cache on device %d", name, a.device, device);
+      *out = ptr;
+      return OSCAR_OK;
+    case cudaMemoryTypeManaged:
+      *out = ptr;
+      return OSCAR_OK;
+    case cudaMemoryTypeHost:
+      if (a.devicePointer == nullptr)
+        return fail(OSCAR_ERR_INVALID_ARG, "%s: page-locked host memory not mapped for the device", name);
+      *out = a.devicePointer;
+      return OSCAR_OK;
+    default:
+      return fail(OSCAR_ERR_INVALID_ARG, "%s is pageable host memory: pass device or page-locked host memory", name);
+  }
+}
+
+template <typename T>
+oscar_status device_view_as(T* ptr, const char* name, int device, T** out) {
+  const void* r = nullptr;
+  const oscar_status s = device_view(ptr, name, device, &r);
+  if (s == OSCAR_OK) *out = const_cast<T*>(static_cast<const T*>(r));
+  return s;
+}
+
 oscar_status check_slots(const oscar_cache* c, int32_t n, const int32_t* ids, std::vector<char>& seen) {
   seen.assign(c->cfg.max_batch, 0);
   for (int32_t i = 0; i < n; ++i) {
@@ -393,6 +432,8 @@ oscar_status oscar_decode_attention(oscar_cache* c, int32_t n_seqs, const int32_
     const float scale = softmax_scale == 0.0f ? 1.0f / std::sqrt((float)kHeadDim) : softmax_scale;
     DeviceGuard dg(c->cfg.device);
     if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+    if ((s = device_view_as(q, "q", c->cfg.device, &q)) != OSCAR_OK) return s;
+    if ((s = device_view_as(out, "out", c->cfg.device, &out)) != OSCAR_OK) return s;
     uint32_t* err_word = reinterpret_cast<uint32_t*>(c->arena);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (n_seqs <= kDecodeSeqsSmall)
@@ -448,6 +489,14 @@ oscar_status oscar_append_decode(oscar_cache* c, int32_t n_seqs, const int32_t* 
         return fail(OSCAR_ERR_CAPACITY, "sequence %d would reach %d tokens > max_seq_len %d", seq_ids[i], lens[i],
                     c->cfg.max_seq_len);
       if (lens[i] % kGroup == 0) closes = true;
+    }
+    {
+      DeviceGuard dg(c->cfg.device);
+      if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+      if ((s = device_view_as(k_new, "k_new", c->cfg.device, &k_new)) != OSCAR_OK) return s;
+      if ((s = device_view_as(v_new, "v_new", c->cfg.device, &v_new)) != OSCAR_OK) return s;
+      if ((s = device_view_as(q, "q", c->cfg.device, &q)) != OSCAR_OK) return s;
+      if ((s = device_view_as(out, "out", c->cfg.device, &out)) != OSCAR_OK) return s;
     }
     if (closes) {
       // a group closes: it is attended quantised, so the quantiser runs first
