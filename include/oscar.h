@@ -151,7 +151,8 @@ oscar_status oscar_cache_length(const oscar_cache* cache, int32_t seq, int32_t* 
  *   cu_new   host int32 [n_seqs + 1], cu_new[0] = 0, non-decreasing;
  *            sequence i appends rows cu_new[i] .. cu_new[i+1]-1
  *   k, v     device bf16 [cu_new[n_seqs], Hkv, 128] (rows of the raw, i.e.
- *            unrotated, keys and values; 16-byte aligned)
+ *            unrotated, keys and values; 16-byte aligned); host memory fails
+ *            with OSCAR_ERR_INVALID_ARG
  * Every 128-token group that fills is rotated, norm-scaled and quantised
  * (keys) and quantised (values) from its bf16 tokens (earlier ones from the
  * window, new ones from k/v) into its block; the remaining tokens go to the
@@ -202,8 +203,8 @@ oscar_status oscar_decode_attention(oscar_cache* cache, int32_t n_seqs, const in
  * summary, section "まとめと今後の展望", notes that the quantisation
  * overhead weighs relatively more at short context; this call removes one
  * launch from most decode steps.
- *   k_new, v_new  bf16 [n_seqs, Hkv, 128], the new token of each sequence
- *                 (16-byte aligned; device or page-locked host memory)
+ *   k_new, v_new  device bf16 [n_seqs, Hkv, 128], the new token of each
+ *                 sequence (16-byte aligned)
  *   other arguments as for oscar_decode_attention (q and out may be host
  *   buffers in the same way).
  * When no sequence's new length is a multiple of 128 (127 steps in 128),

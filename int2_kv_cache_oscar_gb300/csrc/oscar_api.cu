@@ -92,7 +92,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // memory (cudaHostAlloc, cudaHostRegister) through its device mapping, which
 // the kernels then read or write in place (over NVLink-C2C on Grace systems)
 // instead of the caller staging copies.  Pageable host memory is refused.
-oscar_status device_view(const void* ptr, const char* name, int device, const void** out) {
+oscar_status device_view(const void* ptr, const char* name, int device, const void** out, bool allow_host = true) {
   cudaPointerAttributes a;
   const cudaError_t e = cudaPointerGetAttributes(&a, ptr);
   if (e != cudaSuccess) {
@@ -106,9 +106,11 @@ oscar_status device_view(const void* ptr, const char* name, int device, const vo
       *out = ptr;
       return OSCAR_OK;
     case cudaMemoryTypeManaged:
+      if (!allow_host) return fail(OSCAR_ERR_INVALID_ARG, "%s must be device memory", name);
       *out = ptr;
       return OSCAR_OK;
     case cudaMemoryTypeHost:
+      if (!allow_host) return fail(OSCAR_ERR_INVALID_ARG, "%s must be device memory", name);
       if (a.devicePointer == nullptr)
         return fail(OSCAR_ERR_INVALID_ARG, "%s: page-locked host memory not mapped for the device", name);
       *out = a.devicePointer;
@@ -119,9 +121,9 @@ oscar_status device_view(const void* ptr, const char* name, int device, const vo
 }
 
 template <typename T>
-oscar_status device_view_as(T* ptr, const char* name, int device, T** out) {
+oscar_status device_view_as(T* ptr, const char* name, int device, T** out, bool allow_host = true) {
   const void* r = nullptr;
-  const oscar_status s = device_view(ptr, name, device, &r);
+  const oscar_status s = device_view(ptr, name, device, &r, allow_host);
   if (s == OSCAR_OK) *out = const_cast<T*>(static_cast<const T*>(r));
   return s;
 }
@@ -371,6 +373,9 @@ oscar_status oscar_quantize_append(oscar_cache* c, int32_t n_seqs, const int32_t
     }
     DeviceGuard dg(c->cfg.device);
     if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+    // appended rows: device memory only
+    if ((s = device_view_as(k, "k", c->cfg.device, &k, false)) != OSCAR_OK) return s;
+    if ((s = device_view_as(v, "v", c->cfg.device, &v, false)) != OSCAR_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const uint16_t* kp = static_cast<const uint16_t*>(k);
     const uint16_t* vp = static_cast<const uint16_t*>(v);
@@ -493,8 +498,8 @@ oscar_status oscar_append_decode(oscar_cache* c, int32_t n_seqs, const int32_t* 
     {
       DeviceGuard dg(c->cfg.device);
       if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
-      if ((s = device_view_as(k_new, "k_new", c->cfg.device, &k_new)) != OSCAR_OK) return s;
-      if ((s = device_view_as(v_new, "v_new", c->cfg.device, &v_new)) != OSCAR_OK) return s;
+      if ((s = device_view_as(k_new, "k_new", c->cfg.device, &k_new, false)) != OSCAR_OK) return s;
+      if ((s = device_view_as(v_new, "v_new", c->cfg.device, &v_new, false)) != OSCAR_OK) return s;
       if ((s = device_view_as(q, "q", c->cfg.device, &q)) != OSCAR_OK) return s;
       if ((s = device_view_as(out, "out", c->cfg.device, &out)) != OSCAR_OK) return s;
     }

@@ -1,7 +1,8 @@
-"""Decode calls with page-locked host buffers: the kernels read q (and the new
-token of the fused call) and write out in place through the device mapping.
-The results must equal those of the same calls with device buffers bit for
-bit; pageable host memory must be refused before anything is enqueued."""
+"""Decode calls with page-locked host buffers: the kernels read q and write
+out in place through the device mapping.  The results must equal those of the
+same calls with device buffers bit for bit; pageable host memory, and host
+memory where only device memory is accepted (appended rows), must be refused
+before anything is enqueued."""
 import pytest
 import torch
 
@@ -60,8 +61,8 @@ def test_append_decode_host_buffers_match_device():
         o_dev = torch.empty((B, hq, 128), dtype=torch.bfloat16, device="cuda")
         a.append_decode(ids, kn.cuda(), vn.cuda(), q.cuda(), hq, o_dev, ws_a)
         o_host = torch.empty((B, hq, 128), dtype=torch.bfloat16).pin_memory()
-        kh, vh, qh = kn.pin_memory(), vn.pin_memory(), q.pin_memory()   # alive until the kernels ran
-        b.append_decode(ids, kh, vh, qh, hq, o_host, ws_b)
+        qh = q.pin_memory()                  # alive until the kernels ran
+        b.append_decode(ids, kn.cuda(), vn.cuda(), qh, hq, o_host, ws_b)
         torch.cuda.synchronize()
         assert torch.equal(o_host, o_dev.cpu()), f"step {step}"
     ra, rb = U.read_arena(a), U.read_arena(b)
@@ -84,9 +85,12 @@ def test_pageable_host_buffers_are_refused():
             c.decode([0], q, hq, o, ws)
         assert e.value.status == O_.OSCAR_ERR_INVALID_ARG
         assert "pageable" in str(e.value)
-    kn = torch.zeros((1, 2, 128), dtype=torch.bfloat16)
-    with pytest.raises(O_.OscarError) as e:
+    kn = torch.zeros((1, 2, 128), dtype=torch.bfloat16).pin_memory()
+    with pytest.raises(O_.OscarError) as e:      # the new token: device memory only
         c.append_decode([0], kn, kn.cuda(), q_dev, hq, o_dev, ws)
+    assert e.value.status == O_.OSCAR_ERR_INVALID_ARG
+    with pytest.raises(O_.OscarError) as e:      # appends: device memory only
+        c.append([0], [0, 1], kn, kn.cuda())
     assert e.value.status == O_.OSCAR_ERR_INVALID_ARG
     assert c.length(0) == 300                    # nothing appended
     torch.cuda.synchronize()
