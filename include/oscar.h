@@ -107,20 +107,26 @@ enum {
  *   +4096   K scale s_c, float32 [128] (per channel)
  *   +4608   K zero  z_c, float32 [128]
  *   +5120   K norm  n_t, float32 [128] (per token, position order)
- *   +5632   V codes, 4,096 B, fragment order of X[row = channel][col = token]
- *   +9728   V scale/zero: per token t (32 B): s[t][0..3] then z[t][0..3]
- *           (float32), one pair per 32-channel group
+ *   +5632   V codes, 4,096 B, fragment words of X[row = channel][col = token]
+ *           in "V order"
+ *   +9728   V scale s[t][0..3], float32 [128][4] (per token, one per
+ *           32-channel group)
+ *   +11776  V zero  z[t][0..3], float32 [128][4]
  * meta_bits 16: the same sections with float16 metadata:
  *   +0 K codes, +4096 K scale, +4352 K zero, +4608 K norm (float16 [128]
- *   each), +4864 V codes, +8960 V scale/zero (per token 16 B: s[t][0..3]
- *   then z[t][0..3], float16); 11,008 bytes, 86 per token and head.
+ *   each), +4864 V codes, +8960 V scale, +9984 V zero (float16 [128][4]
+ *   each); 11,008 bytes, 86 per token and head.
  *
- * Fragment order of a 128x128 matrix of 2-bit codes X[row][col]: 32-bit word
- * number  w = ((mt*32 + lane)*4 + 2*j + r)  holds the 16 codes with
+ * Fragment words of a 128x128 matrix of 2-bit codes X[row][col]: the 32-bit
+ * word F(mt, lane, j, r) holds the 16 codes with
  *   row = 16*mt + (lane >> 2) + 8*r,
  *   col = 16*(4*j + kk) + 8*hf + 2*(lane & 3) + e,   kk in 0..3, hf, e in {0,1},
- * code at bits [b, b+1] with b = 16*e + 4*kk + 2*hf.
- * (mt in 0..7, lane in 0..31, r, j in {0,1}; words are little-endian.)
+ * code at bits [b, b+1] with b = 16*e + 4*kk + 2*hf
+ * (mt in 0..7, lane in 0..31, r, j in {0,1}; words are little-endian).
+ * "Fragment order" (K codes) stores F(mt, lane, j, r) as word
+ *   w = (mt*32 + lane)*4 + 2*j + r,
+ * "V order" (V codes) as word
+ *   w = ((mt*2 + j)*32 + lane)*2 + r.
  */
 
 /* Arena bytes needed by `cfg`.  Pure host arithmetic. */

@@ -17,7 +17,8 @@ constexpr int kOffKScale = 4096;
 constexpr int kOffKZero = 4608;
 constexpr int kOffKNorm = 5120;
 constexpr int kOffVCodes = 5632;
-constexpr int kOffVSZ = 9728;
+constexpr int kOffVScale = 9728;
+constexpr int kOffVZero = 11776;
 constexpr int kBlockBytes = 13824;
 
 // The same block with float16 metadata (scales, zeros, norms).
@@ -25,8 +26,15 @@ constexpr int kOff16KScale = 4096;
 constexpr int kOff16KZero = 4352;
 constexpr int kOff16KNorm = 4608;
 constexpr int kOff16VCodes = 4864;
-constexpr int kOff16VSZ = 8960;
+constexpr int kOff16VScale = 8960;
+constexpr int kOff16VZero = 9984;
 constexpr int kBlockBytes16 = 11008;
+
+// Byte offset, within the value-code section, of fragment word pair (r = 0, 1)
+// of m-tile mt, token half j and lane ("V order": a warp's pairs for one
+// (mt, j) are 256 contiguous bytes).  Key codes keep the "K order"
+// ((mt * 32 + lane) * 4 + 2 j + r) * 4 (a lane's four words are contiguous).
+__host__ __device__ constexpr int vword_off(int mt, int j, int lane) { return ((mt * 2 + j) * 32 + lane) * 8; }
 
 // Block layout by metadata width: section offsets, block size, bytes per
 // metadata element.
@@ -36,7 +44,8 @@ struct Blk {
   static constexpr int kKZero = M16 ? kOff16KZero : kOffKZero;
   static constexpr int kKNorm = M16 ? kOff16KNorm : kOffKNorm;
   static constexpr int kVCodes = M16 ? kOff16VCodes : kOffVCodes;
-  static constexpr int kVSZ = M16 ? kOff16VSZ : kOffVSZ;
+  static constexpr int kVScale = M16 ? kOff16VScale : kOffVScale;
+  static constexpr int kVZero = M16 ? kOff16VZero : kOffVZero;
   static constexpr int kBytes = M16 ? kBlockBytes16 : kBlockBytes;
   static constexpr int kMeta = M16 ? 2 : 4;
 };
@@ -252,13 +261,24 @@ struct Meta {
       return reinterpret_cast<const float*>(a)[i];
     }
   }
-  // value scales (which = 0) or zeros (which = 1) of token t, groups 0..3
-  __device__ static float4 vsz4(const uint8_t* vsz, int t, int which) {
+  // the four value scales (or zeros) of token t, one per 32-channel group
+  __device__ static float4 v4(const uint8_t* a, int t) {
     if constexpr (M16) {
-      const uint2 h = *reinterpret_cast<const uint2*>(vsz + 16 * t + 8 * which);
+      const uint2 h = *reinterpret_cast<const uint2*>(a + 8 * t);
       return make_float4(half_lo_to_float(h.x), half_hi_to_float(h.x), half_lo_to_float(h.y), half_hi_to_float(h.y));
     } else {
-      return *reinterpret_cast<const float4*>(vsz + 32 * t + 16 * which);
+      return *reinterpret_cast<const float4*>(a + 16 * t);
+    }
+  }
+  // those of tokens t and t + 1, t even (one 16-byte load with float16 metadata)
+  __device__ static void v4x2(const uint8_t* a, int t, float4& s0, float4& s1) {
+    if constexpr (M16) {
+      const uint4 h = *reinterpret_cast<const uint4*>(a + 8 * t);
+      s0 = make_float4(half_lo_to_float(h.x), half_hi_to_float(h.x), half_lo_to_float(h.y), half_hi_to_float(h.y));
+      s1 = make_float4(half_lo_to_float(h.z), half_hi_to_float(h.z), half_lo_to_float(h.w), half_hi_to_float(h.w));
+    } else {
+      s0 = *reinterpret_cast<const float4*>(a + 16 * t);
+      s1 = *reinterpret_cast<const float4*>(a + 16 * t + 16);
     }
   }
 };

@@ -352,7 +352,8 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       const uint8_t* ksc = blk + B::kKScale;
       const uint8_t* kze = blk + B::kKZero;
       const uint8_t* knm = blk + B::kKNorm;
-      const uint8_t* vsz = blk + B::kVSZ;
+      const uint8_t* vsc = blk + B::kVScale;
+      const uint8_t* vze = blk + B::kVZero;
 
       // ---- B fragments of the score contraction, and q_rot . z
       uint32_t bk[8][2];
@@ -445,8 +446,8 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
         const int t0 = 16 * mt + g;
         pb[t0] = sc[mt].x;
         pb[t0 + 8] = sc[mt].y;
-        const float4 z0 = MR::vsz4(vsz, t0, 1);
-        const float4 z1 = MR::vsz4(vsz, t0 + 8, 1);
+        const float4 z0 = MR::v4(vze, t0);
+        const float4 z1 = MR::v4(vze, t0 + 8);
         zacc[0] = fmaf(sc[mt].x, z0.x, fmaf(sc[mt].y, z1.x, zacc[0]));
         zacc[1] = fmaf(sc[mt].x, z0.y, fmaf(sc[mt].y, z1.y, zacc[1]));
         zacc[2] = fmaf(sc[mt].x, z0.z, fmaf(sc[mt].y, z1.z, zacc[2]));
@@ -466,13 +467,13 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
           uint2 vw[8];
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt)
-            vw[mt] = *reinterpret_cast<const uint2*>(blk + B::kVCodes + ((mt * 32 + lane) * 4 + 2 * jh) * 4);
+            vw[mt] = *reinterpret_cast<const uint2*>(blk + B::kVCodes + vword_off(mt, jh, lane));
 #pragma unroll
           for (int kk2 = 0; kk2 < 4; ++kk2) {
             const int t = 16 * (4 * jh + kk2) + 2 * tig + 8 * half;   // this lane's two tokens
             const float2 pr = __fmul2_rn(*reinterpret_cast<const float2*>(pbh + t), make_float2(fsc[kk2], fsc[kk2]));
-            const float4 s0 = MR::vsz4(vsz, t, 0);
-            const float4 s1 = MR::vsz4(vsz, t + 1, 0);
+            float4 s0, s1;
+            MR::v4x2(vsc, t, s0, s1);
 #pragma unroll
             for (int gr = 0; gr < kVGroups; ++gr) {
               const float sa = gr == 0 ? s0.x : gr == 1 ? s0.y : gr == 2 ? s0.z : s0.w;

@@ -279,9 +279,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint8_t* ksc = blk + B::kKScale;
     const uint8_t* kze = blk + B::kKZero;
     const uint8_t* knm = blk + B::kKNorm;
-    const uint8_t* vsz = blk + B::kVSZ;
+    const uint8_t* vsc = blk + B::kVScale;
+    const uint8_t* vze = blk + B::kVZero;
     const uint4* kc = reinterpret_cast<const uint4*>(blk + kOffKCodes);
-    const uint4* vc = reinterpret_cast<const uint4*>(blk + B::kVCodes);
 
     float qz0 = 0.0f, qz1 = 0.0f;   // q_rot . z of the lane's rows (times 2^F), from the first half
     float qzt0 = 0.0f, qzt1 = 0.0f;
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int t = 64 * hh + 8 * ntl + 2 * tig + e;
-          const float4 z4 = MR::vsz4(vsz, t, 1);
+          const float4 z4 = MR::v4(vze, t);
           zacc[0][0] = fmaf(sc[ntl][e], z4.x, zacc[0][0]);
           zacc[0][1] = fmaf(sc[ntl][e], z4.y, zacc[0][1]);
           zacc[0][2] = fmaf(sc[ntl][e], z4.z, zacc[0][2]);
@@ -387,17 +387,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       uint32_t vw[16];   // word (j = hh, r) of channel m-tile mt: channel tile nt = 2 mt + r
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        const uint4 w4 = vc[mt * 32 + lane];
-        vw[2 * mt] = hh ? w4.z : w4.x;
-        vw[2 * mt + 1] = hh ? w4.w : w4.y;
+        const uint2 w2 = *reinterpret_cast<const uint2*>(blk + B::kVCodes + vword_off(mt, hh, lane));
+        vw[2 * mt] = w2.x;
+        vw[2 * mt + 1] = w2.y;
       }
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const int t0 = 64 * hh + 16 * kk + 2 * tig, t1 = t0 + 8;
-        const float4 sa = MR::vsz4(vsz, t0, 0);
-        const float4 sb = MR::vsz4(vsz, t0 + 1, 0);
-        const float4 sc4 = MR::vsz4(vsz, t1, 0);
-        const float4 sd = MR::vsz4(vsz, t1 + 1, 0);
+        float4 sa, sb, sc4, sd;
+        MR::v4x2(vsc, t0, sa, sb);
+        MR::v4x2(vsc, t1, sc4, sd);
         const float* p00 = sc[2 * kk];       // tokens t0, t0+1: rows g (0, 1), g + 8 (2, 3)
         const float* p01 = sc[2 * kk + 1];   // tokens t1, t1+1
         const float f0 = fsc[kk][0], f1 = fsc[kk][1];

@@ -215,12 +215,12 @@ __global__ void __launch_bounds__(kQThreads, 2)
           }
         }
       }
-      if constexpr (M16) {   // per token 16 B: s[0..3] then z[0..3], float16 (exact: already rounded)
-        *reinterpret_cast<uint32_t*>(blk + B::kVSZ + 16 * t + 4 * half) = pack_half2(sv[0], sv[1]);
-        *reinterpret_cast<uint32_t*>(blk + B::kVSZ + 16 * t + 8 + 4 * half) = pack_half2(zv[0], zv[1]);
+      if constexpr (M16) {   // s[t][0..3] and z[t][0..3], float16 (exact: already rounded)
+        *reinterpret_cast<uint32_t*>(blk + B::kVScale + 8 * t + 4 * half) = pack_half2(sv[0], sv[1]);
+        *reinterpret_cast<uint32_t*>(blk + B::kVZero + 8 * t + 4 * half) = pack_half2(zv[0], zv[1]);
       } else {
-        *reinterpret_cast<float2*>(blk + kOffVSZ + 32 * t + 8 * half) = make_float2(sv[0], sv[1]);
-        *reinterpret_cast<float2*>(blk + kOffVSZ + 32 * t + 16 + 8 * half) = make_float2(zv[0], zv[1]);
+        *reinterpret_cast<float2*>(blk + kOffVScale + 16 * t + 8 * half) = make_float2(sv[0], sv[1]);
+        *reinterpret_cast<float2*>(blk + kOffVZero + 16 * t + 8 * half) = make_float2(zv[0], zv[1]);
       }
     }
 
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
     }
     __syncthreads();
 
-    // ---- coalesced stores of both code matrices (256 x 16 B each)
+    // ---- coalesced stores of both code matrices (K: 256 x 16 B; V: 2 x 256 x 8 B, V order)
     {
       const int u = tid;
       reinterpret_cast<uint4*>(blk + kOffKCodes)[u] = reinterpret_cast<const uint4*>(S.kw)[u];
@@ -385,7 +385,8 @@ __global__ void __launch_bounds__(kQThreads, 2)
           wv[2 * j + r] = w;
         }
       }
-      reinterpret_cast<uint4*>(blk + B::kVCodes)[u] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      *reinterpret_cast<uint2*>(blk + B::kVCodes + vword_off(mt, 0, lane)) = make_uint2(wv[0], wv[1]);
+      *reinterpret_cast<uint2*>(blk + B::kVCodes + vword_off(mt, 1, lane)) = make_uint2(wv[2], wv[3]);
     }
     if (tid == 0) {
       float m = S.red[0];

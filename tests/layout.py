@@ -3,10 +3,12 @@ include/oscar.h (not from the CUDA sources): unpacks a 13,824-byte group
 block into canonical arrays, and packs canonical codes into fragment order
 (used only to check that the two are inverse).
 
-Fragment order of a 128x128 matrix of 2-bit codes X[row][col]: 32-bit word
-w = ((mt*32 + lane)*4 + 2*j + r) holds the 16 codes with
-row = 16*mt + (lane >> 2) + 8*r and col = 16*(4*j + kk) + 8*hf + 2*(lane & 3) + e,
-the code sitting at bits [b, b+1], b = 16*e + 4*kk + 2*hf.
+Fragment words of a 128x128 matrix of 2-bit codes X[row][col]: word
+F(mt, lane, j, r) holds the 16 codes with row = 16*mt + (lane >> 2) + 8*r and
+col = 16*(4*j + kk) + 8*hf + 2*(lane & 3) + e, the code sitting at bits
+[b, b+1], b = 16*e + 4*kk + 2*hf.  K codes store F(mt, lane, j, r) as word
+(mt*32 + lane)*4 + 2*j + r ("k" order), V codes as ((mt*2 + j)*32 + lane)*2 + r
+("v" order).
 """
 from __future__ import annotations
 
@@ -15,17 +17,27 @@ import numpy as np
 D = 128
 G = 128
 BLOCK_BYTES = 13824
-OFF_KCODES, OFF_KSCALE, OFF_KZERO, OFF_KNORM, OFF_VCODES, OFF_VSZ = 0, 4096, 4608, 5120, 5632, 9728
+OFF_KCODES, OFF_KSCALE, OFF_KZERO, OFF_KNORM, OFF_VCODES = 0, 4096, 4608, 5120, 5632
+OFF_VSCALE, OFF_VZERO = 9728, 11776
 # the same block with float16 metadata (meta_bits = 16)
 BLOCK_BYTES16 = 11008
-OFF16_KSCALE, OFF16_KZERO, OFF16_KNORM, OFF16_VCODES, OFF16_VSZ = 4096, 4352, 4608, 4864, 8960
+OFF16_KSCALE, OFF16_KZERO, OFF16_KNORM, OFF16_VCODES = 4096, 4352, 4608, 4864
+OFF16_VSCALE, OFF16_VZERO = 8960, 9984
 
 
 def block_bytes(meta_bits: int = 32) -> int:
     return BLOCK_BYTES16 if meta_bits == 16 else BLOCK_BYTES
 
 
-def _index_tables():
+def _word(order: str, mt: int, lane: int, j: int, r: int) -> int:
+    if order == "k":
+        return (mt * 32 + lane) * 4 + 2 * j + r
+    if order == "v":
+        return ((mt * 2 + j) * 32 + lane) * 2 + r
+    raise ValueError(order)
+
+
+def _index_tables(order: str):
     rows = np.zeros((1024, 16), np.int64)
     cols = np.zeros((1024, 16), np.int64)
     bits = np.zeros((1024, 16), np.int64)
@@ -33,7 +45,7 @@ def _index_tables():
         for lane in range(32):
             for j in range(2):
                 for r in range(2):
-                    w = (mt * 32 + lane) * 4 + 2 * j + r
+                    w = _word(order, mt, lane, j, r)
                     n = 0
                     for kk in range(4):
                         for hf in range(2):
@@ -45,21 +57,23 @@ def _index_tables():
     return rows, cols, bits
 
 
-_ROWS, _COLS, _BITS = _index_tables()
+_TABLES = {o: _index_tables(o) for o in ("k", "v")}
 
 
-def unpack_fragment(words: np.ndarray) -> np.ndarray:
+def unpack_fragment(words: np.ndarray, order: str = "k") -> np.ndarray:
     """uint32 [1024] (little-endian words) -> uint8 codes [128, 128] X[row][col]."""
+    rows, cols, bits = _TABLES[order]
     words = np.asarray(words, dtype=np.uint32).reshape(1024)
-    vals = (words[:, None].astype(np.int64) >> _BITS) & 3
+    vals = (words[:, None].astype(np.int64) >> bits) & 3
     out = np.zeros((G, D), np.uint8)
-    out[_ROWS, _COLS] = vals
+    out[rows, cols] = vals
     return out
 
 
-def pack_fragment(codes: np.ndarray) -> np.ndarray:
+def pack_fragment(codes: np.ndarray, order: str = "k") -> np.ndarray:
+    rows, cols, bits = _TABLES[order]
     codes = np.asarray(codes, np.int64)
-    vals = codes[_ROWS, _COLS] << _BITS
+    vals = codes[rows, cols] << bits
     return np.bitwise_or.reduce(vals, axis=1).astype(np.uint32)
 
 
@@ -70,20 +84,20 @@ def parse_block(raw: np.ndarray, meta_bits: int = 32) -> dict:
         raw = np.ascontiguousarray(np.asarray(raw, np.uint8).reshape(BLOCK_BYTES16))
         kcodes = unpack_fragment(raw[OFF_KCODES:OFF_KCODES + 4096].view("<u4"))
         f16 = lambda a, n: raw[a:a + 2 * n].view("<f2").astype(np.float32)
-        vcodes_t = unpack_fragment(raw[OFF16_VCODES:OFF16_VCODES + 4096].view("<u4"))
-        vsz = raw[OFF16_VSZ:OFF16_VSZ + 2048].view("<f2").astype(np.float32).reshape(G, 8)
+        vcodes_t = unpack_fragment(raw[OFF16_VCODES:OFF16_VCODES + 4096].view("<u4"), "v")
         return dict(kcodes=kcodes, kscale=f16(OFF16_KSCALE, 128), kzero=f16(OFF16_KZERO, 128),
-                    knorm=f16(OFF16_KNORM, 128), vcodes=vcodes_t.T.copy(), vscale=vsz[:, :4].copy(),
-                    vzero=vsz[:, 4:].copy())
+                    knorm=f16(OFF16_KNORM, 128), vcodes=vcodes_t.T.copy(),
+                    vscale=f16(OFF16_VSCALE, 512).reshape(G, 4), vzero=f16(OFF16_VZERO, 512).reshape(G, 4))
     raw = np.ascontiguousarray(np.asarray(raw, np.uint8).reshape(BLOCK_BYTES))
     kcodes = unpack_fragment(raw[OFF_KCODES:OFF_KCODES + 4096].view("<u4"))        # [token, ch]
     kscale = raw[OFF_KSCALE:OFF_KSCALE + 512].view("<f4").copy()
     kzero = raw[OFF_KZERO:OFF_KZERO + 512].view("<f4").copy()
     knorm = raw[OFF_KNORM:OFF_KNORM + 512].view("<f4").copy()
-    vcodes_t = unpack_fragment(raw[OFF_VCODES:OFF_VCODES + 4096].view("<u4"))      # [ch, token]
-    vsz = raw[OFF_VSZ:OFF_VSZ + 4096].view("<f4").reshape(G, 8)
+    vcodes_t = unpack_fragment(raw[OFF_VCODES:OFF_VCODES + 4096].view("<u4"), "v")  # [ch, token]
+    vscale = raw[OFF_VSCALE:OFF_VSCALE + 2048].view("<f4").reshape(G, 4).copy()
+    vzero = raw[OFF_VZERO:OFF_VZERO + 2048].view("<f4").reshape(G, 4).copy()
     return dict(kcodes=kcodes, kscale=kscale, kzero=kzero, knorm=knorm,
-                vcodes=vcodes_t.T.copy(), vscale=vsz[:, :4].copy(), vzero=vsz[:, 4:].copy())
+                vcodes=vcodes_t.T.copy(), vscale=vscale, vzero=vzero)
 
 
 def bf16_bits_to_f64(u16: np.ndarray) -> np.ndarray:

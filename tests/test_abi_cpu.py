@@ -98,12 +98,19 @@ def test_layout_reader_roundtrip():
     from tests import layout
     rng = np.random.default_rng(5)
     codes = rng.integers(0, 4, (128, 128)).astype(np.uint8)
-    words = layout.pack_fragment(codes)
-    assert np.array_equal(layout.unpack_fragment(words), codes)
-    # every (row, col) appears exactly once; 16 codes per word
-    seen = np.zeros((128, 128), int)
-    np.add.at(seen, (layout._ROWS, layout._COLS), 1)
-    assert np.all(seen == 1)
+    for order in ("k", "v"):
+        words = layout.pack_fragment(codes, order)
+        assert np.array_equal(layout.unpack_fragment(words, order), codes)
+        # every (row, col) appears exactly once; 16 codes per word
+        rows, cols, _ = layout._TABLES[order]
+        seen = np.zeros((128, 128), int)
+        np.add.at(seen, (rows, cols), 1)
+        assert np.all(seen == 1)
+    # the two orders hold the same words, permuted: word pair (r = 0, 1) of
+    # (mt, j, lane) is 8 contiguous bytes at ((mt*2 + j)*32 + lane)*8 in V order
+    wk = layout.pack_fragment(codes, "k").reshape(8, 32, 2, 2)        # [mt][lane][j][r]
+    wv = layout.pack_fragment(codes, "v").reshape(8, 2, 32, 2)        # [mt][j][lane][r]
+    assert np.array_equal(wk.transpose(0, 2, 1, 3), wv)
 
 
 def test_layout_reader_fp16_block():
@@ -122,10 +129,36 @@ def test_layout_reader_fp16_block():
     raw[4096:4352] = ks.view(np.uint8)
     raw[4352:4608] = kz.view(np.uint8)
     raw[4608:4864] = kn.view(np.uint8)
-    raw[4864:8960] = layout.pack_fragment(vc.T).view(np.uint8)
-    raw[8960:11008] = np.concatenate([vs, vz], axis=1).reshape(-1).view(np.uint8)
+    raw[4864:8960] = layout.pack_fragment(vc.T, "v").view(np.uint8)
+    raw[8960:9984] = vs.reshape(-1).view(np.uint8)
+    raw[9984:11008] = vz.reshape(-1).view(np.uint8)
     b = layout.parse_block(raw, 16)
     assert np.array_equal(b["kcodes"], kc) and np.array_equal(b["vcodes"], vc)
     assert np.array_equal(b["kscale"], ks.astype(np.float32)) and np.array_equal(b["knorm"], kn.astype(np.float32))
     assert np.array_equal(b["kzero"], kz.astype(np.float32))
     assert np.array_equal(b["vscale"], vs.astype(np.float32)) and np.array_equal(b["vzero"], vz.astype(np.float32))
+
+
+def test_layout_reader_fp32_block():
+    """The float32-metadata block reader against a block assembled by hand
+    from the header's offsets."""
+    import numpy as np
+    from tests import layout
+    rng = np.random.default_rng(7)
+    kc = rng.integers(0, 4, (128, 128)).astype(np.uint8)
+    vc = rng.integers(0, 4, (128, 128)).astype(np.uint8)
+    ks, kz, kn = (rng.standard_normal(128).astype(np.float32) for _ in range(3))
+    vs = rng.standard_normal((128, 4)).astype(np.float32)
+    vz = rng.standard_normal((128, 4)).astype(np.float32)
+    raw = np.zeros(13824, np.uint8)
+    raw[0:4096] = layout.pack_fragment(kc).view(np.uint8)
+    raw[4096:4608] = ks.view(np.uint8)
+    raw[4608:5120] = kz.view(np.uint8)
+    raw[5120:5632] = kn.view(np.uint8)
+    raw[5632:9728] = layout.pack_fragment(vc.T, "v").view(np.uint8)
+    raw[9728:11776] = vs.reshape(-1).view(np.uint8)
+    raw[11776:13824] = vz.reshape(-1).view(np.uint8)
+    b = layout.parse_block(raw)
+    assert np.array_equal(b["kcodes"], kc) and np.array_equal(b["vcodes"], vc)
+    for name, ref in [("kscale", ks), ("kzero", kz), ("knorm", kn), ("vscale", vs), ("vzero", vz)]:
+        assert np.array_equal(b[name], ref), name
