@@ -606,6 +606,34 @@ def run_cpu_sample(steps: int):
     return json.loads(m.group(1))
 
 
+def run_cpu_sample_all_cores(steps: int):
+    """The same sample in up to 8 concurrent single-threaded processes, one per
+    KV head (the oracle as it stands, on more cores): wall time of a full
+    8-head step = the slowest head's step time x the rounds needed."""
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count() or 1
+    n = max(1, min(HKV, cores))
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = ("import json, bench; print('CPUJSON' + json.dumps(bench.cpu_sample_worker(%d)))" % steps)
+    procs = [subprocess.Popen([sys.executable, "-c", code], cwd=ROOT, env=env, stdout=subprocess.PIPE,
+                              stderr=subprocess.PIPE, text=True) for _ in range(n)]
+    per_head = []
+    for pr in procs:
+        out, err = pr.communicate(timeout=1200)
+        m = re.search(r"CPUJSON(\{.*\})", out)
+        if not m:
+            raise RuntimeError("CPU oracle sample failed:\n" + out[-2000:] + err[-2000:])
+        per_head.append(json.loads(m.group(1))["decode_s_per_head"])
+    rounds = -(-HKV // n)
+    us = max(per_head) * rounds * 1e6
+    return {"value": round(us, 1), "unit": "us/step", "cores": n, "kind": "oracle",
+            "sample": f"oracle decode (float64 numpy) of the 128K-token cache, one KV head (4 query heads) per "
+                      f"single-threaded process, {n} processes at once, {rounds} round(s) for the 8 heads"}
+
+
 def cpu_baseline_obj(js, kind="oracle"):
     us = js["decode_s_per_head"] * HKV * 1e6
     return {"value": round(us, 1), "unit": "us/step", "cores": 1, "kind": kind,
@@ -682,12 +710,16 @@ def main():
             dist.destroy_process_group()
         return
 
-    cpu = None
+    cpu = cpu_all = None
     if not args.no_cpu:
         try:
             cpu = cpu_baseline_obj(run_cpu_sample(3))
         except Exception as e:  # reported, not fatal
             cpu = {"value": None, "unit": "us/step", "cores": 1, "kind": "oracle", "sample": f"failed: {e}"}
+        try:
+            cpu_all = run_cpu_sample_all_cores(3)
+        except Exception as e:  # reported, not fatal
+            cpu_all = {"value": None, "unit": "us/step", "kind": "oracle", "sample": f"failed: {e}"}
 
     traffic = profiled_traffic()
     line = {
@@ -719,6 +751,7 @@ def main():
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
         "cpu_baseline": cpu,
+        "cpu_baseline_all_cores": cpu_all,
     }
     line.update(res["extra"])
     print(json.dumps(line))
