@@ -276,7 +276,7 @@ def gpu_arm(args, rank, world):
         quant_read = CTX * HKV * 512
         quant_write = CTX * HKV * 108
         quant_gbs = (quant_read + quant_write) / (q_us * 1e-6) / 1e9
-        launches += K * (-(-(CTX // 128) // 900))   # quantise kernels per 128K append
+        launches += K * (-(-(CTX // 128) // 2000))  # quantise kernels per 128K append (2000 groups per launch)
         outb = torch.empty((1, HQ, D), dtype=torch.bfloat16, device="cuda")
         ws = cache.workspace(1, HQ)
 
@@ -360,7 +360,7 @@ def gpu_arm(args, rank, world):
             c16.append([0], [0, CTX], k, v)
 
         q16_us, _ = timer.run(quantize16, K, Wm)
-        launches += K * (-(-(CTX // 128) // 900))
+        launches += K * (-(-(CTX // 128) // 2000))
         ws16 = c16.workspace(1, HQ)
         d16_us, k16_us = timer.run(lambda: c16.decode([0], q, HQ, outb, ws16), K, Wm,
                                    kernel_events=lambda a, b: O_.oscar_set_timing_events(a, b))

@@ -22,8 +22,41 @@ struct QuantTask {
   int32_t kind;  // 0 = quantise a group (+ optional tail), 1 = window append only
 };
 
+// A QuantTask as the kernel reads it, 16 bytes, so that a whole 128K-token
+// append (1,024 tasks) fits in one launch's parameters:
+//   a = slot | n_win << 24 | kind << 31   (kind 1: the n_win bits hold
+//                                          tail_pos mod 128)
+//   b = group | tail_count << 24
+//   c = in_row, d = tail_in_row
+// A kind-0 task's tail always starts on a group boundary (tail_pos mod 128
+// = 0).  slot and group are below 2^24 (max_batch * Hkv <= 2^24; groups of
+// an int32 length), n_win and tail_count below 128.
+struct PackedTask {
+  uint32_t a, b;
+  int32_t c, d;
+  __host__ __device__ int slot() const { return (int)(a & 0xFFFFFFu); }
+  __host__ __device__ int kind() const { return (int)(a >> 31); }
+  __host__ __device__ int n_win() const { return kind() ? 0 : (int)((a >> 24) & 0x7Fu); }
+  __host__ __device__ int tail_pos_mod() const { return kind() ? (int)((a >> 24) & 0x7Fu) : 0; }
+  __host__ __device__ int group() const { return (int)(b & 0xFFFFFFu); }
+  __host__ __device__ int tail_count() const { return (int)((b >> 24) & 0x7Fu); }
+  __host__ __device__ int in_row() const { return c; }
+  __host__ __device__ int tail_in_row() const { return d; }
+};
+static_assert(sizeof(PackedTask) == 16, "16-byte tasks");
+
+inline PackedTask pack_task(const QuantTask& t) {
+  PackedTask p;
+  const uint32_t low7 = (uint32_t)(t.kind ? (t.tail_pos & 127) : t.n_win) & 0x7Fu;
+  p.a = ((uint32_t)t.slot & 0xFFFFFFu) | (low7 << 24) | ((uint32_t)(t.kind & 1) << 31);
+  p.b = ((uint32_t)(t.kind ? 0 : t.group) & 0xFFFFFFu) | (((uint32_t)t.tail_count & 0x7Fu) << 24);
+  p.c = t.in_row;
+  p.d = t.tail_in_row;
+  return p;
+}
+
 constexpr int kQuantPlanSmall = 64;
-constexpr int kQuantPlanLarge = 900;
+constexpr int kQuantPlanLarge = 2000;   // 32 + 2000 * 16 bytes of plan: within the 32,764-byte parameter limit
 
 template <int CAP>
 struct QuantPlan {
@@ -33,8 +66,9 @@ struct QuantPlan {
   int32_t pad;
   int64_t blocks_off;
   int64_t windows_off;
-  QuantTask t[CAP];
+  PackedTask t[CAP];
 };
+static_assert(sizeof(QuantPlan<kQuantPlanLarge>) + 3 * sizeof(void*) <= 32764, "kernel parameter limit");
 
 // meta16: the float16-metadata block layout (see include/oscar.h)
 cudaError_t launch_quantize_small(const QuantPlan<kQuantPlanSmall>& plan, uint8_t* arena, const uint16_t* k,

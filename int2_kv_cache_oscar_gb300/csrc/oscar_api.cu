@@ -149,7 +149,7 @@ oscar_status run_quant_plan(oscar_cache* c, const std::vector<QuantTask>& tasks,
   plan.max_groups = c->layout.max_groups;
   plan.blocks_off = c->layout.blocks_off;
   plan.windows_off = c->layout.windows_off;
-  for (size_t i = begin; i < end; ++i) plan.t[i - begin] = tasks[i];
+  for (size_t i = begin; i < end; ++i) plan.t[i - begin] = pack_task(tasks[i]);
   cudaError_t e;
   if constexpr (CAP == kQuantPlanSmall)
     e = launch_quantize_small(plan, c->arena, k, v, c->meta16, stream);

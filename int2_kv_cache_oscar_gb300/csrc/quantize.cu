@@ -135,20 +135,20 @@ __global__ void __launch_bounds__(kQThreads, 2)
   QuantSmem& S = *reinterpret_cast<QuantSmem*>(smem_raw);
   const int head = blockIdx.y;
   const int tid = threadIdx.x;
-  const QuantTask T = plan.t[blockIdx.x];
+  const PackedTask T = plan.t[blockIdx.x];
   const int hkv = plan.hkv;
-  const int64_t sh = (int64_t)T.slot * hkv + head;
+  const int64_t sh = (int64_t)T.slot() * hkv + head;
   uint8_t* win = arena + plan.windows_off + sh * kWindowBytes;
   uint16_t* win_k = reinterpret_cast<uint16_t*>(win);
   uint16_t* win_v = win_k + kGroup * kHeadDim;
 
-  if (T.kind == 0) {
+  if (T.kind() == 0) {
     using B = Blk<M16>;
-    uint8_t* blk = arena + plan.blocks_off + (sh * plan.max_groups + T.group) * (int64_t)B::kBytes;
+    uint8_t* blk = arena + plan.blocks_off + (sh * plan.max_groups + T.group()) * (int64_t)B::kBytes;
     const int t = tid >> 1;          // token of the group
     const int half = tid & 1;        // channels [64 half, 64 half + 64)
-    const bool from_win = t < T.n_win;
-    const int64_t row = (int64_t)T.in_row + (t - T.n_win);
+    const bool from_win = t < T.n_win();
+    const int64_t row = (int64_t)T.in_row() + (t - T.n_win());
     const uint16_t* ksrc = (from_win ? win_k + t * kHeadDim : kin + (row * hkv + head) * kHeadDim) + 64 * half;
     const uint16_t* vsrc = (from_win ? win_v + t * kHeadDim : vin + (row * hkv + head) * kHeadDim) + 64 * half;
 
@@ -394,17 +394,17 @@ __global__ void __launch_bounds__(kQThreads, 2)
       for (int i = 1; i < kQThreads / 32; ++i) m = fmaxf(m, S.red[i]);
       atomicMax(reinterpret_cast<unsigned int*>(arena + kMetaHeader) + sh, __float_as_uint(m));
     }
-    if (T.tail_count <= 0) return;
+    if (T.tail_count() <= 0) return;
     // the window reads above completed before the first __syncthreads
   }
 
   // ---- window append: rows tail_in_row.. -> window slots (tail_pos + i) mod 128
   {
-    const int count = T.tail_count;
+    const int count = T.tail_count();
     for (int idx = tid; idx < count * 16; idx += kQThreads) {
       const int i = idx >> 4, q = idx & 15;
-      const int64_t row = (int64_t)T.tail_in_row + i;
-      const int slot = (T.tail_pos + i) & (kGroup - 1);
+      const int64_t row = (int64_t)T.tail_in_row() + i;
+      const int slot = (T.tail_pos_mod() + i) & (kGroup - 1);
       const uint4* ks = reinterpret_cast<const uint4*>(kin + (row * hkv + head) * kHeadDim);
       const uint4* vs = reinterpret_cast<const uint4*>(vin + (row * hkv + head) * kHeadDim);
       reinterpret_cast<uint4*>(win_k + slot * kHeadDim)[q] = __ldg(ks + q);
