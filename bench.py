@@ -103,6 +103,11 @@ class ClockSampler:
                 stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            # nvidia-smi can take seconds to start: wait (bounded) for its first
+            # sample so that the measurements that follow are covered
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 15.0 and self.proc.poll() is None:
+                time.sleep(0.05)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
