@@ -1,0 +1,101 @@
+"""GPU compression against closed forms (no oracle involved).
+
+The rotation is the normalised Sylvester Hadamard matrix H_d = Hu / sqrt(128),
+Hu[i][j] = (-1)^popcount(i & j) (OScaR abstract; ai-papers.net "OScaRの提案手法":
+Canalized Rotation, then Omni-Token Scaling, then per-channel INT2).
+
+* Keys whose rows are columns pi(t) of Hu (entries +-1, exact in bf16):
+  Hu k = 128 e_pi(t) exactly, so the norm is sqrt(128^2 / 128) = sqrt(128),
+  k_hat = e_pi(t), every channel holds one 1 and 127 zeros over the group:
+  scale fl32(1/3), zero 0, code 3 at channel pi(t) and 0 elsewhere.  Pins
+  the transform's order and normalisation and the packing of key codes.
+* Keys whose rows are basis vectors e_pi(t): k_hat = Hu e_pi(t) / sqrt(128),
+  norm 1; channel 0 is constant (+1/sqrt(128), scale 0, code 0), every other
+  channel splits evenly between +-1/sqrt(128): code 3 where
+  Hu[c][pi(t)] = +1, else 0.
+* Values on 4 dyadic levels z + s * code per token and 32-channel group, both
+  extremes present: codes, s and z come back exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+D = G = 128
+
+
+def _sylvester():
+    i = np.arange(D)
+    pc = np.vectorize(lambda x: bin(x).count("1"))(i[:, None] & i[None, :])
+    return np.where(pc % 2 == 0, 1.0, -1.0)
+
+
+def _values(rng, hkv):
+    """[G, hkv, D] values z + s * code with s = 0.25, z = -1.5 and both extreme
+    levels in every 32-channel group of every token; returns (v, codes)."""
+    codes = rng.integers(0, 4, size=(G, hkv, D))
+    for gr in range(4):
+        codes[:, :, 32 * gr] = 0
+        codes[:, :, 32 * gr + 1] = 3
+    return -1.5 + 0.25 * codes, codes
+
+
+def _run(keys, values, hkv):
+    cache = U.lib().OscarCache(1, hkv, G)
+    k = torch.tensor(keys, dtype=torch.float32).to(torch.bfloat16)
+    v = torch.tensor(values, dtype=torch.float32).to(torch.bfloat16)
+    assert torch.equal(k.double(), torch.tensor(keys)) and torch.equal(v.double(), torch.tensor(values))
+    cache.append([0], [0, G], k.cuda(), v.cuda())
+    U.lib().oscar_cache_check(cache.handle)
+    arena = U.read_arena(cache)
+    return [U.gpu_head(cache, arena, 0, h) for h in range(hkv)]
+
+
+def _check_values(g, vcodes):
+    assert np.array_equal(g.values.codes[0], vcodes)
+    assert np.all(g.values.scale[0] == np.float32(0.25)) and np.all(g.values.zero[0] == np.float32(-1.5))
+
+
+def test_hadamard_columns_give_one_hot_codes():
+    rng = np.random.default_rng(11)
+    hkv = 2
+    Hu = _sylvester()
+    perms = [rng.permutation(D) for _ in range(hkv)]
+    keys = np.stack([Hu[:, perms[h]].T for h in range(hkv)], axis=1)   # [t, h, c] = Hu[c][pi_h(t)]
+    values, vcodes = _values(rng, hkv)
+    heads = _run(keys, values, hkv)
+    for h, g in enumerate(heads):
+        expect = np.zeros((G, D), np.uint8)
+        expect[np.arange(G), perms[h]] = 3
+        assert np.array_equal(g.keys.codes[0], expect), f"head {h}: key codes"
+        assert np.all(g.keys.scale[0] == np.float32(1.0) / np.float32(3.0)), f"head {h}: key scales"
+        assert np.all(g.keys.zero[0] == 0.0), f"head {h}: key zeros"
+        assert np.all(g.keys.norm[0] == np.sqrt(np.float32(128.0))), f"head {h}: norms"
+        _check_values(g, vcodes[:, h])
+
+
+def test_basis_vectors_give_hadamard_sign_codes():
+    rng = np.random.default_rng(12)
+    hkv = 2
+    Hu = _sylvester()
+    perms = [rng.permutation(D) for _ in range(hkv)]
+    keys = np.zeros((G, hkv, D))
+    for h in range(hkv):
+        keys[np.arange(G), h, perms[h]] = 1.0
+    values, vcodes = _values(rng, hkv)
+    heads = _run(keys, values, hkv)
+    r = np.float32(1.0) / np.sqrt(np.float32(128.0))          # 1 / sqrt(128), as float32
+    for h, g in enumerate(heads):
+        cols = Hu[:, perms[h]].T                                # [t, c] = Hu[c][pi(t)]
+        expect = np.where(cols > 0, 3, 0).astype(np.uint8)
+        expect[:, 0] = 0                                        # channel 0: constant, scale 0
+        assert np.array_equal(g.keys.codes[0], expect), f"head {h}: key codes"
+        assert np.all(g.keys.norm[0] == 1.0), f"head {h}: norms"
+        assert g.keys.scale[0][0] == 0.0 and g.keys.zero[0][0] == r
+        s = (np.float32(2.0) * r) / np.float32(3.0)
+        assert np.all(np.abs(g.keys.scale[0][1:] - s) <= 1e-6 * s), f"head {h}: key scales"
+        assert np.all(np.abs(g.keys.zero[0][1:] + r) <= 1e-6 * r), f"head {h}: key zeros"
+        _check_values(g, vcodes[:, h])
