@@ -9,11 +9,12 @@
 //
 // Kernel structure (persistent CTAs, 2 per SM; 4 consumer warps + 1 producer
 // warp):
-//   * the producer streams whole 13,824-byte group blocks (codes, scales,
-//     zeros, norms of K and V) into a 6-stage shared-memory ring with 1-D
-//     bulk copies (cp.async.bulk + mbarrier transaction counts) and publishes
-//     how many uses of each stage it has issued, so that a consumer waits on
-//     a stage's barrier only for a phase that exists (no parity aliasing);
+//   * the producer streams whole group blocks (codes, scales, zeros, norms of
+//     K and V; 13,824 bytes, or 11,008 with float16 metadata) into a 7-stage
+//     (8-stage) shared-memory ring with 1-D bulk copies (cp.async.bulk +
+//     mbarrier transaction counts) and publishes how many uses of each stage
+//     it has issued, so that a consumer waits on a stage's barrier only for a
+//     phase that exists (no parity aliasing);
 //   * each consumer warp takes every 4th group and runs both contractions on
 //     the tensor cores with mma.sync m16n8k16: the 2-bit codes are the A
 //     operand, taken straight from the packed words with one AND each (an
