@@ -574,9 +574,10 @@ def profile_case(args):
 
 # ------------------------------------------------------------- CPU oracle
 
-def cpu_sample_worker(steps: int):
+def cpu_sample_worker(steps: int, warmup: int = 0):
     """Runs in a fresh single-threaded process: oracle decode of 1 of the 8
-    KV heads of the 128K workload (4 query heads), timed per step."""
+    KV heads of the 128K workload (4 query heads); `warmup` untimed decodes,
+    then `steps` timed ones."""
     import numpy as np
     import torch
 
@@ -591,6 +592,8 @@ def cpu_sample_worker(steps: int):
     hc = OR.build_head_cache(k[:, 0].double().numpy(), v[:, 0].double().numpy())
     t_quant = time.perf_counter() - t0
     qn = q[0].double().numpy()
+    for _ in range(warmup):
+        OR.decode_head(qn, hc)
     times = []
     for _ in range(steps):
         t0 = time.perf_counter()
@@ -599,10 +602,10 @@ def cpu_sample_worker(steps: int):
     return {"decode_s_per_head": statistics.mean(times), "quant_s_per_head": t_quant}
 
 
-def run_cpu_sample(steps: int):
+def run_cpu_sample(steps: int, warmup: int = 0):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    code = ("import json, bench; print('CPUJSON' + json.dumps(bench.cpu_sample_worker(%d)))" % steps)
+    code = ("import json, bench; print('CPUJSON' + json.dumps(bench.cpu_sample_worker(%d, %d)))" % (steps, warmup))
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
                        timeout=900)
     m = re.search(r"CPUJSON(\{.*\})", r.stdout)
@@ -683,10 +686,10 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        js = run_cpu_sample(max(1, args.steps // 4))
+        js = run_cpu_sample(args.steps, args.warmup)
         cb = cpu_baseline_obj(js)
         line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "us/step",
-                "n_gpus": args.gpus, "steps": max(1, args.steps // 4), "warmup": 0,
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": round(cb["value"] / 1e3, 3), "higher_is_better": False,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": config, "cpu_baseline": cb,
