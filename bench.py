@@ -97,9 +97,12 @@ class ClockSampler:
 
     def __enter__(self):
         try:
+            # nvidia-smi block-buffers a pipe: line-buffer it where stdbuf exists
+            import shutil
+            pre = ["stdbuf", "-oL"] if shutil.which("stdbuf") else []
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", str(self.index)], stdout=subprocess.PIPE,
+                pre + ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                       "-lms", "200", "-i", str(self.index)], stdout=subprocess.PIPE,
                 stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
