@@ -1,4 +1,4 @@
-"""GPU compression against closed forms (no oracle involved).
+"""GPU compression against closed forms, and degenerate inputs.
 
 The rotation is the normalised Sylvester Hadamard matrix H_d = Hu / sqrt(128),
 Hu[i][j] = (-1)^popcount(i & j) (OScaR abstract; ai-papers.net "OScaRの提案手法":
@@ -15,6 +15,8 @@ Canalized Rotation, then Omni-Token Scaling, then per-channel INT2).
   Hu[c][pi(t)] = +1, else 0.
 * Values on 4 dyadic levels z + s * code per token and 32-channel group, both
   extremes present: codes, s and z come back exactly.
+The first two tests use no oracle; the degenerate-input case (zero-norm
+tokens, an all-zero key group, an all-zero value group) is checked against it.
 """
 import numpy as np
 import pytest
@@ -99,3 +101,47 @@ def test_basis_vectors_give_hadamard_sign_codes():
         assert np.all(np.abs(g.keys.scale[0][1:] - s) <= 1e-6 * s), f"head {h}: key scales"
         assert np.all(np.abs(g.keys.zero[0][1:] + r) <= 1e-6 * r), f"head {h}: key zeros"
         _check_values(g, vcodes[:, h])
+
+
+def test_zero_norm_tokens_and_constant_channels():
+    """Degenerate inputs: all-zero key tokens (norm 0, k_hat = 0: score 0,
+    still in the softmax), a whole group of zero keys (every rotated channel
+    constant: scale 0, codes 0), and a 32-channel value group that is zero in
+    every token of a group (scale 0, zero 0, codes 0); quantisation and decode
+    against the oracle, the zero tokens' norms exactly 0."""
+    from int2_kv_cache_oscar_gb300 import workloads as W
+    from oracle import oscar_oracle as O
+    from tests import parity as P
+
+    gen = torch.Generator().manual_seed(13)
+    L, hkv, hq = 3 * G + 40, 2, 8
+    k, v = W.make_sequence_kv(L, hkv, W.LLAMA_RECIPE, gen)
+    zero_tok = [5, 77, 128 + 3, 300, 3 * G + 7]
+    k[zero_tok] = 0
+    k[G:2 * G, 0, :] = 0                 # head 0: group 1 entirely zero
+    v[:G, 1, 32:64] = 0                  # head 1: value group 1 zero across tokens of group 0
+    cache = U.lib().OscarCache(1, hkv, L + 8)
+    U.append_all(cache, [0], [k], [v], chunk=100)
+    q = W.make_q(1, hq, seed=14)
+    out = torch.empty((1, hq, 128), dtype=torch.bfloat16, device="cuda")
+    cache.decode([0], q.cuda(), hq, out, cache.workspace(1, hq))
+    U.lib().oscar_cache_check(cache.handle)
+    arena = U.read_arena(cache)
+    got, qn = U.f64(out), U.f64(q)
+    for h in range(hkv):
+        g = U.gpu_head(cache, arena, 0, h)
+        r = U.oracle_head(k, v, h)
+        P.assert_codes(g.keys.codes, r.keys.codes, r.keys.pre, f"head {h} K codes")
+        P.assert_codes(g.values.codes, r.values.codes, r.values.pre, f"head {h} V codes")
+        for name in ("scale", "zero", "norm"):
+            P.assert_meta(getattr(g.keys, name), getattr(r.keys, name), f"head {h} K {name}")
+        norms = g.keys.norm.reshape(-1)
+        for t in zero_tok:
+            if t < 3 * G:
+                assert norms[t] == 0.0, f"head {h}: token {t} norm {norms[t]}"
+        P.assert_decode(got[0, 4 * h:4 * h + 4], O.decode_head(qn[0, 4 * h:4 * h + 4], g), f"head {h} decode")
+    g0 = U.gpu_head(cache, arena, 0, 0)
+    assert np.all(g0.keys.norm[1] == 0) and np.all(g0.keys.scale[1] == 0) and np.all(g0.keys.codes[1] == 0)
+    g1 = U.gpu_head(cache, arena, 0, 1)
+    assert np.all(g1.values.scale[0][:, 1] == 0) and np.all(g1.values.zero[0][:, 1] == 0)
+    assert np.all(g1.values.codes[0][:, 32:64] == 0)
