@@ -232,10 +232,12 @@ oscar_status oscar_append_decode(oscar_cache* cache, int32_t n_seqs, const int32
  * the decode path's scores and values (OScaR abstract; ai-papers.net
  * "OScaRの提案手法").  Call it before appending the chunk; the chunk's own
  * causal attention is merged in by the caller with lse.
- *   q            device bf16 [n_q, num_q_heads, 128], 16-byte aligned
- *   out          device bf16 [n_q, num_q_heads, 128], 16-byte aligned
- *   lse          device fp32 [n_q, num_q_heads] or NULL: ln sum_t exp(s_t)
- *                per row (natural log, scores times softmax_scale)
+ *   q            bf16 [n_q, num_q_heads, 128], 16-byte aligned
+ *   out          bf16 [n_q, num_q_heads, 128], 16-byte aligned
+ *   lse          fp32 [n_q, num_q_heads] or NULL: ln sum_t exp(s_t) per row
+ *                (natural log, scores times softmax_scale)
+ *   q, out and lse may be device or page-locked host memory (see
+ *   oscar_decode_attention); other memory fails with OSCAR_ERR_INVALID_ARG.
  *   softmax_scale  0 means 1 / sqrt(128)
  * Any GQA ratio.  Needs no workspace.  The sequence must be non-empty.
  */
@@ -291,7 +293,8 @@ oscar_status oscar_cache_check(oscar_cache* cache, void* stream);
  * split-K structure over a plain bf16 cache.
  *   k_cache, v_cache  device bf16 [n_seqs_cap, Hkv, max_seq_len, 128]
  *   seq_ids / seq_lens host int32 [n_seqs]: slot and length (>= 1) of each
- *   q, out            device bf16 [n_seqs, num_q_heads, 128]
+ *   q, out            bf16 [n_seqs, num_q_heads, 128], device or page-locked
+ *                     host memory (the caches and the workspace: device only)
  * Scores are q . k_t * softmax_scale in float32, softmax and P.V in float32.
  */
 oscar_status oscar_bf16_decode_workspace_bytes(int32_t n_seqs, int32_t num_kv_heads,

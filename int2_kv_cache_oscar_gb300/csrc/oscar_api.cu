@@ -439,6 +439,7 @@ oscar_status oscar_decode_attention(oscar_cache* c, int32_t n_seqs, const int32_
     if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
     if ((s = device_view_as(q, "q", c->cfg.device, &q)) != OSCAR_OK) return s;
     if ((s = device_view_as(out, "out", c->cfg.device, &out)) != OSCAR_OK) return s;
+    if ((s = device_view_as(workspace, "workspace", c->cfg.device, &workspace, false)) != OSCAR_OK) return s;
     uint32_t* err_word = reinterpret_cast<uint32_t*>(c->arena);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (n_seqs <= kDecodeSeqsSmall)
@@ -574,6 +575,13 @@ oscar_status oscar_prefill_attention(oscar_cache* c, int32_t seq, int32_t n_q, c
   P.err_word = reinterpret_cast<uint32_t*>(c->arena);
   DeviceGuard dg(c->cfg.device);
   if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+  {
+    // q, out and lse: device or page-locked host memory (plain loads and stores)
+    oscar_status sv;
+    if ((sv = device_view_as(P.q, "q", c->cfg.device, &P.q)) != OSCAR_OK) return sv;
+    if ((sv = device_view_as(P.out, "out", c->cfg.device, &P.out)) != OSCAR_OK) return sv;
+    if (P.lse != nullptr && (sv = device_view_as(P.lse, "lse", c->cfg.device, &P.lse)) != OSCAR_OK) return sv;
+  }
   cudaError_t e = launch_prefill(P, c->arena, c->meta16, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return ok();
@@ -682,6 +690,14 @@ oscar_status oscar_bf16_decode_attention(int32_t n_seqs, const int32_t* seq_ids,
     const int sms = num_sms(dev);
     if (sms <= 0) return fail(OSCAR_ERR_CUDA, "cannot query the SM count");
     const float scale = softmax_scale == 0.0f ? 1.0f / std::sqrt((float)kHeadDim) : softmax_scale;
+    // the caches are read with tensor copies (device memory only); q and out
+    // may be page-locked host memory as for oscar_decode_attention
+    oscar_status sv;
+    if ((sv = device_view_as(k_cache, "k_cache", dev, &k_cache, false)) != OSCAR_OK) return sv;
+    if ((sv = device_view_as(v_cache, "v_cache", dev, &v_cache, false)) != OSCAR_OK) return sv;
+    if ((sv = device_view_as(q, "q", dev, &q)) != OSCAR_OK) return sv;
+    if ((sv = device_view_as(out, "out", dev, &out)) != OSCAR_OK) return sv;
+    if ((sv = device_view_as(workspace, "workspace", dev, &workspace, false)) != OSCAR_OK) return sv;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const uint16_t* kc = static_cast<const uint16_t*>(k_cache);
     const uint16_t* vc = static_cast<const uint16_t*>(v_cache);

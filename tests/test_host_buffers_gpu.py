@@ -95,3 +95,37 @@ def test_pageable_host_buffers_are_refused():
     assert c.length(0) == 300                    # nothing appended
     torch.cuda.synchronize()
     O_.oscar_cache_check(c.handle)
+
+
+def test_prefill_host_buffers_and_refusals():
+    O_ = U.lib()
+    (c,) = _caches([2048 + 33], 2, seed=106, n=1)
+    hq, n_q = 8, 19
+    gen = torch.Generator().manual_seed(107)
+    q = torch.randn((n_q, hq, 128), generator=gen).to(torch.bfloat16)
+    o_dev = torch.empty((n_q, hq, 128), dtype=torch.bfloat16, device="cuda")
+    l_dev = torch.empty((n_q, hq), dtype=torch.float32, device="cuda")
+    O_.oscar_prefill_attention(c.handle, 0, q.cuda(), hq, 0.0, o_dev, l_dev)
+    q_h = q.pin_memory()
+    o_h = torch.zeros((n_q, hq, 128), dtype=torch.bfloat16).pin_memory()
+    l_h = torch.zeros((n_q, hq), dtype=torch.float32).pin_memory()
+    O_.oscar_prefill_attention(c.handle, 0, q_h, hq, 0.0, o_h, l_h)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o_dev.cpu()) and torch.equal(l_h, l_dev.cpu())
+    with pytest.raises(O_.OscarError) as e:           # pageable output
+        O_.oscar_prefill_attention(c.handle, 0, q_h, hq, 0.0, torch.zeros_like(o_h), l_h)
+    assert e.value.status == O_.OSCAR_ERR_INVALID_ARG
+
+
+def test_bf16_reference_refuses_host_caches():
+    O_ = U.lib()
+    L, hkv, hq = 256, 2, 8
+    kc = torch.zeros((1, hkv, L, 128), dtype=torch.bfloat16).pin_memory()
+    vc = torch.zeros((1, hkv, L, 128), dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros((1, hq, 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(q)
+    ws = torch.empty(O_.oscar_bf16_decode_workspace_bytes(1, hkv, hq), dtype=torch.uint8, device="cuda")
+    with pytest.raises(O_.OscarError) as e:
+        O_.oscar_bf16_decode_attention([0], [L], kc, vc, hkv, L, q, hq, 0.0, out, ws)
+    assert e.value.status == O_.OSCAR_ERR_INVALID_ARG
+
