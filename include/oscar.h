@@ -180,7 +180,9 @@ oscar_status oscar_decode_workspace_bytes(const oscar_cache* cache, int32_t n_se
  *   seq_ids      host int32 [n_seqs]; every slot must have length >= 1
  *   q            bf16 [n_seqs, num_q_heads, 128] (unrotated queries), 16-byte
  *                aligned, in device memory or page-locked host memory
- *   num_q_heads  multiple of Hkv with num_q_heads / Hkv <= 4
+ *   num_q_heads  any multiple of Hkv; the kernels serve up to 4 query heads
+ *                of a KV head per pass, so num_q_heads / Hkv = 5..8 takes two
+ *                passes over the cache, 9..12 three, and so on
  *   softmax_scale  0 means 1 / sqrt(128)
  *   out          bf16 [n_seqs, num_q_heads, 128], 16-byte aligned, in device
  *                memory or page-locked host memory

@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kThreadsB, 2)
     // B operand of the score contraction: column n = g is query head g (zero beyond gqa)
     uint32_t qb[8][2];
     {
-      const uint16_t* qrow = p.h.q + ((int64_t)b * p.h.hq + j * gqa + (g < gqa ? g : 0)) * kHeadDim;
+      const uint16_t* qrow = p.h.q + ((int64_t)b * p.h.hq + j * p.h.q_group + p.h.q_head0 + (g < gqa ? g : 0)) * kHeadDim;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const int c = 16 * ks + 2 * tig;

@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
         locate_unit(p, uu, b, j, gg, ng);
         uint2 qr = make_uint2(0u, 0u);
         if (warp < gqa)
-          qr = *reinterpret_cast<const uint2*>(p.h.q + ((int64_t)b * p.h.hq + j * gqa + warp) * kHeadDim + 4 * lane);
+          qr = *reinterpret_cast<const uint2*>(p.h.q + ((int64_t)b * p.h.hq + j * p.h.q_group + p.h.q_head0 + warp) * kHeadDim + 4 * lane);
         const uint32_t vr = reinterpret_cast<const uint32_t*>(arena + kMetaHeader)[(int64_t)p.seq[b].slot * hkv + j];
         if (i == 0) { qpre0 = qr; vpre0 = vr; } else { qpre1 = qr; vpre1 = vr; }
         const int64_t row_end = p.seq[b].ubase + (int64_t)(j + 1) * ng;
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
         const uint2 raw = seg_idx == 0   ? qpre0
                           : seg_idx == 1 ? qpre1
                                          : *reinterpret_cast<const uint2*>(
-                                               p.h.q + ((int64_t)b * p.h.hq + j * gqa + h) * kHeadDim + 4 * lane);
+                                               p.h.q + ((int64_t)b * p.h.hq + j * p.h.q_group + p.h.q_head0 + h) * kHeadDim + 4 * lane);
         qv[0] = bf16_lo(raw.x);
         qv[1] = bf16_hi(raw.x);
         qv[2] = bf16_lo(raw.y);
@@ -627,7 +627,7 @@ __global__ void __launch_bounds__(kCombineThreads)
     abort_flag = 0;
     fence_mbar_init();
   }
-  qs[h][c] = active ? __uint_as_float((uint32_t)p.h.q[((int64_t)b * p.h.hq + j * gqa + h) * kHeadDim + c] << 16)
+  qs[h][c] = active ? __uint_as_float((uint32_t)p.h.q[((int64_t)b * p.h.hq + j * p.h.q_group + p.h.q_head0 + h) * kHeadDim + c] << 16)
                     : 0.0f;
   if (fused && tid < 32) {
     // the new token: 16 x 16 bytes of K (tid < 16) and of V, into shared row
@@ -766,7 +766,7 @@ __global__ void __launch_bounds__(kCombineThreads)
   }
   if (active) {
     const float ov = Oh / Lh;
-    p.h.out[((int64_t)b * p.h.hq + j * gqa + h) * kHeadDim + c] = (uint16_t)f32_to_bf16_bits(ov);
+    p.h.out[((int64_t)b * p.h.hq + j * p.h.q_group + p.h.q_head0 + h) * kHeadDim + c] = (uint16_t)f32_to_bf16_bits(ov);
   }
 }
 

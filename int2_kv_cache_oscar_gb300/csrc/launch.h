@@ -93,17 +93,17 @@ struct DecodeSeq {
 struct DecodeHeader {
   int32_t n_seqs;
   int32_t hkv;
-  int32_t gqa;           // query heads per KV head (<= kMaxGqa)
+  int32_t gqa;           // query heads of each KV head served by this launch (<= kMaxGqa)
   int32_t hq;
   int32_t max_groups;    // INT2: groups per (slot, head); bf16: max_seq_len
   int32_t n_ctas;        // main-kernel CTAs (N)
   int32_t bf16_mode;     // 1: bf16 reference cache (64-token units, no window)
-  int32_t pad;
+  int32_t q_group;       // query heads per KV head in the q / out layout (hq / hkv >= gqa)
   int64_t n_units;       // T
   int64_t blocks_off;
   int64_t windows_off;
   float scale_log2;      // softmax_scale * log2(e)
-  int32_t pad2;
+  int32_t q_head0;       // this launch's first query head within each KV head's group
   const uint16_t* q;
   uint16_t* out;
   float* partials;

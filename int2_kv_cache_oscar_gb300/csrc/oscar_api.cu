@@ -193,17 +193,17 @@ oscar_status run_decode(int device, int sms, int ctas_per_sm, int32_t n, const i
   std::memset(&P, 0, sizeof(P));
   int64_t rows = 0;
   fill_decode(P, n, slots, lens, hkv, bf16_mode, rows);
-  const int gqa = hq / hkv;
+  const int q_group = hq / hkv;
   const int64_t T = P.h.n_units;
   const int64_t maxN = (int64_t)sms * ctas_per_sm;
   const int64_t N = T < maxN ? T : maxN;
-  const size_t need = partial_bytes(N + rows, gqa);
+  const size_t need = partial_bytes(N + rows, q_group < kMaxGqa ? q_group : kMaxGqa);
   if (ws_bytes < need)
     return fail(OSCAR_ERR_CAPACITY, "workspace too small: %zu < %zu bytes", ws_bytes, need);
   P.h.n_seqs = n;
   P.h.hkv = hkv;
-  P.h.gqa = gqa;
   P.h.hq = hq;
+  P.h.q_group = q_group;
   P.h.max_groups = max_groups;
   P.h.n_ctas = (int32_t)N;
   P.h.bf16_mode = bf16_mode;
@@ -216,14 +216,23 @@ oscar_status run_decode(int device, int sms, int ctas_per_sm, int32_t n, const i
   P.h.err_word = err_word;
   P.h.k_new = static_cast<const uint16_t*>(k_new);
   P.h.v_new = static_cast<const uint16_t*>(v_new);
-  cudaError_t e;
-  if (bf16_mode)
-    e = launch_decode_bf16(P, kc, vc, stream, g_ev_start, g_ev_stop);
-  else
-    e = launch_decode_int2(P, arena, meta16, stream, g_ev_start, g_ev_stop);
-  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  e = launch_combine(P, arena, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  // The kernels serve at most kMaxGqa query heads of a KV head per launch (mma
+  // columns = heads x {hi, lo}); larger groups run as consecutive passes, each
+  // streaming the cache again.  Stream order keeps a pass's main kernel from
+  // overlapping the previous pass's combine on the shared workspace, and a
+  // fused step's passes all store the same new token.
+  for (int head0 = 0; head0 < q_group; head0 += kMaxGqa) {
+    P.h.gqa = q_group - head0 < kMaxGqa ? q_group - head0 : kMaxGqa;
+    P.h.q_head0 = head0;
+    cudaError_t e;
+    if (bf16_mode)
+      e = launch_decode_bf16(P, kc, vc, stream, g_ev_start, g_ev_stop);
+    else
+      e = launch_decode_int2(P, arena, meta16, stream, g_ev_start, g_ev_stop);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    e = launch_combine(P, arena, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  }
   (void)device;
   return OSCAR_OK;
 }
@@ -405,7 +414,8 @@ oscar_status oscar_decode_workspace_bytes(const oscar_cache* c, int32_t n_seqs, 
   const int hkv = c->cfg.num_kv_heads;
   if (num_q_heads % hkv != 0) return fail(OSCAR_ERR_INVALID_ARG, "num_q_heads must be a multiple of Hkv");
   const int64_t slots = (int64_t)c->sms * decode_int2_ctas_per_sm() + (int64_t)n_seqs * hkv;
-  *out_bytes = partial_bytes(slots, num_q_heads / hkv);
+  const int per_pass = num_q_heads / hkv < kMaxGqa ? num_q_heads / hkv : kMaxGqa;   // heads per decode pass
+  *out_bytes = partial_bytes(slots, per_pass);
   return ok();
 }
 
@@ -420,8 +430,6 @@ oscar_status oscar_decode_attention(oscar_cache* c, int32_t n_seqs, const int32_
     const int hkv = c->cfg.num_kv_heads;
     if (num_q_heads < hkv || num_q_heads % hkv != 0)
       return fail(OSCAR_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of Hkv");
-    if (num_q_heads / hkv > kMaxGqa)
-      return fail(OSCAR_ERR_UNSUPPORTED, "at most %d query heads per KV head", kMaxGqa);
     if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 16))
       return fail(OSCAR_ERR_INVALID_ARG, "q, out and workspace must be 16-byte aligned");
     if (!(softmax_scale >= 0.0f) || std::isinf(softmax_scale))
@@ -473,8 +481,6 @@ oscar_status oscar_append_decode(oscar_cache* c, int32_t n_seqs, const int32_t* 
     const int hkv = c->cfg.num_kv_heads;
     if (num_q_heads < hkv || num_q_heads % hkv != 0)
       return fail(OSCAR_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of Hkv");
-    if (num_q_heads / hkv > kMaxGqa)
-      return fail(OSCAR_ERR_UNSUPPORTED, "at most %d query heads per KV head", kMaxGqa);
     if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 16))
       return fail(OSCAR_ERR_INVALID_ARG, "k_new, v_new, q, out and workspace must be 16-byte aligned");
     if (!(softmax_scale >= 0.0f) || std::isinf(softmax_scale))
@@ -655,7 +661,8 @@ oscar_status oscar_bf16_decode_workspace_bytes(int32_t n_seqs, int32_t num_kv_he
   const int sms = num_sms(dev);
   if (sms <= 0) return fail(OSCAR_ERR_CUDA, "cannot query the SM count");
   const int64_t slots = (int64_t)sms * decode_bf16_ctas_per_sm() + (int64_t)n_seqs * num_kv_heads;
-  *out_bytes = partial_bytes(slots, num_q_heads / num_kv_heads);
+  const int per_pass = num_q_heads / num_kv_heads < kMaxGqa ? num_q_heads / num_kv_heads : kMaxGqa;
+  *out_bytes = partial_bytes(slots, per_pass);
   return ok();
 }
 
@@ -672,8 +679,6 @@ oscar_status oscar_bf16_decode_attention(int32_t n_seqs, const int32_t* seq_ids,
     if (num_kv_heads < 1 || max_seq_len < 1) return fail(OSCAR_ERR_INVALID_ARG, "bad num_kv_heads / max_seq_len");
     if (num_q_heads < num_kv_heads || num_q_heads % num_kv_heads != 0)
       return fail(OSCAR_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of Hkv");
-    if (num_q_heads / num_kv_heads > kMaxGqa)
-      return fail(OSCAR_ERR_UNSUPPORTED, "at most %d query heads per KV head", kMaxGqa);
     if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 16) ||
         !aligned(workspace, 16))
       return fail(OSCAR_ERR_INVALID_ARG, "buffers must be 16-byte aligned");

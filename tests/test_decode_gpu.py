@@ -88,8 +88,9 @@ def test_ragged_batch_decode_and_split_invariance():
         assert np.abs(alone[0] - got[i]).max() <= 2 * 2.0 ** -8 * max(1.0, np.abs(got[i]).max())
 
 
-@pytest.mark.parametrize("gqa", [1, 2, 4])
+@pytest.mark.parametrize("gqa", [1, 2, 4, 5, 8])
 def test_gqa_group_sizes(gqa):
+    """Ratios above 4 run as passes of up to 4 query heads per KV head."""
     hkv = 4
     hq = hkv * gqa
     gen = torch.Generator().manual_seed(30 + gqa)
@@ -140,9 +141,6 @@ def test_decode_bad_args():
         cache.decode([0], q, 36, out, ws)                  # 36 % 8 != 0
     assert e.value.status == O_.OSCAR_ERR_INVALID_ARG
     with pytest.raises(O_.OscarError) as e:
-        cache.decode([0], q, 64, out, ws)                  # gqa 8 > 4
-    assert e.value.status == O_.OSCAR_ERR_UNSUPPORTED
-    with pytest.raises(O_.OscarError) as e:
         cache.decode([0], q, 32, out, ws[:64])             # workspace too small
     assert e.value.status == O_.OSCAR_ERR_CAPACITY
 
@@ -187,3 +185,22 @@ def test_bf16_reference_decode(lens):
             ref = O.attention_exact(qn[b, 4 * j:4 * j + 4], U.f64(ks[b][:, j]), U.f64(vs[b][:, j]))
             worst = max(worst, P.assert_decode(got[b, 4 * j:4 * j + 4], ref, f"bf16 ref seq {b} head {j}"))
     print("bf16 reference max err", worst)
+
+
+def test_bf16_reference_decode_gqa8():
+    """The BF16 reference with 8 query heads per KV head (two passes)."""
+    O_ = U.lib()
+    gen = torch.Generator().manual_seed(72)
+    L, hkv, hq = 3000, 2, 16
+    k, v = W.make_sequence_kv(L, hkv, W.LLAMA_RECIPE, gen)
+    kc, vc = _bf16_cache([k], [v], L)
+    q = W.make_q(1, hq, seed=73)
+    out = torch.empty((1, hq, 128), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(O_.oscar_bf16_decode_workspace_bytes(1, hkv, hq), dtype=torch.uint8, device="cuda")
+    O_.oscar_bf16_decode_attention([0], [L], kc, vc, hkv, L, q.cuda(), hq, 0.0, out, ws)
+    torch.cuda.synchronize()
+    got, qn = U.f64(out), U.f64(q)
+    for j in range(hkv):
+        ref = O.attention_exact(qn[0, 8 * j:8 * j + 8], U.f64(k[:, j]), U.f64(v[:, j]))
+        P.assert_decode(got[0, 8 * j:8 * j + 8], ref, f"bf16 ref gqa 8 head {j}")
+

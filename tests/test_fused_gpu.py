@@ -86,3 +86,34 @@ def test_append_decode_bad_args_change_nothing():
         O_.oscar_append_decode(c.handle, [0, 0], kn, kn, q, HQ, 0.0, out, ws)
     assert e.value.status == O_.OSCAR_ERR_INVALID_ARG
     assert c.length(0) == 10 and c.length(1) == 20
+
+
+def test_append_decode_gqa8_matches_separate_calls():
+    """8 query heads per KV head: the fused step runs two decode passes, each
+    storing the new token; outputs and cache bytes equal the separate calls'."""
+    lens = [127, 300]             # step 0 closes a group of sequence 0
+    ids = list(range(len(lens)))
+    hq = 8 * HKV
+    a, b = _prefilled(lens, seed=33)
+    gen = torch.Generator().manual_seed(34)
+    wa, wb = a.workspace(len(ids), hq), b.workspace(len(ids), hq)
+    oa = torch.empty((len(ids), hq, 128), dtype=torch.bfloat16, device="cuda")
+    ob = torch.empty_like(oa)
+    for step in range(3):
+        kn = torch.randn((len(ids), HKV, 128), generator=gen).to(torch.bfloat16).cuda()
+        vn = torch.randn((len(ids), HKV, 128), generator=gen).to(torch.bfloat16).cuda()
+        q = torch.randn((len(ids), hq, 128), generator=gen).to(torch.bfloat16).cuda()
+        a.append(ids, list(range(len(ids) + 1)), kn, vn)
+        a.decode(ids, q, hq, oa, wa)
+        b.append_decode(ids, kn, vn, q, hq, ob, wb)
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ob), f"step {step}: fused output differs"
+        arena = U.read_arena(b)
+        got, qn = U.f64(ob), U.f64(q)
+        for i, s in enumerate(ids):
+            for j in range(HKV):
+                ref = O.decode_head(qn[i, j * 8:(j + 1) * 8], U.gpu_head(b, arena, s, j))
+                P.assert_decode(got[i, j * 8:(j + 1) * 8], ref, f"gqa 8 step {step} seq {s} head {j}")
+    ra, rb = U.read_arena(a), U.read_arena(b)
+    for s in ids:
+        assert np.array_equal(U.live_bytes(a, ra, s), U.live_bytes(b, rb, s))

@@ -40,8 +40,13 @@ def test_noalloc_decode_matches_workspace_decode_twice():
         g, r = U.f64(got), U.f64(ref)
         assert np.all(np.isfinite(g))
         P.assert_decode(g, r, f"no-alloc call {call}")
-    # a call needing more partials than the built-in scratch is refused
-    big = O_.OscarCache(1, 8, 128)
+    # a call needing more partials than the built-in scratch is refused before
+    # anything runs: 256 sequences x 8 KV heads of records (buffers sized for
+    # the call all the same)
+    n_big = 256
+    big = O_.OscarCache(n_big, 8, 128)
+    q_big = torch.zeros((n_big, 32, 128), dtype=torch.bfloat16, device="cuda")
+    o_big = torch.empty_like(q_big)
     with pytest.raises(O_.OscarError) as e:
-        O_.oscar_decode_attention_noalloc(big.handle, [0], q[:1], 32 * 8, 0.0, got[:1])
-    assert e.value.status in (O_.OSCAR_ERR_CAPACITY, O_.OSCAR_ERR_UNSUPPORTED)
+        O_.oscar_decode_attention_noalloc(big.handle, list(range(n_big)), q_big, 32, 0.0, o_big)
+    assert e.value.status == O_.OSCAR_ERR_CAPACITY
