@@ -573,8 +573,8 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
 //   merge:  m* = max(m_window, m_i), o = (sum 2^(m_i - m*) o_i) /
 //           (sum 2^(m_i - m*) l_i), written as bf16.
 constexpr int kCombineThreads = 128 * kMaxGqa;
-constexpr int kCombinePartBytes = 96 * 1024;   // partial records staged per chunk
-constexpr int kCombineSmem = kWindowBytes + kCombinePartBytes;
+constexpr int kCombinePartBytes = 96 * 1024;   // at most this many bytes of partial records per chunk
+constexpr int kCombineSmem = kWindowBytes + kCombinePartBytes;   // largest launch
 constexpr int kCombineMaxChunk = kCombinePartBytes / (kPartialFloats * 4);
 
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -583,9 +583,12 @@ template <int MAXS>
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const __grid_constant__ DecodeParams<MAXS> p, const uint8_t* __restrict__ arena) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  uint16_t* wk = reinterpret_cast<uint16_t*>(smem_raw);                 // [128][128] bf16
-  uint16_t* wv = wk + kGroup * kHeadDim;                                // [128][128] bf16
-  float* part = reinterpret_cast<float*>(smem_raw + kWindowBytes);      // partial records
+  // dynamic shared memory, sized per launch: window keys [wrows][128], window
+  // values [wrows][128] (bf16), then a chunk of partial records
+  const int wrows = p.h.comb_wrows;
+  uint16_t* wk = reinterpret_cast<uint16_t*>(smem_raw);
+  uint16_t* wv = wk + wrows * kHeadDim;
+  float* part = reinterpret_cast<float*>(smem_raw + 2 * wrows * kHeadDim * 2);
   __shared__ __align__(16) float qs[kMaxGqa][kHeadDim];
   __shared__ float pw[kMaxGqa][kGroup];                                 // window probabilities
   __shared__ float wts[kMaxGqa][kCombineMaxChunk];
@@ -619,7 +622,7 @@ __global__ void __launch_bounds__(kCombineThreads)
     count = cta_of_unit(U + ng - 1, T, N) - first + 1;
   }
   const int rec_bytes = gqa * kPartialFloats * 4;          // one slot: gqa records
-  const int per_chunk = kCombinePartBytes / rec_bytes;
+  const int per_chunk = p.h.comb_part_bytes / rec_bytes;
   const int64_t nchunks = (count + per_chunk - 1) / per_chunk;
 
   if (tid == 0) {
@@ -811,7 +814,7 @@ cudaError_t launch_combine(const DecodeParams<MAXS>& p, const uint8_t* arena, cu
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.h.n_seqs * p.h.hkv);
   cfg.blockDim = dim3(kCombineThreads);
-  cfg.dynamicSmemBytes = kCombineSmem;
+  cfg.dynamicSmemBytes = (size_t)2 * p.h.comb_wrows * kHeadDim * 2 + p.h.comb_part_bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

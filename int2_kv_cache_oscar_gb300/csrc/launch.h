@@ -113,6 +113,10 @@ struct DecodeHeader {
   // bf16 rows instead of the arena, and stored into the arena window
   const uint16_t* k_new;
   const uint16_t* v_new;
+  // combine staging, sized by the host for this launch: window rows (the
+  // longest window of the batch) and bytes of partial records per chunk
+  int32_t comb_wrows;
+  int32_t comb_part_bytes;
 };
 
 template <int MAXS>

@@ -221,9 +221,33 @@ oscar_status run_decode(int device, int sms, int ctas_per_sm, int32_t n, const i
   // streaming the cache again.  Stream order keeps a pass's main kernel from
   // overlapping the previous pass's combine on the shared workspace, and a
   // fused step's passes all store the same new token.
+  // combine staging: the longest window of the batch, and the most split-K
+  // records any row has (same split as the kernels: unit u in CTA
+  // ((u + 1) N - 1) / T), so that small stages let several combine CTAs share an SM
+  int wrows = 0;
+  int64_t max_count = 1;
+  for (int32_t i = 0; i < n; ++i) {
+    if (!bf16_mode) wrows = std::max(wrows, lens[i] % kGroup);
+    const int64_t units = bf16_mode ? (lens[i] + 63) / 64 : lens[i] / kGroup;
+    if (units == 0 || T == 0) continue;
+    for (int j = 0; j < hkv; ++j) {
+      const int64_t U = P.seq[i].ubase + (int64_t)j * units;
+      const int64_t first = ((U + 1) * N - 1) / T, last = ((U + units) * N - 1) / T;
+      max_count = std::max(max_count, last - first + 1);
+    }
+  }
+  // Sized staging pays when the combine has more CTAs (one per row) than the
+  // GPU has SMs: several then share an SM once the main grid is gone.  With
+  // fewer, the full size keeps combine CTAs off SMs where a main CTA still runs
+  // (measured: sharing one slows short contexts, 8K 15.3 -> 16.4 us).
+  const bool pack = (int64_t)n * hkv > sms;
+  P.h.comb_wrows = pack ? (wrows + 7) & ~7 : kGroup;   // multiples of 8 rows keep 16-byte alignment
   for (int head0 = 0; head0 < q_group; head0 += kMaxGqa) {
     P.h.gqa = q_group - head0 < kMaxGqa ? q_group - head0 : kMaxGqa;
     P.h.q_head0 = head0;
+    const int64_t rec_bytes = (int64_t)P.h.gqa * kPartialFloats * 4;
+    const int64_t cap = (96 * 1024) / rec_bytes;          // records of one chunk at most
+    P.h.comb_part_bytes = (int32_t)((pack ? std::min(max_count, cap) : cap) * rec_bytes);
     cudaError_t e;
     if (bf16_mode)
       e = launch_decode_bf16(P, kc, vc, stream, g_ev_start, g_ev_stop);
