@@ -123,6 +123,30 @@ def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
     return ctypes.c_void_p(0 if t is None else t.data_ptr())
 
 
+def _buf(t, dtype, shape, name: str, optional: bool = False) -> ctypes.c_void_p:
+    """Pointer of a caller buffer after the checks the C ABI cannot make (it
+    receives bare pointers): a torch tensor of `dtype`, dense row-major, whose
+    leading dimension is at least shape[0] (the kernels use that many rows) and
+    whose other dimensions equal the rest of `shape` (they set the strides);
+    None entries are unchecked.  A smaller or differently strided buffer would
+    otherwise let a kernel read or write past it."""
+    if t is None and optional:
+        return ctypes.c_void_p(0)
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None:
+        ok = t.dim() == len(shape) and (shape[0] is None or t.shape[0] >= shape[0]) and \
+            all(e is None or t.shape[i] == e for i, e in enumerate(shape) if i > 0)
+        if not ok:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)} "
+                             "(leading dimension at least, None: any)")
+    return ctypes.c_void_p(t.data_ptr())
+
+
 def make_config(max_batch: int, num_kv_heads: int, max_seq_len: int, device: int = 0,
                 head_dim: int = HEAD_DIM, group_size: int = GROUP,
                 value_group: int = VALUE_GROUP, meta_bits: int = 32) -> oscar_cache_config:
@@ -138,7 +162,7 @@ def oscar_cache_required_bytes(cfg: oscar_cache_config) -> int:
 
 def oscar_cache_create(cfg: oscar_cache_config, arena: torch.Tensor) -> ctypes.c_void_p:
     h = ctypes.c_void_p(0)
-    _check(_lib.oscar_cache_create(ctypes.byref(cfg), _ptr(arena),
+    _check(_lib.oscar_cache_create(ctypes.byref(cfg), _buf(arena, torch.uint8, None, "arena"),
                                    arena.numel() * arena.element_size(), ctypes.byref(h)))
     return h
 
@@ -159,8 +183,14 @@ def oscar_cache_length(handle, seq: int) -> int:
 
 def oscar_quantize_append(handle, seq_ids: Sequence[int], cu_new: Sequence[int],
                           k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
-    _check(_lib.oscar_quantize_append(handle, len(seq_ids), _i32(seq_ids), _i32(cu_new),
-                                      _ptr(k), _ptr(v), _stream(stream)))
+    rows = int(cu_new[-1]) if len(seq_ids) > 0 else 0
+    if rows == 0:
+        kp = vp = ctypes.c_void_p(0)
+    else:
+        kp = _buf(k, torch.bfloat16, (rows, None, HEAD_DIM), "k")
+        vp = _buf(v, torch.bfloat16, (rows,) + tuple(k.shape[1:]), "v")
+    _check(_lib.oscar_quantize_append(handle, len(seq_ids), _i32(seq_ids), _i32(cu_new), kp, vp,
+                                      _stream(stream)))
 
 
 def oscar_decode_workspace_bytes(handle, n_seqs: int, num_q_heads: int) -> int:
@@ -172,18 +202,23 @@ def oscar_decode_workspace_bytes(handle, n_seqs: int, num_q_heads: int) -> int:
 def oscar_decode_attention(handle, seq_ids: Sequence[int], q: torch.Tensor, num_q_heads: int,
                            softmax_scale: float, out: torch.Tensor, workspace: torch.Tensor,
                            stream=None) -> None:
-    _check(_lib.oscar_decode_attention(handle, len(seq_ids), _i32(seq_ids), _ptr(q), num_q_heads,
-                                       ctypes.c_float(softmax_scale), _ptr(out), _ptr(workspace),
-                                       workspace.numel() * workspace.element_size(),
-                                       _stream(stream)))
+    shape = (len(seq_ids), num_q_heads, HEAD_DIM)
+    _check(_lib.oscar_decode_attention(handle, len(seq_ids), _i32(seq_ids), _buf(q, torch.bfloat16, shape, "q"),
+                                       num_q_heads, ctypes.c_float(softmax_scale),
+                                       _buf(out, torch.bfloat16, shape, "out"),
+                                       _buf(workspace, torch.uint8, None, "workspace"),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def oscar_decode_attention_noalloc(handle, seq_ids: Sequence[int], q: torch.Tensor, num_q_heads: int,
                                    softmax_scale: float, out: torch.Tensor, stream=None) -> None:
     """Decode without a workspace: the partials go to the library's built-in
     device scratch (for callers that cannot allocate device memory)."""
-    _check(_lib.oscar_decode_attention_noalloc(handle, len(seq_ids), _i32(seq_ids), _ptr(q), num_q_heads,
-                                               ctypes.c_float(softmax_scale), _ptr(out), _stream(stream)))
+    shape = (len(seq_ids), num_q_heads, HEAD_DIM)
+    _check(_lib.oscar_decode_attention_noalloc(handle, len(seq_ids), _i32(seq_ids),
+                                               _buf(q, torch.bfloat16, shape, "q"), num_q_heads,
+                                               ctypes.c_float(softmax_scale),
+                                               _buf(out, torch.bfloat16, shape, "out"), _stream(stream)))
 
 
 def oscar_append_decode(handle, seq_ids: Sequence[int], k_new: torch.Tensor, v_new: torch.Tensor,
@@ -191,8 +226,13 @@ def oscar_append_decode(handle, seq_ids: Sequence[int], k_new: torch.Tensor, v_n
                         workspace: torch.Tensor, stream=None) -> None:
     """Append one token per sequence and decode, in one call (one launch when
     no group closes)."""
-    _check(_lib.oscar_append_decode(handle, len(seq_ids), _i32(seq_ids), _ptr(k_new), _ptr(v_new), _ptr(q),
-                                    num_q_heads, ctypes.c_float(softmax_scale), _ptr(out), _ptr(workspace),
+    shape = (len(seq_ids), num_q_heads, HEAD_DIM)
+    kp = _buf(k_new, torch.bfloat16, (len(seq_ids), None, HEAD_DIM), "k_new")
+    vp = _buf(v_new, torch.bfloat16, (len(seq_ids),) + tuple(k_new.shape[1:]), "v_new")
+    _check(_lib.oscar_append_decode(handle, len(seq_ids), _i32(seq_ids), kp, vp,
+                                    _buf(q, torch.bfloat16, shape, "q"), num_q_heads,
+                                    ctypes.c_float(softmax_scale), _buf(out, torch.bfloat16, shape, "out"),
+                                    _buf(workspace, torch.uint8, None, "workspace"),
                                     workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
@@ -201,8 +241,12 @@ def oscar_prefill_attention(handle, seq: int, q: torch.Tensor, num_q_heads: int,
     """Attention of a chunk's queries q [n_q, num_q_heads, 128] over the
     sequence's cached tokens; out gets the rows, lse (fp32 [n_q, heads]) their
     log-sum-exp."""
-    _check(_lib.oscar_prefill_attention(handle, seq, q.shape[0], _ptr(q), num_q_heads,
-                                        ctypes.c_float(softmax_scale), _ptr(out), _ptr(lse), _stream(stream)))
+    qp = _buf(q, torch.bfloat16, (None, num_q_heads, HEAD_DIM), "q")
+    n_q = q.shape[0]
+    _check(_lib.oscar_prefill_attention(handle, seq, n_q, qp, num_q_heads, ctypes.c_float(softmax_scale),
+                                        _buf(out, torch.bfloat16, (n_q, num_q_heads, HEAD_DIM), "out"),
+                                        _buf(lse, torch.float32, (n_q, num_q_heads), "lse", optional=True),
+                                        _stream(stream)))
 
 
 def oscar_cache_bytes(handle, seq: int, kind: int) -> int:
@@ -239,10 +283,17 @@ def oscar_bf16_decode_attention(seq_ids: Sequence[int], seq_lens: Sequence[int],
                                 max_seq_len: int, q: torch.Tensor, num_q_heads: int,
                                 softmax_scale: float, out: torch.Tensor, workspace: torch.Tensor,
                                 stream=None) -> None:
+    cshape = (None, num_kv_heads, max_seq_len, HEAD_DIM)
+    if isinstance(k_cache, torch.Tensor) and len(seq_ids) > 0 and k_cache.dim() == 4 and \
+            max(int(s) for s in seq_ids) >= k_cache.shape[0]:
+        raise ValueError("seq_ids index past the caches' first dimension")
+    shape = (len(seq_ids), num_q_heads, HEAD_DIM)
     _check(_lib.oscar_bf16_decode_attention(
-        len(seq_ids), _i32(seq_ids), _i32(seq_lens), _ptr(k_cache), _ptr(v_cache), num_kv_heads,
-        max_seq_len, _ptr(q), num_q_heads, ctypes.c_float(softmax_scale), _ptr(out),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+        len(seq_ids), _i32(seq_ids), _i32(seq_lens), _buf(k_cache, torch.bfloat16, cshape, "k_cache"),
+        _buf(v_cache, torch.bfloat16, cshape, "v_cache"), num_kv_heads, max_seq_len,
+        _buf(q, torch.bfloat16, shape, "q"), num_q_heads, ctypes.c_float(softmax_scale),
+        _buf(out, torch.bfloat16, shape, "out"), _buf(workspace, torch.uint8, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def oscar_set_timing_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]):
@@ -281,6 +332,8 @@ class OscarCache:
         return oscar_cache_length(self.handle, seq)
 
     def append(self, seq_ids, cu_new, k, v, stream=None):
+        if isinstance(k, torch.Tensor) and k.dim() == 3 and k.shape[1] != self.num_kv_heads:
+            raise ValueError(f"k has {k.shape[1]} KV heads, the cache {self.num_kv_heads}")
         oscar_quantize_append(self.handle, seq_ids, cu_new, k, v, stream)
 
     def workspace(self, n_seqs: int, num_q_heads: int) -> torch.Tensor:
@@ -293,5 +346,7 @@ class OscarCache:
 
     def append_decode(self, seq_ids, k_new, v_new, q, num_q_heads, out, workspace, softmax_scale=0.0,
                       stream=None):
+        if isinstance(k_new, torch.Tensor) and k_new.dim() == 3 and k_new.shape[1] != self.num_kv_heads:
+            raise ValueError(f"k_new has {k_new.shape[1]} KV heads, the cache {self.num_kv_heads}")
         oscar_append_decode(self.handle, seq_ids, k_new, v_new, q, num_q_heads, softmax_scale, out, workspace,
                             stream)

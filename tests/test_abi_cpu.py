@@ -162,3 +162,43 @@ def test_layout_reader_fp32_block():
     assert np.array_equal(b["kcodes"], kc) and np.array_equal(b["vcodes"], vc)
     for name, ref in [("kscale", ks), ("kzero", kz), ("knorm", kn), ("vscale", vs), ("vzero", vz)]:
         assert np.array_equal(b[name], ref), name
+
+
+def test_binding_checks_buffers_before_any_call():
+    """The C ABI sees bare pointers, so the binding checks what it can: dtype,
+    contiguity and the shape each call implies.  These raise before the
+    library is called (no handle and no GPU needed)."""
+    import pytest
+    import torch
+
+    from int2_kv_cache_oscar_gb300 import oscar as O
+
+    q = torch.zeros((2, 32, 128), dtype=torch.bfloat16)
+    out = torch.zeros_like(q)
+    ws = torch.zeros(1024, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="shape"):           # q for 16 heads, 32 requested
+        O.oscar_decode_attention(None, [0, 1], q[:, :16].contiguous(), 32, 0.0, out, ws)
+    with pytest.raises(ValueError, match="shape"):           # 3 sequences, q for 2
+        O.oscar_decode_attention(None, [0, 1, 2], q, 32, 0.0, out, ws)
+    with pytest.raises(ValueError, match="contiguous"):
+        O.oscar_decode_attention(None, [0, 1], q.transpose(0, 1), 32, 0.0, out, ws)
+    with pytest.raises(ValueError, match="bfloat16"):
+        O.oscar_decode_attention(None, [0, 1], q.float(), 32, 0.0, out, ws)
+    with pytest.raises(TypeError):
+        O.oscar_decode_attention(None, [0, 1], [1, 2], 32, 0.0, out, ws)
+    k = torch.zeros((10, 8, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="shape"):           # cu_new says 12 rows
+        O.oscar_quantize_append(None, [0], [0, 12], k, k)
+    with pytest.raises(ValueError, match="shape"):           # v differs from k
+        O.oscar_quantize_append(None, [0], [0, 10], k, k[:, :4].contiguous())
+    with pytest.raises(ValueError, match="shape"):           # lse for 16 heads
+        O.oscar_prefill_attention(None, 0, q, 32, 0.0, out, torch.zeros((2, 16), dtype=torch.float32))
+    with pytest.raises(ValueError, match="shape"):           # lse for 1 query row of 2
+        O.oscar_prefill_attention(None, 0, q, 32, 0.0, out, torch.zeros((1, 32), dtype=torch.float32))
+    with pytest.raises(ValueError, match="shape"):           # k_new for 1 sequence, 2 decoded
+        O.oscar_append_decode(None, [0, 1], torch.zeros((1, 8, 128), dtype=torch.bfloat16),
+                              torch.zeros((1, 8, 128), dtype=torch.bfloat16), q, 32, 0.0, out, ws)
+    with pytest.raises(ValueError, match="first dimension"):  # seq id past the caches
+        kc = torch.zeros((1, 8, 256, 128), dtype=torch.bfloat16)
+        O.oscar_bf16_decode_attention([0, 1], [10, 10], kc, kc, 8, 256, q, 32, 0.0, out, ws)
+

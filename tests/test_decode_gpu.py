@@ -137,8 +137,9 @@ def test_decode_bad_args():
     gen = torch.Generator().manual_seed(2)
     k, v = W.make_sequence_kv(200, 8, W.LLAMA_RECIPE, gen)
     U.append_all(cache, [0], [k], [v])
+    q36 = torch.zeros((1, 36, 128), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(O_.OscarError) as e:
-        cache.decode([0], q, 36, out, ws)                  # 36 % 8 != 0
+        cache.decode([0], q36, 36, torch.empty_like(q36), ws)   # 36 % 8 != 0
     assert e.value.status == O_.OSCAR_ERR_INVALID_ARG
     with pytest.raises(O_.OscarError) as e:
         cache.decode([0], q, 32, out, ws[:64])             # workspace too small

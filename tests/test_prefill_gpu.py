@@ -73,8 +73,9 @@ def test_prefill_bad_args():
     assert e.value.status == O_.OSCAR_ERR_INVALID_ARG
     k = torch.zeros((10, 2, 128), dtype=torch.bfloat16, device="cuda")
     cache.append([0], [0, 10], k, k)
+    q7 = torch.zeros((3, 7, 128), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(O_.OscarError) as e:
-        O_.oscar_prefill_attention(cache.handle, 0, q, 7, 0.0, out)     # heads not a multiple of Hkv
+        O_.oscar_prefill_attention(cache.handle, 0, q7, 7, 0.0, torch.empty_like(q7))  # heads not a multiple of Hkv
     assert e.value.status == O_.OSCAR_ERR_INVALID_ARG
     with pytest.raises(O_.OscarError) as e:
         O_.oscar_prefill_attention(cache.handle, 5, q, 8, 0.0, out)     # slot out of range
