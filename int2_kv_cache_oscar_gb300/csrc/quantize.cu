@@ -16,7 +16,8 @@
 //      being loaded into registers.
 //   2. K: unnormalised fast Walsh-Hadamard transform, H_d = Hu / sqrt(128):
 //      6 butterfly stages in registers (packed f32x2), the 7th across the
-//      thread pair with shuffles;
+//      thread pair with shuffles of half the values (after it each thread
+//      holds channels [32 half, + 32) and [64 + 32 half, + 32));
 //      n_t = sqrt(|Hu k|^2 / 128); k_hat = Hu k / |Hu k| (= H_d k / n_t).
 //   3. Per-channel min/max of k_hat over the 128 tokens (shared memory,
 //      16-token slices, then 8 slices).
@@ -35,33 +36,35 @@ namespace oscar {
 namespace {
 
 constexpr int kQThreads = 256;   // two threads per token: channels [0, 64) and [64, 128)
-constexpr int kKhStride = 136;   // floats per k_hat row: channels [0, 64) at 0, [64, 128) at 68
 constexpr int kVbStride = 144;   // bytes per value-code row (4 channels) in shared memory
 constexpr int kVbRows = kHeadDim / 4;
 constexpr float kMagic = 12582912.0f;                          // 1.5 * 2^23
 constexpr uint32_t kMagicBits = 0x4B400000u;
 
 struct QuantSmem {
-  alignas(16) float kh[kGroup * kKhStride];          // k_hat[t][kh_col(c)]; float4 stores / loads
+  alignas(16) float kh[kGroup * kHeadDim];           // k_hat[t][4 kh_slot(t, c / 4) + c % 4]; float4 stores / loads
   alignas(16) uint8_t vb[kVbRows * kVbStride + 16];  // value codes [channel / 4][permuted token]; uint4 loads
   alignas(16) float4 rmin[8][kHeadDim / 4];          // per 16-token slice: channel minima
   alignas(16) float4 rmax[8][kHeadDim / 4];          // per 16-token slice: channel maxima
   alignas(16) uint32_t kw[1024];                     // key code words, fragment order; uint4 loads
-  alignas(16) float4 kq[kHeadDim / 2 + 1];           // per channel pair (1/s, 1/s', -z, -z'), see kq_index
+  alignas(16) float4 kq[kHeadDim / 2 + 4];           // per channel pair (1/s, 1/s', -z, -z'), see kq_index
   float red[kQThreads / 32];
 };
 static_assert(offsetof(QuantSmem, vb) % 16 == 0 && offsetof(QuantSmem, kw) % 16 == 0, "alignment");
 static_assert(offsetof(QuantSmem, kq) % 16 == 0, "alignment");
-static_assert((kKhStride * 4) % 16 == 0 && kVbStride % 16 == 0, "rows must keep 16-byte alignment");
+static_assert(kVbStride % 16 == 0, "rows must keep 16-byte alignment");
 
-// Column of channel c in a k_hat row: the upper 64 channels are shifted by 16
-// bytes, so that the two threads of a token write different banks and a
-// warp's 16-byte row accesses are conflict-free.
-__device__ __forceinline__ int kh_col(int c) { return c + ((c >> 6) << 2); }
+// Physical float4 slot of float4 column q (channels 4q .. 4q + 3) of k_hat
+// row t.  The 8 threads of a quarter warp (tokens t .. t + 3, both threads of
+// each) store columns 8 h + i and 16 + 8 h + i (thread h of the pair): the
+// XOR sends them to 8 different bank groups.  It only permutes slots within
+// aligned groups of 8, so a warp reading a whole row stays conflict-free.
+__device__ __forceinline__ int kh_slot(int t, int q) { return q ^ (((t & 3) << 1) | ((q >> 3) & 1)); }
 
-// Entry of channel pair (c, c + 1) in the key-parameter table; the upper half
-// is shifted by one entry (16 bytes) for the same reason.
-__device__ __forceinline__ int kq_index(int c) { return (c >> 1) + (c >> 6); }
+// Entry of channel pair (c, c + 1) in the key-parameter table: every 32
+// channels shift by one more entry (16 bytes), so that the two threads of a
+// token (channels c and c + 32 at the same step) read different banks.
+__device__ __forceinline__ int kq_index(int c) { return (c >> 1) + (c >> 5); }
 
 // Rounded code decision of a pair against (1/s, -z): the float bits of
 // fl32(fl32(x - z) * inv) + 1.5 * 2^23, i.e. 0x4B400000 + code.  x >= z and
@@ -152,12 +155,13 @@ __global__ void __launch_bounds__(kQThreads, 2)
     const uint16_t* ksrc = (from_win ? win_k + t * kHeadDim : kin + (row * hkv + head) * kHeadDim) + 64 * half;
     const uint16_t* vsrc = (from_win ? win_v + t * kHeadDim : vin + (row * hkv + head) * kHeadDim) + 64 * half;
 
-    // this thread's half key row (64 bf16), in flight while the values are processed
+    // this thread's half key row (64 bf16), in flight while the values are
+    // processed; thread 1 of the pair holds its two 32-channel halves swapped
     uint4 kr[8];
     {
       const uint4* ks4 = reinterpret_cast<const uint4*>(ksrc);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) kr[i] = __ldg(ks4 + i);
+      for (int i = 0; i < 8; ++i) kr[i] = __ldg(ks4 + (i ^ (4 * half)));
     }
 
     // ---- values: per-token INT2 over this thread's two 32-channel groups
@@ -225,8 +229,9 @@ __global__ void __launch_bounds__(kQThreads, 2)
     }
 
     // ---- keys: rotation (6 butterfly stages in registers + 1 across the
-    // thread pair), norm, unit vector
-    float2 x[32];                      // channels 64 half + 2i, + 2i + 1
+    // thread pair), norm, unit vector.  x[i] holds channels 64 half + 2 i',
+    // + 1 with i' = i (thread 0) or i ^ 16 (thread 1: halves swapped).
+    float2 x[32];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       x[4 * i + 0] = bf16x2_to_float2(kr[i].x);
@@ -237,9 +242,9 @@ __global__ void __launch_bounds__(kQThreads, 2)
     // stage h = 1: within each pair
 #pragma unroll
     for (int i = 0; i < 32; ++i) x[i] = make_float2(x[i].x + x[i].y, x[i].x - x[i].y);
-    // stages h = 2 .. 32: pairs (i, i + h/2) of float2
+    // stages h = 2 .. 16: pairs (i, i + h/2) of float2, the same in both layouts
 #pragma unroll
-    for (int hb = 0; hb < 5; ++hb) {
+    for (int hb = 0; hb < 4; ++hb) {
 #pragma unroll
       for (int n = 0; n < 16; ++n) {
         const int h = 1 << hb;
@@ -249,16 +254,32 @@ __global__ void __launch_bounds__(kQThreads, 2)
         x[j + h] = __fadd2_rn(a, make_float2(-b.x, -b.y));
       }
     }
-    // stage h = 64 across the thread pair (the partner holds channel c +- 64)
-    {
-      const float2 sgn = half ? make_float2(-1.0f, -1.0f) : make_float2(1.0f, 1.0f);
+    // stage h = 32 (pairs (j, j + 16)), in thread 1 with the roles swapped:
+    // x[j] = b - a (minus the difference, in the slot of channel c + 32) and
+    // x[j + 16] = a + b, so both layouts stay as they are
+    const float2 sg = half ? make_float2(-1.0f, -1.0f) : make_float2(1.0f, 1.0f);
+    const float2 nsg = make_float2(-sg.x, -sg.y);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float2 y = make_float2(__shfl_xor_sync(0xffffffffu, x[i].x, 1), __shfl_xor_sync(0xffffffffu, x[i].y, 1));
-        x[i] = __ffma2_rn(x[i], sgn, y);   // a + b, or a - b
-      }
+    for (int j = 0; j < 16; ++j) {
+      const float2 a = x[j], b = x[j + 16];
+      x[j] = __ffma2_rn(b, sg, a);
+      x[j + 16] = __ffma2_rn(b, nsg, a);
     }
-    float* krow = &S.kh[t * kKhStride];
+    // stage h = 64 across the thread pair: each thread sends x[16 .. 31] and
+    // keeps x[0 .. 15]; the pairs (channel c, c + 64) meet as
+    //   thread 0: own a_c (c < 32),       received b_c       -> a + b, a - b
+    //   thread 1: own -b_c (c in 32..63), received a_c       -> a + b, a - b
+    // after which x[k] holds channels 32 half + 2k, + 1 and x[k + 16]
+    // channels 64 + 32 half + 2k, + 1 in both threads.
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float2 own = x[k];
+      const float2 rcv = make_float2(__shfl_xor_sync(0xffffffffu, x[k + 16].x, 1),
+                                     __shfl_xor_sync(0xffffffffu, x[k + 16].y, 1));
+      x[k] = __ffma2_rn(own, sg, rcv);
+      x[k + 16] = __ffma2_rn(rcv, nsg, own);
+    }
+    float* krow = &S.kh[t * kHeadDim];
     float2 sq2 = make_float2(0.0f, 0.0f), sq2b = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
@@ -281,9 +302,12 @@ __global__ void __launch_bounds__(kQThreads, 2)
         reinterpret_cast<float*>(blk + kOffKNorm)[t] = norm;
     }
     {
-      float4* dst = reinterpret_cast<float4*>(krow + 68 * half);
+      float4* dst = reinterpret_cast<float4*>(krow);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) dst[i] = make_float4(x[2 * i].x, x[2 * i].y, x[2 * i + 1].x, x[2 * i + 1].y);
+      for (int i = 0; i < 16; ++i) {     // float4 column 8 half + i (i < 8) or 8 + 8 half + i
+        const int q = (i < 8 ? 8 * half : 8 + 8 * half) + i;
+        dst[kh_slot(t, q)] = make_float4(x[2 * i].x, x[2 * i].y, x[2 * i + 1].x, x[2 * i + 1].y);
+      }
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
@@ -293,12 +317,12 @@ __global__ void __launch_bounds__(kQThreads, 2)
     // ---- per-channel key parameters: 16-token slices of 4 channels, then 8 slices
     {
       const int cq = tid & 31, ts = tid >> 5;
-      const int col = kh_col(4 * cq);
-      float4 mn = *reinterpret_cast<const float4*>(&S.kh[(16 * ts) * kKhStride + col]);
+      const float4* rows = reinterpret_cast<const float4*>(&S.kh[(16 * ts) * kHeadDim]);
+      float4 mn = rows[kh_slot(0, cq)];
       float4 mx = mn;
 #pragma unroll
       for (int r = 1; r < 16; ++r) {
-        const float4 v = *reinterpret_cast<const float4*>(&S.kh[(16 * ts + r) * kKhStride + col]);
+        const float4 v = rows[r * (kHeadDim / 4) + kh_slot(r, cq)];
         mn.x = fminf(mn.x, v.x); mn.y = fminf(mn.y, v.y); mn.z = fminf(mn.z, v.z); mn.w = fminf(mn.w, v.w);
         mx.x = fmaxf(mx.x, v.x); mx.y = fmaxf(mx.y, v.y); mx.z = fmaxf(mx.z, v.z); mx.w = fmaxf(mx.w, v.w);
       }
@@ -334,28 +358,36 @@ __global__ void __launch_bounds__(kQThreads, 2)
     }
     __syncthreads();
 
-    // ---- key codes of token t, channels of half: the 4 fragment words with j = half
+    // ---- key codes of token t: this thread's channels fill half of each of
+    // the token's fragment words (j = 0: channels [32 half, + 32), slots kk =
+    // 2 half, 2 half + 1; j = 1: channels [64 + 32 half, + 32)); the pair
+    // swaps halves so that thread `half` completes the 4 words with j = half
     {
       const int mt = t >> 4, g = t & 7, r = (t >> 3) & 1;
+      uint32_t wa[4] = {0u, 0u, 0u, 0u}, wb[4] = {0u, 0u, 0u, 0u};   // j = 0, j = 1, per tig; bits as if half = 0
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int tig = k & 3, hf = (k >> 2) & 1, kkl = k >> 3;
+        const int sft = 4 * kkl + 2 * hf;
+        const float4 pa = S.kq[kq_index(32 * half + 2 * k)];
+        const float4 pb = S.kq[kq_index(64 + 32 * half + 2 * k)];
+        const uint2 ca = code_bits2(x[k], make_float2(pa.x, pa.y), make_float2(pa.z, pa.w));
+        const uint2 cb = code_bits2(x[k + 16], make_float2(pb.x, pb.y), make_float2(pb.z, pb.w));
+        if constexpr (M16) {
+          wa[tig] |= (clamped_code(ca.x) << sft) | (clamped_code(ca.y) << (16 + sft));
+          wb[tig] |= (clamped_code(cb.x) << sft) | (clamped_code(cb.y) << (16 + sft));
+        } else {
+          wa[tig] += (ca.x << sft) + (ca.y << (16 + sft));
+          wb[tig] += (cb.x << sft) + (cb.y << (16 + sft));
+        }
+      }
+      const int up = 8 * half;   // slots kk = 2, 3 of the words
 #pragma unroll
       for (int tig = 0; tig < 4; ++tig) {
-        uint32_t w = M16 ? 0u : 0u - key_word_magic();
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const int i = 16 * kk + 8 * hf + 2 * tig;          // channels 64 half + i, + i + 1 (e = 0, 1)
-            const float4 pq = S.kq[kq_index(64 * half + i)];
-            const uint2 cb = code_bits2(x[i >> 1], make_float2(pq.x, pq.y), make_float2(pq.z, pq.w));
-            if constexpr (M16) {
-              w |= clamped_code(cb.x) << (4 * kk + 2 * hf);
-              w |= clamped_code(cb.y) << (16 + 4 * kk + 2 * hf);
-            } else {
-              w += cb.x << (4 * kk + 2 * hf);
-              w += cb.y << (16 + 4 * kk + 2 * hf);
-            }
-          }
-        }
+        const uint32_t keep = (half ? wb[tig] : wa[tig]) << up;
+        const uint32_t send = (half ? wa[tig] : wb[tig]) << up;
+        const uint32_t got = __shfl_xor_sync(0xffffffffu, send, 1);
+        const uint32_t w = M16 ? (keep | got) : (keep + got - key_word_magic());
         S.kw[((mt * 32 + 4 * g + tig) * 4) + 2 * half + r] = w;
       }
     }
