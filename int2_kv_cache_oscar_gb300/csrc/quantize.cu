@@ -21,8 +21,9 @@
 //      n_t = sqrt(|Hu k|^2 / 128); k_hat = Hu k / |Hu k| (= H_d k / n_t).
 //   3. Per-channel min/max of k_hat over the 128 tokens (shared memory,
 //      16-token slices, then 8 slices).
-//   4. Codes of k_hat, packed straight into the fragment-order words.
-//   5. Coalesced 16-byte stores of both code matrices.
+//   4. Codes of k_hat, packed straight into the fragment-order words and
+//      stored; the value code words are stored in V order from the staged
+//      bytes after the first barrier.
 // Every code decision is fl32(fl32(x - z) * fl32(1/s)) rounded half to even;
 // the packed f32x2 operations round each lane exactly like the scalar ones.
 #include <cstddef>
@@ -46,11 +47,10 @@ struct QuantSmem {
   alignas(16) uint8_t vb[kVbRows * kVbStride + 16];  // value codes [channel / 4][permuted token]; uint4 loads
   alignas(16) float4 rmin[8][kHeadDim / 4];          // per 16-token slice: channel minima
   alignas(16) float4 rmax[8][kHeadDim / 4];          // per 16-token slice: channel maxima
-  alignas(16) uint32_t kw[1024];                     // key code words, fragment order; uint4 loads
   alignas(16) float4 kq[kHeadDim / 2 + 4];           // per channel pair (1/s, 1/s', -z, -z'), see kq_index
   float red[kQThreads / 32];
 };
-static_assert(offsetof(QuantSmem, vb) % 16 == 0 && offsetof(QuantSmem, kw) % 16 == 0, "alignment");
+static_assert(offsetof(QuantSmem, vb) % 16 == 0, "alignment");
 static_assert(offsetof(QuantSmem, kq) % 16 == 0, "alignment");
 static_assert(kVbStride % 16 == 0, "rows must keep 16-byte alignment");
 
@@ -314,6 +314,33 @@ __global__ void __launch_bounds__(kQThreads, 2)
     if ((tid & 31) == 0) S.red[tid >> 5] = smax;
     __syncthreads();
 
+    // ---- value code words, V order (the staged bytes are complete)
+    {
+      const int u = tid;
+      const int mt = u >> 5, lane = u & 31, g = lane >> 2, tig = lane & 3;
+      uint32_t wv[4];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int rowc = 16 * mt + g + 8 * r;
+          const int sh = 2 * (rowc & 3);                 // this channel's bits in each byte
+          const uint4 b = *reinterpret_cast<const uint4*>(&S.vb[vb_row(rowc >> 2) + (tig * 2 + j) * 16]);
+          const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+          uint32_t w = 0;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t cw = (bw[kk] >> sh) & 0x03030303u;
+            const uint32_t y = (cw | (cw >> 6)) & 0x000F000Fu;
+            w |= y << (4 * kk);
+          }
+          wv[2 * j + r] = w;
+        }
+      }
+      *reinterpret_cast<uint2*>(blk + B::kVCodes + vword_off(mt, 0, lane)) = make_uint2(wv[0], wv[1]);
+      *reinterpret_cast<uint2*>(blk + B::kVCodes + vword_off(mt, 1, lane)) = make_uint2(wv[2], wv[3]);
+    }
+
     // ---- per-channel key parameters: 16-token slices of 4 channels, then 8 slices
     {
       const int cq = tid & 31, ts = tid >> 5;
@@ -382,43 +409,15 @@ __global__ void __launch_bounds__(kQThreads, 2)
         }
       }
       const int up = 8 * half;   // slots kk = 2, 3 of the words
+      uint32_t* kcodes = reinterpret_cast<uint32_t*>(blk + kOffKCodes);
 #pragma unroll
       for (int tig = 0; tig < 4; ++tig) {
         const uint32_t keep = (half ? wb[tig] : wa[tig]) << up;
         const uint32_t send = (half ? wa[tig] : wb[tig]) << up;
         const uint32_t got = __shfl_xor_sync(0xffffffffu, send, 1);
         const uint32_t w = M16 ? (keep | got) : (keep + got - key_word_magic());
-        S.kw[((mt * 32 + 4 * g + tig) * 4) + 2 * half + r] = w;
+        kcodes[((mt * 32 + 4 * g + tig) * 4) + 2 * half + r] = w;
       }
-    }
-    __syncthreads();
-
-    // ---- coalesced stores of both code matrices (K: 256 x 16 B; V: 2 x 256 x 8 B, V order)
-    {
-      const int u = tid;
-      reinterpret_cast<uint4*>(blk + kOffKCodes)[u] = reinterpret_cast<const uint4*>(S.kw)[u];
-      const int mt = u >> 5, lane = u & 31, g = lane >> 2, tig = lane & 3;
-      uint32_t wv[4];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int rowc = 16 * mt + g + 8 * r;
-          const int sh = 2 * (rowc & 3);                 // this channel's bits in each byte
-          const uint4 b = *reinterpret_cast<const uint4*>(&S.vb[vb_row(rowc >> 2) + (tig * 2 + j) * 16]);
-          const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
-          uint32_t w = 0;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t cw = (bw[kk] >> sh) & 0x03030303u;
-            const uint32_t y = (cw | (cw >> 6)) & 0x000F000Fu;
-            w |= y << (4 * kk);
-          }
-          wv[2 * j + r] = w;
-        }
-      }
-      *reinterpret_cast<uint2*>(blk + B::kVCodes + vword_off(mt, 0, lane)) = make_uint2(wv[0], wv[1]);
-      *reinterpret_cast<uint2*>(blk + B::kVCodes + vword_off(mt, 1, lane)) = make_uint2(wv[2], wv[3]);
     }
     if (tid == 0) {
       float m = S.red[0];
