@@ -157,8 +157,9 @@ oscar_status oscar_cache_length(const oscar_cache* cache, int32_t seq, int32_t* 
  *   cu_new   host int32 [n_seqs + 1], cu_new[0] = 0, non-decreasing;
  *            sequence i appends rows cu_new[i] .. cu_new[i+1]-1
  *   k, v     device bf16 [cu_new[n_seqs], Hkv, 128] (rows of the raw, i.e.
- *            unrotated, keys and values; 16-byte aligned); host memory fails
- *            with OSCAR_ERR_INVALID_ARG
+ *            unrotated, keys and values; 16-byte aligned, and read with
+ *            32-byte loads, which are faster, when both are 32-byte
+ *            aligned); host memory fails with OSCAR_ERR_INVALID_ARG
  * Every 128-token group that fills is rotated, norm-scaled and quantised
  * (keys) and quantised (values) from its bf16 tokens (earlier ones from the
  * window, new ones from k/v) into its block; the remaining tokens go to the

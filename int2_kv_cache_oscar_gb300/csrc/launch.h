@@ -63,7 +63,7 @@ struct QuantPlan {
   int32_t n_tasks;
   int32_t hkv;
   int32_t max_groups;
-  int32_t pad;
+  int32_t wide;          // 1: k and v are 32-byte aligned (32-byte row loads)
   int64_t blocks_off;
   int64_t windows_off;
   PackedTask t[CAP];

@@ -147,6 +147,7 @@ oscar_status run_quant_plan(oscar_cache* c, const std::vector<QuantTask>& tasks,
   plan.n_tasks = (int32_t)(end - begin);
   plan.hkv = c->cfg.num_kv_heads;
   plan.max_groups = c->layout.max_groups;
+  plan.wide = (aligned(k, 32) && aligned(v, 32)) ? 1 : 0;   // the arena's window rows are 256-byte aligned
   plan.blocks_off = c->layout.blocks_off;
   plan.windows_off = c->layout.windows_off;
   for (size_t i = begin; i < end; ++i) plan.t[i - begin] = pack_task(tasks[i]);

@@ -119,6 +119,14 @@ __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
 
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) { return make_float2(bf16_lo(u), bf16_hi(u)); }
 
+// 32 bytes from global memory (32-byte aligned p), read once: each load of
+// the pair's two threads fills whole 32-byte sectors.
+__device__ __forceinline__ void ld_row32(const void* p, uint4& lo, uint4& hi) {
+  asm("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
+      : "l"(p));
+}
+
 // Sum of (0x4B400000 << shift) over the shifts of one key-code word
 // (16 e + 4 kk + 2 hf), modulo 2^32: the float bits' constant part,
 // subtracted once per word.
@@ -160,8 +168,13 @@ __global__ void __launch_bounds__(kQThreads, 2)
     uint4 kr[8];
     {
       const uint4* ks4 = reinterpret_cast<const uint4*>(ksrc);
+      if (plan.wide) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) kr[i] = __ldg(ks4 + (i ^ (4 * half)));
+        for (int i = 0; i < 4; ++i) ld_row32(ks4 + 2 * (i ^ (2 * half)), kr[2 * i], kr[2 * i + 1]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) kr[i] = __ldg(ks4 + (i ^ (4 * half)));
+      }
     }
 
     // ---- values: per-token INT2 over this thread's two 32-channel groups
@@ -169,8 +182,13 @@ __global__ void __launch_bounds__(kQThreads, 2)
     {
       uint4 vr[8];
       const uint4* vs4 = reinterpret_cast<const uint4*>(vsrc);
+      if (plan.wide) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) vr[i] = __ldg(vs4 + i);
+        for (int i = 0; i < 4; ++i) ld_row32(vs4 + 2 * i, vr[2 * i], vr[2 * i + 1]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) vr[i] = __ldg(vs4 + i);
+      }
       const int pt = vb_perm(t);
       float sv[2], zv[2];
 #pragma unroll

@@ -135,3 +135,32 @@ def test_cache_bytes():
     assert O_.oscar_cache_bytes(cache.handle, 2, O_.OSCAR_BYTES_USED) == 8 * 2 * 13824
     # full groups: 65536 / 13824 = 4.74x smaller than bf16
     assert abs(65536 / 13824 - 4.7407) < 1e-3
+
+
+def test_16_byte_aligned_inputs_match_32_byte_aligned():
+    """Inputs that are 16- but not 32-byte aligned take the 16-byte row loads
+    (the 32-byte loads need 32-byte alignment); the arena must be identical
+    to the one built from 32-byte aligned inputs, windows and a group closed
+    from window + new rows included."""
+    w = W.llama_layer(2 * 128 + 90, seed=21)
+    ks, vs, _ = W.make_workload_tensors(w)
+    k, v = ks[0], vs[0]
+    O_ = U.lib()
+    states = []
+    for offset in (0, 8):                     # bf16 elements: 0 or 16 bytes past a 256-byte boundary
+        cache = O_.OscarCache(1, 8, 1024)
+        for p0, n in ((0, 100), (100, 200), (300, 46)):
+            bk = torch.empty(n * 8 * 128 + offset, dtype=torch.bfloat16, device="cuda")
+            bv = torch.empty_like(bk)
+            kk = bk[offset:].view(n, 8, 128)
+            vv = bv[offset:].view(n, 8, 128)
+            kk.copy_(k[p0:p0 + n])
+            vv.copy_(v[p0:p0 + n])
+            assert (kk.data_ptr() % 32 == 0) == (offset == 0) and kk.data_ptr() % 16 == 0
+            cache.append([0], [0, n], kk, vv)
+        O_.oscar_cache_check(cache.handle)
+        states.append(U.live_bytes(cache, U.read_arena(cache), 0))
+    assert np.array_equal(states[0], states[1])
+    cache = O_.OscarCache(1, 8, 1024)
+    U.append_all(cache, [0], ks, vs, chunk=100)
+    _compare_cache(cache, [0], ks, vs, {})
