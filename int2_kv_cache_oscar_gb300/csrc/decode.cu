@@ -37,7 +37,7 @@ namespace {
 constexpr int kConsumers = 4;
 constexpr int kDecThreads = (kConsumers + 1) * 32;
 constexpr int kCtasPerSm = 2;
-constexpr int kPbStride = kGroup + 8;  // probability rows, padded against bank conflicts
+constexpr int kPbStride = kGroup + 16;  // probability rows (see pb_col)
 
 // Ring geometry by metadata width: 7 stages of 13,824 B, or 8 of 11,008 B
 // (float16 metadata), two CTAs per SM either way.
@@ -78,6 +78,13 @@ static_assert(kCtasPerSm * (sizeof(DecSmemT<false>) + 1024) <= 233472 &&
                   kCtasPerSm * (sizeof(DecSmemT<true>) + 1024) <= 233472,
               "two CTAs per SM");
 
+
+// Column of token (or channel) t in probability row `row` (a query head):
+// rows 2 and 3 swap 8-column blocks.  With the 144-float row stride, the
+// score stores (lane (g, tig): row tig, column 16 mt + g) and the P.V
+// factor loads (float2; lane (g, tig): row g / 2, column 16 k + 2 tig +
+// 8 (g & 1)) are both free of bank conflicts.
+__device__ __forceinline__ int pb_col(int row, int t) { return t ^ (8 * ((row >> 1) & 1)); }
 
 __device__ __forceinline__ float pow2f(int e) {
   e = max(-126, min(127, e));
@@ -445,8 +452,8 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const int t0 = 16 * mt + g;
-        pb[t0] = sc[mt].x;
-        pb[t0 + 8] = sc[mt].y;
+        pb[pb_col(tig, t0)] = sc[mt].x;
+        pb[pb_col(tig, t0 + 8)] = sc[mt].y;
         const float4 z0 = MR::v4(vze, t0);
         const float4 z1 = MR::v4(vze, t0 + 8);
         zacc[0] = fmaf(sc[mt].x, z0.x, fmaf(sc[mt].y, z1.x, zacc[0]));
@@ -472,7 +479,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
 #pragma unroll
           for (int kk2 = 0; kk2 < 4; ++kk2) {
             const int t = 16 * (4 * jh + kk2) + 2 * tig + 8 * half;   // this lane's two tokens
-            const float2 pr = __fmul2_rn(*reinterpret_cast<const float2*>(pbh + t), make_float2(fsc[kk2], fsc[kk2]));
+            const float2 pr = __fmul2_rn(*reinterpret_cast<const float2*>(pbh + pb_col(hb, t)), make_float2(fsc[kk2], fsc[kk2]));
             float4 s0, s1;
             MR::v4x2(vsc, t, s0, s1);
 #pragma unroll
@@ -522,8 +529,8 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const float zg = zs[mt >> 1];
-        S.pbuf[warp][tig][16 * mt + g] = fmaf(o_acc[mt].x, kv, zg);
-        S.pbuf[warp][tig][16 * mt + g + 8] = fmaf(o_acc[mt].y, kv, zg);
+        S.pbuf[warp][tig][pb_col(tig, 16 * mt + g)] = fmaf(o_acc[mt].x, kv, zg);
+        S.pbuf[warp][tig][pb_col(tig, 16 * mt + g + 8)] = fmaf(o_acc[mt].y, kv, zg);
       }
     }
     named_bar_sync(1, kConsumers * 32);
@@ -541,7 +548,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
         for (int w = 0; w < kConsumers; ++w) {
           const float mw = S.mst[w][h];
           const float f = (mw == -INFINITY) ? 0.0f : exp2f(mw - M);
-          o = fmaf(f, S.pbuf[w][h][c], o);
+          o = fmaf(f, S.pbuf[w][h][pb_col(h, c)], o);
           l = fmaf(f, S.lst[w][h], l);
         }
         part[h * kPartialFloats + c] = o;
