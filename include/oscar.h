@@ -110,8 +110,9 @@ enum {
  *   +5632   V codes, 4,096 B, fragment words of X[row = channel][col = token]
  *           in "V order"
  *   +9728   V scale s[t][0..3], float32 [128][4] (per token, one per
- *           32-channel group)
- *   +11776  V zero  z[t][0..3], float32 [128][4]
+ *           32-channel group), token t in row t ^ ((t >> 3) & 1)
+ *           (neighbouring tokens swap rows where bit 3 of t is set)
+ *   +11776  V zero  z[t][0..3], float32 [128][4], rows as the V scale
  * meta_bits 16: the same sections with float16 metadata:
  *   +0 K codes, +4096 K scale, +4352 K zero, +4608 K norm (float16 [128]
  *   each), +4864 V codes, +8960 V scale, +9984 V zero (float16 [128][4]

@@ -30,6 +30,13 @@ constexpr int kOff16VScale = 8960;
 constexpr int kOff16VZero = 9984;
 constexpr int kBlockBytes16 = 11008;
 
+// Row of token t in the float32 value scale and zero arrays ([128][4]):
+// tokens t and t ^ 1 trade places where bit 3 of t is set.  Decode lanes read
+// the scales of tokens t and t + 8 (the two threads of a B-column pair) in
+// the same 128-bit load; unswizzled those rows are 128 bytes apart, in the
+// same banks.  An involution: the stored row p holds token vmeta_row(p).
+__host__ __device__ constexpr int vmeta_row(int t) { return t ^ ((t >> 3) & 1); }
+
 // Byte offset, within the value-code section, of fragment word pair (r = 0, 1)
 // of m-tile mt, token half j and lane ("V order": a warp's pairs for one
 // (mt, j) are 256 contiguous bytes).  Key codes keep the "K order"
@@ -267,7 +274,7 @@ struct Meta {
       const uint2 h = *reinterpret_cast<const uint2*>(a + 8 * t);
       return make_float4(half_lo_to_float(h.x), half_hi_to_float(h.x), half_lo_to_float(h.y), half_hi_to_float(h.y));
     } else {
-      return *reinterpret_cast<const float4*>(a + 16 * t);
+      return *reinterpret_cast<const float4*>(a + 16 * vmeta_row(t));
     }
   }
   // those of tokens t and t + 1, t even (one 16-byte load with float16 metadata)
@@ -277,8 +284,8 @@ struct Meta {
       s0 = make_float4(half_lo_to_float(h.x), half_hi_to_float(h.x), half_lo_to_float(h.y), half_hi_to_float(h.y));
       s1 = make_float4(half_lo_to_float(h.z), half_hi_to_float(h.z), half_lo_to_float(h.w), half_hi_to_float(h.w));
     } else {
-      s0 = *reinterpret_cast<const float4*>(a + 16 * t);
-      s1 = *reinterpret_cast<const float4*>(a + 16 * t + 16);
+      s0 = *reinterpret_cast<const float4*>(a + 16 * vmeta_row(t));       // the pair's other row
+      s1 = *reinterpret_cast<const float4*>(a + 16 * vmeta_row(t + 1));   // when bit 3 of t is set
     }
   }
 };

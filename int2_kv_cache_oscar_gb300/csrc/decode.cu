@@ -334,6 +334,16 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     // bit-position weights of this lane's k-rows: 2^p for the score zero term,
     // 2^(Fv - p) for the value factors
     float zwk[4], fsc[4];
+    // lane-constant parts of the swizzled shared-memory columns (token bit 3
+    // is fixed for every access below): probability rows (pb_col) and the
+    // float32 value scale / zero rows (vmeta_row), each relative to its
+    // 16-token block
+    const int pbs0 = g ^ (8 * ((tig >> 1) & 1));                      // row tig, token g
+    const int pbs1 = (g + 8) ^ (8 * ((tig >> 1) & 1));                // row tig, token g + 8
+    const int pbl = (2 * tig + 8 * half) ^ (8 * ((hb >> 1) & 1));     // row hb, tokens 2 tig + 8 half, + 1
+    const int vsl0 = 16 * (2 * tig + 8 * half + half);                // bytes: token 2 tig + 8 half
+    const int vsl1 = 16 * (2 * tig + 8 * half + 1 - half);            //        token 2 tig + 8 half + 1
+    const int vzl0 = 16 * g, vzl1 = 16 * ((g + 8) ^ 1);               //        tokens g, g + 8
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const int pp = half ? frag_p(2 * kk + 1) : frag_p(2 * kk);
@@ -452,10 +462,16 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const int t0 = 16 * mt + g;
-        pb[pb_col(tig, t0)] = sc[mt].x;
-        pb[pb_col(tig, t0 + 8)] = sc[mt].y;
-        const float4 z0 = MR::v4(vze, t0);
-        const float4 z1 = MR::v4(vze, t0 + 8);
+        pb[16 * mt + pbs0] = sc[mt].x;
+        pb[16 * mt + pbs1] = sc[mt].y;
+        float4 z0, z1;
+        if constexpr (M16) {
+          z0 = MR::v4(vze, t0);
+          z1 = MR::v4(vze, t0 + 8);
+        } else {
+          z0 = *reinterpret_cast<const float4*>(vze + 256 * mt + vzl0);
+          z1 = *reinterpret_cast<const float4*>(vze + 256 * mt + vzl1);
+        }
         zacc[0] = fmaf(sc[mt].x, z0.x, fmaf(sc[mt].y, z1.x, zacc[0]));
         zacc[1] = fmaf(sc[mt].x, z0.y, fmaf(sc[mt].y, z1.y, zacc[1]));
         zacc[2] = fmaf(sc[mt].x, z0.z, fmaf(sc[mt].y, z1.z, zacc[2]));
@@ -479,9 +495,15 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
 #pragma unroll
           for (int kk2 = 0; kk2 < 4; ++kk2) {
             const int t = 16 * (4 * jh + kk2) + 2 * tig + 8 * half;   // this lane's two tokens
-            const float2 pr = __fmul2_rn(*reinterpret_cast<const float2*>(pbh + pb_col(hb, t)), make_float2(fsc[kk2], fsc[kk2]));
+            const float2 pr = __fmul2_rn(*reinterpret_cast<const float2*>(pbh + 16 * (4 * jh + kk2) + pbl),
+                                         make_float2(fsc[kk2], fsc[kk2]));
             float4 s0, s1;
-            MR::v4x2(vsc, t, s0, s1);
+            if constexpr (M16) {
+              MR::v4x2(vsc, t, s0, s1);
+            } else {
+              s0 = *reinterpret_cast<const float4*>(vsc + 256 * (4 * jh + kk2) + vsl0);
+              s1 = *reinterpret_cast<const float4*>(vsc + 256 * (4 * jh + kk2) + vsl1);
+            }
 #pragma unroll
             for (int gr = 0; gr < kVGroups; ++gr) {
               const float sa = gr == 0 ? s0.x : gr == 1 ? s0.y : gr == 2 ? s0.z : s0.w;
@@ -529,8 +551,8 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const float zg = zs[mt >> 1];
-        S.pbuf[warp][tig][pb_col(tig, 16 * mt + g)] = fmaf(o_acc[mt].x, kv, zg);
-        S.pbuf[warp][tig][pb_col(tig, 16 * mt + g + 8)] = fmaf(o_acc[mt].y, kv, zg);
+        S.pbuf[warp][tig][16 * mt + pbs0] = fmaf(o_acc[mt].x, kv, zg);
+        S.pbuf[warp][tig][16 * mt + pbs1] = fmaf(o_acc[mt].y, kv, zg);
       }
     }
     named_bar_sync(1, kConsumers * 32);

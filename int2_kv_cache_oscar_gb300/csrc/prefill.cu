@@ -371,7 +371,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int t = 64 * hh + 8 * ntl + 2 * tig + e;
-          const float4 z4 = MR::v4(vze, t);
+          // float32 zeros: token t is in row t ^ 1 when bit 3 (ntl & 1) is set
+          const float4 z4 = M16 ? MR::v4(vze, t)
+                                : *reinterpret_cast<const float4*>(vze + 16 * (64 * hh + 8 * ntl + 2 * tig +
+                                                                              (e ^ (ntl & 1))));
           zacc[0][0] = fmaf(sc[ntl][e], z4.x, zacc[0][0]);
           zacc[0][1] = fmaf(sc[ntl][e], z4.y, zacc[0][1]);
           zacc[0][2] = fmaf(sc[ntl][e], z4.z, zacc[0][2]);
@@ -395,8 +398,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int kk = 0; kk < 4; ++kk) {
         const int t0 = 64 * hh + 16 * kk + 2 * tig, t1 = t0 + 8;
         float4 sa, sb, sc4, sd;
-        MR::v4x2(vsc, t0, sa, sb);
-        MR::v4x2(vsc, t1, sc4, sd);
+        if constexpr (M16) {
+          MR::v4x2(vsc, t0, sa, sb);
+          MR::v4x2(vsc, t1, sc4, sd);
+        } else {   // float32 rows: t0, t0 + 1 in place (bit 3 clear); t1, t1 + 1 swapped (bit 3 set)
+          sa = *reinterpret_cast<const float4*>(vsc + 16 * t0);
+          sb = *reinterpret_cast<const float4*>(vsc + 16 * t0 + 16);
+          sc4 = *reinterpret_cast<const float4*>(vsc + 16 * t1 + 16);
+          sd = *reinterpret_cast<const float4*>(vsc + 16 * t1);
+        }
         const float* p00 = sc[2 * kk];       // tokens t0, t0+1: rows g (0, 1), g + 8 (2, 3)
         const float* p01 = sc[2 * kk + 1];   // tokens t1, t1+1
         const float f0 = fsc[kk][0], f1 = fsc[kk][1];

@@ -241,8 +241,9 @@ __global__ void __launch_bounds__(kQThreads, 2)
         *reinterpret_cast<uint32_t*>(blk + B::kVScale + 8 * t + 4 * half) = pack_half2(sv[0], sv[1]);
         *reinterpret_cast<uint32_t*>(blk + B::kVZero + 8 * t + 4 * half) = pack_half2(zv[0], zv[1]);
       } else {
-        *reinterpret_cast<float2*>(blk + kOffVScale + 16 * t + 8 * half) = make_float2(sv[0], sv[1]);
-        *reinterpret_cast<float2*>(blk + kOffVZero + 16 * t + 8 * half) = make_float2(zv[0], zv[1]);
+        const int vr = 16 * vmeta_row(t) + 8 * half;
+        *reinterpret_cast<float2*>(blk + kOffVScale + vr) = make_float2(sv[0], sv[1]);
+        *reinterpret_cast<float2*>(blk + kOffVZero + vr) = make_float2(zv[0], zv[1]);
       }
     }
 

@@ -19,6 +19,8 @@ G = 128
 BLOCK_BYTES = 13824
 OFF_KCODES, OFF_KSCALE, OFF_KZERO, OFF_KNORM, OFF_VCODES = 0, 4096, 4608, 5120, 5632
 OFF_VSCALE, OFF_VZERO = 9728, 11776
+# float32 value scales / zeros: token t is stored in row t ^ ((t >> 3) & 1)
+VMETA_ROW = np.array([t ^ ((t >> 3) & 1) for t in range(128)])
 # the same block with float16 metadata (meta_bits = 16)
 BLOCK_BYTES16 = 11008
 OFF16_KSCALE, OFF16_KZERO, OFF16_KNORM, OFF16_VCODES = 4096, 4352, 4608, 4864
@@ -94,8 +96,9 @@ def parse_block(raw: np.ndarray, meta_bits: int = 32) -> dict:
     kzero = raw[OFF_KZERO:OFF_KZERO + 512].view("<f4").copy()
     knorm = raw[OFF_KNORM:OFF_KNORM + 512].view("<f4").copy()
     vcodes_t = unpack_fragment(raw[OFF_VCODES:OFF_VCODES + 4096].view("<u4"), "v")  # [ch, token]
-    vscale = raw[OFF_VSCALE:OFF_VSCALE + 2048].view("<f4").reshape(G, 4).copy()
-    vzero = raw[OFF_VZERO:OFF_VZERO + 2048].view("<f4").reshape(G, 4).copy()
+    rows = VMETA_ROW                                                               # token t in row rows[t]
+    vscale = raw[OFF_VSCALE:OFF_VSCALE + 2048].view("<f4").reshape(G, 4)[rows].copy()
+    vzero = raw[OFF_VZERO:OFF_VZERO + 2048].view("<f4").reshape(G, 4)[rows].copy()
     return dict(kcodes=kcodes, kscale=kscale, kzero=kzero, knorm=knorm,
                 vcodes=vcodes_t.T.copy(), vscale=vscale, vzero=vzero)
 

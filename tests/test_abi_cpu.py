@@ -156,8 +156,11 @@ def test_layout_reader_fp32_block():
     raw[4608:5120] = kz.view(np.uint8)
     raw[5120:5632] = kn.view(np.uint8)
     raw[5632:9728] = layout.pack_fragment(vc.T, "v").view(np.uint8)
-    raw[9728:11776] = vs.reshape(-1).view(np.uint8)
-    raw[11776:13824] = vz.reshape(-1).view(np.uint8)
+    rows = [t ^ ((t >> 3) & 1) for t in range(128)]          # header: token t in row t ^ ((t >> 3) & 1)
+    vs_st, vz_st = np.empty_like(vs), np.empty_like(vz)
+    vs_st[rows], vz_st[rows] = vs, vz
+    raw[9728:11776] = vs_st.reshape(-1).view(np.uint8)
+    raw[11776:13824] = vz_st.reshape(-1).view(np.uint8)
     b = layout.parse_block(raw)
     assert np.array_equal(b["kcodes"], kc) and np.array_equal(b["vcodes"], vc)
     for name, ref in [("kscale", ks), ("kzero", kz), ("knorm", kn), ("vscale", vs), ("vzero", vz)]:
