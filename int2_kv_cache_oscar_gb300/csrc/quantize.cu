@@ -119,6 +119,14 @@ __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
 
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) { return make_float2(bf16_lo(u), bf16_hi(u)); }
 
+// a * m + c on the integer multiply-add path (m is opaque to the compiler, so
+// the packing below stays off the shift / logic pipe)
+__device__ __forceinline__ uint32_t imad(uint32_t a, uint32_t m, uint32_t c) {
+  uint32_t d;
+  asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(m), "r"(c));
+  return d;
+}
+
 // 32 bytes from global memory (32-byte aligned p), read once: each load of
 // the pair's two threads fills whole 32-byte sectors.
 __device__ __forceinline__ void ld_row32(const void* p, uint4& lo, uint4& hi) {
@@ -146,6 +154,9 @@ __global__ void __launch_bounds__(kQThreads, 2)
   QuantSmem& S = *reinterpret_cast<QuantSmem*>(smem_raw);
   const int head = blockIdx.y;
   const int tid = threadIdx.x;
+  // 1 << 2i for the packing multiply-adds; the zero term keeps them opaque
+  const uint32_t zero = (uint32_t)tid >> 31;
+  const uint32_t p4 = 4u | zero, p16 = 16u | zero, p64 = 64u | zero;
   const PackedTask T = plan.t[blockIdx.x];
   const int hkv = plan.hkv;
   const int64_t sh = (int64_t)T.slot() * hkv + head;
@@ -231,7 +242,8 @@ __global__ void __launch_bounds__(kQThreads, 2)
                   (clamped_code(c23.y) << 6);
             } else {
               // low bytes are the codes (the float bits' constant part has a zero low byte)
-              b = (c01.x & 0xffu) | ((c01.y & 0xffu) << 2) | ((c23.x & 0xffu) << 4) | ((c23.y & 0xffu) << 6);
+              // low byte: the codes (the float bits' constant part has a zero low byte)
+              b = imad(c23.y, p64, imad(c23.x, p16, imad(c01.y, p4, c01.x)));
             }
             S.vb[vb_row(gi * 8 + 2 * i + qq) + pt] = (uint8_t)b;
           }
