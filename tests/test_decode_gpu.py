@@ -205,3 +205,43 @@ def test_bf16_reference_decode_gqa8():
         ref = O.attention_exact(qn[0, 8 * j:8 * j + 8], U.f64(k[:, j]), U.f64(v[:, j]))
         P.assert_decode(got[0, 8 * j:8 * j + 8], ref, f"bf16 ref gqa 8 head {j}")
 
+
+
+def test_decode_captured_in_cuda_graph():
+    """A decode call enqueues only kernel launches (no synchronisation, no
+    allocation), so it can be captured in a CUDA graph; the plan (lengths,
+    unit split) is fixed at capture.  Replays of the graph with new query
+    values in the same buffer must equal eager calls bit for bit."""
+    lens = [3000, 129, 8192 + 50]
+    gen = torch.Generator().manual_seed(31)
+    ks, vs = [], []
+    for L in lens:
+        k, v = W.make_sequence_kv(L, 8, W.LLAMA_RECIPE, gen)
+        ks.append(k)
+        vs.append(v)
+    cache = U.lib().OscarCache(3, 8, max(lens))
+    U.append_all(cache, [0, 1, 2], ks, vs, chunk=1000)
+    hq, B = 32, len(lens)
+    q = torch.empty((B, hq, 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(q)
+    ws = cache.workspace(B, hq)
+    q.copy_(W.make_q(B, hq, seed=32))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        cache.decode([0, 1, 2], q, hq, out, ws)          # warm the launch path outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cache.decode([0, 1, 2], q, hq, out, ws)
+    for seed in (33, 34):
+        q.copy_(W.make_q(B, hq, seed=seed))
+        g.replay()
+        torch.cuda.synchronize()
+        replayed = out.clone()
+        eager = torch.empty_like(out)
+        cache.decode([0, 1, 2], q, hq, eager, cache.workspace(B, hq))
+        torch.cuda.synchronize()
+        assert torch.equal(replayed, eager), f"seed {seed}"
+    U.lib().oscar_cache_check(cache.handle)
