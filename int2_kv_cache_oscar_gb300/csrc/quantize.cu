@@ -9,7 +9,8 @@
 // cited in the qiita.com NOVA-KV article).
 //
 // One CTA = one (group, KV head), 256 threads; the thread pair (2t, 2t+1)
-// owns token t, each thread 64 of its channels.
+// owns token t, each thread 64 of its channels (128 bytes of the key row and
+// of the value row, read with 32-byte loads when the inputs allow).
 //   1. V: per 32-channel group min/max (on packed bf16 pairs: exact), s =
 //      (max-min)/3, z = min, codes; codes go to shared memory (transposed,
 //      four channels per byte), s/z to the block.  The key row is already
