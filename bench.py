@@ -448,16 +448,21 @@ def gpu_arm(args, rank, world):
             qc = torch.randn((C, HQ, D), generator=genp, device="cuda").to(torch.bfloat16)
             oc = torch.empty_like(qc)
             lc = torch.empty((C, HQ), dtype=torch.float32, device="cuda")
-            tp, _ = timer.run(lambda: O_.oscar_prefill_attention(c.handle, 0, qc, HQ, 0.0, oc, lc), K, Wm)
-            launches += K
+            pnb = O_.oscar_prefill_workspace_bytes(c.handle, 0, C, HQ)
+            pws = torch.empty(max(pnb, 16), dtype=torch.uint8, device="cuda") if pnb else None
+            parts = pnb // (C * HQ * 528) if pnb else 1       # records: Hkv x (C x HQ / Hkv) rows x 528 B
+            tp, _ = timer.run(lambda: O_.oscar_prefill_attention(c.handle, 0, qc, HQ, 0.0, oc, lc, workspace=pws),
+                              K, Wm)
+            launches += K * (2 if parts > 1 else 1)        # split history: the parts, then the merge
             flops = 4.0 * C * HQ * L * D                    # q.k and p.v, 2 flops per multiply-add
             tf = flops / (tp * 1e-6) / 1e12
             bf16_peak = read_peak_tflops()
             out["prefill"] = {"chunk": C, "ctx": L, "us": round(tp, 1), "tflops": round(tf, 1),
                               "bound": "tensor", "peak_tflops": bf16_peak,
                               "frac_of_bf16_peak": round(tf / bf16_peak, 3) if bf16_peak else None,
+                              "history_parts": parts,
                               "note": "fp16 hi+lo operands: 2 mma per product term"}
-            del c, ks, vs, qc, oc, lc
+            del c, ks, vs, qc, oc, lc, pws
             torch.cuda.empty_cache()
 
         # ---------------- ragged serving stream: 8 sequences, 4K..128K
@@ -534,8 +539,10 @@ def profile_case(args):
         qc = torch.randn((C, HQ, D), generator=genp, device="cuda").to(torch.bfloat16)
         oc = torch.empty_like(qc)
         lc = torch.empty((C, HQ), dtype=torch.float32, device="cuda")
+        pnb = O_.oscar_prefill_workspace_bytes(c.handle, 0, C, HQ)
+        pws = torch.empty(pnb, dtype=torch.uint8, device="cuda") if pnb else None
         for _ in range(args.steps):
-            O_.oscar_prefill_attention(c.handle, 0, qc, HQ, 0.0, oc, lc)
+            O_.oscar_prefill_attention(c.handle, 0, qc, HQ, 0.0, oc, lc, workspace=pws)
         torch.cuda.synchronize()
         O_.oscar_cache_check(c.handle)
         print("profile prefill done")

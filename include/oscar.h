@@ -243,11 +243,27 @@ oscar_status oscar_append_decode(oscar_cache* cache, int32_t n_seqs, const int32
  *   q, out and lse may be device or page-locked host memory (see
  *   oscar_decode_attention); other memory fails with OSCAR_ERR_INVALID_ARG.
  *   softmax_scale  0 means 1 / sqrt(128)
- * Any GQA ratio.  Needs no workspace.  The sequence must be non-empty.
+ *   workspace    NULL, or device memory (16-byte aligned) of workspace_bytes
+ *                for partial results: the history's groups are then split
+ *                into parts processed by separate CTAs and merged by a
+ *                second kernel, so that the CTAs fill whole waves of SMs.
+ *                As many parts are used as fit, up to the number that
+ *                oscar_prefill_workspace_bytes sizes; NULL (or too small for
+ *                two parts) runs unsplit.  Results agree within rounding.
+ * Any GQA ratio.  The sequence must be non-empty.
  */
 oscar_status oscar_prefill_attention(oscar_cache* cache, int32_t seq, int32_t n_q, const void* q,
                                      int32_t num_q_heads, float softmax_scale, void* out, float* lse,
-                                     void* stream);
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes that let oscar_prefill_attention split the history of
+ * sequence `seq` (at its current length) for n_q queries of num_q_heads
+ * heads: parts x Hkv x n_q x (num_q_heads / Hkv) x 528 bytes, 0 when no
+ * split pays off (short histories, or rows that already fill the SMs).
+ */
+oscar_status oscar_prefill_workspace_bytes(const oscar_cache* cache, int32_t seq, int32_t n_q,
+                                           int32_t num_q_heads, size_t* out_bytes);
 
 /*
  * Decode that allocates nothing and takes no workspace.  The OScaR pages have

@@ -147,12 +147,19 @@ struct PrefillParams {
   int64_t blocks_off;
   int64_t windows_off;
   float scale_log2;      // softmax_scale * log2(e)
-  int32_t pad;
+  int32_t n_parts;       // the groups are split into this many parts (grid.z); 1: no split
   const uint16_t* q;     // [n_q, hq, d] bf16
   uint16_t* out;         // [n_q, hq, d] bf16
   float* lse;            // [n_q, hq] fp32 natural-log log-sum-exp, or NULL
   uint32_t* err_word;
+  // n_parts > 1: partial records [part][KV head][row][kPrefillRecFloats]
+  // (o unnormalised = sum p v, then m in log2 units and l), merged by a
+  // second kernel
+  float* parts;
 };
+
+// Floats of one partial prefill record (o[128], m, l, 2 pad).
+constexpr int kPrefillRecFloats = 132;
 
 cudaError_t launch_prefill(const PrefillParams& p, const uint8_t* arena, bool meta16, cudaStream_t stream);
 

@@ -569,8 +569,43 @@ oscar_status oscar_append_decode(oscar_cache* c, int32_t n_seqs, const int32_t* 
   }
 }
 
+// Parts the prefill splits a history of ng groups into, for CTAs of 128 rows
+// over hkv KV heads on `sms` SMs (one CTA per SM): the fewest parts whose
+// CTAs fill at least 95 % of their waves, with at least 8 groups a part, else
+// the best fill among those; capped by the workspace (max_parts).
+static int prefill_parts(int64_t rows, int hkv, int ng, int sms, int64_t max_parts) {
+  if (ng < 16 || sms < 1 || max_parts < 2) return 1;
+  const int64_t ctas = ((rows + 127) / 128) * hkv;
+  int best = 1;
+  double best_fill = 0.0;
+  for (int parts = 1; parts <= 32 && parts <= ng / 8 && parts <= max_parts; ++parts) {
+    const int64_t n = ctas * parts;
+    const double fill = (double)n / (double)(((n + sms - 1) / sms) * sms);
+    if (fill > best_fill + 1e-9) {
+      best_fill = fill;
+      best = parts;
+    }
+    if (fill >= 0.95) break;
+  }
+  return best;
+}
+
+oscar_status oscar_prefill_workspace_bytes(const oscar_cache* c, int32_t seq, int32_t n_q, int32_t num_q_heads,
+                                           size_t* out_bytes) {
+  if (!c || !out_bytes) return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+  if (seq < 0 || seq >= c->cfg.max_batch) return fail(OSCAR_ERR_INVALID_ARG, "seq %d out of range", seq);
+  const int hkv = c->cfg.num_kv_heads;
+  if (n_q < 1 || num_q_heads < hkv || num_q_heads % hkv != 0)
+    return fail(OSCAR_ERR_INVALID_ARG, "bad n_q / num_q_heads");
+  const int64_t rows = (int64_t)n_q * (num_q_heads / hkv);
+  const int parts = prefill_parts(rows, hkv, c->len[seq] / kGroup, num_sms(c->cfg.device), 32);
+  *out_bytes = parts > 1 ? (size_t)parts * hkv * rows * kPrefillRecFloats * sizeof(float) : 0;
+  return ok();
+}
+
 oscar_status oscar_prefill_attention(oscar_cache* c, int32_t seq, int32_t n_q, const void* q, int32_t num_q_heads,
-                                     float softmax_scale, void* out, float* lse, void* stream) {
+                                     float softmax_scale, void* out, float* lse, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
   if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
   if (seq < 0 || seq >= c->cfg.max_batch) return fail(OSCAR_ERR_INVALID_ARG, "seq %d out of range", seq);
   if (n_q < 1) return fail(OSCAR_ERR_INVALID_ARG, "n_q must be >= 1");
@@ -578,8 +613,8 @@ oscar_status oscar_prefill_attention(oscar_cache* c, int32_t seq, int32_t n_q, c
   const int hkv = c->cfg.num_kv_heads;
   if (num_q_heads < hkv || num_q_heads % hkv != 0)
     return fail(OSCAR_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of Hkv");
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(lse, 4))
-    return fail(OSCAR_ERR_INVALID_ARG, "q and out must be 16-byte aligned, lse 4-byte aligned");
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(lse, 4) || !aligned(workspace, 16))
+    return fail(OSCAR_ERR_INVALID_ARG, "q, out and workspace must be 16-byte aligned, lse 4-byte aligned");
   if (!(softmax_scale >= 0.0f) || std::isinf(softmax_scale))
     return fail(OSCAR_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
   const int L = c->len[seq];
@@ -606,6 +641,18 @@ oscar_status oscar_prefill_attention(oscar_cache* c, int32_t seq, int32_t n_q, c
   P.err_word = reinterpret_cast<uint32_t*>(c->arena);
   DeviceGuard dg(c->cfg.device);
   if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+  // split the history when the workspace holds the partial records
+  const size_t rec_set = (size_t)hkv * rows * kPrefillRecFloats * sizeof(float);   // one part's records
+  P.n_parts = workspace != nullptr ? prefill_parts(rows, hkv, P.ng, num_sms(c->cfg.device),
+                                                   (int64_t)(workspace_bytes / rec_set))
+                                   : 1;
+  if (P.n_parts > 1) {
+    float* wd = nullptr;
+    const oscar_status sw = device_view_as(static_cast<float*>(workspace), "workspace", c->cfg.device, &wd,
+                                           /*allow_host=*/false);
+    if (sw != OSCAR_OK) return sw;
+    P.parts = wd;
+  }
   {
     // q, out and lse: device or page-locked host memory (plain loads and stores)
     oscar_status sv;

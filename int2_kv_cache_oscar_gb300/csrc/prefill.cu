@@ -171,8 +171,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int j = blockIdx.y;                 // KV head
-  const int ng = p.ng;
-  const uint8_t* blocks = arena + p.blocks_off + ((int64_t)p.slot * p.hkv + j) * p.max_groups * (int64_t)B::kBytes;
+  // this CTA's part of the history: groups [g_begin, g_end); the last part
+  // also takes the window
+  const int part = blockIdx.z;
+  const int g_begin = (int)(((int64_t)part * p.ng) / p.n_parts);
+  const int g_end = (int)(((int64_t)(part + 1) * p.ng) / p.n_parts);
+  const int ng = g_end - g_begin;
+  const uint8_t* blocks = arena + p.blocks_off +
+                          (((int64_t)p.slot * p.hkv + j) * p.max_groups + g_begin) * (int64_t)B::kBytes;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPfStages; ++s) {
@@ -461,7 +467,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   }
 
   // ---- the window (bf16 rows after the last group), on bf16 tensor cores
-  const int wlen = p.wlen;
+  const int wlen = part == p.n_parts - 1 ? p.wlen : 0;
   if (wlen > 0) {   // every warp is done with the ring (barrier above)
     uint16_t* wk = reinterpret_cast<uint16_t*>(S.stage[0]);
     uint16_t* wv = wk + kGroup * kHeadDim;
@@ -567,6 +573,23 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       zs[rr][gv] = z;
     }
   }
+  if (p.n_parts > 1) {
+    // partial record of each of the lane's rows: o unnormalised, m, l
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int row = row0 + g + 8 * rr;
+      if (row >= p.rows) continue;
+      float* rec = p.parts + (((int64_t)part * p.hkv + j) * p.rows + row) * kPrefillRecFloats;
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        const float z = zs[rr][nt >> 2];
+        *reinterpret_cast<float2*>(rec + 8 * nt + 2 * tig) =
+            make_float2(fmaf(oacc[nt][2 * rr], kv, z), fmaf(oacc[nt][2 * rr + 1], kv, z));
+      }
+      if (tig == 0) *reinterpret_cast<float2*>(rec + kHeadDim) = make_float2(m_run[rr], rr ? l1 : l0);
+    }
+    return;
+  }
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
     const int row = row0 + g + 8 * rr;
@@ -586,6 +609,43 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   }
 }
 
+// Merge of the history parts: one warp per (KV head, row), 4 channels per
+// lane.  m* = max m_i, l = sum 2^(m_i - m*) l_i, o = sum 2^(m_i - m*) o_i / l,
+// lse = (m* + log2 l) ln 2.
+constexpr int kPfMergeWarps = 8;
+
+__global__ void __launch_bounds__(kPfMergeWarps * 32)
+    prefill_merge_kernel(const __grid_constant__ PrefillParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (int64_t)blockIdx.x * kPfMergeWarps + (threadIdx.x >> 5);   // KV head * rows + row
+  if (gw >= (int64_t)p.hkv * p.rows) return;
+  const int j = (int)(gw / p.rows), row = (int)(gw % p.rows);
+  const int64_t stride = (int64_t)p.hkv * p.rows * kPrefillRecFloats;   // between parts
+  const float* rec = p.parts + gw * kPrefillRecFloats;
+  float M = -INFINITY;
+  for (int i = 0; i < p.n_parts; ++i) M = fmaxf(M, rec[i * stride + kHeadDim]);
+  float l = 0.0f;
+  float4 o = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  for (int i = 0; i < p.n_parts; ++i) {
+    const float* r = rec + i * stride;
+    const float mi = r[kHeadDim];
+    const float w = mi == -INFINITY ? 0.0f : exp2f(mi - M);
+    l = fmaf(w, r[kHeadDim + 1], l);
+    const float4 v = *reinterpret_cast<const float4*>(r + 4 * lane);
+    o.x = fmaf(w, v.x, o.x);
+    o.y = fmaf(w, v.y, o.y);
+    o.z = fmaf(w, v.z, o.z);
+    o.w = fmaf(w, v.w, o.w);
+  }
+  const float inv = 1.0f / l;
+  const int qi = row / p.gqa, h = j * p.gqa + row % p.gqa;
+  uint2 packed;
+  packed.x = f32_to_bf16_bits(o.x * inv) | (f32_to_bf16_bits(o.y * inv) << 16);
+  packed.y = f32_to_bf16_bits(o.z * inv) | (f32_to_bf16_bits(o.w * inv) << 16);
+  *reinterpret_cast<uint2*>(p.out + ((int64_t)qi * p.hq + h) * kHeadDim + 4 * lane) = packed;
+  if (lane == 0 && p.lse != nullptr) p.lse[(int64_t)qi * p.hq + h] = (M + log2f(l)) * 0.69314718055994530942f;
+}
+
 }  // namespace
 
 namespace {
@@ -595,8 +655,12 @@ cudaError_t launch_prefill_t(const PrefillParams& p, const uint8_t* arena, cudaS
   const int smem = (int)sizeof(PfSmem);
   cudaError_t e = ensure_smem_attr(prefill_int2_kernel<M16>, smem, attr_done);
   if (e != cudaSuccess) return e;
-  const dim3 grid((p.rows + kPfRows - 1) / kPfRows, p.hkv);
+  const dim3 grid((p.rows + kPfRows - 1) / kPfRows, p.hkv, p.n_parts);
   prefill_int2_kernel<M16><<<grid, kPfThreads, smem, stream>>>(p, arena);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.n_parts <= 1) return e;
+  const int64_t warps = (int64_t)p.hkv * p.rows;
+  prefill_merge_kernel<<<(unsigned)((warps + kPfMergeWarps - 1) / kPfMergeWarps), kPfMergeWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 }  // namespace

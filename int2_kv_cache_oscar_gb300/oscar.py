@@ -75,7 +75,8 @@ def _load() -> ctypes.CDLL:
         "oscar_set_timing_events": [P, P],
         "oscar_decode_attention_noalloc": [P, I32, I32P, P, I32, ctypes.c_float, P, P],
         "oscar_append_decode": [P, I32, I32P, P, P, P, I32, ctypes.c_float, P, P, SZ, P],
-        "oscar_prefill_attention": [P, I32, I32, P, I32, ctypes.c_float, P, P, P],
+        "oscar_prefill_attention": [P, I32, I32, P, I32, ctypes.c_float, P, P, P, SZ, P],
+        "oscar_prefill_workspace_bytes": [P, I32, I32, I32, ctypes.POINTER(SZ)],
     }
     for name, args in sigs.items():
         f = getattr(lib, name)
@@ -236,17 +237,27 @@ def oscar_append_decode(handle, seq_ids: Sequence[int], k_new: torch.Tensor, v_n
                                     workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
+def oscar_prefill_workspace_bytes(handle, seq: int, n_q: int, num_q_heads: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(_lib.oscar_prefill_workspace_bytes(handle, seq, n_q, num_q_heads, ctypes.byref(out)))
+    return out.value
+
+
 def oscar_prefill_attention(handle, seq: int, q: torch.Tensor, num_q_heads: int, softmax_scale: float,
-                            out: torch.Tensor, lse: Optional[torch.Tensor] = None, stream=None) -> None:
+                            out: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                            workspace: Optional[torch.Tensor] = None, stream=None) -> None:
     """Attention of a chunk's queries q [n_q, num_q_heads, 128] over the
     sequence's cached tokens; out gets the rows, lse (fp32 [n_q, heads]) their
-    log-sum-exp."""
+    log-sum-exp.  With a workspace (uint8, see oscar_prefill_workspace_bytes)
+    the history is split across more CTAs and merged."""
     qp = _buf(q, torch.bfloat16, (None, num_q_heads, HEAD_DIM), "q")
     n_q = q.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel()
     _check(_lib.oscar_prefill_attention(handle, seq, n_q, qp, num_q_heads, ctypes.c_float(softmax_scale),
                                         _buf(out, torch.bfloat16, (n_q, num_q_heads, HEAD_DIM), "out"),
                                         _buf(lse, torch.float32, (n_q, num_q_heads), "lse", optional=True),
-                                        _stream(stream)))
+                                        _buf(workspace, torch.uint8, (None,), "workspace", optional=True),
+                                        ctypes.c_size_t(ws_bytes), _stream(stream)))
 
 
 def oscar_cache_bytes(handle, seq: int, kind: int) -> int:

@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 LSE_TOL = 1e-3
 
 
-def _run(L, hkv, hq, n_q, seed, scale=0.0):
+def _run(L, hkv, hq, n_q, seed, scale=0.0, split=False):
     O_ = U.lib()
     gen = torch.Generator().manual_seed(seed)
     k, v = W.make_sequence_kv(L, hkv, W.LLAMA_RECIPE, gen)
@@ -29,7 +29,12 @@ def _run(L, hkv, hq, n_q, seed, scale=0.0):
     q = torch.randn((n_q, hq, 128), generator=gen).to(torch.bfloat16)
     out = torch.empty((n_q, hq, 128), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((n_q, hq), dtype=torch.float32, device="cuda")
-    O_.oscar_prefill_attention(cache.handle, 0, q.cuda(), hq, scale, out, lse)
+    ws = None
+    if split:
+        nb = O_.oscar_prefill_workspace_bytes(cache.handle, 0, n_q, hq)
+        assert nb > 0, "expected a split history"
+        ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    O_.oscar_prefill_attention(cache.handle, 0, q.cuda(), hq, scale, out, lse, workspace=ws)
     torch.cuda.synchronize()
     O_.oscar_cache_check(cache.handle)
     arena = U.read_arena(cache)
@@ -46,7 +51,42 @@ def _run(L, hkv, hq, n_q, seed, scale=0.0):
         e = float(np.abs(l_gpu - l_ref).max())
         assert e <= LSE_TOL, f"L={L} head {j}: lse error {e:.2e}"
         worst_lse = max(worst_lse, e)
-    print(f"prefill L={L} hkv={hkv} hq={hq} n_q={n_q}: max|o err|={worst:.2e} max|lse err|={worst_lse:.2e}")
+    print(f"prefill L={L} hkv={hkv} hq={hq} n_q={n_q} split={split}: max|o err|={worst:.2e} "
+          f"max|lse err|={worst_lse:.2e}")
+    return out, lse
+
+
+@pytest.mark.parametrize("L", [8192 + 100, 8192, 2048 + 1])
+def test_prefill_split_history(L):
+    """With a workspace the history is split into parts (separate CTAs) and
+    merged; the rows still meet the oracle's rule, and agree with the unsplit
+    call within rounding (the merge changes only the summation order)."""
+    o1, l1 = _run(L, hkv=2, hq=8, n_q=37, seed=91, split=True)
+    o0, l0 = _run(L, hkv=2, hq=8, n_q=37, seed=91)
+    a, b = o1.float(), o0.float()
+    assert bool(((a - b).abs() <= 2e-3 + b.abs() * 2.0 ** -7).all())     # within one bf16 ulp (+ 2e-3)
+    assert float((l1 - l0).abs().max()) <= 1e-4
+
+
+def test_prefill_workspace_too_small_runs_unsplit():
+    O_ = U.lib()
+    gen = torch.Generator().manual_seed(95)
+    k, v = W.make_sequence_kv(4096, 2, W.LLAMA_RECIPE, gen)
+    cache = O_.OscarCache(1, 2, 4096)
+    U.append_all(cache, [0], [k], [v])
+    q = torch.randn((5, 8, 128), generator=gen).to(torch.bfloat16).cuda()
+    nb = O_.oscar_prefill_workspace_bytes(cache.handle, 0, 5, 8)
+    assert nb > 0
+    out_a, out_b = torch.empty_like(q), torch.empty_like(q)
+    O_.oscar_prefill_attention(cache.handle, 0, q, 8, 0.0, out_a)
+    one_part = 2 * 5 * 4 * 528                       # Hkv x rows x a 528-byte record
+    small = torch.empty(one_part + 16, dtype=torch.uint8, device="cuda")   # room for one part, not two
+    O_.oscar_prefill_attention(cache.handle, 0, q, 8, 0.0, out_b, workspace=small)
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, out_b)
+    with pytest.raises(O_.OscarError):      # host memory is not a workspace
+        O_.oscar_prefill_attention(cache.handle, 0, q, 8, 0.0, out_b,
+                                   workspace=torch.empty(nb, dtype=torch.uint8).pin_memory())
 
 
 @pytest.mark.parametrize("L", [8192 + 100, 1024, 100, 129, 1])
