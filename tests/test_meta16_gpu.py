@@ -112,14 +112,18 @@ def test_meta16_prefill_and_fused_step():
     q = torch.randn((n_q, hq, 128), generator=gen).to(torch.bfloat16)
     out = torch.empty((n_q, hq, 128), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((n_q, hq), dtype=torch.float32, device="cuda")
-    O_.oscar_prefill_attention(c.handle, 0, q.cuda(), hq, 0.0, out, lse)
     arena = U.read_arena(c)
-    got, gl, qn = U.f64(out), lse.cpu().numpy(), U.f64(q)
-    for j in range(2):
-        rows = qn[:, 4 * j:4 * j + 4].reshape(-1, 128)
-        o_ref, l_ref = O.history_attention(rows, U.gpu_head(c, arena, 0, j))
-        P.assert_decode(got[:, 4 * j:4 * j + 4].reshape(-1, 128), o_ref, f"prefill head {j}")
-        assert np.abs(gl[:, 4 * j:4 * j + 4].reshape(-1) - l_ref).max() <= 1e-3
+    qn = U.f64(q)
+    nb = O_.oscar_prefill_workspace_bytes(c.handle, 0, n_q, hq)
+    assert nb > 0                                   # 16 groups: the history splits
+    for ws in (None, torch.empty(nb, dtype=torch.uint8, device="cuda")):
+        O_.oscar_prefill_attention(c.handle, 0, q.cuda(), hq, 0.0, out, lse, workspace=ws)
+        got, gl = U.f64(out), lse.cpu().numpy()
+        for j in range(2):
+            rows = qn[:, 4 * j:4 * j + 4].reshape(-1, 128)
+            o_ref, l_ref = O.history_attention(rows, U.gpu_head(c, arena, 0, j))
+            P.assert_decode(got[:, 4 * j:4 * j + 4].reshape(-1, 128), o_ref, f"prefill head {j} split {ws is not None}")
+            assert np.abs(gl[:, 4 * j:4 * j + 4].reshape(-1) - l_ref).max() <= 1e-3
     # fused decode step against separate calls on a twin cache
     c2, _, _ = _cache([2048 + 50], 2, seed=95)
     kn = torch.randn((1, 2, 128), generator=gen).to(torch.bfloat16).cuda()
