@@ -245,3 +245,19 @@ def test_decode_captured_in_cuda_graph():
         torch.cuda.synchronize()
         assert torch.equal(replayed, eager), f"seed {seed}"
     U.lib().oscar_cache_check(cache.handle)
+
+
+def test_sixteen_kv_heads():
+    """16 KV heads (GQA 4, 64 query heads): quantise and decode across the
+    wider head dimension of every launch, two ragged sequences."""
+    lens = [2 * 128 + 33, 5 * 128]
+    gen = torch.Generator().manual_seed(41)
+    ks, vs = [], []
+    for L in lens:
+        k, v = W.make_sequence_kv(L, 16, W.LLAMA_RECIPE, gen)
+        ks.append(k)
+        vs.append(v)
+    cache = U.lib().OscarCache(2, 16, 1024)
+    U.append_all(cache, [0, 1], ks, vs, chunk=200)
+    q = W.make_q(2, 64, seed=42)
+    _check(cache, [0, 1], ks, vs, q, 64, what="16 KV heads")

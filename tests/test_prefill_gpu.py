@@ -120,3 +120,8 @@ def test_prefill_bad_args():
     with pytest.raises(O_.OscarError) as e:
         O_.oscar_prefill_attention(cache.handle, 5, q, 8, 0.0, out)     # slot out of range
     assert e.value.status == O_.OSCAR_ERR_INVALID_ARG
+
+
+def test_prefill_gqa8():
+    """8 query heads per KV head (rows = queries x 8 per KV head)."""
+    _run(2048 + 40, hkv=2, hq=16, n_q=11, seed=97)
