@@ -28,7 +28,11 @@
 //     codes, whose words are the B fragments of 8-channel tiles;
 //   * online softmax in the log2 domain per row; value zeros and the key
 //     zero term on the CUDA cores;
-//   * the window last, on bf16 mma (q and k are exact bf16; P as bf16 hi + lo).
+//   * the window last, on bf16 mma (q and k are exact bf16; P as bf16 hi + lo);
+//   * with a workspace, grid.z splits the history's groups into parts (the
+//     last part also takes the window) so that the CTAs fill whole waves of
+//     SMs; each part writes per-row records (o unnormalised, m, l) that
+//     prefill_merge_kernel combines.
 #include <cstddef>
 
 #include "common.cuh"
