@@ -32,6 +32,22 @@ def test_header_declares_the_path_calls():
         assert n in names
 
 
+def test_header_is_plain_c(tmp_path):
+    """The boundary is a C ABI: the header compiles as strict C99 on its own
+    (no C++ or CUDA types leak into the declarations)."""
+    import shutil
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "oscar.h"\nint main(void) { oscar_cache* c = 0; size_t n = 0;\n'
+                   '  return (int)(oscar_cache_bytes(c, -1, 0, &n) == OSCAR_OK); }\n')
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", inc, "-c", str(src),
+                        "-o", str(tmp_path / "use_header.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_every_declared_symbol_is_exported(O):
     lib = O.raw_library()
     missing = [n for n in _declared() if not hasattr(lib, n)]
