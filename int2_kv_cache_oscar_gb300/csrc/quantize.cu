@@ -76,16 +76,17 @@ __device__ __forceinline__ int kq_index(int c) { return (c >> 1) + (c >> 5); }
 // fl32(fl32(x - z) * inv) + 1.5 * 2^23, i.e. 0x4B400000 + code.  x >= z and
 // x <= max keep the product in [0, 3] (s == 0 gives inv = 0, code 0), so no
 // clamp is needed and the code is the low byte.  Every step is rounded, so an
-// exact tie k + 1/2 goes to the even code: the difference is one packed add
-// (a packed add cannot absorb the product before it, see the k_hat scaling),
-// the product and the magic add are scalar __fmul_rn / __fadd_rn, which are
-// never fused into a multiply-add.  A packed multiply is not used here: the
-// compiler may fuse it with a following packed add even when both carry an
-// explicit rounding mode, which moves ties to the unrounded product's side.
+// exact tie k + 1/2 goes to the even code: the difference and the magic add
+// are packed adds (a packed add cannot absorb the product before it, see the
+// k_hat scaling), the products scalar __fmul_rn, which is never fused into a
+// multiply-add.  A packed multiply is not used here: the compiler may fuse it
+// with a following packed add even when both carry an explicit rounding mode,
+// which moves ties to the unrounded product's side.
 __device__ __forceinline__ uint2 code_bits2(float2 x, float2 inv, float2 negz) {
   const float2 d = __fadd2_rn(x, negz);
-  const float vx = __fmul_rn(d.x, inv.x), vy = __fmul_rn(d.y, inv.y);
-  return make_uint2(__float_as_uint(__fadd_rn(vx, kMagic)), __float_as_uint(__fadd_rn(vy, kMagic)));
+  const float2 v = make_float2(__fmul_rn(d.x, inv.x), __fmul_rn(d.y, inv.y));
+  const float2 c = __fadd2_rn(v, make_float2(kMagic, kMagic));
+  return make_uint2(__float_as_uint(c.x), __float_as_uint(c.y));
 }
 
 // Key decisions of a pair, one rounding each: the float bits of
