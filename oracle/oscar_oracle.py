@@ -31,9 +31,12 @@ notes of the repository):
   key); the key is divided by it; a zero-norm key becomes the zero vector.
 * Asymmetric INT2: over the quantisation group, s = (max - min) / 3 and
   z = min, computed in float64 and stored as float32; code =
-  clamp(round_half_even((x - z) / s), 0, 3), the rounding decision taken in
-  float32 (the parameters' precision) as fl32(fl32(x - z) * fl32(1 / s));
-  s == 0 gives code 0 (dequantised value z).  Dequantised value = code * s + z.
+  clamp(round_half_even((x - z) / s), 0, 3) with (x - z) / s evaluated in
+  float64 from the exact values of the stored parameters, so that the
+  decision is the one the stored scale and zero define (an exact tie goes
+  to the even code; a value a hair below a tie goes down even where a float32
+  evaluation would round it onto the tie); s == 0 gives code 0 (dequantised
+  value z).  Dequantised value = code * s + z.
 * Keys: per channel over groups of G = 128 consecutive tokens aligned at
   absolute positions 128 g.  Values: per token over groups of 32 consecutive
   channels.
@@ -133,19 +136,17 @@ def int2_params(x_min: np.ndarray, x_max: np.ndarray, meta_bits: int = 32):
 def int2_codes(x: np.ndarray, s32: np.ndarray, z32: np.ndarray):
     """Codes and pre-rounding values of x against broadcastable s32, z32.
 
-    The rounding decision is taken in float32, the precision of the stored
-    parameters: pre = fl32(fl32(x - z) * fl32(1 / s)), every operation rounded
-    to nearest; code = clamp(round_half_even(pre), 0, 3); s == 0 gives code 0.
-    x is first rounded to float32 (exact for bf16 values).
+    pre = (x - z) / s in float64 from the exact values of the stored
+    parameters; code = clamp(round_half_even(pre), 0, 3); s == 0 gives code 0
+    (and pre 0: every x of such a group equals z).
     """
-    x32 = np.asarray(x, dtype=np.float64).astype(np.float32)
-    s = np.asarray(s32, dtype=np.float32)
-    z = np.asarray(z32, dtype=np.float32)
-    ok = s > np.float32(0)
-    inv = np.where(ok, np.float32(1) / np.where(ok, s, np.float32(1)), np.float32(0)).astype(np.float32)
-    pre = ((x32 - z).astype(np.float32) * inv).astype(np.float32)
+    x = np.asarray(x, dtype=np.float64)
+    s = np.asarray(s32, dtype=np.float64)
+    z = np.asarray(z32, dtype=np.float64)
+    ok = s > 0.0
+    pre = np.where(ok, (x - z) / np.where(ok, s, 1.0), 0.0)
     codes = np.clip(np.rint(pre), 0, MAX_CODE).astype(np.uint8)
-    return codes, pre.astype(np.float64)
+    return codes, pre
 
 
 def int2_dequant(codes: np.ndarray, s32: np.ndarray, z32: np.ndarray) -> np.ndarray:

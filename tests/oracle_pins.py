@@ -10,7 +10,8 @@ What fixes each check:
   routine, a hand-typed H_8) and its algebra (orthogonality, symmetry, the
   all-ones vector, energy spreading of a spike, norm preservation);
 * the norm identity k = n * H^T k_hat of Omni-Token Scaling;
-* a hand-derived worked example of the asymmetric INT2 quantiser;
+* hand-derived worked examples of the asymmetric INT2 quantiser, one of
+  them with quotients a hair off a tie;
 * closed forms: keys that are scaled Hadamard columns rotate to one-hot
   vectors, so their codes, scales and norms are known exactly;
 * losslessness on inputs already on the 4 levels;
@@ -136,6 +137,38 @@ def check_worked_example():
         return "worked example pre-rounding values wrong"
     if not np.array_equal(O.dequant_values(g)[0, :32], t[:, 3]):
         return "worked example dequantised values wrong"
+
+
+def check_near_tie_example():
+    """Hand-derived near-tie example (tests/golden/int2_asym_near_tie.txt):
+    the code follows the exact (x - z) / s of the stored float32 scale, also
+    where a float32 evaluation of that quotient lands on a tie."""
+    from fractions import Fraction
+    rows = []
+    with open(os.path.join(GOLDEN, "int2_asym_near_tie.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                g, x, num, den, code = line.split()
+                rows.append((g, float(x), Fraction(int(num), int(den)), int(code)))
+    names = ["A", "B", "C", "A"]
+    x = np.zeros((1, D))
+    for gi, name in enumerate(names):
+        vals = [r[1] for r in rows if r[0] == name]
+        x[0, 32 * gi:32 * gi + 32] = [vals[i % len(vals)] for i in range(32)]
+    g = O.quantize_value_group(x)
+    want_s = {"A": np.float32(11184811 / 2 ** 25), "B": np.float32(41943039 / (3 * 2 ** 25)),
+              "C": np.float32(0.5)}
+    for gi, name in enumerate(names):
+        if g.scale[0, gi] != want_s[name]:
+            return f"near-tie example: group {name} scale {g.scale[0, gi]!r}"
+        vals = [r for r in rows if r[0] == name]
+        for i in range(32):
+            _, xv, pre, code = vals[i % len(vals)]
+            if g.codes[0, 32 * gi + i] != code:
+                return f"near-tie example: group {name} x = {xv} code {g.codes[0, 32 * gi + i]} != {code}"
+            if abs(Fraction(float(g.pre[0, 32 * gi + i])) - pre) > Fraction(1, 2 ** 50) * max(pre, 1):
+                return f"near-tie example: group {name} x = {xv} pre-rounding value wrong"
 
 
 def check_value_lossless():
@@ -368,7 +401,7 @@ def check_gqa_mapping():
 ALL_CHECKS = [
     check_hadamard_scipy, check_hadamard_golden8, check_hadamard_algebra,
     check_energy_spreading, check_norm_preserved, check_norm_identity,
-    check_worked_example, check_value_lossless, check_key_onehot_closed_form,
+    check_worked_example, check_near_tie_example, check_value_lossless, check_key_onehot_closed_form,
     check_error_bound, check_constant_channel, check_group_alignment,
     check_brute_force_attention, check_single_token, check_zero_query_mean,
     check_dominant_score, check_window_only_exact, check_lossless_keys_exact,

@@ -46,6 +46,28 @@ def _codes_half_up(x, s32, z32):
     return np.clip(np.floor(pre + 0.5), 0, 3).astype(np.uint8), pre
 
 
+def _codes_fp32_reciprocal(x, s32, z32):
+    """The decision taken in float32 as fl32(fl32(x - z) * fl32(1 / s))."""
+    x32 = np.asarray(x, np.float64).astype(np.float32)
+    s = np.asarray(s32, np.float32)
+    z = np.asarray(z32, np.float32)
+    ok = s > 0
+    inv = np.where(ok, np.float32(1) / np.where(ok, s, np.float32(1)), np.float32(0)).astype(np.float32)
+    pre = ((x32 - z).astype(np.float32) * inv).astype(np.float32)
+    return np.clip(np.rint(pre), 0, 3).astype(np.uint8), pre.astype(np.float64)
+
+
+def _codes_fp32_division(x, s32, z32):
+    """The decision taken in float32 as fl32(fl32(x - z) / s)."""
+    x32 = np.asarray(x, np.float64).astype(np.float32)
+    s = np.asarray(s32, np.float32)
+    z = np.asarray(z32, np.float32)
+    ok = s > 0
+    pre = np.where(ok, (x32 - z).astype(np.float32) / np.where(ok, s, np.float32(1)), np.float32(0))
+    pre = pre.astype(np.float32)
+    return np.clip(np.rint(pre), 0, 3).astype(np.uint8), pre.astype(np.float64)
+
+
 def _dequant_no_zero(codes, s32, z32):
     return codes.astype(np.float64) * np.asarray(s32, np.float64)
 
@@ -122,6 +144,8 @@ MUTATIONS = {
     "scale_over_4_levels": ("int2_params", _params_div4),
     "codes_floor": ("int2_codes", _codes_floor),
     "codes_round_half_up": ("int2_codes", _codes_half_up),
+    "codes_fp32_reciprocal": ("int2_codes", _codes_fp32_reciprocal),
+    "codes_fp32_division": ("int2_codes", _codes_fp32_division),
     "dequant_drops_zero": ("int2_dequant", _dequant_no_zero),
     "key_params_wrong_axis": ("quantize_key_group", _key_group_channel_axis),
     "score_drops_norm": ("decode_scores", _scores_no_norm),
