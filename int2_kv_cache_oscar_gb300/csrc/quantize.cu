@@ -25,12 +25,13 @@
 //   4. Codes of k_hat, packed straight into the fragment-order words and
 //      stored; the value code words are stored in V order from the staged
 //      bytes after the first barrier.
-// A value code is fl32(fl32(x - z) * fl32(1/s)) rounded half to even.  A key
-// code is fl32(x - z) * fl32(1/s) rounded once to the nearest integer (half
-// to even) by a fused multiply-add with 1.5 * 2^23: the two forms differ only
-// where the rounded product is an exact tie, which the fp32 k_hat makes rare
-// (3e-8 of the codes of the benchmark keys, always inside the 1e-3-step
-// boundary window), while the bf16 values hit exact ties often.  The packed
+// A code is round_half_even((x - z) / s) of the stored s and z, clamped.
+// Key codes: fl32(x - z) * fl32(1/s) rounded once to the nearest integer by
+// a fused multiply-add with 1.5 * 2^23; with the fp32 k_hat, quotients within
+// a few ulp of a tie are rare (about 1e-7 of the benchmark keys' codes, always
+// inside the 1e-3-step boundary window).  Value codes: bf16 values make exact
+// ties, and quotients a hair off a tie, common (about 1e-4 of the codes), so
+// the value decision is made exact there, see value_coefficients.  The packed
 // f32x2 operations round each lane exactly like the scalar ones.
 #include <cstddef>
 
@@ -72,21 +73,60 @@ __device__ __forceinline__ int kh_slot(int t, int q) { return q ^ (((t & 3) << 1
 // token (channels c and c + 32 at the same step) read different banks.
 __device__ __forceinline__ int kq_index(int c) { return (c >> 1) + (c >> 5); }
 
-// Rounded code decision of a pair against (1/s, -z): the float bits of
-// fl32(fl32(x - z) * inv) + 1.5 * 2^23, i.e. 0x4B400000 + code.  x >= z and
-// x <= max keep the product in [0, 3] (s == 0 gives inv = 0, code 0), so no
-// clamp is needed and the code is the low byte.  Every step is rounded, so an
-// exact tie k + 1/2 goes to the even code: the difference and the magic add
-// are packed adds (a packed add cannot absorb the product before it, see the
-// k_hat scaling), the products scalar __fmul_rn, which is never fused into a
-// multiply-add.  A packed multiply is not used here: the compiler may fuse it
-// with a following packed add even when both carry an explicit rounding mode,
-// which moves ties to the unrounded product's side.
-__device__ __forceinline__ uint2 code_bits2(float2 x, float2 inv, float2 negz) {
+// Value decisions.  With d = x - z (exact: x, z and max - min are bf16
+// values, or the float16 zero, in float32) and r = fl32(1/s), the quotient
+// P = d r, evaluated as below, is within 4 2^-24 P of d / s (the roundings
+// of r, of the coefficient b and of the two multiply-adds).  That decides
+// every code except where d / s is within that distance of a boundary
+// j + 1/2, and bf16 values put d / s there in two ways:
+//   * exactly on the tie (2 d = (2j + 1) s): half to even, i.e. down at 0.5
+//     and 2.5, up at 1.5;
+//   * a hair off it, when 6 d = (2j + 1) (max - min) and s = fl32((max -
+//     min) / 3) is rounded: then d / s = (j + 1/2) (max - min) / (3 s) sits
+//     on the side opposite to the rounding of s, at most 2.5 2^-24 away
+//     (only j = 1 occurs: at j = 0, 2 the same d makes (max - min) / 3 exact).
+// Each group's decision therefore evaluates P' = a d^2 + b d + c (two
+// multiply-adds) and rounds P' to the nearest integer:
+//   * s == (max - min) / 3 exactly, or float16 parameters (whose ties do not
+//     come from the rounding of s): P' = P - kappa (P - 1)(P - 2), which moves
+//     0.5 and 2.5 down by 3 kappa / 4 and 1.5 up by kappa / 4 (2.6 times the
+//     evaluation error there) and everything else by at most 2 kappa;
+//   * s rounded up / down: P' = P (1 -+ lambda), which moves the near-ties at
+//     1.5 to their side by 1.5 lambda (more than the evaluation error plus
+//     their distance from the tie) and everything else by at most 3 lambda.
+// Quotients that are neither ties nor near-ties but lie within 2 kappa of a
+// boundary can still round to the wrong side; on the benchmark values that
+// is 1 value code in 1.4e8 (CPU emulation), inside the boundary window.
+constexpr float kTieKappa = 0x1p-18f;
+constexpr float kTieLambda = 0x1p-20f;
+
+// Coefficients (a, b, c) of a value group's decision polynomial from its
+// range max - min (exact), stored scale s and r = 1/s (0 when s == 0: every
+// code is then 0).  sign_from_range: the stored s is the float32 (max - min)
+// / 3, whose rounding direction is the sign of 3 s - (max - min), exact as
+// one multiply-add.
+__device__ __forceinline__ float3 value_coefficients(float range, float s, float r, bool sign_from_range) {
+  int sg = 0;
+  if (sign_from_range) {
+    const float e = __fmaf_rn(3.0f, s, -range);
+    sg = (e > 0.0f) - (e < 0.0f);
+  }
+  if (sg == 0)
+    return make_float3(__fmul_rn(__fmul_rn(r, r), -kTieKappa), __fmul_rn(r, 1.0f + 3.0f * kTieKappa),
+                       -2.0f * kTieKappa);
+  return make_float3(0.0f, __fmul_rn(r, sg > 0 ? 1.0f - kTieLambda : 1.0f + kTieLambda), 0.0f);
+}
+
+// Value decisions of a pair: the float bits of fl32(P') + 1.5 * 2^23, i.e.
+// 0x4B400000 + code.  For float32 parameters P' lies in [-2 kappa, 3 (1 +
+// 2 lambda)], so the code is the low byte without a clamp.  The magic add
+// cannot merge with the multiply-add before it.
+__device__ __forceinline__ uint2 value_code_bits2(float2 x, float2 negz, float2 a, float2 b, float2 c) {
   const float2 d = __fadd2_rn(x, negz);
-  const float2 v = make_float2(__fmul_rn(d.x, inv.x), __fmul_rn(d.y, inv.y));
-  const float2 c = __fadd2_rn(v, make_float2(kMagic, kMagic));
-  return make_uint2(__float_as_uint(c.x), __float_as_uint(c.y));
+  const float2 u = __ffma2_rn(a, d, b);
+  const float2 p = __ffma2_rn(u, d, c);
+  const float2 y = __fadd2_rn(p, make_float2(kMagic, kMagic));
+  return make_uint2(__float_as_uint(y.x), __float_as_uint(y.y));
 }
 
 // Key decisions of a pair, one rounding each: the float bits of
@@ -243,20 +283,21 @@ __global__ void __launch_bounds__(kQThreads, 2)
         zv[g2] = zq;
         smax = fmaxf(smax, sc);
         const int gi = 2 * half + g2;
-        const float2 inv2 = make_float2(inv, inv), negz2 = make_float2(-zq, -zq);
+        const float3 co = value_coefficients(mx - mn, sc, inv, !M16);
+        const float2 ca = make_float2(co.x, co.x), cb = make_float2(co.y, co.y), cc = make_float2(co.z, co.z);
+        const float2 negz2 = make_float2(-zq, -zq);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const uint32_t ws[4] = {w4[i].x, w4[i].y, w4[i].z, w4[i].w};
 #pragma unroll
           for (int qq = 0; qq < 2; ++qq) {   // channels gi*32 + 8i + 4qq .. + 3
-            const uint2 c01 = code_bits2(bf16x2_to_float2(ws[2 * qq]), inv2, negz2);
-            const uint2 c23 = code_bits2(bf16x2_to_float2(ws[2 * qq + 1]), inv2, negz2);
+            const uint2 c01 = value_code_bits2(bf16x2_to_float2(ws[2 * qq]), negz2, ca, cb, cc);
+            const uint2 c23 = value_code_bits2(bf16x2_to_float2(ws[2 * qq + 1]), negz2, ca, cb, cc);
             uint32_t b;
             if constexpr (M16) {
               b = clamped_code(c01.x) | (clamped_code(c01.y) << 2) | (clamped_code(c23.x) << 4) |
                   (clamped_code(c23.y) << 6);
             } else {
-              // low bytes are the codes (the float bits' constant part has a zero low byte)
               // low byte: the codes (the float bits' constant part has a zero low byte)
               b = imad(c23.y, p64, imad(c23.x, p16, imad(c01.y, p4, c01.x)));
             }

@@ -2,7 +2,8 @@
 
 * Codes: bit-exact, except where the oracle's pre-rounding value lies within
   1e-3 of a decision boundary j + 1/2 (j = 0, 1, 2); the rate of such allowed
-  mismatches over all codes must be <= 1e-5.
+  mismatches over all codes must be <= 1e-5.  The oracle decides a code as
+  round_half_even((x - z) / s) in float64 from its own stored parameters.
 * Scales, zeros and norms (float32): |x_gpu - x_ref| <= 1e-6 |x_ref|; exact
   when x_ref == 0.
 * Decode outputs (bf16): |o_gpu - o_ref| <= 2e-3 + ulp_bf16(o_ref) / 2, where
@@ -18,21 +19,31 @@ META_REL = 1e-6
 DECODE_ABS = 2e-3
 
 
-def code_mismatches(gpu: np.ndarray, ref: np.ndarray, pre: np.ndarray):
-    """Return (n_mismatch, n_outside_window, n_total)."""
+def near_boundary(pre: np.ndarray) -> np.ndarray:
+    """Where the oracle's pre-rounding value lies within 1e-3 of j + 1/2."""
+    p = np.asarray(pre, np.float64)
+    return np.min(np.abs(p[..., None] - np.array([0.5, 1.5, 2.5])), axis=-1) < BOUNDARY_WINDOW
+
+
+def code_mismatches(gpu: np.ndarray, ref: np.ndarray, pre: np.ndarray, excused=None):
+    """Return (n_mismatch, n_outside_window, n_total).  `excused` (a boolean
+    mask broadcastable to the codes, optional) marks codes decided against
+    parameters that legitimately differ between the two sides; mismatches
+    there are not counted."""
     gpu = np.asarray(gpu)
     ref = np.asarray(ref)
     bad = gpu != ref
+    if excused is not None:
+        bad &= ~np.broadcast_to(excused, bad.shape)
     n_bad = int(bad.sum())
     if n_bad == 0:
         return 0, 0, gpu.size
-    p = np.asarray(pre)[bad]
-    near = np.min(np.abs(p[:, None] - np.array([0.5, 1.5, 2.5])[None, :]), axis=1) < BOUNDARY_WINDOW
+    near = near_boundary(np.asarray(pre)[bad])
     return n_bad, int((~near).sum()), gpu.size
 
 
-def assert_codes(gpu, ref, pre, what=""):
-    n_bad, n_out, n = code_mismatches(gpu, ref, pre)
+def assert_codes(gpu, ref, pre, what="", excused=None):
+    n_bad, n_out, n = code_mismatches(gpu, ref, pre, excused)
     assert n_out == 0, f"{what}: {n_out} code mismatches outside the boundary window"
     assert n_bad <= MAX_BOUNDARY_RATE * n, \
         f"{what}: boundary mismatch rate {n_bad}/{n} > {MAX_BOUNDARY_RATE}"

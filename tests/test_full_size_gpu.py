@@ -47,22 +47,29 @@ def _check_groups(g_head, k_tok, v_tok, what):
     kk = k_tok[:128 * ng].reshape(ng, 128, 128)
     vv = v_tok[:128 * ng].reshape(ng, 128, 128)
     rk, rv = O.quantize_key_group(kk), O.quantize_value_group(vv)
-    n_bad = n_tot = 0
+    counts = {}
     for name, gc, rc in (("K", g_head.keys.codes, rk), ("V", g_head.values.codes, rv)):
         b, n_out, n = P.code_mismatches(gc, rc.codes, rc.pre)
         assert n_out == 0, f"{what}: {n_out} {name} code mismatches outside the boundary window"
-        n_bad, n_tot = n_bad + b, n_tot + n
+        counts[name] = np.array([b, n])
     P.assert_meta(g_head.keys.scale, rk.scale, f"{what} K scale")
     P.assert_meta(g_head.keys.zero, rk.zero, f"{what} K zero")
     P.assert_meta(g_head.keys.norm, rk.norm, f"{what} K norm")
     P.assert_meta(g_head.values.scale, rv.scale, f"{what} V scale")
     P.assert_meta(g_head.values.zero, rv.zero, f"{what} V zero")
-    return n_bad, n_tot
+    return counts
 
 
-def _rate_ok(n_bad, n_tot, what):
-    assert n_bad <= P.MAX_BOUNDARY_RATE * n_tot, f"{what}: boundary mismatch rate {n_bad}/{n_tot}"
-    print(f"{what}: {n_bad}/{n_tot} boundary code mismatches")
+def _add(acc, counts):
+    for name, c in counts.items():
+        acc[name] = acc.get(name, 0) + c
+    return acc
+
+
+def _rate_ok(acc, what):
+    for name, (n_bad, n_tot) in sorted(acc.items()):
+        assert n_bad <= P.MAX_BOUNDARY_RATE * n_tot, f"{what}: {name} boundary mismatch rate {n_bad}/{n_tot}"
+        print(f"{what}: {name} codes {n_bad}/{n_tot} boundary mismatches (rate {n_bad / n_tot:.2e})")
 
 
 def _check_decode(got, qn, g_head, k_tok, v_tok, what):
@@ -83,17 +90,16 @@ def test_128k_decode_and_sampled_groups():
     U.lib().oscar_cache_check(cache.handle)
     arena = U.read_arena(cache)
     got, qn = U.f64(out), U.f64(q)
-    bad = tot = 0
+    acc = {}
     for head in (0, 5):
         g = U.gpu_head(cache, arena, 0, head)
         assert g.num_groups == 1024 and g.window_k.shape[0] == 0
         kt, vt = U.f64(k[:, head]), U.f64(v[:, head])
-        b, n = _check_groups(g, kt, vt, f"128K head {head}")
-        bad, tot = bad + b, tot + n
+        _add(acc, _check_groups(g, kt, vt, f"128K head {head}"))
         worst, exact = _check_decode(got[0, 4 * head:4 * head + 4], qn[0, 4 * head:4 * head + 4], g, kt, vt,
                                      f"128K head {head}")
         print(f"128K head {head}: decode max|gpu - oracle(gpu cache)| = {worst:.2e}, vs unquantised {exact:.2e}")
-    _rate_ok(bad, tot, "128K, 2 heads")
+    _rate_ok(acc, "128K, 2 heads")
 
 
 def test_batch32_32k_decode_sampled():
@@ -113,17 +119,16 @@ def test_batch32_32k_decode_sampled():
     U.lib().oscar_cache_check(cache.handle)
     arena = U.read_arena(cache)
     got, qn = U.f64(out), U.f64(q)
-    bad = tot = 0
+    acc = {}
     for b, head in ((0, 3), (17, 6), (31, 0)):
         g = U.gpu_head(cache, arena, b, head)
         kt, vt = U.f64(ks[b][:, head]), U.f64(vs[b][:, head])
-        nb, n = _check_groups(g, kt, vt, f"batch seq {b} head {head}")
-        bad, tot = bad + nb, tot + n
+        _add(acc, _check_groups(g, kt, vt, f"batch seq {b} head {head}"))
         worst, exact = _check_decode(got[b, 4 * head:4 * head + 4], qn[b, 4 * head:4 * head + 4], g, kt, vt,
                                      f"batch seq {b} head {head}")
         print(f"batch 32x32K seq {b} head {head}: decode max|gpu - oracle(gpu cache)| = {worst:.2e}, "
               f"vs unquantised {exact:.2e}")
-    _rate_ok(bad, tot, "batch 32x32K, 3 heads")
+    _rate_ok(acc, "batch 32x32K, 3 heads")
 
 
 def test_ragged_stream_sampled():
@@ -156,7 +161,7 @@ def test_ragged_stream_sampled():
     O_.oscar_cache_check(cache.handle)
     arena = U.read_arena(cache)
     got, qn = U.f64(out), U.f64(q)
-    bad = tot = 0
+    acc = {}
     for i, head in ((int(np.argmax(lens)), 2), (int(np.argmin(lens)), 7)):
         L0 = lens[i]
         assert cache.length(i) == L0 + steps
@@ -165,11 +170,10 @@ def test_ragged_stream_sampled():
         g = U.gpu_head(cache, arena, i, head)
         closed = list(range(L0 // 128, (L0 + steps) // 128))        # groups closed during the stream
         assert len(closed) >= 2
-        nb, n = _check_groups(g, kt, vt, f"stream seq {i} head {head}")
-        bad, tot = bad + nb, tot + n
+        _add(acc, _check_groups(g, kt, vt, f"stream seq {i} head {head}"))
         assert np.array_equal(g.window_k, kt[128 * ((L0 + steps) // 128):])
         worst, exact = _check_decode(got[i, 4 * head:4 * head + 4], qn[i, 4 * head:4 * head + 4], g, kt, vt,
                                      f"stream seq {i} head {head}")
         print(f"stream seq {i} (L {L0} + {steps}) head {head}: groups closed {closed}; decode max|gpu - oracle| = "
               f"{worst:.2e}, vs unquantised {exact:.2e}")
-    _rate_ok(bad, tot, "stream, 2 heads")
+    _rate_ok(acc, "stream, 2 heads")

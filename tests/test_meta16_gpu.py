@@ -5,8 +5,10 @@ values that the GPU and the oracle compute with different rounding orders
 (k_hat in float32 against float64; a float32 division against a float64 one
 rounded twice), so they agree exactly except where the two float32 values
 straddle a float16 rounding boundary: each must lie within one float16 ulp of
-the oracle's.  Codes are then checked against the oracle's decision taken with
-the GPU's stored parameters, under the boundary rule.  Decode, prefill and the
+the oracle's.  Codes are checked against the oracle's own decision (its own
+float16 parameters) under the boundary rule; a mismatch is excused only where
+the code was decided against a parameter that differs by that ulp, and those
+are counted apart.  Decode, prefill and the
 fused step are checked against the oracle over the GPU's own cache, with the
 decode rule.
 """
@@ -44,7 +46,7 @@ def test_meta16_quantize_parity(chunk):
     c, ks, vs = _cache([8192 + 100], 8, seed=91, chunk=chunk)
     arena = U.read_arena(c)
     straddles = n_params = 0
-    n_bad = n_tot = 0
+    counts = {"K": [0, 0, 0], "V": [0, 0, 0]}     # boundary mismatches, excused mismatches, codes
     for h in range(8):
         g = U.gpu_head(c, arena, 0, h)
         r = U.oracle_head(ks[0], vs[0], h, meta_bits=16)
@@ -57,23 +59,26 @@ def test_meta16_quantize_parity(chunk):
             assert np.all(d <= _f16_ulp(rv) * 1.0001), f"{what} head {h}: more than one float16 ulp apart"
             straddles += int(np.count_nonzero(d))
             n_params += d.size
-        # codes: the oracle's decision with the GPU's stored parameters
-        kg = U.f64(ks[0][:, h])[: ng * 128].reshape(ng, 128, 128)
-        _, k_hat = O.omni_token_scaling(O.canalized_rotation(kg))
-        codes, pre = O.int2_codes(k_hat, g.keys.scale[:, None, :], g.keys.zero[:, None, :])
-        b, n = P.assert_codes(g.keys.codes, codes, pre, f"K codes head {h}")
-        n_bad += b
-        n_tot += n
-        vg = U.f64(vs[0][:, h])[: ng * 128].reshape(ng, 128, 4, 32)
-        codes, pre = O.int2_codes(vg, g.values.scale[..., None], g.values.zero[..., None])
-        b, n = P.assert_codes(g.values.codes, codes.reshape(ng, 128, 128), pre.reshape(ng, 128, 128),
-                              f"V codes head {h}")
-        n_bad += b
-        n_tot += n
+        # codes: the oracle's own decision (its own float16 parameters).  A
+        # mismatch is excused only where the code was decided against a
+        # parameter whose stored float16 differs between the two sides (the
+        # one-ulp straddles counted above), and is otherwise held to the
+        # boundary rule.
+        k_diff = (g.keys.scale != r.keys.scale) | (g.keys.zero != r.keys.zero)          # [ng, 128 channels]
+        v_diff = (g.values.scale != r.values.scale) | (g.values.zero != r.values.zero)  # [ng, 128 tokens, 4]
+        cases = (("K", g.keys.codes, r.keys, np.broadcast_to(k_diff[:, None, :], g.keys.codes.shape)),
+                 ("V", g.values.codes, r.values, np.repeat(v_diff, 32, axis=-1)))
+        for name, gc, rc, excused in cases:
+            b, n = P.assert_codes(gc, rc.codes, rc.pre, f"{name} codes head {h}", excused=excused)
+            counts[name][0] += b
+            counts[name][1] += int(np.count_nonzero((gc != rc.codes) & excused))
+            counts[name][2] += n
         assert np.array_equal(g.window_k, r.window_k) and np.array_equal(g.window_v, r.window_v)
-    assert n_bad <= P.MAX_BOUNDARY_RATE * n_tot
-    print(f"meta16 quantise: {straddles}/{n_params} parameters one float16 ulp from the oracle; "
-          f"{n_bad}/{n_tot} boundary code mismatches")
+    for name, (b, e, n) in counts.items():
+        assert b <= P.MAX_BOUNDARY_RATE * n, f"{name}: boundary mismatch rate {b}/{n}"
+        print(f"meta16 quantise {name}: {b}/{n} boundary code mismatches; {e} mismatches where a stored "
+              f"parameter differs by one float16 ulp")
+    print(f"meta16 quantise: {straddles}/{n_params} parameters one float16 ulp from the oracle")
 
 
 def test_meta16_chunking_is_bit_identical():

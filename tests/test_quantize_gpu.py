@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 
 def _compare_cache(cache, slots, ks, vs, report):
     arena = U.read_arena(cache)
-    n_bad = n_tot = 0
+    counts = {"K": [0, 0], "V": [0, 0]}
     worst = {"kscale": 0.0, "kzero": 0.0, "knorm": 0.0, "vscale": 0.0, "vzero": 0.0}
     for i, s in enumerate(slots):
         L = ks[i].shape[0]
@@ -24,21 +24,20 @@ def _compare_cache(cache, slots, ks, vs, report):
             r = U.oracle_head(ks[i], vs[i], h)
             assert g.num_groups == r.num_groups
             if r.num_groups:
-                b, n = P.assert_codes(g.keys.codes, r.keys.codes, r.keys.pre, f"K codes slot {s} head {h}")
-                n_bad += b
-                n_tot += n
-                b, n = P.assert_codes(g.values.codes, r.values.codes, r.values.pre, f"V codes slot {s} head {h}")
-                n_bad += b
-                n_tot += n
+                for name, gc, rc in (("K", g.keys, r.keys), ("V", g.values, r.values)):
+                    b, n = P.assert_codes(gc.codes, rc.codes, rc.pre, f"{name} codes slot {s} head {h}")
+                    counts[name][0] += b
+                    counts[name][1] += n
                 worst["kscale"] = max(worst["kscale"], P.assert_meta(g.keys.scale, r.keys.scale, "K scale"))
                 worst["kzero"] = max(worst["kzero"], P.assert_meta(g.keys.zero, r.keys.zero, "K zero"))
                 worst["knorm"] = max(worst["knorm"], P.assert_meta(g.keys.norm, r.keys.norm, "K norm"))
                 worst["vscale"] = max(worst["vscale"], P.assert_meta(g.values.scale, r.values.scale, "V scale"))
                 worst["vzero"] = max(worst["vzero"], P.assert_meta(g.values.zero, r.values.zero, "V zero"))
             assert np.array_equal(g.window_k, r.window_k) and np.array_equal(g.window_v, r.window_v)
-    assert n_bad <= P.MAX_BOUNDARY_RATE * max(n_tot, 1), f"boundary mismatch rate {n_bad}/{n_tot}"
+    for name, (n_bad, n_tot) in counts.items():
+        assert n_bad <= P.MAX_BOUNDARY_RATE * max(n_tot, 1), f"{name} boundary mismatch rate {n_bad}/{n_tot}"
+        report[f"{name}_code_mismatch"] = (n_bad, n_tot)
     report.update(worst)
-    report["code_mismatch"] = (n_bad, n_tot)
     return report
 
 
