@@ -584,79 +584,68 @@ def profile_case(args):
 
 # ------------------------------------------------------------- CPU oracle
 
-def cpu_sample_worker(steps: int, warmup: int = 0):
-    """Runs in a fresh single-threaded process: oracle decode of 1 of the 8
-    KV heads of the 128K workload (4 query heads); `warmup` untimed decodes,
-    then `steps` timed ones."""
-    import numpy as np
+def _cpu_step_worker(rank, n, steps, warmup, barrier, queue):
+    """One of n spawned single-threaded processes of the CPU oracle step: it
+    builds the oracle caches of KV heads rank, rank + n, ... of the 128K
+    workload, then runs `warmup` + `steps` decode steps, each bracketed by
+    barriers shared with the other processes, and reports its own time per
+    step.  A step's wall time is the slowest process's."""
+    os.environ.update(OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+                      CUDA_VISIBLE_DEVICES="")
     import torch
 
     from int2_kv_cache_oscar_gb300 import workloads as W
     from oracle import oscar_oracle as OR
 
+    torch.set_num_threads(1)
     gen = torch.Generator()
     gen.manual_seed(2)
-    k, v = W.make_sequence_kv(CTX, 1, W.LLAMA_RECIPE, gen)
-    q = W.make_q(1, 4, seed=2)
-    t0 = time.perf_counter()
-    hc = OR.build_head_cache(k[:, 0].double().numpy(), v[:, 0].double().numpy())
-    t_quant = time.perf_counter() - t0
-    qn = q[0].double().numpy()
-    for _ in range(warmup):
-        OR.decode_head(qn, hc)
+    k, v = W.make_sequence_kv(CTX, HKV, W.LLAMA_RECIPE, gen)
+    q = W.make_q(1, HQ, seed=2)[0].double().numpy()
+    heads = list(range(rank, HKV, n))
+    gq = HQ // HKV
+    caches = {h: OR.build_head_cache(k[:, h].double().numpy(), v[:, h].double().numpy()) for h in heads}
+    del k, v
     times = []
-    for _ in range(steps):
+    for it in range(warmup + steps):
+        barrier.wait()
         t0 = time.perf_counter()
-        OR.decode_head(qn, hc)
-        times.append(time.perf_counter() - t0)
-    return {"decode_s_per_head": statistics.mean(times), "quant_s_per_head": t_quant}
+        for h in heads:
+            OR.decode_head(q[h * gq:(h + 1) * gq], caches[h])
+        dt = time.perf_counter() - t0
+        barrier.wait()
+        if it >= warmup:
+            times.append(dt)
+    queue.put((rank, times))
 
 
-def run_cpu_sample(steps: int, warmup: int = 0):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    code = ("import json, bench; print('CPUJSON' + json.dumps(bench.cpu_sample_worker(%d, %d)))" % (steps, warmup))
-    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
-                       timeout=900)
-    m = re.search(r"CPUJSON(\{.*\})", r.stdout)
-    if not m:
-        raise RuntimeError("CPU oracle sample failed:\n" + r.stdout[-2000:] + r.stderr[-2000:])
-    return json.loads(m.group(1))
+def run_cpu_steps(steps: int, warmup: int = 0):
+    """Full decode steps of the oracle (all 8 KV heads, 32 query heads, 128K
+    tokens), in one single-threaded process per host core up to 8.  Returns
+    the mean wall time of a step (the slowest process of each step) and the
+    processes used."""
+    import multiprocessing as mp
 
-
-def run_cpu_sample_all_cores(steps: int):
-    """The same sample in up to 8 concurrent single-threaded processes, one per
-    KV head (the oracle as it stands, on more cores): wall time of a full
-    8-head step = the slowest head's step time x the rounds needed."""
     try:
         cores = len(os.sched_getaffinity(0))
     except AttributeError:
         cores = os.cpu_count() or 1
     n = max(1, min(HKV, cores))
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    code = ("import json, bench; print('CPUJSON' + json.dumps(bench.cpu_sample_worker(%d)))" % steps)
-    procs = [subprocess.Popen([sys.executable, "-c", code], cwd=ROOT, env=env, stdout=subprocess.PIPE,
-                              stderr=subprocess.PIPE, text=True) for _ in range(n)]
-    per_head = []
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(n)
+    queue = ctx.Queue()
+    procs = [ctx.Process(target=_cpu_step_worker, args=(r, n, steps, warmup, barrier, queue)) for r in range(n)]
     for pr in procs:
-        out, err = pr.communicate(timeout=1200)
-        m = re.search(r"CPUJSON(\{.*\})", out)
-        if not m:
-            raise RuntimeError("CPU oracle sample failed:\n" + out[-2000:] + err[-2000:])
-        per_head.append(json.loads(m.group(1))["decode_s_per_head"])
+        pr.start()
+    per_rank = dict(queue.get(timeout=1800) for _ in range(n))
+    for pr in procs:
+        pr.join(timeout=60)
+    step_s = [max(per_rank[r][i] for r in range(n)) for i in range(steps)]
     rounds = -(-HKV // n)
-    us = max(per_head) * rounds * 1e6
-    return {"value": round(us, 1), "unit": "us/step", "cores": n, "kind": "oracle",
-            "sample": f"oracle decode (float64 numpy) of the 128K-token cache, one KV head (4 query heads) per "
-                      f"single-threaded process, {n} processes at once, {rounds} round(s) for the 8 heads"}
-
-
-def cpu_baseline_obj(js, kind="oracle"):
-    us = js["decode_s_per_head"] * HKV * 1e6
-    return {"value": round(us, 1), "unit": "us/step", "cores": 1, "kind": kind,
-            "sample": "oracle decode (float64 numpy) of 1 of the 8 KV heads (4 query heads) over the "
-                      "128K-token cache, scaled x8 to the full step; 1 thread"}
+    return {"value": round(statistics.mean(step_s) * 1e6, 1), "unit": "us/step", "cores": n, "kind": "oracle",
+            "sample": f"{steps} full decode steps of the oracle (float64 numpy) over the 128K-token cache: all 8 KV "
+                      f"heads, 32 query heads; {n} single-threaded processes ({rounds} head(s) each), each step "
+                      f"between barriers, its time the slowest process's; no scaling"}
 
 
 # --------------------------------------------------------------------- main
@@ -696,8 +685,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        js = run_cpu_sample(args.steps, args.warmup)
-        cb = cpu_baseline_obj(js)
+        cb = run_cpu_steps(args.steps, args.warmup)
         line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "us/step",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": round(cb["value"] / 1e3, 3), "higher_is_better": False,
@@ -728,16 +716,12 @@ def main():
             dist.destroy_process_group()
         return
 
-    cpu = cpu_all = None
+    cpu = None
     if not args.no_cpu:
         try:
-            cpu = cpu_baseline_obj(run_cpu_sample(3))
+            cpu = run_cpu_steps(3, 1)
         except Exception as e:  # reported, not fatal
-            cpu = {"value": None, "unit": "us/step", "cores": 1, "kind": "oracle", "sample": f"failed: {e}"}
-        try:
-            cpu_all = run_cpu_sample_all_cores(3)
-        except Exception as e:  # reported, not fatal
-            cpu_all = {"value": None, "unit": "us/step", "kind": "oracle", "sample": f"failed: {e}"}
+            cpu = {"value": None, "unit": "us/step", "kind": "oracle", "sample": f"failed: {e}"}
 
     traffic = profiled_traffic()
     line = {
@@ -769,7 +753,6 @@ def main():
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
         "cpu_baseline": cpu,
-        "cpu_baseline_all_cores": cpu_all,
     }
     line.update(res["extra"])
     print(json.dumps(line))
