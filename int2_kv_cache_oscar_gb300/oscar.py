@@ -65,6 +65,7 @@ def _load() -> ctypes.CDLL:
         "oscar_quantize_append": [P, I32, I32P, I32P, P, P, P],
         "oscar_decode_workspace_bytes": [P, I32, I32, ctypes.POINTER(SZ)],
         "oscar_decode_attention": [P, I32, I32P, P, I32, ctypes.c_float, P, P, SZ, P],
+        "oscar_decode_attention_f32": [P, I32, I32P, P, I32, ctypes.c_float, P, P, SZ, P],
         "oscar_cache_bytes": [P, I32, I32, ctypes.POINTER(SZ)],
         "oscar_cache_block_offset": [P, I32, I32, I32, ctypes.POINTER(SZ)],
         "oscar_cache_window_offset": [P, I32, I32, ctypes.POINTER(SZ)],
@@ -211,6 +212,19 @@ def oscar_decode_attention(handle, seq_ids: Sequence[int], q: torch.Tensor, num_
                                        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
+def oscar_decode_attention_f32(handle, seq_ids: Sequence[int], q: torch.Tensor, num_q_heads: int,
+                               softmax_scale: float, out: torch.Tensor, workspace: torch.Tensor,
+                               stream=None) -> None:
+    """The same decode with float32 outputs (the merged result before any
+    bf16 rounding)."""
+    shape = (len(seq_ids), num_q_heads, HEAD_DIM)
+    _check(_lib.oscar_decode_attention_f32(handle, len(seq_ids), _i32(seq_ids), _buf(q, torch.bfloat16, shape, "q"),
+                                           num_q_heads, ctypes.c_float(softmax_scale),
+                                           _buf(out, torch.float32, shape, "out"),
+                                           _buf(workspace, torch.uint8, None, "workspace"),
+                                           workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
 def oscar_decode_attention_noalloc(handle, seq_ids: Sequence[int], q: torch.Tensor, num_q_heads: int,
                                    softmax_scale: float, out: torch.Tensor, stream=None) -> None:
     """Decode without a workspace: the partials go to the library's built-in
@@ -354,6 +368,10 @@ class OscarCache:
     def decode(self, seq_ids, q, num_q_heads, out, workspace, softmax_scale=0.0, stream=None):
         oscar_decode_attention(self.handle, seq_ids, q, num_q_heads, softmax_scale, out, workspace,
                                stream)
+
+    def decode_f32(self, seq_ids, q, num_q_heads, out, workspace, softmax_scale=0.0, stream=None):
+        oscar_decode_attention_f32(self.handle, seq_ids, q, num_q_heads, softmax_scale, out, workspace,
+                                   stream)
 
     def append_decode(self, seq_ids, k_new, v_new, q, num_q_heads, out, workspace, softmax_scale=0.0,
                       stream=None):
