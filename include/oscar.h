@@ -89,14 +89,9 @@ enum {
  * must be 256-byte aligned):
  *
  *   [0, 256)                       status words; word 0 = device error flags
- *   [256, D)                       per (slot, kv head): float32 bit pattern of
+ *   [256, M)                       per (slot, kv head): float32 bit pattern of
  *                                  the largest value scale s_v quantised so
- *                                  far (4 bytes each), D = 256 + 4*max_batch*Hkv
- *   [D, M)                         per (slot, kv head): uint32 decode ticket,
- *                                  zero between calls (the decode counts the
- *                                  partial records of a row here and the
- *                                  CTA completing the row merges them and
- *                                  zeroes it), M = 256-aligned end
+ *                                  far (4 bytes each), M = 256-aligned end
  *   blocks  (base = M)             one block of B bytes per
  *                                  (slot, kv head, group g):
  *                                  base + ((slot*Hkv + head)*max_groups + g)*B,
@@ -183,9 +178,7 @@ oscar_status oscar_decode_workspace_bytes(const oscar_cache* cache, int32_t n_se
 
 /*
  * Single-query decode attention over the packed cache (split-K flash
- * decoding, GQA, ragged batch), one kernel launch per pass: the grid splits
- * every (sequence, KV head) row over the SMs, and the CTA that completes a
- * row merges its partial results (log-sum-exp) and writes the output.
+ * decoding, GQA, ragged batch).
  *   seq_ids      host int32 [n_seqs]; every slot must have length >= 1
  *   q            bf16 [n_seqs, num_q_heads, 128] (unrotated queries), 16-byte
  *                aligned, in device memory or page-locked host memory
@@ -207,8 +200,6 @@ oscar_status oscar_decode_workspace_bytes(const oscar_cache* cache, int32_t n_se
  * a decode step from host inputs to host outputs needs no staging copies.
  * Pageable host memory and device memory of another device fail with
  * OSCAR_ERR_INVALID_ARG before anything is enqueued.
- * Decode calls on one cache must not overlap on the GPU (they share the
- * arena's row tickets): issue them on one stream or order them.
  */
 oscar_status oscar_decode_attention(oscar_cache* cache, int32_t n_seqs, const int32_t* seq_ids,
                                     const void* q, int32_t num_q_heads, float softmax_scale,
@@ -241,8 +232,8 @@ oscar_status oscar_decode_attention_f32(oscar_cache* cache, int32_t n_seqs, cons
  *   other arguments as for oscar_decode_attention (q and out may be host
  *   buffers in the same way).
  * When no sequence's new length is a multiple of 128 (127 steps in 128),
- * the step is one decode launch: the decode attends the new token as the
- * last window row straight from k_new / v_new and stores it into the
+ * the step is one decode launch: the combine kernel attends the new token as
+ * the last window row straight from k_new / v_new and stores it into the
  * window.  When a group closes, the quantiser runs first (two launches), so
  * the group is attended quantised.  All arguments are validated before
  * anything is enqueued; on error nothing changes.
@@ -327,8 +318,7 @@ oscar_status oscar_cache_window_offset(const oscar_cache* cache, int32_t seq, in
 
 /* Synchronise `stream`, then read the device error flags of the arena.
  * Returns OSCAR_ERR_DEVICE_TIMEOUT if a kernel's bounded wait gave up since
- * the last check (and clears the flags and the decode's row tickets, which a
- * kernel that gave up may have left counted), OSCAR_OK otherwise. */
+ * the last check (and clears the flags), OSCAR_OK otherwise. */
 oscar_status oscar_cache_check(oscar_cache* cache, void* stream);
 
 /*

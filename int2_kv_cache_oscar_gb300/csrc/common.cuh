@@ -68,8 +68,7 @@ constexpr uint32_t kSpinLimit = 1u << 24;
 constexpr uint32_t kErrTimeout = 1u;
 
 struct ArenaLayout {
-  int64_t meta_bytes;     // header + per (slot, head) s_v maxima + decode tickets, 256-aligned
-  int64_t tickets_off;    // per (slot, head) uint32 decode tickets (zero between calls)
+  int64_t meta_bytes;     // header + per (slot, head) s_v maxima, 256-aligned
   int64_t blocks_off;
   int64_t windows_off;
   int64_t total;
@@ -80,8 +79,7 @@ __host__ __device__ inline ArenaLayout arena_layout(int32_t max_batch, int32_t h
                                                     int32_t block_bytes = kBlockBytes) {
   ArenaLayout L;
   L.max_groups = (max_len + kGroup - 1) / kGroup;
-  L.tickets_off = kMetaHeader + (int64_t)max_batch * hkv * 4;
-  int64_t meta = L.tickets_off + (int64_t)max_batch * hkv * 4;
+  int64_t meta = kMetaHeader + (int64_t)max_batch * hkv * 4;
   L.meta_bytes = (meta + 255) / 256 * 256;
   L.blocks_off = L.meta_bytes;
   int64_t blocks = (int64_t)max_batch * hkv * L.max_groups * block_bytes;
@@ -139,45 +137,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking test of whether phase `parity` of `bar` has completed.
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// try_wait that may suspend the thread in hardware until the phase completes
-// or about kSuspendNs nanoseconds pass, so that a waiting warp takes no issue
-// slots from the warps that compute.
-constexpr uint32_t kSuspendNs = 1000;
-__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
-      : "memory");
-  return ok != 0;
-}
-
-// Tries of a bounded wait: at most about 2 s when every try suspends for
-// kSuspendNs, less when tries return early.
-constexpr uint32_t kWaitTries = 1u << 21;
-
-// Wait for phase `parity` of `bar`, bounded.  On timeout, sets the CTA abort
-// flag and the device error word; once the abort flag is set every later
-// wait returns immediately so that the CTA still reaches its barriers and
-// exits.  err_word may be NULL (no device status word).
+// Wait for phase `parity` of `bar` with a bounded spin.  On timeout, sets the
+// CTA abort flag and the device error word; once the abort flag is set every
+// later wait returns immediately so that the CTA still reaches its barriers
+// and exits.  err_word may be NULL (no device status word).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                                   uint32_t* err_word) {
-  for (uint32_t i = 0; i < kWaitTries; ++i) {
-    if (mbar_try_wait_suspend(bar, parity)) return true;
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    __nanosleep(64);   // in case the try returned early: no spinning on the issue slots
   }
   *abort_flag = 1;
   if (err_word != nullptr) atomicOr(err_word, kErrTimeout);
@@ -194,7 +162,6 @@ __device__ __forceinline__ bool wait_issued(const volatile uint32_t* issued, uin
   for (uint32_t i = 0; i < kSpinLimit; ++i) {
     if (*issued > n) return true;
     if (*abort_flag) return false;
-    __nanosleep(32);   // leave the issue slots to the warps that compute
   }
   *abort_flag = 1;
   if (err_word != nullptr) atomicOr(err_word, kErrTimeout);

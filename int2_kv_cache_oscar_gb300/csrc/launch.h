@@ -117,10 +117,7 @@ struct DecodeHeader {
   // longest window of the batch) and bytes of partial records per chunk
   int32_t comb_wrows;
   int32_t comb_part_bytes;
-  // fused INT2 decode: one counter per (slot, KV head) in the arena (zero
-  // between calls), and the output type (0: bf16, 1: float32)
-  uint32_t* tickets;
-  int32_t out_f32;
+  int32_t out_f32;       // the combine writes float32 outputs (else bf16)
   int32_t pad_;
 };
 
@@ -180,12 +177,5 @@ cudaError_t launch_decode_bf16(const DecodeParams<MAXS>& p, const uint16_t* kc, 
                                cudaStream_t stream, cudaEvent_t ev_start, cudaEvent_t ev_stop);
 template <int MAXS>
 cudaError_t launch_combine(const DecodeParams<MAXS>& p, const uint8_t* arena, cudaStream_t stream);
-
-// The fused INT2 decode (one launch per pass): p.seq lists units as
-// fused_units_of_len; p.h.n_ctas CTAs of one per SM.
-int fused_units_of_len(int len);
-template <int MAXS>
-cudaError_t launch_fused_decode(const DecodeParams<MAXS>& p, uint8_t* arena, bool meta16, cudaStream_t stream,
-                                cudaEvent_t ev_start, cudaEvent_t ev_stop);
 
 }  // namespace oscar

@@ -189,7 +189,7 @@ oscar_status run_decode(int device, int sms, int ctas_per_sm, int32_t n, const i
                         int64_t windows_off, const uint8_t* arena, uint32_t* err_word, const uint16_t* kc,
                         const uint16_t* vc, const void* q, void* out, void* ws, size_t ws_bytes,
                         cudaStream_t stream, const void* k_new = nullptr, const void* v_new = nullptr,
-                        bool meta16 = false) {
+                        bool meta16 = false, bool out_f32 = false) {
   DecodeParams<MAXS> P;
   std::memset(&P, 0, sizeof(P));
   int64_t rows = 0;
@@ -220,6 +220,7 @@ oscar_status run_decode(int device, int sms, int ctas_per_sm, int32_t n, const i
   P.h.err_word = err_word;
   P.h.k_new = static_cast<const uint16_t*>(k_new);
   P.h.v_new = static_cast<const uint16_t*>(v_new);
+  P.h.out_f32 = out_f32 ? 1 : 0;
   // The kernels serve at most kMaxGqa query heads of a KV head per launch (mma
   // columns = heads x {hi, lo}); larger groups run as consecutive passes, each
   // streaming the cache again.  Stream order keeps a pass's main kernel from
@@ -263,120 +264,6 @@ oscar_status run_decode(int device, int sms, int ctas_per_sm, int32_t n, const i
   }
   (void)device;
   return OSCAR_OK;
-}
-
-// One fused INT2 decode step (per pass of at most kMaxGqa query heads of
-// each KV head): the units of every (sequence, KV head) row are its groups
-// and its window in 16-token pieces; one persistent CTA per SM.
-template <int MAXS>
-oscar_status run_fused_decode(oscar_cache* c, int32_t n, const int32_t* slots, const int32_t* lens, int hq,
-                              float scale, const void* q, void* out, bool out_f32, void* ws, size_t ws_bytes,
-                              cudaStream_t stream, const void* k_new = nullptr, const void* v_new = nullptr) {
-  DecodeParams<MAXS> P;
-  std::memset(&P, 0, sizeof(P));
-  const int hkv = c->cfg.num_kv_heads;
-  int64_t ubase = 0;
-  for (int32_t i = 0; i < n; ++i) {
-    P.seq[i].slot = slots[i];
-    P.seq[i].len = lens[i];
-    P.seq[i].ubase = ubase;
-    P.seq[i].rank = i;          // every row has at least one unit
-    P.seq[i].pad = 0;
-    ubase += (int64_t)hkv * fused_units_of_len(lens[i]);
-  }
-  const int64_t T = ubase;
-  const int64_t N = std::min<int64_t>(T, std::min(c->sms, 160));   // the kernel merges at most 160 records a row
-  const int q_group = hq / hkv;
-  const size_t need = partial_bytes(N + (int64_t)n * hkv, q_group < kMaxGqa ? q_group : kMaxGqa);
-  if (ws_bytes < need)
-    return fail(OSCAR_ERR_CAPACITY, "workspace too small: %zu < %zu bytes", ws_bytes, need);
-  P.h.n_seqs = n;
-  P.h.hkv = hkv;
-  P.h.hq = hq;
-  P.h.q_group = q_group;
-  P.h.max_groups = c->layout.max_groups;
-  P.h.n_ctas = (int32_t)N;
-  P.h.bf16_mode = 0;
-  P.h.n_units = T;
-  P.h.blocks_off = c->layout.blocks_off;
-  P.h.windows_off = c->layout.windows_off;
-  P.h.scale_log2 = scale * 1.4426950408889634f;
-  P.h.q = static_cast<const uint16_t*>(q);
-  P.h.out = static_cast<uint16_t*>(out);
-  P.h.partials = static_cast<float*>(ws);
-  P.h.err_word = reinterpret_cast<uint32_t*>(c->arena);
-  P.h.k_new = static_cast<const uint16_t*>(k_new);
-  P.h.v_new = static_cast<const uint16_t*>(v_new);
-  P.h.tickets = reinterpret_cast<uint32_t*>(c->arena + c->layout.tickets_off);
-  P.h.out_f32 = out_f32 ? 1 : 0;
-  // Query-head groups larger than kMaxGqa run as consecutive passes (stream
-  // order keeps them apart on the shared workspace and tickets); a fused
-  // step's passes all store the same new token.
-  for (int head0 = 0; head0 < q_group; head0 += kMaxGqa) {
-    P.h.gqa = q_group - head0 < kMaxGqa ? q_group - head0 : kMaxGqa;
-    P.h.q_head0 = head0;
-    const cudaError_t e = launch_fused_decode(P, c->arena, c->meta16, stream, g_ev_start, g_ev_stop);
-    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  }
-  return OSCAR_OK;
-}
-
-// Validation shared by the decode entry points; on success `lens` holds the
-// lengths the step attends to (with the appended token for a fused step).
-oscar_status check_decode_args(oscar_cache* c, int32_t n_seqs, const int32_t* seq_ids, const void* q,
-                               int32_t num_q_heads, float softmax_scale, const void* out, const void* workspace,
-                               std::vector<int32_t>& lens, int extra) {
-  if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
-  if (n_seqs < 1) return fail(OSCAR_ERR_INVALID_ARG, "n_seqs must be >= 1");
-  if (n_seqs > kDecodeSeqsLarge) return fail(OSCAR_ERR_CAPACITY, "at most %d sequences per call", kDecodeSeqsLarge);
-  if (!seq_ids || !q || !out || !workspace) return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
-  const int hkv = c->cfg.num_kv_heads;
-  if (num_q_heads < hkv || num_q_heads % hkv != 0)
-    return fail(OSCAR_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of Hkv");
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 16))
-    return fail(OSCAR_ERR_INVALID_ARG, "q, out and workspace must be 16-byte aligned");
-  if (!(softmax_scale >= 0.0f) || std::isinf(softmax_scale))
-    return fail(OSCAR_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
-  std::vector<char> seen;
-  oscar_status s = check_slots(c, n_seqs, seq_ids, seen);
-  if (s != OSCAR_OK) return s;
-  lens.resize(n_seqs);
-  for (int32_t i = 0; i < n_seqs; ++i) {
-    lens[i] = c->len[seq_ids[i]] + extra;
-    if (lens[i] < 1) return fail(OSCAR_ERR_INVALID_ARG, "sequence %d is empty", seq_ids[i]);
-    if (lens[i] > c->cfg.max_seq_len)
-      return fail(OSCAR_ERR_CAPACITY, "sequence %d would reach %d tokens > max_seq_len %d", seq_ids[i], lens[i],
-                  c->cfg.max_seq_len);
-  }
-  return OSCAR_OK;
-}
-
-// oscar_decode_attention and oscar_decode_attention_f32.
-oscar_status decode_call(oscar_cache* c, int32_t n_seqs, const int32_t* seq_ids, const void* q, int32_t num_q_heads,
-                         float softmax_scale, void* out, bool out_f32, void* workspace, size_t workspace_bytes,
-                         void* stream) {
-  try {
-    std::vector<int32_t> lens;
-    oscar_status s = check_decode_args(c, n_seqs, seq_ids, q, num_q_heads, softmax_scale, out, workspace, lens, 0);
-    if (s != OSCAR_OK) return s;
-    const float scale = softmax_scale == 0.0f ? 1.0f / std::sqrt((float)kHeadDim) : softmax_scale;
-    DeviceGuard dg(c->cfg.device);
-    if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
-    if ((s = device_view_as(q, "q", c->cfg.device, &q)) != OSCAR_OK) return s;
-    if ((s = device_view_as(out, "out", c->cfg.device, &out)) != OSCAR_OK) return s;
-    if ((s = device_view_as(workspace, "workspace", c->cfg.device, &workspace, false)) != OSCAR_OK) return s;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (n_seqs <= kDecodeSeqsSmall)
-      s = run_fused_decode<kDecodeSeqsSmall>(c, n_seqs, seq_ids, lens.data(), num_q_heads, scale, q, out, out_f32,
-                                             workspace, workspace_bytes, st);
-    else
-      s = run_fused_decode<kDecodeSeqsLarge>(c, n_seqs, seq_ids, lens.data(), num_q_heads, scale, q, out, out_f32,
-                                             workspace, workspace_bytes, st);
-    if (s != OSCAR_OK) return s;
-    return ok();
-  } catch (const std::exception& ex) {
-    return fail(OSCAR_ERR_INVALID_ARG, "host allocation failed: %s", ex.what());
-  }
 }
 
 }  // namespace
@@ -561,6 +448,65 @@ oscar_status oscar_decode_workspace_bytes(const oscar_cache* c, int32_t n_seqs, 
   return ok();
 }
 
+}  // extern "C"
+
+namespace {
+
+// oscar_decode_attention and oscar_decode_attention_f32 (out_f32: float32 outputs).
+oscar_status decode_call(oscar_cache* c, int32_t n_seqs, const int32_t* seq_ids, const void* q, int32_t num_q_heads,
+                         float softmax_scale, void* out, bool out_f32, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  try {
+    if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+    if (n_seqs < 1) return fail(OSCAR_ERR_INVALID_ARG, "n_seqs must be >= 1");
+    if (n_seqs > kDecodeSeqsLarge) return fail(OSCAR_ERR_CAPACITY, "at most %d sequences per call", kDecodeSeqsLarge);
+    if (!seq_ids || !q || !out || !workspace) return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+    const int hkv = c->cfg.num_kv_heads;
+    if (num_q_heads < hkv || num_q_heads % hkv != 0)
+      return fail(OSCAR_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of Hkv");
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 16))
+      return fail(OSCAR_ERR_INVALID_ARG, "q, out and workspace must be 16-byte aligned");
+    if (!(softmax_scale >= 0.0f) || std::isinf(softmax_scale))
+      return fail(OSCAR_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
+    std::vector<char> seen;
+    oscar_status s = check_slots(c, n_seqs, seq_ids, seen);
+    if (s != OSCAR_OK) return s;
+    std::vector<int32_t> lens(n_seqs);
+    for (int32_t i = 0; i < n_seqs; ++i) {
+      lens[i] = c->len[seq_ids[i]];
+      if (lens[i] < 1) return fail(OSCAR_ERR_INVALID_ARG, "sequence %d is empty", seq_ids[i]);
+    }
+    const float scale = softmax_scale == 0.0f ? 1.0f / std::sqrt((float)kHeadDim) : softmax_scale;
+    DeviceGuard dg(c->cfg.device);
+    if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
+    if ((s = device_view_as(q, "q", c->cfg.device, &q)) != OSCAR_OK) return s;
+    if ((s = device_view_as(out, "out", c->cfg.device, &out)) != OSCAR_OK) return s;
+    if ((s = device_view_as(workspace, "workspace", c->cfg.device, &workspace, false)) != OSCAR_OK) return s;
+    uint32_t* err_word = reinterpret_cast<uint32_t*>(c->arena);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n_seqs <= kDecodeSeqsSmall)
+      s = run_decode<kDecodeSeqsSmall>(c->cfg.device, c->sms, decode_int2_ctas_per_sm(), n_seqs, seq_ids,
+                                       lens.data(), hkv, num_q_heads, scale, 0, c->layout.max_groups,
+                                       c->layout.blocks_off, c->layout.windows_off, c->arena, err_word, nullptr,
+                                       nullptr, q, out, workspace, workspace_bytes, st, nullptr, nullptr,
+                                       c->meta16, out_f32);
+    else
+      s = run_decode<kDecodeSeqsLarge>(c->cfg.device, c->sms, decode_int2_ctas_per_sm(), n_seqs, seq_ids,
+                                       lens.data(), hkv, num_q_heads, scale, 0, c->layout.max_groups,
+                                       c->layout.blocks_off, c->layout.windows_off, c->arena, err_word, nullptr,
+                                       nullptr, q, out, workspace, workspace_bytes, st, nullptr, nullptr,
+                                       c->meta16, out_f32);
+    if (s != OSCAR_OK) return s;
+    return ok();
+  } catch (const std::exception& ex) {
+    return fail(OSCAR_ERR_INVALID_ARG, "host allocation failed: %s", ex.what());
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
 oscar_status oscar_decode_attention(oscar_cache* c, int32_t n_seqs, const int32_t* seq_ids, const void* q,
                                     int32_t num_q_heads, float softmax_scale, void* out, void* workspace,
                                     size_t workspace_bytes, void* stream) {
@@ -630,14 +576,20 @@ oscar_status oscar_append_decode(oscar_cache* c, int32_t n_seqs, const int32_t* 
     const float scale = softmax_scale == 0.0f ? 1.0f / std::sqrt((float)kHeadDim) : softmax_scale;
     DeviceGuard dg(c->cfg.device);
     if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
-    if ((s = device_view_as(workspace, "workspace", c->cfg.device, &workspace, false)) != OSCAR_OK) return s;
+    uint32_t* err_word = reinterpret_cast<uint32_t*>(c->arena);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (n_seqs <= kDecodeSeqsSmall)
-      s = run_fused_decode<kDecodeSeqsSmall>(c, n_seqs, seq_ids, lens.data(), num_q_heads, scale, q, out, false,
-                                             workspace, workspace_bytes, st, k_new, v_new);
+      s = run_decode<kDecodeSeqsSmall>(c->cfg.device, c->sms, decode_int2_ctas_per_sm(), n_seqs, seq_ids,
+                                       lens.data(), hkv, num_q_heads, scale, 0, c->layout.max_groups,
+                                       c->layout.blocks_off, c->layout.windows_off, c->arena, err_word, nullptr,
+                                       nullptr, q, out, workspace, workspace_bytes, st, k_new, v_new,
+                                       c->meta16);
     else
-      s = run_fused_decode<kDecodeSeqsLarge>(c, n_seqs, seq_ids, lens.data(), num_q_heads, scale, q, out, false,
-                                             workspace, workspace_bytes, st, k_new, v_new);
+      s = run_decode<kDecodeSeqsLarge>(c->cfg.device, c->sms, decode_int2_ctas_per_sm(), n_seqs, seq_ids,
+                                       lens.data(), hkv, num_q_heads, scale, 0, c->layout.max_groups,
+                                       c->layout.blocks_off, c->layout.windows_off, c->arena, err_word, nullptr,
+                                       nullptr, q, out, workspace, workspace_bytes, st, k_new, v_new,
+                                       c->meta16);
     if (s != OSCAR_OK) return s;
     for (int32_t i = 0; i < n_seqs; ++i) c->len[seq_ids[i]] = lens[i];
     return ok();
@@ -794,9 +746,7 @@ oscar_status oscar_cache_check(oscar_cache* c, void* stream) {
   e = cudaMemcpy(&word, c->arena, 4, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
   if (word != 0) {
-    // a kernel that gave up may have left row tickets counted: clear them too
     cudaMemset(c->arena, 0, 4);
-    cudaMemset(c->arena + c->layout.tickets_off, 0, (size_t)c->cfg.max_batch * c->cfg.num_kv_heads * 4);
     return fail(OSCAR_ERR_DEVICE_TIMEOUT, "a kernel wait timed out (flags 0x%x)", word);
   }
   return ok();
