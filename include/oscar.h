@@ -316,6 +316,18 @@ oscar_status oscar_cache_block_offset(const oscar_cache* cache, int32_t seq, int
 oscar_status oscar_cache_window_offset(const oscar_cache* cache, int32_t seq, int32_t kv_head,
                                        size_t* out_offset);
 
+/*
+ * Test hook of the failure path: the next INT2 decode launch made on the
+ * calling thread (oscar_decode_attention, _f32 or oscar_append_decode) has
+ * one bulk copy of its first CTA left unissued, and its bounded waits give up
+ * after 2^14 polls instead of 2^24.  The consumer waiting for that copy then
+ * gives up, the kernel sets the arena's error flag, skips its remaining work
+ * and returns (no fault, no hang; the results of that call are undefined),
+ * and oscar_cache_check reports OSCAR_ERR_DEVICE_TIMEOUT.  Later calls are
+ * unaffected.  Not for production use.
+ */
+oscar_status oscar_test_arm_wait_timeout(void);
+
 /* Synchronise `stream`, then read the device error flags of the arena.
  * Returns OSCAR_ERR_DEVICE_TIMEOUT if a kernel's bounded wait gave up since
  * the last check (and clears the flags), OSCAR_OK otherwise. */

@@ -142,8 +142,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // later wait returns immediately so that the CTA still reaches its barriers
 // and exits.  err_word may be NULL (no device status word).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                                  uint32_t* err_word) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+                                                  uint32_t* err_word, uint32_t limit = kSpinLimit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
   }
@@ -158,8 +158,8 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 // the same parity, so the parity test cannot be fooled when several consumer
 // warps share a ring.
 __device__ __forceinline__ bool wait_issued(const volatile uint32_t* issued, uint32_t n, volatile int* abort_flag,
-                                            uint32_t* err_word) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+                                            uint32_t* err_word, uint32_t limit = kSpinLimit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (*issued > n) return true;
     if (*abort_flag) return false;
   }

@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     if (lane != 0) return;
     int64_t k = 0;
     int64_t u = u0;
-    if (!mbar_wait_bounded(&S.qready, 0, &S.abort_flag, p.h.err_word)) goto drain;
+    if (!mbar_wait_bounded(&S.qready, 0, &S.abort_flag, p.h.err_word, p.h.spin_limit)) goto drain;
     while (u < u1) {
       int b, j, g, ng;
       locate_unit(p, u, b, j, g, ng);
@@ -194,12 +194,17 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       for (; u < seg_end; ++u, ++k, src += kStageBytes) {
         const int s = (int)(k % kStages);
         if (k >= kStages) {
-          if (!mbar_wait_bounded(&S.empty[s], (uint32_t)(((k / kStages) - 1) & 1), &S.abort_flag, p.h.err_word)) {
+          if (!mbar_wait_bounded(&S.empty[s], (uint32_t)(((k / kStages) - 1) & 1), &S.abort_flag, p.h.err_word,
+                                 p.h.spin_limit)) {
             goto drain;
           }
         }
-        mbar_arrive_expect_tx(&S.full[s], kStageBytes);
-        bulk_g2s(S.stage[s], src, kStageBytes, &S.full[s]);
+        // (failure-path test: the copy of one unit of CTA 0 is never issued,
+        // so the phase its consumer waits for never completes)
+        if (!(cta == 0 && k == p.h.fault_unit)) {
+          mbar_arrive_expect_tx(&S.full[s], kStageBytes);
+          bulk_g2s(S.stage[s], src, kStageBytes, &S.full[s]);
+        }
         reinterpret_cast<volatile uint32_t*>(S.issued)[s] = (uint32_t)(k / kStages) + 1;
       }
     }
@@ -209,7 +214,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       const int64_t first = k > kStages ? k - kStages : 0;
       for (int64_t kk = first; kk < k; ++kk) {
         const int s = (int)(kk % kStages);
-        for (uint32_t i = 0; i < kSpinLimit; ++i)
+        for (uint32_t i = 0; i < p.h.spin_limit; ++i)
           if (mbar_try_wait(&S.full[s], (uint32_t)((kk / kStages) & 1))) break;
       }
     }
@@ -364,8 +369,8 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
          kk += kConsumers) {
       const int s = (int)(kk % kStages);
       const uint32_t use = (uint32_t)(kk / kStages);
-      if (!wait_issued(&S.issued[s], use, &S.abort_flag, p.h.err_word)) continue;
-      if (!mbar_wait_bounded(&S.full[s], use & 1, &S.abort_flag, p.h.err_word)) continue;
+      if (!wait_issued(&S.issued[s], use, &S.abort_flag, p.h.err_word, p.h.spin_limit)) continue;
+      if (!mbar_wait_bounded(&S.full[s], use & 1, &S.abort_flag, p.h.err_word, p.h.spin_limit)) continue;
       const uint8_t* blk = S.stage[s];
       const uint8_t* ksc = blk + B::kKScale;
       const uint8_t* kze = blk + B::kKZero;

@@ -118,7 +118,11 @@ struct DecodeHeader {
   int32_t comb_wrows;
   int32_t comb_part_bytes;
   int32_t out_f32;       // the combine writes float32 outputs (else bf16)
-  int32_t pad_;
+  // bounded waits of the INT2 main kernel give up after this many polls; a
+  // test of that path sets fault_unit >= 0: CTA 0's producer then leaves that
+  // unit's copy unissued (its consumer's wait runs out), and a small limit
+  uint32_t spin_limit;
+  int32_t fault_unit;
 };
 
 template <int MAXS>

@@ -32,6 +32,9 @@ namespace {
 thread_local std::string g_err;
 thread_local cudaEvent_t g_ev_start = nullptr;
 thread_local cudaEvent_t g_ev_stop = nullptr;
+// armed by oscar_test_arm_wait_timeout: the next INT2 decode launch on this
+// thread leaves one copy unissued and gives up its waits early
+thread_local bool g_arm_timeout = false;
 
 oscar_status fail(oscar_status s, const char* fmt, ...) {
   char buf[512];
@@ -221,6 +224,13 @@ oscar_status run_decode(int device, int sms, int ctas_per_sm, int32_t n, const i
   P.h.k_new = static_cast<const uint16_t*>(k_new);
   P.h.v_new = static_cast<const uint16_t*>(v_new);
   P.h.out_f32 = out_f32 ? 1 : 0;
+  P.h.spin_limit = kSpinLimit;
+  P.h.fault_unit = -1;
+  if (g_arm_timeout && !bf16_mode) {
+    g_arm_timeout = false;
+    P.h.spin_limit = 1u << 14;
+    P.h.fault_unit = 0;
+  }
   // The kernels serve at most kMaxGqa query heads of a KV head per launch (mma
   // columns = heads x {hi, lo}); larger groups run as consecutive passes, each
   // streaming the cache again.  Stream order keeps a pass's main kernel from
@@ -882,6 +892,11 @@ oscar_status oscar_decode_attention_noalloc(oscar_cache* c, int32_t n_seqs, cons
   }
   return oscar_decode_attention(c, n_seqs, seq_ids, q, num_q_heads, softmax_scale, out, scratch,
                                 kNoAllocScratchBytes, stream);
+}
+
+oscar_status oscar_test_arm_wait_timeout(void) {
+  g_arm_timeout = true;
+  return ok();
 }
 
 oscar_status oscar_set_timing_events(void* start_event, void* stop_event) {

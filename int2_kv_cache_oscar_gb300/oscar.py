@@ -74,6 +74,7 @@ def _load() -> ctypes.CDLL:
         "oscar_bf16_decode_attention": [I32, I32P, I32P, P, P, I32, I32, P, I32, ctypes.c_float, P, P,
                                         SZ, P],
         "oscar_set_timing_events": [P, P],
+        "oscar_test_arm_wait_timeout": [],
         "oscar_decode_attention_noalloc": [P, I32, I32P, P, I32, ctypes.c_float, P, P],
         "oscar_append_decode": [P, I32, I32P, P, P, P, I32, ctypes.c_float, P, P, SZ, P],
         "oscar_prefill_attention": [P, I32, I32, P, I32, ctypes.c_float, P, P, P, SZ, P],
@@ -319,6 +320,12 @@ def oscar_bf16_decode_attention(seq_ids: Sequence[int], seq_lens: Sequence[int],
         _buf(q, torch.bfloat16, shape, "q"), num_q_heads, ctypes.c_float(softmax_scale),
         _buf(out, torch.bfloat16, shape, "out"), _buf(workspace, torch.uint8, None, "workspace"),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def oscar_test_arm_wait_timeout() -> None:
+    """Test hook: the next INT2 decode on this thread leaves one copy unissued
+    so that a bounded device wait runs out (see include/oscar.h)."""
+    _check(_lib.oscar_test_arm_wait_timeout())
 
 
 def oscar_set_timing_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]):
