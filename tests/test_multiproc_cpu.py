@@ -52,3 +52,17 @@ def test_single_process_is_identity():
     import bench
     assert bench.max_over_ranks([1.5, 2.5]) == [1.5, 2.5]
     assert bench.replica_throughput(100.0, 1) == pytest.approx(1e4)
+
+
+def test_cycled_cache_copies_exceed_twice_l2():
+    """The bench cycles its steps over cache copies: between two uses of a
+    copy the others read more than 2x L2 (or one copy alone exceeds it)."""
+    import bench
+    l2 = 126 << 20
+    for nbytes in (7 << 20, 33554432, 113246208, 134 << 20, 253 << 20, 906 << 20):
+        c = bench.copies_for(nbytes, l2)
+        if c == 1:
+            assert nbytes > 2 * l2
+        else:
+            assert (c - 1) * nbytes >= 2 * l2
+    assert bench.copies_for(113246208, l2) == 4
