@@ -200,6 +200,13 @@ oscar_status oscar_decode_workspace_bytes(const oscar_cache* cache, int32_t n_se
  * a decode step from host inputs to host outputs needs no staging copies.
  * Pageable host memory and device memory of another device fail with
  * OSCAR_ERR_INVALID_ARG before anything is enqueued.
+ * Stream order: the main kernel is launched as a programmatic dependent of
+ * the kernel before it in `stream`.  Before it waits for that kernel it only
+ * copies cache blocks of groups closed before the previous decode call on
+ * this cache, when that call used the same stream (the library tracks its
+ * appends and decodes); q, the workspace and all other inputs are read after
+ * the wait, so a preceding kernel may produce q.  The arena must be written
+ * through this library only.
  */
 oscar_status oscar_decode_attention(oscar_cache* cache, int32_t n_seqs, const int32_t* seq_ids,
                                     const void* q, int32_t num_q_heads, float softmax_scale,
@@ -327,6 +334,14 @@ oscar_status oscar_cache_window_offset(const oscar_cache* cache, int32_t seq, in
  * unaffected.  Not for production use.
  */
 oscar_status oscar_test_arm_wait_timeout(void);
+
+/* Test hook: for each of the n_seqs slots in seq_ids, the number of leading
+ * groups whose blocks the next decode on `stream` would copy before its grid
+ * dependency wait (INT32_MAX: all of them), from the host's record of the
+ * appends, resets and decodes enqueued on this cache.  out: host int32
+ * [n_seqs].  Enqueues nothing. */
+oscar_status oscar_test_settled_groups(const oscar_cache* cache, int32_t n_seqs,
+                                       const int32_t* seq_ids, void* stream, int32_t* out);
 
 /* Synchronise `stream`, then read the device error flags of the arena.
  * Returns OSCAR_ERR_DEVICE_TIMEOUT if a kernel's bounded wait gave up since

@@ -15,6 +15,11 @@
 //     mbarrier transaction counts) and publishes how many uses of each stage
 //     it has issued, so that a consumer waits on a stage's barrier only for a
 //     phase that exists (no parity aliasing);
+//   * the grid is a programmatic dependent of the kernel before it: the
+//     producer fills the ring with blocks of settled groups (ones no running
+//     kernel can be writing; the host tracks appends) before the grid
+//     dependency wait, so back-to-back steps overlap one step's ring fill
+//     with the previous step's combine; everything else waits;
 //   * each consumer warp takes every 4th group and runs both contractions on
 //     the tensor cores with mma.sync m16n8k16: the 2-bit codes are the A
 //     operand, taken straight from the packed words with one AND each (an
@@ -37,6 +42,11 @@ namespace {
 constexpr int kConsumers = 4;
 constexpr int kDecThreads = (kConsumers + 1) * 32;
 constexpr int kCtasPerSm = 2;
+// Ring stages filled before the grid dependency wait.  Back-to-back 128K
+// steps (CUDA graph): 1, 2, 3, 4, 7 stages -> 30.1, 30.0, 30.2, 30.6, 31.8 us
+// (31.3 us without the early fill); more stages crowd the previous kernel's
+// own loads.
+constexpr int kPreWaitStages = 2;
 constexpr int kPbStride = kGroup + 16;  // probability rows (see pb_col)
 
 // Ring geometry by metadata width: 7 stages of 13,824 B, or 8 of 11,008 B
@@ -46,6 +56,9 @@ struct Ring {
   static constexpr int kStages = M16 ? 8 : 7;
   static constexpr int kStageBytes = Blk<M16>::kBytes;
 };
+
+static_assert(kPreWaitStages <= Ring<false>::kStages && kPreWaitStages <= Ring<true>::kStages,
+              "the pre-wait fill uses each stage once (no free-slot waits)");
 
 template <bool M16>
 struct DecSmemT {
@@ -142,6 +155,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Waits until the kernels this grid depends on have completed and their
+// writes are visible (returns at once when it was launched without a
+// programmatic dependency).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 template <int MAXS, bool M16>
 __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     decode_int2_kernel(const __grid_constant__ DecodeParams<MAXS> p, const uint8_t* __restrict__ arena) {
@@ -173,17 +191,39 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     fence_mbar_init();
   }
   __syncthreads();
-  // Every CTA of this grid is resident from the start (persistent grid), so
-  // the dependent combine may be scheduled now: its CTAs take SMs as these
-  // exit and attend to the window meanwhile; its griddepcontrol.wait still
-  // waits for this whole grid to complete before reading the partials.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == kConsumers) {
     // ------------------------------------------------------------ producer
     if (lane != 0) return;
     int64_t k = 0;
     int64_t u = u0;
+    // Use k of the ring: stage k mod kStages, one block.  (Failure-path test:
+    // the copy of one unit of CTA 0 is never issued, so the phase its
+    // consumer waits for never completes.)
+    auto issue = [&](int64_t kk, const uint8_t* src) {
+      const int s = (int)(kk % kStages);
+      if (!(cta == 0 && kk == p.h.fault_unit)) {
+        mbar_arrive_expect_tx(&S.full[s], kStageBytes);
+        bulk_g2s(S.stage[s], src, kStageBytes, &S.full[s]);
+      }
+      reinterpret_cast<volatile uint32_t*>(S.issued)[s] = (uint32_t)(kk / kStages) + 1;
+    };
+    // Ring fill before the grid dependency wait: blocks of settled groups
+    // (no kernel that may still run can be writing them), kPreWaitStages at
+    // most.  Launched as a programmatic dependent, this grid starts while the
+    // previous kernel finishes, and these copies overlap its tail.
+    while (u < u1 && k < kPreWaitStages) {
+      int b, j, g, ng;
+      locate_unit(p, u, b, j, g, ng);
+      const int64_t row_end = p.seq[b].ubase + (int64_t)(j + 1) * ng;
+      const int64_t seg_end = row_end < u1 ? row_end : u1;
+      const int settled = p.seq[b].settled;
+      const uint8_t* src = blocks + (((int64_t)p.seq[b].slot * hkv + j) * p.h.max_groups + g) * kStageBytes;
+      for (; u < seg_end && k < kPreWaitStages && g < settled; ++u, ++k, ++g, src += kStageBytes) issue(k, src);
+      if (u < seg_end) break;         // an unsettled group (or the ring is full)
+    }
+    grid_dependency_wait();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (!mbar_wait_bounded(&S.qready, 0, &S.abort_flag, p.h.err_word, p.h.spin_limit)) goto drain;
     while (u < u1) {
       int b, j, g, ng;
@@ -199,13 +239,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
             goto drain;
           }
         }
-        // (failure-path test: the copy of one unit of CTA 0 is never issued,
-        // so the phase its consumer waits for never completes)
-        if (!(cta == 0 && k == p.h.fault_unit)) {
-          mbar_arrive_expect_tx(&S.full[s], kStageBytes);
-          bulk_g2s(S.stage[s], src, kStageBytes, &S.full[s]);
-        }
-        reinterpret_cast<volatile uint32_t*>(S.issued)[s] = (uint32_t)(k / kStages) + 1;
+        issue(k, src);
       }
     }
   drain:
@@ -230,9 +264,20 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
   const int gqa = p.h.gqa;
   const float scale_log2 = p.h.scale_log2;
 
+  // The queries, the value-scale maxima and the workspace are outputs of the
+  // kernels before this one: wait for them.  Every CTA of this persistent grid
+  // is resident from the start, so the dependent combine may be scheduled now:
+  // its CTAs take SMs as these exit and attend to the window meanwhile (its
+  // own grid dependency wait still waits for this whole grid).  Triggering
+  // only after the wait keeps every kernel before this one complete by the
+  // time a dependent of the combine starts.
+  grid_dependency_wait();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   // The query rows and value-scale maxima of this CTA's first two segments
-  // are requested before the producer's first bulk copy (it waits on qready):
-  // requested after it they would queue behind every CTA's initial ring fill.
+  // are requested before the producer's copies past the ring fill (it waits
+  // on qready): requested after them they would queue behind every CTA's
+  // copies.
   uint2 qpre0 = make_uint2(0u, 0u), qpre1 = make_uint2(0u, 0u);
   uint32_t vpre0 = 0u, vpre1 = 0u;
   {
@@ -611,8 +656,6 @@ constexpr int kCombinePartBytes = 96 * 1024;   // at most this many bytes of par
 constexpr int kCombineSmem = kWindowBytes + kCombinePartBytes;   // largest launch
 constexpr int kCombineMaxChunk = kCombinePartBytes / (kPartialFloats * 4);
 
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 template <int MAXS>
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const __grid_constant__ DecodeParams<MAXS> p, const uint8_t* __restrict__ arena) {
@@ -750,6 +793,10 @@ __global__ void __launch_bounds__(kCombineThreads)
   // ---- merge: window state + partial records, chunk by chunk (heads in parallel);
   // chunk ck arrives on phase ck + 1 of the barrier
   grid_dependency_wait();            // the main kernel's partials are complete and visible
+  // The next decode's main kernel may start now (it copies only blocks of
+  // settled groups before its own wait, and every kernel before this one has
+  // completed).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int64_t ck = 0; ck < nchunks; ++ck) {
     const int64_t c0 = ck * per_chunk;
     const int n = (int)((count - c0) < per_chunk ? (count - c0) : per_chunk);
@@ -830,8 +877,20 @@ cudaError_t launch_decode_int2_t(const DecodeParams<MAXS>& p, const uint8_t* are
   cudaError_t e = ensure_smem_attr(decode_int2_kernel<MAXS, M16>, smem, attr_done);
   if (e != cudaSuccess) return e;
   if (ev_start) cudaEventRecord(ev_start, stream);
-  decode_int2_kernel<MAXS, M16><<<p.h.n_ctas, kDecThreads, smem, stream>>>(p, arena);
-  e = cudaGetLastError();
+  // programmatic dependent launch: the grid may start while the previous
+  // kernel in the stream finishes (see the producer's ring fill)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.h.n_ctas);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_int2_kernel<MAXS, M16>, p, arena);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (ev_stop) cudaEventRecord(ev_stop, stream);
   return e;
 }

@@ -87,7 +87,10 @@ struct DecodeSeq {
   int32_t len;
   int64_t ubase;  // first unit of this sequence
   int32_t rank;   // number of earlier sequences with >= 1 unit
-  int32_t pad;
+  // INT2: groups 0..settled-1 of each of this sequence's rows were written by
+  // kernels that have completed before this launch can start (the host tracks
+  // appends), so their blocks may be copied before the grid dependency wait
+  int32_t settled;
 };
 
 struct DecodeHeader {

@@ -25,6 +25,16 @@ struct oscar_cache {
   ArenaLayout layout;
   std::vector<int32_t> len;  // host mirror of every slot's length
   int sms;
+  // Pre-wait copies of the decode kernel (see DecodeSeq::settled): per slot,
+  // the lowest group an append may have written since the last decode call
+  // (INT32_MAX: none).  Every kernel enqueued before a decode call has
+  // completed by the time a later decode's main kernel starts on the same
+  // stream (each kernel of the chain triggers its dependents only after its
+  // own grid dependency wait), so a decode on the stream of the previous one
+  // may copy the blocks of groups below that bound early.
+  std::vector<int32_t> fresh_from;
+  bool decoded = false;          // a decode was enqueued on last_stream
+  cudaStream_t last_stream = nullptr;
 };
 
 namespace {
@@ -178,7 +188,7 @@ void fill_decode(DecodeParams<MAXS>& P, int32_t n, const int32_t* slots, const i
     P.seq[i].len = len;
     P.seq[i].ubase = ubase;
     P.seq[i].rank = rank;
-    P.seq[i].pad = 0;
+    P.seq[i].settled = 0;
     ubase += (int64_t)hkv * units;
     if (units > 0) ++rank;
   }
@@ -192,11 +202,13 @@ oscar_status run_decode(int device, int sms, int ctas_per_sm, int32_t n, const i
                         int64_t windows_off, const uint8_t* arena, uint32_t* err_word, const uint16_t* kc,
                         const uint16_t* vc, const void* q, void* out, void* ws, size_t ws_bytes,
                         cudaStream_t stream, const void* k_new = nullptr, const void* v_new = nullptr,
-                        bool meta16 = false, bool out_f32 = false) {
+                        bool meta16 = false, bool out_f32 = false, const int32_t* settled = nullptr) {
   DecodeParams<MAXS> P;
   std::memset(&P, 0, sizeof(P));
   int64_t rows = 0;
   fill_decode(P, n, slots, lens, hkv, bf16_mode, rows);
+  if (settled)
+    for (int32_t i = 0; i < n; ++i) P.seq[i].settled = settled[i];
   const int q_group = hq / hkv;
   const int64_t T = P.h.n_units;
   const int64_t maxN = (int64_t)sms * ctas_per_sm;
@@ -233,9 +245,10 @@ oscar_status run_decode(int device, int sms, int ctas_per_sm, int32_t n, const i
   }
   // The kernels serve at most kMaxGqa query heads of a KV head per launch (mma
   // columns = heads x {hi, lo}); larger groups run as consecutive passes, each
-  // streaming the cache again.  Stream order keeps a pass's main kernel from
-  // overlapping the previous pass's combine on the shared workspace, and a
-  // fused step's passes all store the same new token.
+  // streaming the cache again.  A pass's main kernel writes the shared
+  // workspace only after its grid dependency wait (the previous pass's
+  // combine has completed), and a fused step's passes all store the same new
+  // token.
   // combine staging: the longest window of the batch, and the most split-K
   // records any row has (same split as the kernels: unit u in CTA
   // ((u + 1) N - 1) / T), so that small stages let several combine CTAs share an SM
@@ -271,6 +284,9 @@ oscar_status run_decode(int device, int sms, int ctas_per_sm, int32_t n, const i
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     e = launch_combine(P, arena, stream);
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    // a later pass's main kernel starts after this pass's main kernel has
+    // completed, and with it every kernel before it: all groups are settled
+    for (int32_t i = 0; i < n; ++i) P.seq[i].settled = INT32_MAX;
   }
   (void)device;
   return OSCAR_OK;
@@ -318,6 +334,7 @@ oscar_status oscar_cache_create(const oscar_cache_config* cfg, void* device_aren
     c->arena_bytes = arena_bytes;
     c->layout = L;
     c->len.assign(cfg->max_batch, 0);
+    c->fresh_from.assign(cfg->max_batch, 0);
     c->sms = sms;
     *out = c;
     return ok();
@@ -344,10 +361,13 @@ oscar_status oscar_cache_reset(oscar_cache* c, int32_t seq, void* stream) {
   else
     e = cudaMemsetAsync(meta + (size_t)seq * hkv * 4, 0, (size_t)hkv * 4, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(reset)");
-  if (seq < 0)
+  if (seq < 0) {
     std::fill(c->len.begin(), c->len.end(), 0);
-  else
+    std::fill(c->fresh_from.begin(), c->fresh_from.end(), 0);
+  } else {
     c->len[seq] = 0;
+    c->fresh_from[seq] = 0;
+  }
   return ok();
 }
 
@@ -439,7 +459,12 @@ oscar_status oscar_quantize_append(oscar_cache* c, int32_t n_seqs, const int32_t
       }
       if (s != OSCAR_OK) return s;  // earlier chunks may already be enqueued
     }
-    for (int32_t i = 0; i < n_seqs; ++i) c->len[seq_ids[i]] += cu_new[i + 1] - cu_new[i];
+    for (int32_t i = 0; i < n_seqs; ++i) {
+      const int32_t slot = seq_ids[i];
+      const int32_t L0 = c->len[slot], L1 = L0 + (cu_new[i + 1] - cu_new[i]);
+      if (L1 / kGroup > L0 / kGroup) c->fresh_from[slot] = std::min(c->fresh_from[slot], L0 / kGroup);
+      c->len[slot] = L1;
+    }
     return ok();
   } catch (const std::exception& ex) {
     return fail(OSCAR_ERR_INVALID_ARG, "host allocation failed: %s", ex.what());
@@ -461,6 +486,25 @@ oscar_status oscar_decode_workspace_bytes(const oscar_cache* c, int32_t n_seqs, 
 }  // extern "C"
 
 namespace {
+
+// Per decoded sequence, the groups whose blocks the main kernel may copy
+// before its grid dependency wait (none unless the previous decode on this
+// cache ran on the same stream).
+std::vector<int32_t> settled_groups(const oscar_cache* c, int32_t n, const int32_t* ids, cudaStream_t st) {
+  std::vector<int32_t> r(n, 0);
+  if (c->decoded && c->last_stream == st)
+    for (int32_t i = 0; i < n; ++i) r[i] = c->fresh_from[ids[i]];
+  return r;
+}
+
+// After a decode is enqueued: appends before it have completed when the next
+// decode on this stream starts.
+void note_decode(oscar_cache* c, int32_t n, const int32_t* ids, cudaStream_t st) {
+  if (!(c->decoded && c->last_stream == st)) std::fill(c->fresh_from.begin(), c->fresh_from.end(), 0);
+  for (int32_t i = 0; i < n; ++i) c->fresh_from[ids[i]] = INT32_MAX;
+  c->decoded = true;
+  c->last_stream = st;
+}
 
 // oscar_decode_attention and oscar_decode_attention_f32 (out_f32: float32 outputs).
 oscar_status decode_call(oscar_cache* c, int32_t n_seqs, const int32_t* seq_ids, const void* q, int32_t num_q_heads,
@@ -494,19 +538,21 @@ oscar_status decode_call(oscar_cache* c, int32_t n_seqs, const int32_t* seq_ids,
     if ((s = device_view_as(workspace, "workspace", c->cfg.device, &workspace, false)) != OSCAR_OK) return s;
     uint32_t* err_word = reinterpret_cast<uint32_t*>(c->arena);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const std::vector<int32_t> settled = settled_groups(c, n_seqs, seq_ids, st);
     if (n_seqs <= kDecodeSeqsSmall)
       s = run_decode<kDecodeSeqsSmall>(c->cfg.device, c->sms, decode_int2_ctas_per_sm(), n_seqs, seq_ids,
                                        lens.data(), hkv, num_q_heads, scale, 0, c->layout.max_groups,
                                        c->layout.blocks_off, c->layout.windows_off, c->arena, err_word, nullptr,
                                        nullptr, q, out, workspace, workspace_bytes, st, nullptr, nullptr,
-                                       c->meta16, out_f32);
+                                       c->meta16, out_f32, settled.data());
     else
       s = run_decode<kDecodeSeqsLarge>(c->cfg.device, c->sms, decode_int2_ctas_per_sm(), n_seqs, seq_ids,
                                        lens.data(), hkv, num_q_heads, scale, 0, c->layout.max_groups,
                                        c->layout.blocks_off, c->layout.windows_off, c->arena, err_word, nullptr,
                                        nullptr, q, out, workspace, workspace_bytes, st, nullptr, nullptr,
-                                       c->meta16, out_f32);
+                                       c->meta16, out_f32, settled.data());
     if (s != OSCAR_OK) return s;
+    note_decode(c, n_seqs, seq_ids, st);
     return ok();
   } catch (const std::exception& ex) {
     return fail(OSCAR_ERR_INVALID_ARG, "host allocation failed: %s", ex.what());
@@ -529,6 +575,22 @@ oscar_status oscar_decode_attention_f32(oscar_cache* c, int32_t n_seqs, const in
                                         size_t workspace_bytes, void* stream) {
   return decode_call(c, n_seqs, seq_ids, q, num_q_heads, softmax_scale, out, true, workspace, workspace_bytes,
                      stream);
+}
+
+oscar_status oscar_test_settled_groups(const oscar_cache* c, int32_t n_seqs, const int32_t* seq_ids, void* stream,
+                                       int32_t* out) {
+  try {
+    if (!c || !seq_ids || !out) return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+    if (n_seqs < 0) return fail(OSCAR_ERR_INVALID_ARG, "n_seqs < 0");
+    std::vector<char> seen;
+    oscar_status s = check_slots(c, n_seqs, seq_ids, seen);
+    if (s != OSCAR_OK) return s;
+    const std::vector<int32_t> r = settled_groups(c, n_seqs, seq_ids, static_cast<cudaStream_t>(stream));
+    for (int32_t i = 0; i < n_seqs; ++i) out[i] = r[i];
+    return ok();
+  } catch (const std::exception& ex) {
+    return fail(OSCAR_ERR_INVALID_ARG, "host allocation failed: %s", ex.what());
+  }
 }
 
 oscar_status oscar_append_decode(oscar_cache* c, int32_t n_seqs, const int32_t* seq_ids, const void* k_new,
@@ -588,19 +650,21 @@ oscar_status oscar_append_decode(oscar_cache* c, int32_t n_seqs, const int32_t* 
     if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
     uint32_t* err_word = reinterpret_cast<uint32_t*>(c->arena);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const std::vector<int32_t> settled = settled_groups(c, n_seqs, seq_ids, st);
     if (n_seqs <= kDecodeSeqsSmall)
       s = run_decode<kDecodeSeqsSmall>(c->cfg.device, c->sms, decode_int2_ctas_per_sm(), n_seqs, seq_ids,
                                        lens.data(), hkv, num_q_heads, scale, 0, c->layout.max_groups,
                                        c->layout.blocks_off, c->layout.windows_off, c->arena, err_word, nullptr,
                                        nullptr, q, out, workspace, workspace_bytes, st, k_new, v_new,
-                                       c->meta16);
+                                       c->meta16, false, settled.data());
     else
       s = run_decode<kDecodeSeqsLarge>(c->cfg.device, c->sms, decode_int2_ctas_per_sm(), n_seqs, seq_ids,
                                        lens.data(), hkv, num_q_heads, scale, 0, c->layout.max_groups,
                                        c->layout.blocks_off, c->layout.windows_off, c->arena, err_word, nullptr,
                                        nullptr, q, out, workspace, workspace_bytes, st, k_new, v_new,
-                                       c->meta16);
+                                       c->meta16, false, settled.data());
     if (s != OSCAR_OK) return s;
+    note_decode(c, n_seqs, seq_ids, st);
     for (int32_t i = 0; i < n_seqs; ++i) c->len[seq_ids[i]] = lens[i];
     return ok();
   } catch (const std::exception& ex) {

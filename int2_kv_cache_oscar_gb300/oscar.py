@@ -75,6 +75,7 @@ def _load() -> ctypes.CDLL:
                                         SZ, P],
         "oscar_set_timing_events": [P, P],
         "oscar_test_arm_wait_timeout": [],
+        "oscar_test_settled_groups": [P, I32, I32P, P, I32P],
         "oscar_decode_attention_noalloc": [P, I32, I32P, P, I32, ctypes.c_float, P, P],
         "oscar_append_decode": [P, I32, I32P, P, P, P, I32, ctypes.c_float, P, P, SZ, P],
         "oscar_prefill_attention": [P, I32, I32, P, I32, ctypes.c_float, P, P, P, SZ, P],
@@ -326,6 +327,15 @@ def oscar_test_arm_wait_timeout() -> None:
     """Test hook: the next INT2 decode on this thread leaves one copy unissued
     so that a bounded device wait runs out (see include/oscar.h)."""
     _check(_lib.oscar_test_arm_wait_timeout())
+
+
+def oscar_test_settled_groups(cache, seq_ids: Sequence[int], stream=None) -> list:
+    """Test hook: per slot, the leading groups the next decode on `stream`
+    would copy before its grid dependency wait (see include/oscar.h)."""
+    handle = cache.handle if isinstance(cache, OscarCache) else cache
+    out = (ctypes.c_int32 * max(len(seq_ids), 1))()
+    _check(_lib.oscar_test_settled_groups(handle, len(seq_ids), _i32(seq_ids), _stream(stream), out))
+    return [int(out[i]) for i in range(len(seq_ids))]
 
 
 def oscar_set_timing_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]):
