@@ -17,7 +17,7 @@ LIB = os.path.join(PKG, "liboscar.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
-SOURCES = ["quantize.cu", "decode.cu", "prefill.cu", "bf16_decode.cu", "oscar_api.cu"]
+SOURCES = ["quantize.cu", "decode.cu", "prefill.cu", "prefill_tc.cu", "bf16_decode.cu", "oscar_api.cu"]
 
 
 def _nvcc() -> str:

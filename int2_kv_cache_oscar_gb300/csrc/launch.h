@@ -171,6 +171,8 @@ struct PrefillParams {
 constexpr int kPrefillRecFloats = 132;
 
 cudaError_t launch_prefill(const PrefillParams& p, const uint8_t* arena, bool meta16, cudaStream_t stream);
+// the tcgen05 history kernel (prefill_tc.cu); launch_prefill adds the merge of split parts
+cudaError_t launch_prefill_tc(const PrefillParams& p, const uint8_t* arena, bool meta16, cudaStream_t stream);
 
 int num_sms(int device);
 int decode_int2_ctas_per_sm();
