@@ -43,7 +43,7 @@ namespace oscar {
 namespace {
 
 constexpr int kTcRows = 128;
-constexpr int kTcThreads = 8 * 32;
+constexpr int kTcThreads = 12 * 32;
 constexpr int kTcStages = 3;
 constexpr int kNS = 144;                 // score B rows (and value B rows with the zero rows): 128 + 16
 constexpr int kBBytes = kNS * kHeadDim * 2;
@@ -79,9 +79,13 @@ struct TcSmem {
   float zmax[2][4];                                   // per builder warp: max |z^V| (double-buffered)
   int gz[2];                                          // the value-zero rows carry 2^gz (double-buffered)
   float fexp[kTcRows];                                // 2^-(F_row + 2) * scale_log2
+  float pmax[2][kTcRows];                             // row maxima of the two token halves
+  float lpart[kTcRows];                               // the second half's sum of p
   alignas(8) uint64_t full[kTcStages];
   uint64_t zred, sdone, pready, odone;
-  uint64_t meta_k, meta_v;   // the norms / the zero exponent of a group are in shared memory (builders -> rows)
+  // steps whose key / value operands (and norms / zero exponent) are complete:
+  // monotonic counts, since the builders may run a step ahead of a waiter
+  uint32_t kready, vready;
   uint32_t nissued[kTcStages];
   uint32_t tmem_base;
   int abort_flag;
@@ -102,6 +106,29 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile
   *abort_flag = 1;
   if (err != nullptr) atomicOr(err, kErrTimeout);
   return false;
+}
+
+// Bounded wait until a count published by another role exceeds n (then the
+// writes before the count are visible), with the same back-off.
+__device__ __forceinline__ bool tc_wait_count(const uint32_t* cnt, uint32_t n, volatile int* abort_flag,
+                                              uint32_t* err) {
+  for (uint32_t i = 0; i < (1u << 22); ++i) {
+    if (*reinterpret_cast<const volatile uint32_t*>(cnt) > n) {
+      __threadfence_block();
+      return true;
+    }
+    if (*abort_flag) return false;
+    if (i >= 4) __nanosleep(i < 64 ? 32 : 128);
+  }
+  *abort_flag = 1;
+  if (err != nullptr) atomicOr(err, kErrTimeout);
+  return false;
+}
+
+// Publish count n (after this thread's barrier with the writers).
+__device__ __forceinline__ void publish(uint32_t* cnt, uint32_t n) {
+  __threadfence_block();
+  *reinterpret_cast<volatile uint32_t*>(cnt) = n;
 }
 
 __device__ __forceinline__ float tc_pow2(int e) {
@@ -325,12 +352,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(&S.sdone, 1);
     mbar_init(&S.pready, 1);
     mbar_init(&S.odone, 1);
-    mbar_init(&S.meta_k, 1);
-    mbar_init(&S.meta_v, 1);
+    S.kready = 0;
+    S.vready = 0;
     S.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == 8) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" :: "r"(smem_u32(&S.tmem_base)),
                  "r"(kTCols) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -339,7 +366,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // staging area, then each row thread stores its row into TMEM
   float* qst = reinterpret_cast<float*>(S.v1);                    // [128][128] rotated q * 2^F (v1, v2)
   uint32_t* qraw = reinterpret_cast<uint32_t*>(S.k1);             // [128][64] raw bf16 pairs
-  for (int r = warp; r < kTcRows; r += 8) {
+  for (int r = warp; r < kTcRows; r += 12) {
     const int row = blockIdx.x * kTcRows + r;
     uint2 raw = make_uint2(0u, 0u);
     if (row < p.rows) {
@@ -408,20 +435,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();   // the staging areas are free again
   tfence_after();
 
-  if (warp >= 4) {
+  if (warp >= 8) {
     // =============================================================== builders
     // Every builder runs the same barriers in every step; after a wait gives
     // up (abort) the work is skipped but the control flow stays the same.
-    const int b = tid - 128;     // token (key codes, value zero rows) or channel (value codes)
-    const int bw = warp - 4;
+    const int b = tid - 256;     // token (key codes, value zero rows) or channel (value codes)
+    const int bw = warp - 8;
     const float gv = tc_pow2(Gv);
-    const bool lead = b == 0;    // also streams the blocks and issues the MMAs
-    const uint32_t idS = idesc_f16(kNS, false), idO = idesc_f16(kHeadDim, false), idZ = idesc_f16(16, false);
-    const uint32_t idW = idesc_f16(kHeadDim, true);
-    const uint32_t sk1 = smem_u32(S.k1), sk2 = smem_u32(S.k2), sv1 = smem_u32(S.v1), sv2 = smem_u32(S.v2);
+    const bool lead = b == 0;    // also streams the group blocks
     const uint8_t* wsrc = arena + p.windows_off + ((int64_t)p.slot * p.hkv + j) * kWindowBytes;
-    bool o_started = false;
-    uint32_t n_sdone = 0, n_odone = 0;   // commits issued to each barrier (lead)
     if (lead) {
       for (int k = 0; k < ng && k < kTcStages; ++k) {
         mbar_arrive_expect_tx(&S.full[k], B::kBytes);
@@ -429,32 +451,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         S.nissued[k] = 1;
       }
     }
-    // P.V of step kp (lead): the rows have written its P; the value operands
-    // of step kp are complete (built in the previous iteration)
-    auto issue_pv = [&](int kp) {
-      if (!tc_wait(&S.pready, (uint32_t)(kp & 1), &S.abort_flag, p.err_word)) return;
-      tfence_after();
-      const bool win = kp == ng;
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t ah = tmem + p_col(ks, false), al = tmem + p_col(ks, true);
-        const uint64_t dv1 = sdesc(sv1 + 2 * ks * kLboB, kLboB, kSbo);
-        if (win) {
-          mma_ts(tmem + kTO, ah, dv1, idW, o_started || ks > 0);
-          mma_ts(tmem + kTO, al, dv1, idW, true);
-        } else {
-          const uint64_t dv2 = sdesc(sv2 + 2 * ks * kLboV2, kLboV2, kSbo);
-          const uint64_t dvz = sdesc(sv1 + 2 * ks * kLboB + (kHeadDim / 8) * 128, kLboB, kSbo);
-          mma_ts(tmem + kTO, ah, dv1, idO, o_started || ks > 0);
-          mma_ts(tmem + kTO, al, dv1, idO, true);
-          mma_ts(tmem + kTO, ah, dv2, idO, true);
-          mma_ts(tmem + kTZ, ah, dvz, idZ, ks > 0);
-          mma_ts(tmem + kTZ, al, dvz, idZ, true);
-        }
-      }
-      o_started = true;
-      mma_commit(&S.odone);
-      ++n_odone;
-    };
     for (int k = 0; k < nsteps; ++k) {
       const bool win = k == ng;
       const int s = k % kTcStages;
@@ -479,25 +475,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       async_fence();
       bar_sync_threads(2, 128);
-      if (lead) mbar_arrive(&S.meta_k);
-      if (lead && ok) {
-        // the P.V of step k - 1 goes first (the scores of step k overwrite its P)
-        if (k > 0) issue_pv(k - 1);
-        tfence_after();
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t dk1 = sdesc(sk1 + 2 * ks * kLboB, kLboB, kSbo);
-          if (win) {
-            mma_ts(tmem + kTS, tmem + kTQraw + 8 * ks, dk1, idW, ks > 0);
-          } else {
-            const uint64_t dk2 = sdesc(sk2 + 2 * ks * kLboB, kLboB, kSbo);
-            mma_ts(tmem + kTS, tmem + kTQ + 8 * ks, dk1, idS, ks > 0);
-            mma_ts(tmem + kTS, tmem + kTQ + 64 + 8 * ks, dk1, idS, true);
-            mma_ts(tmem + kTS, tmem + kTQ + 8 * ks, dk2, idS, true);
-          }
-        }
-        mma_commit(&S.sdone);
-        ++n_sdone;
-      }
+      if (lead) publish(&S.kready, (uint32_t)(k + 1));
       // ---- value operands of step k, once the P.V of step k - 1 is done
       ok = ok && (k == 0 || tc_wait(&S.odone, (uint32_t)((k - 1) & 1), &S.abort_flag, p.err_word));
       if (win) {
@@ -515,6 +493,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         async_fence();
         bar_sync_threads(2, 128);
+        if (lead) publish(&S.vready, (uint32_t)(k + 1));
         continue;
       }
       float zm = 0.0f;
@@ -588,7 +567,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       async_fence();
       bar_sync_threads(2, 128);
-      if (lead) mbar_arrive(&S.meta_v);
+      if (lead) publish(&S.vready, (uint32_t)(k + 1));
       if (lead && ok && k + kTcStages < ng) {
         // the block is consumed: refill its stage
         async_fence();
@@ -597,28 +576,69 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         S.nissued[s] += 1;
       }
     }
-    if (lead) {
-      if (nsteps > 0 && !S.abort_flag) issue_pv(nsteps - 1);
-      // before TMEM is freed: the last committed MMAs have completed (bounded,
-      // whatever the abort state: MMAs always complete)
-      for (int q = 0; q < 2; ++q) {
-        const uint32_t n = q ? n_odone : n_sdone;
-        if (n == 0) continue;
-        for (uint32_t i = 0; i < kSpinLimit; ++i)
-          if (mbar_try_wait(q ? &S.odone : &S.sdone, (n - 1) & 1)) break;
-      }
-    }
   } else {
     // =================================================================== rows
-    // As for the builders: the same barriers in every step, work skipped after an abort.
-    const int r = tid;
+    // Warps w and w + 4 share rows 32 (w & 3) .. + 31 (their TMEM lanes) and
+    // split the tokens: half 0 takes tokens 0..63 and owns O, the zero sums
+    // and the output; half 1 takes tokens 64..127.  As for the builders: the
+    // same barriers in every step, work skipped after an abort.  Thread 0 also
+    // issues every tcgen05.mma: the scores of step k + 1 right after the P.V
+    // of step k (the scores overwrite its P).
+    const int half = warp >> 2;
+    const int r = 32 * (warp & 3) + lane;
     const int row = blockIdx.x * kTcRows + r;
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const bool issuer = tid == 0;
     const float fr = S.fexp[r];
-    float m_used = -INFINITY, l = 0.0f;
+    float m_used = -INFINITY, l = 0.0f;   // l: this half's sum of p
     float zacc[kVGroups] = {0.0f, 0.0f, 0.0f, 0.0f};
     bool ok = true;
-    // the value-zero term of step kz (after its P.V), folded into zacc
+    const uint32_t idS = idesc_f16(kNS, false), idO = idesc_f16(kHeadDim, false), idZ = idesc_f16(16, false);
+    const uint32_t idW = idesc_f16(kHeadDim, true);
+    const uint32_t sk1 = smem_u32(S.k1), sk2 = smem_u32(S.k2), sv1 = smem_u32(S.v1), sv2 = smem_u32(S.v2);
+    uint32_t n_sdone = 0, n_odone = 0;   // commits issued (issuer)
+    auto issue_scores = [&](int ks_step) {
+      if (!tc_wait_count(&S.kready, (uint32_t)ks_step, &S.abort_flag, p.err_word)) return;
+      tfence_after();
+      const bool w = ks_step == ng;
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint64_t dk1 = sdesc(sk1 + 2 * ks * kLboB, kLboB, kSbo);
+        if (w) {
+          mma_ts(tmem + kTS, tmem + kTQraw + 8 * ks, dk1, idW, ks > 0);
+        } else {
+          const uint64_t dk2 = sdesc(sk2 + 2 * ks * kLboB, kLboB, kSbo);
+          mma_ts(tmem + kTS, tmem + kTQ + 8 * ks, dk1, idS, ks > 0);
+          mma_ts(tmem + kTS, tmem + kTQ + 64 + 8 * ks, dk1, idS, true);
+          mma_ts(tmem + kTS, tmem + kTQ + 8 * ks, dk2, idS, true);
+        }
+      }
+      mma_commit(&S.sdone);
+      ++n_sdone;
+    };
+    auto issue_pv = [&](int kp) {
+      if (!tc_wait_count(&S.vready, (uint32_t)kp, &S.abort_flag, p.err_word)) return;
+      tfence_after();
+      const bool w = kp == ng;
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t ah = tmem + p_col(ks, false), al = tmem + p_col(ks, true);
+        const uint64_t dv1 = sdesc(sv1 + 2 * ks * kLboB, kLboB, kSbo);
+        if (w) {
+          mma_ts(tmem + kTO, ah, dv1, idW, kp > 0 || ks > 0);
+          mma_ts(tmem + kTO, al, dv1, idW, true);
+        } else {
+          const uint64_t dv2 = sdesc(sv2 + 2 * ks * kLboV2, kLboV2, kSbo);
+          const uint64_t dvz = sdesc(sv1 + 2 * ks * kLboB + (kHeadDim / 8) * 128, kLboB, kSbo);
+          mma_ts(tmem + kTO, ah, dv1, idO, kp > 0 || ks > 0);
+          mma_ts(tmem + kTO, al, dv1, idO, true);
+          mma_ts(tmem + kTO, ah, dv2, idO, true);
+          mma_ts(tmem + kTZ, ah, dvz, idZ, ks > 0);
+          mma_ts(tmem + kTZ, al, dvz, idZ, true);
+        }
+      }
+      mma_commit(&S.odone);
+      ++n_odone;
+    };
+    // the value-zero term of step kz (after its P.V), folded into zacc (half 0)
     auto take_z = [&](int kz) {
       uint32_t zr[16];
       tld16(lane_base + kTZ, zr);
@@ -627,53 +647,54 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int gr = 0; gr < 4; ++gr) zacc[gr] = fmaf(__uint_as_float(zr[gr]) + __uint_as_float(zr[4 + gr]), iz, zacc[gr]);
     };
+    if (issuer && nsteps > 0) issue_scores(0);
+    const int t0 = 64 * half;   // this half's first token
     for (int k = 0; k < nsteps; ++k) {
       const bool win = k == ng;
       const uint32_t par = (uint32_t)(k & 1);
       // the scores of step k are done, and with them the P.V of step k - 1
       ok = ok && tc_wait(&S.sdone, par, &S.abort_flag, p.err_word);
-      ok = ok && (win || tc_wait(&S.meta_k, par, &S.abort_flag, p.err_word));
-      ok = ok && (k == 0 || k - 1 == ng || tc_wait(&S.meta_v, (uint32_t)((k - 1) & 1), &S.abort_flag, p.err_word));
+      ok = ok && (win || tc_wait_count(&S.kready, (uint32_t)k, &S.abort_flag, p.err_word));
+      ok = ok && (k == 0 || tc_wait_count(&S.vready, (uint32_t)(k - 1), &S.abort_flag, p.err_word));
       ok = __all_sync(0xffffffffu, ok);   // TMEM loads and stores are warp-collective
+      float mx = -INFINITY;
+      float dz = 0.0f;
+      const float4* nrm4 = reinterpret_cast<const float4*>(S.nrm[k & 1]);
+      const float fs = win ? p.scale_log2 : 0.0f;
+      const float psc = win ? tc_pow2(Gv) : 1.0f;    // window P.V in the value pieces' units
+      // s - base for tokens c0 + i .. + 3 (log2 units): groups n_t (S_t + dz) fr,
+      // the window S_t scale (-inf past wlen)
+      auto shifted = [&](const uint32_t (&sr)[32], int c0, int i, float base, float2& w01, float2& w23) {
+        const float2 s01 = make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
+        const float2 s23 = make_float2(__uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
+        const float2 nb = make_float2(-base, -base);
+        if (win) {
+          const float2 f2 = make_float2(fs, fs);
+          w01 = __ffma2_rn(s01, f2, nb);
+          w23 = __ffma2_rn(s23, f2, nb);
+          if (c0 + i >= wlen) w01.x = -INFINITY;
+          if (c0 + i + 1 >= wlen) w01.y = -INFINITY;
+          if (c0 + i + 2 >= wlen) w23.x = -INFINITY;
+          if (c0 + i + 3 >= wlen) w23.y = -INFINITY;
+        } else {
+          const float4 n4 = nrm4[(c0 + i) >> 2];
+          const float2 d2 = make_float2(dz, dz), f2 = make_float2(fr, fr);
+          w01 = __ffma2_rn(__fadd2_rn(s01, d2), __fmul2_rn(make_float2(n4.x, n4.y), f2), nb);
+          w23 = __ffma2_rn(__fadd2_rn(s23, d2), __fmul2_rn(make_float2(n4.z, n4.w), f2), nb);
+        }
+      };
       if (ok) {
         tfence_after();
-        if (k > 0) take_z(k - 1);           // before this step's rescale and P.V
-        // score of token t (log2 units): groups n_t (S_t + dz) fr, window S_t scale (t < wlen)
-        float dz = 0.0f;
+        if (half == 0 && k > 0) take_z(k - 1);   // before this step's rescale and P.V
         if (!win) {
           uint32_t zr[16];
           tld16(lane_base + kTS + 128, zr);
           tld_wait();
           dz = __uint_as_float(zr[0]) + __uint_as_float(zr[1]);
         }
-        const float4* nrm4 = reinterpret_cast<const float4*>(S.nrm[k & 1]);
-        const float fs = win ? p.scale_log2 : 0.0f;
-        const float psc = win ? tc_pow2(Gv) : 1.0f;    // window P.V in the value pieces' units
-        // s - base for tokens c0 + i .. + 3 (log2 units): groups n_t (S_t + dz) fr,
-        // the window S_t scale (-inf past wlen)
-        auto shifted = [&](const uint32_t (&sr)[32], int c0, int i, float base, float2& w01, float2& w23) {
-          const float2 s01 = make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
-          const float2 s23 = make_float2(__uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
-          const float2 nb = make_float2(-base, -base);
-          if (win) {
-            const float2 f2 = make_float2(fs, fs);
-            w01 = __ffma2_rn(s01, f2, nb);
-            w23 = __ffma2_rn(s23, f2, nb);
-            if (c0 + i >= wlen) w01.x = -INFINITY;
-            if (c0 + i + 1 >= wlen) w01.y = -INFINITY;
-            if (c0 + i + 2 >= wlen) w23.x = -INFINITY;
-            if (c0 + i + 3 >= wlen) w23.y = -INFINITY;
-          } else {
-            const float4 n4 = nrm4[(c0 + i) >> 2];
-            const float2 d2 = make_float2(dz, dz), f2 = make_float2(fr, fr);
-            w01 = __ffma2_rn(__fadd2_rn(s01, d2), __fmul2_rn(make_float2(n4.x, n4.y), f2), nb);
-            w23 = __ffma2_rn(__fadd2_rn(s23, d2), __fmul2_rn(make_float2(n4.z, n4.w), f2), nb);
-          }
-        };
-        // pass 1: the row maximum (the scores stay in TMEM; pass 2 writes P over them)
-        float mx = -INFINITY;
+        // pass 1: this half's maximum (the scores stay in TMEM; pass 2 writes P over them)
 #pragma unroll 1
-        for (int c0 = 0; c0 < kGroup; c0 += 32) {
+        for (int c0 = t0; c0 < t0 + 64; c0 += 32) {
           uint32_t sr[32];
           tld32(lane_base + kTS + c0, sr);
           tld_wait();
@@ -684,13 +705,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mx = fmaxf(mx, fmaxf(fmaxf(w01.x, w01.y), fmaxf(w23.x, w23.y)));
           }
         }
-        // running maximum: rescale O (TMEM), the zero sums and l only when it
-        // grows by > 8 (per row; the TMEM pass runs for the whole warp when
-        // any of its rows needs it, with factor 1 for the others)
+        S.pmax[half][r] = mx;
+      }
+      named_bar_sync(3, 256);
+      if (ok) {
+        mx = fmaxf(mx, S.pmax[half ^ 1][r]);
+        // running maximum: rescale O (TMEM, half 0), the zero sums and l only when
+        // it grows by > 8 (per row, the same decision in both halves; the TMEM
+        // pass runs for the whole warp when any of its rows needs it)
         const float m_new = fmaxf(m_used, mx);
         const bool need = m_new > m_used + kRescaleLog2 || m_used == -INFINITY;
         const float alpha = !need ? 1.0f : m_used == -INFINITY ? 0.0f : tc_exp2(m_used - m_new);
-        if (k > 0 && __any_sync(0xffffffffu, need)) {   // O is not being written (see above)
+        if (half == 0 && k > 0 && __any_sync(0xffffffffu, need)) {   // O is not being written (see above)
 #pragma unroll 1
           for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
             uint32_t orr[32];
@@ -712,7 +738,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float base = m_used == -INFINITY ? 0.0f : m_used;
         float2 lsum = make_float2(0.0f, 0.0f);
 #pragma unroll 1
-        for (int c0 = 0; c0 < kGroup; c0 += 32) {
+        for (int c0 = t0; c0 < t0 + 64; c0 += 32) {
           uint32_t sr[32];
           tld32(lane_base + kTS + c0, sr);
           tld_wait();
@@ -733,19 +759,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tst_wait();
       tfence_before();
-      named_bar_sync(3, 128);
-      if (r == 0) mbar_arrive(&S.pready);
+      named_bar_sync(3, 256);
+      if (issuer && ok) {
+        issue_pv(k);
+        if (k + 1 < nsteps) issue_scores(k + 1);
+      }
     }
-    // ---- the last P.V, its value-zero term, then the rows out:
+    // ---- the last P.V, its value-zero term, then the rows out (half 0):
     // o = (O 2^-Gv + z) / l, lse = (m + log2 l) ln 2 (the TMEM loads for the
     // whole warp, the stores for rows that exist)
+    if (half == 1) S.lpart[r] = l;
     ok = ok && (nsteps == 0 || tc_wait(&S.odone, (uint32_t)((nsteps - 1) & 1), &S.abort_flag, p.err_word));
-    ok = ok && (nsteps == 0 || nsteps - 1 == ng ||
-                tc_wait(&S.meta_v, (uint32_t)((nsteps - 1) & 1), &S.abort_flag, p.err_word));
     ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
+    named_bar_sync(3, 256);
+    if (half == 0 && ok) {
       tfence_after();
       if (nsteps > 0 && nsteps - 1 != ng) take_z(nsteps - 1);
+      l += S.lpart[r];
       const bool live_row = row < p.rows;
       const float iv = tc_pow2(-Gv);
       const int qi = row / p.gqa, h = j * p.gqa + row % p.gqa;
@@ -785,6 +815,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         p.lse[(int64_t)qi * p.hq + h] = (m_used + log2f(l)) * 0.69314718055994530942f;
       }
     }
+    if (issuer) {
+      // before TMEM is freed: the last committed MMAs have completed (bounded,
+      // whatever the abort state: MMAs always complete)
+      for (int q = 0; q < 2; ++q) {
+        const uint32_t n = q ? n_odone : n_sdone;
+        if (n == 0) continue;
+        for (uint32_t i = 0; i < kSpinLimit; ++i)
+          if (mbar_try_wait(q ? &S.odone : &S.sdone, (n - 1) & 1)) break;
+      }
+    }
   }
 
   // ---- teardown: copies still in flight after an abort, then TMEM
@@ -799,7 +839,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 8) {
     tfence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(kTCols) : "memory");
   }
