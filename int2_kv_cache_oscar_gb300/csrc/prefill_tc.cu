@@ -8,29 +8,36 @@
 // v_hat with v_hat = code s^V + z^V.
 //
 // A CTA takes 128 (query, head) rows of one KV head (M = 128; TMEM lane =
-// row) and a range of the history's groups; 8 warps:
-//   * builders (warps 4-7): per group, expand the packed codes into exact
-//     fp16 B operands in shared memory (no-swizzle K-major core matrices):
+// row) and a range of the history's groups, each group (and the window) as
+// two half-steps of 64 tokens; 13 warps:
+//   * builders (warps 8-11): expand the packed codes into exact fp16 B
+//     operands in shared memory (no-swizzle K-major core matrices), a token
+//     half at a time, as soon as the MMA that read that half last is done:
 //     scores B[token][channel] = code * S_i(c) and values B[channel][token] =
 //     code * S_i^V(t, group), where S_1 + S_2 is the scale split into two
-//     9-significant-bit pieces (so code * S_i, code <= 3, is exact in fp16);
-//     extra B rows carry the key and value zeros (hi + lo).  Key and value
-//     operands have buffers of their own, so the keys of group k + 1 are
-//     built while the rows work on group k.  Their first thread also streams
-//     the group blocks through a ring of bulk copies and issues every
-//     tcgen05.mma: the P.V of group k - 1 and then the scores of group k;
-//   * rows (warps 0-3, thread = row): online softmax over the scores read
-//     from TMEM; P (hi + lo fp16) goes back to TMEM over the scores just read
-//     and is the A operand of P.V; the output accumulator O stays in TMEM and
-//     is rescaled only when a row's maximum grows by more than 8 (log2 units;
-//     P stays below 2^8).
-// Products (hi + lo of the rows' rotated queries, constant in TMEM):
-//   scores  S = Qhi B1 + Qlo B1 + Qhi B2          (N = 144: 128 tokens + zero rows)
-//   values  O += Phi V1 + Plo V1 + Phi V2         (N = 128 channels)
-//           Z  = Phi Vz + Plo Vz                  (N = 16: the value-zero term)
-// dropping only the products of two low parts (relative 2^-20).  The window
-// comes last, on bf16 operands (q and k exact; P as bf16 hi + lo).  With a
-// workspace the history is split into parts (grid.z), each writing per-row
+//     9-significant-bit pieces (code * S_i, code <= 3, is exact in fp16);
+//     extra B rows carry the key and value zeros (hi + lo fp16).  The window's
+//     keys are rotated like the query (H k_t) and split into fp16 hi + lo in
+//     the places of the two pieces.  The first builder also streams the group
+//     blocks through a ring of bulk copies;
+//   * MMA issuer (warp 12): one thread issues every tcgen05.mma;
+//   * rows (warps 0-7; warps w and w + 4 share TMEM lanes 32 (w & 3) ..,
+//     thread = row, each warp group a 32-token chunk of every half): online
+//     softmax over the scores read from TMEM; P (hi + lo) goes to TMEM (two
+//     buffers) as the A operand of P.V; the output accumulator stays in TMEM
+//     and is rescaled only when a row's maximum grows by more than 8 (log2
+//     units; P stays below 2^8).
+// Products per half-step (M = 128 rows, K = 16 per MMA; Qhi, P in TMEM, Qlo
+// in shared memory):
+//   scores  S[0, 144) = Qhi [B1 | zero | B2],  S[0, 80) += Qlo [B1 | zero]
+//   values  [O | Z] += Phi [V1 | zero] + Plo [V1 | zero],  O += Phi V2
+// dropping only the products of two low parts (relative 2^-20).  Each row
+// thread reads S1 + S2 and the zero-term column; Z is the value-zero term
+// sum_t p_t z^V(t) per value group.  The scores of half-step j + 1 are
+// issued as soon as the rows have read those of j, the P.V of j once they
+// have written its P, so the tensor cores work while the rows do.  The window
+// comes last; its P.V is on bf16 operands (V exact; P as bf16 hi + lo).  With
+// a workspace the history is split into parts (grid.z), each writing per-row
 // records (o unnormalised, m, l) that the merge kernel combines.
 #include <cstddef>
 
@@ -43,56 +50,64 @@ namespace oscar {
 namespace {
 
 constexpr int kTcRows = 128;
-constexpr int kTcThreads = 12 * 32;
+constexpr int kTcThreads = 13 * 32;
 constexpr int kTcStages = 3;
-constexpr int kNS = 144;                 // score B rows (and value B rows with the zero rows): 128 + 16
-constexpr int kBBytes = kNS * kHeadDim * 2;
-constexpr int kBVBytes2 = kHeadDim * kGroup * 2;     // value piece 2: 128 channel rows only
-constexpr uint32_t kLboB = (kNS / 8) * 128;          // B: core matrices adjacent along K
-constexpr uint32_t kLboV2 = (kHeadDim / 8) * 128;
+constexpr int kN1 = 80;                  // key piece-1 rows of a token half: 64 tokens + 16 zero rows
+constexpr int kNK = kN1 + 64;            // key B rows of a token half: then the 64 tokens' piece 2
+constexpr int kKBytes = kNK * kHeadDim * 2;
+constexpr int kNV1 = kHeadDim + 16;      // value B rows of piece 1: 128 channels + the zero rows
+constexpr int kV1Bytes = kNV1 * kGroup * 2;
+constexpr int kVBytes = kHeadDim * kGroup * 2;       // value B piece 2: 128 channel rows x 128 tokens
+constexpr uint32_t kLboK = (kNK / 8) * 128;          // B: core matrices adjacent along K
+constexpr uint32_t kLboV1 = (kNV1 / 8) * 128;
+constexpr uint32_t kLboV = (kHeadDim / 8) * 128;
 constexpr uint32_t kSbo = 128;                       // core matrices adjacent along M / N
 // TMEM columns (512 allocated)
-constexpr uint32_t kTQ = 0;        // rotated q * 2^F: hi fp16 pairs [0, 64), lo [64, 128)
-constexpr uint32_t kTQraw = 128;   // raw q, bf16 pairs [128, 192)
-constexpr uint32_t kTS = 192;      // scores [192, 336); P over [192, 320) (see p_col)
-constexpr uint32_t kTO = 336;      // output accumulator [336, 464)
-constexpr uint32_t kTZ = 464;      // value-zero term [464, 480)
+constexpr uint32_t kTQ = 0;        // rotated q * 2^F: hi fp16 pairs [0, 64) (lo in shared memory)
+constexpr uint32_t kTS = 64;       // scores of one half-step [64, 208): piece 1 (+ zero term) [0, 80), piece 2 [80, 144)
+constexpr uint32_t kTP = 208;      // P of half-steps j (buffer j & 1): [208, 272), [272, 336)
+constexpr uint32_t kTO = 336;      // output accumulator [336, 464), then the value-zero sums [464, 480)
+constexpr uint32_t kTZ = kTO + kHeadDim;
 constexpr uint32_t kTCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
 
-// TMEM column of the P pairs of k-step ks (tokens 16 ks .. 16 ks + 15), hi or
-// lo: each 32-token chunk c of the scores becomes [hi of its two k-steps | lo
-// of its two k-steps] in the chunk's own 32 columns.
-__host__ __device__ constexpr uint32_t p_col(int ks, bool lo) {
-  return kTS + 32 * (ks >> 1) + (lo ? 16 : 0) + 8 * (ks & 1);
+// TMEM column of the P pairs of k-step ks of a half (tokens 16 ks .. + 15)
+// in P buffer pb, hi or lo: each 32-token chunk c becomes [hi of its two
+// k-steps | lo of its two k-steps] in the chunk's own 32 columns.
+__host__ __device__ constexpr uint32_t p_col(int pb, int ks, bool lo) {
+  return kTP + 64 * pb + 32 * (ks >> 1) + (lo ? 16 : 0) + 8 * (ks & 1);
 }
 
 struct TcSmem {
-  alignas(1024) uint8_t k1[kBBytes];                  // key B piece 1 (+ zero rows)
-  alignas(1024) uint8_t k2[kBBytes];                  // key B piece 2 (zero rows cleared)
-  alignas(1024) uint8_t v1[kBBytes];                  // value B piece 1 (+ zero rows)
-  alignas(1024) uint8_t v2[kBVBytes2];                // value B piece 2
+  alignas(1024) uint8_t kb[2][kKBytes];               // key B of token half h
+  alignas(1024) uint8_t v1[kV1Bytes];                 // value B piece 1 (+ zero rows)
+  alignas(1024) uint8_t v2[kVBytes];                  // value B piece 2
+  alignas(1024) uint8_t qlo[kTcRows * kHeadDim * 2];  // A: the rows' rotated q * 2^F, fp16 lo part
   alignas(128) uint8_t stage[kTcStages][kBlockBytes];
-  float nrm[2][kGroup];                               // key norms of groups k, k + 1
+  // key norms per step, three deep: the keys of step k + 1 are built while
+  // the rows may still be on step k - 1's second half
+  float nrm[3][kGroup];
   alignas(16) uint16_t s1[kHeadDim], s2[kHeadDim];    // key-scale pieces (fp16) per channel
   alignas(16) uint16_t w1[kVGroups][kGroup], w2[kVGroups][kGroup];   // value-scale pieces [group][token]
-  float zmax[2][4];                                   // per builder warp: max |z^V| (double-buffered)
-  int gz[2];                                          // the value-zero rows carry 2^gz (double-buffered)
+  float wmax[4];                                      // per builder warp: max |k| (window), |z^V| (groups)
+  int fw;                                             // the window keys carry 2^fw
+  int gz;                                             // the value-zero rows carry 2^gz
   float fexp[kTcRows];                                // 2^-(F_row + 2) * scale_log2
-  float pmax[2][kTcRows];                             // row maxima of the two token halves
-  float lpart[kTcRows];                               // the second half's sum of p
+  float pmax[2][2][kTcRows];                          // row maxima of the two token chunks (by half-step parity)
+  float lpart[kTcRows];                               // the second warp group's sum of p
   alignas(8) uint64_t full[kTcStages];
-  uint64_t zred, sdone, pready, odone;
-  // steps whose key / value operands (and norms / zero exponent) are complete:
-  // monotonic counts, since the builders may run a step ahead of a waiter
-  uint32_t kready, vready;
+  uint64_t sdone[2], odone[2];   // scores / P.V of token half h done (one phase per step)
+  // counts, monotonic (a waiter may fall a phase behind): key / value halves
+  // built (2 k + h + 1), row warps done reading the scores / writing P (8 per half-step)
+  uint32_t kready, vready, sread, pcount;
   uint32_t nissued[kTcStages];
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(TcSmem) + 1024 <= 232448, "one CTA per SM");
 static_assert(offsetof(TcSmem, stage) % 128 == 0 && offsetof(TcSmem, full) % 8 == 0, "alignment");
-static_assert(kBBytes + kBVBytes2 >= kTcRows * kHeadDim * 4, "q staging fits in the value buffers");
+static_assert(offsetof(TcSmem, v2) == offsetof(TcSmem, v1) + kV1Bytes && kV1Bytes + kVBytes >= kTcRows * kHeadDim * 4,
+              "q staging fits in the value buffers");
 
 // Bounded wait that backs off: a few immediate polls, then short sleeps, so
 // that waiting warps leave issue slots and shared-memory bandwidth to the
@@ -168,6 +183,11 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, 
                :: "r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"((uint32_t)acc) : "memory");
 }
 
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+               :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)acc) : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(smem_u32(bar))
                : "memory");
@@ -192,6 +212,17 @@ __device__ __forceinline__ void tld16(uint32_t taddr, uint32_t (&r)[16]) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
                  "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
                : "r"(taddr));
+}
+
+__device__ __forceinline__ void tst16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+               :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+                  "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+               : "memory");
+}
+
+__device__ __forceinline__ void tld2(uint32_t taddr, uint32_t (&r)[2]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(taddr));
 }
 
 __device__ __forceinline__ void tst32(uint32_t taddr, const uint32_t (&v)[32]) {
@@ -270,49 +301,25 @@ __device__ __forceinline__ void split_p(float x0, float x1, bool bf16, uint32_t&
   }
 }
 
-// Key operands of one group into k1 / k2 (builder thread b = token and
-// channel b): scale pieces (x 4), zero rows 128, 129 (z hi, lo x 4), cleared
-// rows, the norms, then the codes of token b.
-template <bool M16>
-__device__ __forceinline__ void build_keys(TcSmem& S, const uint8_t* blk, int b, float* nrm) {
-  using B = Blk<M16>;
-  using MR = Meta<M16>;
-  pieces(MR::one(blk + B::kKScale, b) * 4.0f, S.s1[b], S.s2[b]);
-  uint32_t zh, zl;
-  split2(MR::one(blk + B::kKZero, b) * 4.0f, 0.0f, false, zh, zl);
-  *reinterpret_cast<uint16_t*>(S.k1 + canon(128, b, kNS)) = (uint16_t)(zh & 0xffffu);
-  *reinterpret_cast<uint16_t*>(S.k1 + canon(129, b, kNS)) = (uint16_t)(zl & 0xffffu);
-  nrm[b] = MR::one(blk + B::kKNorm, b);
-  for (int i = b; i < 16 * 16 * 2; i += 128) {   // rows 130..143 of k1, 128..143 of k2
-    const int h2 = i >> 8, rr = 128 + ((i >> 4) & 15), kb = i & 15;
-    if (h2 == 0 && rr < 130) continue;
-    *reinterpret_cast<uint4*>((h2 ? S.k2 : S.k1) + canon(rr, 8 * kb, kNS)) = make_uint4(0u, 0u, 0u, 0u);
-  }
-  bar_sync_threads(2, 128);    // the scale pieces are complete
-  const int t = b, mt = t >> 4, g = t & 7, r = (t >> 3) & 1;
-  uint32_t w0[4], w1[4];       // fragment words of token t: channel halves j = 0, 1
+// Normalised Walsh-Hadamard transform of a 128-vector held by one warp (lane
+// = elements 4 lane .. + 3): two stages in registers, five across lanes.
+__device__ __forceinline__ void fwht128_warp(float (&v)[4], int lane) {
+  const float a = v[0] + v[1], bq = v[0] - v[1], c = v[2] + v[3], d = v[2] - v[3];
+  v[0] = a + c;
+  v[2] = a - c;
+  v[1] = bq + d;
+  v[3] = bq - d;
 #pragma unroll
-  for (int tig = 0; tig < 4; ++tig) {
-    const uint4 q4 = *reinterpret_cast<const uint4*>(blk + kOffKCodes + (mt * 32 + 4 * g + tig) * 16);
-    w0[tig] = r ? q4.y : q4.x;
-    w1[tig] = r ? q4.w : q4.z;
-  }
-#pragma unroll 2
-  for (int kb = 0; kb < 16; ++kb) {
-    const int ks = kb >> 1, hf = kb & 1, kk = ks & 3;
-    const uint4 p1 = *reinterpret_cast<const uint4*>(&S.s1[8 * kb]);
-    const uint4 p2 = *reinterpret_cast<const uint4*>(&S.s2[8 * kb]);
-    const uint32_t pa[4] = {p1.x, p1.y, p1.z, p1.w}, pb[4] = {p2.x, p2.y, p2.z, p2.w};
-    uint32_t o1[4], o2[4];
+  for (int o = 1; o < 32; o <<= 1) {
+    const bool upper = (lane & o) != 0;
 #pragma unroll
-    for (int tig = 0; tig < 4; ++tig) {
-      const __half2 cd = code_pair(ks >= 4 ? w1[tig] : w0[tig], 4 * kk + 2 * hf);
-      o1[tig] = h2u(__hmul2(cd, u2h(pa[tig])));
-      o2[tig] = h2u(__hmul2(cd, u2h(pb[tig])));
+    for (int i = 0; i < 4; ++i) {
+      const float other = __shfl_xor_sync(0xffffffffu, v[i], o);
+      v[i] = upper ? other - v[i] : v[i] + other;
     }
-    *reinterpret_cast<uint4*>(S.k1 + canon(t, 8 * kb, kNS)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-    *reinterpret_cast<uint4*>(S.k2 + canon(t, 8 * kb, kNS)) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
   }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] *= 0.088388347648318440550f;   // 1/sqrt(128)
 }
 
 template <bool M16>
@@ -332,6 +339,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int ng = g_end - g_begin;
   const int wlen = part == p.n_parts - 1 ? p.wlen : 0;
   const int nsteps = ng + (wlen > 0 ? 1 : 0);   // the window is the last step
+  const int nh = 2 * nsteps;                    // half-steps
   const uint8_t* blocks = arena + p.blocks_off +
                           (((int64_t)p.slot * p.hkv + j) * p.max_groups + g_begin) * (int64_t)B::kBytes;
   const float vmax = __uint_as_float(
@@ -348,12 +356,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&S.full[s], 1);
       S.nissued[s] = 0;
     }
-    mbar_init(&S.zred, 4);
-    mbar_init(&S.sdone, 1);
-    mbar_init(&S.pready, 1);
-    mbar_init(&S.odone, 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&S.sdone[h], 1);
+      mbar_init(&S.odone[h], 1);
+    }
     S.kready = 0;
     S.vready = 0;
+    S.sread = 0;
+    S.pcount = 0;
     S.abort_flag = 0;
     fence_mbar_init();
   }
@@ -365,37 +375,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // ---- q rows: rotate (warp-cooperative FWHT, lanes = 4 channels) into the
   // staging area, then each row thread stores its row into TMEM
   float* qst = reinterpret_cast<float*>(S.v1);                    // [128][128] rotated q * 2^F (v1, v2)
-  uint32_t* qraw = reinterpret_cast<uint32_t*>(S.k1);             // [128][64] raw bf16 pairs
-  for (int r = warp; r < kTcRows; r += 12) {
+  for (int r = warp; r < kTcRows; r += kTcThreads / 32) {
     const int row = blockIdx.x * kTcRows + r;
     uint2 raw = make_uint2(0u, 0u);
     if (row < p.rows) {
       const int qi = row / p.gqa, h = j * p.gqa + row % p.gqa;
       raw = *reinterpret_cast<const uint2*>(p.q + ((int64_t)qi * p.hq + h) * kHeadDim + 4 * lane);
     }
-    qraw[r * 64 + 2 * lane] = raw.x;
-    qraw[r * 64 + 2 * lane + 1] = raw.y;
     float qv[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-    const float a = qv[0] + qv[1], bq = qv[0] - qv[1], c = qv[2] + qv[3], d = qv[2] - qv[3];
-    qv[0] = a + c;
-    qv[2] = a - c;
-    qv[1] = bq + d;
-    qv[3] = bq - d;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const bool upper = (lane & o) != 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float other = __shfl_xor_sync(0xffffffffu, qv[i], o);
-        qv[i] = upper ? other - qv[i] : qv[i] + other;
-      }
-    }
+    fwht128_warp(qv, lane);
     float mx = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      qv[i] *= 0.088388347648318440550f;   // 1/sqrt(128)
-      mx = fmaxf(mx, fabsf(qv[i]));
-    }
+    for (int i = 0; i < 4; ++i) mx = fmaxf(mx, fabsf(qv[i]));
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     int F = 0;
@@ -413,37 +404,143 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tfence_after();
   const uint32_t tmem = S.tmem_base;
   if (warp < 4) {
-    // row thread r stores hi / lo fp16 pairs and the raw bf16 pairs into its lane
+    // row thread r stores its hi fp16 pairs into its lane, the lo pairs
+    // into the shared-memory A operand (no-swizzle K-major, row r)
     const int r = tid;
     const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
 #pragma unroll 1
     for (int c0 = 0; c0 < 64; c0 += 32) {
-      uint32_t hi[32], lo[32], rw[32];
+      uint32_t hi[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const float x0 = qst[r * kHeadDim + 2 * (c0 + i)], x1 = qst[r * kHeadDim + 2 * (c0 + i) + 1];
-        split2(x0, x1, false, hi[i], lo[i]);
-        rw[i] = qraw[r * 64 + c0 + i];
+        uint32_t lo;
+        split2(x0, x1, false, hi[i], lo);
+        *reinterpret_cast<uint32_t*>(S.qlo + canon(r, 2 * (c0 + i), kTcRows)) = lo;
       }
       tst32(lane_base + kTQ + c0, hi);
-      tst32(lane_base + kTQ + 64 + c0, lo);
-      tst32(lane_base + kTQraw + c0, rw);
     }
     tst_wait();
+    async_fence();   // the lo part is read by the tensor cores
   }
   tfence_before();
-  __syncthreads();   // the staging areas are free again
+  __syncthreads();   // the staging area is free again
   tfence_after();
 
-  if (warp >= 8) {
+  if (warp == 12) {
+    // ============================================================ MMA issuer
+    // One thread issues every tcgen05.mma: the scores of half-step j + 1 as
+    // soon as the rows have read those of j (one score buffer), the P.V of j
+    // once they have written its P.  An issue blocks while the MMA queue is
+    // full, so this thread does nothing else.
+    if (lane == 0) {
+      // every operand address is fixed: descriptors and TMEM columns are set
+      // up once, and each half-step's MMAs are one unrolled sequence (an MMA
+      // issue stalls this thread for its own latency, so nothing else sits
+      // between them)
+      const uint32_t idK = idesc_f16(kNK, false), idK1 = idesc_f16(kN1, false);
+      const uint32_t idO = idesc_f16(kHeadDim, false), idOZ = idesc_f16(kNV1, false), idOW = idesc_f16(kHeadDim, true);
+      const uint64_t dK0 = sdesc(smem_u32(S.kb[0]), kLboK, kSbo), dK1 = sdesc(smem_u32(S.kb[1]), kLboK, kSbo);
+      const uint64_t dQ = sdesc(smem_u32(S.qlo), (kTcRows / 8) * 128, kSbo);   // Qlo: A, 128 rows
+      const uint64_t dV1 = sdesc(smem_u32(S.v1), kLboV1, kSbo), dV2 = sdesc(smem_u32(S.v2), kLboV, kSbo);
+      const uint32_t tS = tmem + kTS, tO = tmem + kTO, tQ = tmem + kTQ;
+      uint32_t n_sd[2] = {0u, 0u}, n_od[2] = {0u, 0u};   // commits issued to each barrier
+      // scores of half-step j: S[0, 144) = Qhi . [B1 | zero | B2] (Qhi from
+      // TMEM), S[0, 80) += Qlo . [B1 | zero] (Qlo from shared memory); the
+      // window's B1 + B2 are H k_t 2^fw as fp16 hi + lo
+      auto issue_scores = [&](int jj) {
+        const int h = jj & 1;
+        if (!tc_wait_count(&S.kready, (uint32_t)jj, &S.abort_flag, p.err_word)) return false;
+        tfence_after();
+        const uint64_t dk = h ? dK1 : dK0;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          mma_ts(tS, tQ + 8 * ks, dk + (uint64_t)((2 * ks * kLboK) >> 4), idK, ks > 0);
+          mma_ss(tS, dQ + (uint64_t)((2 * ks * (kTcRows / 8) * 128) >> 4), dk + (uint64_t)((2 * ks * kLboK) >> 4), idK1,
+                 true);
+        }
+        mma_commit(&S.sdone[h]);
+        ++n_sd[h];
+        return true;
+      };
+      // P.V of half-step j (its 64 tokens are the K dimension):
+      // [O | Z] += Phi V1 + Plo V1 (N = 144: the zero rows give Z), O += Phi V2
+      // (window: O += (Phi + Plo) V, bf16, N = 128)
+      auto issue_pv = [&](int jj) {
+        const int h = jj & 1;
+        if (!tc_wait_count(&S.vready, (uint32_t)jj, &S.abort_flag, p.err_word)) return false;
+        tfence_after();
+        const uint32_t tP = tmem + p_col(jj & 1, 0, false);
+        const uint64_t v1 = dV1 + (uint64_t)((8 * h * kLboV1) >> 4), v2 = dV2 + (uint64_t)((8 * h * kLboV) >> 4);
+        const bool first = jj == 0;
+        if ((jj >> 1) == ng) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t ah = tP + 32 * (ks >> 1) + 8 * (ks & 1);
+            const uint64_t ko = (uint64_t)((2 * ks * kLboV1) >> 4);
+            mma_ts(tO, ah, v1 + ko, idOW, !first || ks > 0);
+            mma_ts(tO, ah + 16, v1 + ko, idOW, true);
+          }
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t ah = tP + 32 * (ks >> 1) + 8 * (ks & 1);
+            const uint64_t ko1 = (uint64_t)((2 * ks * kLboV1) >> 4), ko2 = (uint64_t)((2 * ks * kLboV) >> 4);
+            mma_ts(tO, ah, v1 + ko1, idOZ, !first || ks > 0);
+            mma_ts(tO, ah + 16, v1 + ko1, idOZ, true);
+            mma_ts(tO, ah, v2 + ko2, idO, true);
+          }
+        }
+        mma_commit(&S.odone[h]);
+        ++n_od[h];
+        return true;
+      };
+      bool ok = nh == 0 || issue_scores(0);
+      for (int jj = 0; jj < nh && ok; ++jj) {
+        if (jj + 1 < nh) {
+          ok = tc_wait_count(&S.sread, (uint32_t)(8 * jj + 7), &S.abort_flag, p.err_word);   // all 8 row warps
+          if (!ok) break;
+          tfence_after();
+          ok = issue_scores(jj + 1);
+          if (!ok) break;
+        }
+        ok = tc_wait_count(&S.pcount, (uint32_t)(8 * jj + 7), &S.abort_flag, p.err_word);
+        if (!ok) break;
+        tfence_after();
+        ok = issue_pv(jj);
+      }
+      // before TMEM is freed: the last committed MMAs have completed (bounded,
+      // whatever the abort state: MMAs always complete)
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t n = q < 2 ? n_sd[q] : n_od[q - 2];
+        if (n == 0) continue;
+        uint64_t* bar = q < 2 ? &S.sdone[q] : &S.odone[q - 2];
+        for (uint32_t i = 0; i < kSpinLimit; ++i)
+          if (mbar_try_wait(bar, (n - 1) & 1)) break;
+      }
+    }
+  } else if (warp >= 8) {
     // =============================================================== builders
-    // Every builder runs the same barriers in every step; after a wait gives
-    // up (abort) the work is skipped but the control flow stays the same.
-    const int b = tid - 256;     // token (key codes, value zero rows) or channel (value codes)
+    // The operands are built in token halves, each as soon as the MMA that
+    // last read that half is done, in the order keys(k, 0), values(k - 1, 1),
+    // keys(k, 1), values(k, 0): a half-step of the rows then overlaps one key
+    // half and one value half, each needed a half-step later.  Every builder
+    // runs the same barriers in every task; after a wait gives up (abort) the
+    // work is skipped but the control flow stays the same.
+    const int b = tid - 256;     // channel (scale pieces, value codes) or token (value pieces)
+    const int bt = b & 63, bh = b >> 6;   // token of a half, channel half (key codes, the window)
     const int bw = warp - 8;
     const float gv = tc_pow2(Gv);
     const bool lead = b == 0;    // also streams the group blocks
     const uint8_t* wsrc = arena + p.windows_off + ((int64_t)p.slot * p.hkv + j) * kWindowBytes;
+    bool ok = true;
+    // rows no build writes: key rows 66..79 of each half (64 and 65 carry the
+    // zero), value rows 136..143 (128 + gr and 132 + gr carry the zeros)
+    for (int i = b; i < 2 * 14 * 16; i += 128) {
+      const int h = i / (14 * 16), rr = 66 + (i % (14 * 16)) / 16, kb = i % 16;
+      *reinterpret_cast<uint4*>(S.kb[h] + canon(rr, 8 * kb, kNK)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    *reinterpret_cast<uint4*>(S.v1 + canon(136 + (b >> 4), 8 * (b & 15), kNV1)) = make_uint4(0u, 0u, 0u, 0u);
     if (lead) {
       for (int k = 0; k < ng && k < kTcStages; ++k) {
         mbar_arrive_expect_tx(&S.full[k], B::kBytes);
@@ -451,358 +548,418 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         S.nissued[k] = 1;
       }
     }
-    for (int k = 0; k < nsteps; ++k) {
+    // 2^gz with max |z^V| 2^gz < 2^14 over this CTA's groups: the zero sums
+    // accumulate across groups in these units (token b's zeros of every group)
+    int gz = 0;
+    {
+      float zm = 0.0f;
+#pragma unroll 1
+      for (int k = 0; k < ng; ++k) {
+        const float4 z4 = MR::v4(blocks + (int64_t)k * B::kBytes + B::kVZero, b);
+        zm = fmaxf(zm, fmaxf(fmaxf(fabsf(z4.x), fabsf(z4.y)), fmaxf(fabsf(z4.z), fabsf(z4.w))));
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, o));
+      if (lane == 0) S.wmax[bw] = zm;
+      bar_sync_threads(2, 128);
+      zm = fmaxf(fmaxf(S.wmax[0], S.wmax[1]), fmaxf(S.wmax[2], S.wmax[3]));
+      if (zm > 0.0f && zm <= 3.0e38f) {
+        int e;
+        frexpf(zm, &e);   // zm < 2^e
+        gz = max(-100, min(14 - e, 100));
+      }
+      if (lead) S.gz = gz;   // read by the rows after their last half-step
+      bar_sync_threads(2, 128);   // wmax is free again
+    }
+    const float gzf = tc_pow2(gz);
+    uint32_t zk = 0u;            // key zero of channel b (x 4): fp16 hi | lo << 16
+    int fw = 0;                  // the window keys carry 2^fw
+    // ---- key operands of half h of step k, once the scores that read them last are done
+    auto keys = [&](int k, int h) {
       const bool win = k == ng;
-      const int s = k % kTcStages;
-      const uint32_t par = (uint32_t)(k & 1);
-      // ---- key operands of step k, once the scores of step k - 1 are done
-      bool ok = win || tc_wait(&S.full[s], (uint32_t)((k / kTcStages) & 1), &S.abort_flag, p.err_word);
-      ok = ok && (k == 0 || tc_wait(&S.sdone, (uint32_t)((k - 1) & 1), &S.abort_flag, p.err_word));
-      const uint8_t* blk = S.stage[s];
+      const uint8_t* blk = S.stage[k % kTcStages];
+      if (h == 0) ok = ok && (win || tc_wait(&S.full[k % kTcStages], (uint32_t)((k / kTcStages) & 1), &S.abort_flag, p.err_word));
+      ok = ok && (k == 0 || tc_wait(&S.sdone[h], (uint32_t)((k - 1) & 1), &S.abort_flag, p.err_word));
+      uint8_t* kbh = S.kb[h];
+      const int t = 64 * h + bt;
       if (win) {
-        // the window keys as B[token][channel], bf16 (rows past wlen zero)
-        if (ok) {
-          const uint4* krow = reinterpret_cast<const uint4*>(wsrc + b * kHeadDim * 2);
-#pragma unroll 4
-          for (int kb = 0; kb < 16; ++kb)
-            *reinterpret_cast<uint4*>(S.k1 + canon(b, 8 * kb, kNS)) = b < wlen ? krow[kb] : make_uint4(0u, 0u, 0u, 0u);
+        if (h == 0) {
+          // 2^fw with max |H k| 2^fw < 2^14 over the window (|H k|_inf <=
+          // sqrt(128) max |k|), so that the rotated keys' fp16 pieces stay finite
+          float mx = 0.0f;
+          if (ok) {
+#pragma unroll 1
+            for (int tt = bt; tt < wlen; tt += 64) {
+              const uint4* wk = reinterpret_cast<const uint4*>(wsrc + tt * kHeadDim * 2);
+#pragma unroll 2
+              for (int kb = 8 * bh; kb < 8 * bh + 8; ++kb) {
+                const uint4 u = wk[kb];
+                const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  mx = fmaxf(mx, fmaxf(__uint_as_float((w4[e] << 16) & 0x7FFF0000u), __uint_as_float(w4[e] & 0x7FFF0000u)));
+              }
+            }
+          }
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          if (lane == 0) S.wmax[bw] = mx;
+          bar_sync_threads(2, 128);
+          mx = fmaxf(fmaxf(S.wmax[0], S.wmax[1]), fmaxf(S.wmax[2], S.wmax[3]));
+          fw = 0;
+          if (mx > 0.0f && mx <= 3.0e38f) {
+            int e;
+            frexpf(mx, &e);   // mx < 2^e, |H k| < 2^(e + 4)
+            fw = min(10 - e, 100);   // (keys below 2^-90 are zero in fp16 either way)
+          }
+          if (lead) S.fw = fw;   // read by the rows once the window's scores are done
         }
-        bar_sync_threads(2, 128);   // (matches the barrier inside build_keys)
-      } else if (ok) {
-        build_keys<M16>(S, blk, b, S.nrm[k & 1]);
+        if (ok) {
+          // the window keys rotated (H k, as the query), x 2^fw, as fp16 hi
+          // (row t) + lo (row 80 + t) like a group's two pieces: each warp
+          // takes 16 tokens of the half, lane = channels 4 lane .. + 3
+          const float f = tc_pow2(fw);
+#pragma unroll 1
+          for (int i = 0; i < 16; ++i) {
+            const int tl = 16 * bw + i, tt = 64 * h + tl;
+            const uint2 raw = tt < wlen ? *reinterpret_cast<const uint2*>(wsrc + tt * kHeadDim * 2 + 8 * lane)
+                                        : make_uint2(0u, 0u);
+            float kv[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
+            fwht128_warp(kv, lane);
+            uint32_t h01, l01, h23, l23;
+            split2(kv[0] * f, kv[1] * f, false, h01, l01);
+            split2(kv[2] * f, kv[3] * f, false, h23, l23);
+            *reinterpret_cast<uint2*>(kbh + canon(tl, 4 * lane, kNK)) = make_uint2(h01, h23);
+            *reinterpret_cast<uint2*>(kbh + canon(kN1 + tl, 4 * lane, kNK)) = make_uint2(l01, l23);
+          }
+        }
       } else {
-        bar_sync_threads(2, 128);
+        if (h == 0) {
+          if (ok) {
+            // channel b: scale pieces (x 4), the zero (hi, lo x 4); token b:
+            // its norm (read by the rows)
+            pieces(MR::one(blk + B::kKScale, b) * 4.0f, S.s1[b], S.s2[b]);
+            uint32_t zh, zl;
+            split2(MR::one(blk + B::kKZero, b) * 4.0f, 0.0f, false, zh, zl);
+            zk = (zh & 0xffffu) | (zl << 16);
+            S.nrm[k % 3][b] = MR::one(blk + B::kKNorm, b);
+          }
+          bar_sync_threads(2, 128);    // the scale pieces are complete
+        }
+        if (ok) {
+          *reinterpret_cast<uint16_t*>(kbh + canon(64, b, kNK)) = (uint16_t)(zk & 0xffffu);
+          *reinterpret_cast<uint16_t*>(kbh + canon(65, b, kNK)) = (uint16_t)(zk >> 16);
+          // token t, channels 64 bh .. + 63: the code fragment words of that
+          // channel half; piece 1 to row bt, piece 2 to row 80 + bt
+          const int mt = t >> 4, g = t & 7, r = (t >> 3) & 1;
+          uint32_t w[4];
+#pragma unroll
+          for (int tig = 0; tig < 4; ++tig) {
+            const uint2 q2 = *reinterpret_cast<const uint2*>(blk + kOffKCodes + (mt * 32 + 4 * g + tig) * 16 + 8 * bh);
+            w[tig] = r ? q2.y : q2.x;
+          }
+#pragma unroll 2
+          for (int kb = 8 * bh; kb < 8 * bh + 8; ++kb) {
+            const int kk = (kb >> 1) & 3, hf = kb & 1;
+            const uint4 p1 = *reinterpret_cast<const uint4*>(&S.s1[8 * kb]);
+            const uint4 p2 = *reinterpret_cast<const uint4*>(&S.s2[8 * kb]);
+            const uint32_t pa[4] = {p1.x, p1.y, p1.z, p1.w}, pb[4] = {p2.x, p2.y, p2.z, p2.w};
+            uint32_t o1[4], o2[4];
+#pragma unroll
+            for (int tig = 0; tig < 4; ++tig) {
+              const __half2 cd = code_pair(w[tig], 4 * kk + 2 * hf);
+              o1[tig] = h2u(__hmul2(cd, u2h(pa[tig])));
+              o2[tig] = h2u(__hmul2(cd, u2h(pb[tig])));
+            }
+            *reinterpret_cast<uint4*>(kbh + canon(bt, 8 * kb, kNK)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+            *reinterpret_cast<uint4*>(kbh + canon(kN1 + bt, 8 * kb, kNK)) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+          }
+        }
       }
       async_fence();
       bar_sync_threads(2, 128);
-      if (lead) publish(&S.kready, (uint32_t)(k + 1));
-      // ---- value operands of step k, once the P.V of step k - 1 is done
-      ok = ok && (k == 0 || tc_wait(&S.odone, (uint32_t)((k - 1) & 1), &S.abort_flag, p.err_word));
-      if (win) {
-        if (ok) {
-          // the window values transposed into B[channel][token], bf16
-          const uint16_t* vrow = reinterpret_cast<const uint16_t*>(wsrc + kGroup * kHeadDim * 2 + b * kHeadDim * 2);
-#pragma unroll 1
-          for (int c = 0; c < kHeadDim; c += 8) {
-            const uint4 v8 = b < wlen ? *reinterpret_cast<const uint4*>(vrow + c) : make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t e4[4] = {v8.x, v8.y, v8.z, v8.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              *reinterpret_cast<uint16_t*>(S.v1 + canon(c + i, b, kNS)) = (uint16_t)(e4[i >> 1] >> (16 * (i & 1)));
-          }
-        }
-        async_fence();
-        bar_sync_threads(2, 128);
-        if (lead) publish(&S.vready, (uint32_t)(k + 1));
-        continue;
-      }
-      float zm = 0.0f;
-      if (ok) {
-        // token b: its four value scales as pieces (x 2^Gv), and max |z^V|
+      if (lead) publish(&S.kready, (uint32_t)(2 * k + h + 1));
+    };
+    // ---- value operands of half h of step k, once the P.V that read them last is done
+    auto values = [&](int k, int h) {
+      const bool win = k == ng;
+      const uint8_t* blk = S.stage[k % kTcStages];
+      if (!win && h == 0 && ok) {
+        // token b: its four value scales as pieces (x 2^Gv); only builders read them
         const float4 sv = MR::v4(blk + B::kVScale, b);
-        const float4 zv = MR::v4(blk + B::kVZero, b);
         pieces(sv.x * gv, S.w1[0][b], S.w2[0][b]);
         pieces(sv.y * gv, S.w1[1][b], S.w2[1][b]);
         pieces(sv.z * gv, S.w1[2][b], S.w2[2][b]);
         pieces(sv.w * gv, S.w1[3][b], S.w2[3][b]);
-        zm = fmaxf(fmaxf(fabsf(zv.x), fabsf(zv.y)), fmaxf(fabsf(zv.z), fabsf(zv.w)));
       }
+      ok = ok && (k == 0 || tc_wait(&S.odone[h], (uint32_t)((k - 1) & 1), &S.abort_flag, p.err_word));
+      if (win) {
+        if (ok) {
+          // the window values transposed into B[channel][token], bf16: token
+          // 64 h + bt, channels 64 bh .. + 63
+          const int t = 64 * h + bt;
+          const uint16_t* vrow = reinterpret_cast<const uint16_t*>(wsrc + kGroup * kHeadDim * 2 + t * kHeadDim * 2);
+#pragma unroll 1
+          for (int c = 64 * bh; c < 64 * bh + 64; c += 8) {
+            const uint4 v8 = t < wlen ? *reinterpret_cast<const uint4*>(vrow + c) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t e4[4] = {v8.x, v8.y, v8.z, v8.w};
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, o));
-      if (lane == 0) {
-        S.zmax[k & 1][bw] = zm;
-        mbar_arrive(&S.zred);
-      }
-      ok = ok && tc_wait(&S.zred, par, &S.abort_flag, p.err_word);
-      if (ok) {
-        const float zmx = fmaxf(fmaxf(S.zmax[k & 1][0], S.zmax[k & 1][1]), fmaxf(S.zmax[k & 1][2], S.zmax[k & 1][3]));
-        int Gz = 0;
-        if (zmx > 0.0f) {
-          int e;
-          frexpf(zmx, &e);   // zmx < 2^e
-          Gz = 14 - e;
+            for (int i = 0; i < 8; ++i)
+              *reinterpret_cast<uint16_t*>(S.v1 + canon(c + i, t, kNV1)) = (uint16_t)(e4[i >> 1] >> (16 * (i & 1)));
+          }
         }
-        const float gzf = tc_pow2(Gz);
-        const float4 zv = MR::v4(blk + B::kVZero, b);
-        const float zz[4] = {zv.x * gzf, zv.y * gzf, zv.z * gzf, zv.w * gzf};
-        // rows 128 + gr: z hi, 132 + gr: z lo (B[row][token b]); rows 136..143 zero
-#pragma unroll
-        for (int gr = 0; gr < 4; ++gr) {
-          uint32_t zh, zl;
-          split2(zz[gr], 0.0f, false, zh, zl);
-          *reinterpret_cast<uint16_t*>(S.v1 + canon(128 + gr, b, kNS)) = (uint16_t)(zh & 0xffffu);
-          *reinterpret_cast<uint16_t*>(S.v1 + canon(132 + gr, b, kNS)) = (uint16_t)(zl & 0xffffu);
+      } else {
+        if (ok) {
+          // the zero rows of token 64 h + bt (x 2^gz): 128 + gr z hi, 132 + gr z
+          // lo, for value groups gr = 2 bh, 2 bh + 1
+          const int t = 64 * h + bt;
+          const float4 z4 = MR::v4(blk + B::kVZero, t);
+          uint32_t zh0, zl0, zh1, zl1;
+          split2((bh ? z4.z : z4.x) * gzf, 0.0f, false, zh0, zl0);
+          split2((bh ? z4.w : z4.y) * gzf, 0.0f, false, zh1, zl1);
+          *reinterpret_cast<uint16_t*>(S.v1 + canon(128 + 2 * bh, t, kNV1)) = (uint16_t)(zh0 & 0xffffu);
+          *reinterpret_cast<uint16_t*>(S.v1 + canon(129 + 2 * bh, t, kNV1)) = (uint16_t)(zh1 & 0xffffu);
+          *reinterpret_cast<uint16_t*>(S.v1 + canon(132 + 2 * bh, t, kNV1)) = (uint16_t)(zl0 & 0xffffu);
+          *reinterpret_cast<uint16_t*>(S.v1 + canon(133 + 2 * bh, t, kNV1)) = (uint16_t)(zl1 & 0xffffu);
         }
-#pragma unroll
-        for (int rr = 136; rr < 144; ++rr) *reinterpret_cast<uint16_t*>(S.v1 + canon(rr, b, kNS)) = 0;
-        if (b == 0) S.gz[k & 1] = Gz;   // read by the row threads once this step's P.V is done
-      }
-      bar_sync_threads(2, 128);    // the value-scale pieces are complete
-      if (ok) {
-        const int c = b, mt = c >> 4, g = c & 7, r = (c >> 3) & 1, gr = c >> 5;
-        uint32_t w0[4], w1[4];     // V-order words of channel c: token halves j = 0, 1
-#pragma unroll
-        for (int tig = 0; tig < 4; ++tig) {
-          const uint2 a2 = *reinterpret_cast<const uint2*>(blk + B::kVCodes + ((mt * 2 + 0) * 32 + 4 * g + tig) * 8);
-          const uint2 b2 = *reinterpret_cast<const uint2*>(blk + B::kVCodes + ((mt * 2 + 1) * 32 + 4 * g + tig) * 8);
-          w0[tig] = r ? a2.y : a2.x;
-          w1[tig] = r ? b2.y : b2.x;
-        }
-#pragma unroll 2
-        for (int kb = 0; kb < 16; ++kb) {
-          const int ks = kb >> 1, hf = kb & 1, kk = ks & 3;
-          const uint4 p1 = *reinterpret_cast<const uint4*>(&S.w1[gr][8 * kb]);
-          const uint4 p2 = *reinterpret_cast<const uint4*>(&S.w2[gr][8 * kb]);
-          const uint32_t pa[4] = {p1.x, p1.y, p1.z, p1.w}, pb[4] = {p2.x, p2.y, p2.z, p2.w};
-          uint32_t o1[4], o2[4];
+        if (h == 0) bar_sync_threads(2, 128);    // the value-scale pieces are complete
+        if (ok) {
+          // channel c = b, tokens 64 h .. + 63
+          const int c = b, mt = c >> 4, g = c & 7, r = (c >> 3) & 1, gr = c >> 5;
+          uint32_t w[4];
 #pragma unroll
           for (int tig = 0; tig < 4; ++tig) {
-            const __half2 cd = code_pair(ks >= 4 ? w1[tig] : w0[tig], 4 * kk + 2 * hf);
-            o1[tig] = h2u(__hmul2(cd, u2h(pa[tig])));
-            o2[tig] = h2u(__hmul2(cd, u2h(pb[tig])));
+            const uint2 a2 = *reinterpret_cast<const uint2*>(blk + B::kVCodes + ((mt * 2 + h) * 32 + 4 * g + tig) * 8);
+            w[tig] = r ? a2.y : a2.x;
           }
-          *reinterpret_cast<uint4*>(S.v1 + canon(c, 8 * kb, kNS)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-          *reinterpret_cast<uint4*>(S.v2 + canon(c, 8 * kb, kHeadDim)) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+#pragma unroll 2
+          for (int kb = 8 * h; kb < 8 * h + 8; ++kb) {
+            const int kk = (kb >> 1) & 3, hf = kb & 1;
+            const uint4 p1 = *reinterpret_cast<const uint4*>(&S.w1[gr][8 * kb]);
+            const uint4 p2 = *reinterpret_cast<const uint4*>(&S.w2[gr][8 * kb]);
+            const uint32_t pa[4] = {p1.x, p1.y, p1.z, p1.w}, pb[4] = {p2.x, p2.y, p2.z, p2.w};
+            uint32_t o1[4], o2[4];
+#pragma unroll
+            for (int tig = 0; tig < 4; ++tig) {
+              const __half2 cd = code_pair(w[tig], 4 * kk + 2 * hf);
+              o1[tig] = h2u(__hmul2(cd, u2h(pa[tig])));
+              o2[tig] = h2u(__hmul2(cd, u2h(pb[tig])));
+            }
+            *reinterpret_cast<uint4*>(S.v1 + canon(c, 8 * kb, kNV1)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+            *reinterpret_cast<uint4*>(S.v2 + canon(c, 8 * kb, kHeadDim)) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+          }
         }
       }
       async_fence();
       bar_sync_threads(2, 128);
-      if (lead) publish(&S.vready, (uint32_t)(k + 1));
-      if (lead && ok && k + kTcStages < ng) {
+      if (lead) publish(&S.vready, (uint32_t)(2 * k + h + 1));
+      if (h == 1 && lead && ok && !win && k + kTcStages < ng) {
         // the block is consumed: refill its stage
         async_fence();
+        const int s = k % kTcStages;
         mbar_arrive_expect_tx(&S.full[s], B::kBytes);
         bulk_g2s(S.stage[s], blocks + (int64_t)(k + kTcStages) * B::kBytes, B::kBytes, &S.full[s]);
         S.nissued[s] += 1;
       }
+    };
+    for (int k = 0; k <= nsteps; ++k) {
+      if (k < nsteps) keys(k, 0);
+      if (k > 0) values(k - 1, 1);
+      if (k < nsteps) {
+        keys(k, 1);
+        values(k, 0);
+      }
     }
   } else {
     // =================================================================== rows
-    // Warps w and w + 4 share rows 32 (w & 3) .. + 31 (their TMEM lanes) and
-    // split the tokens: half 0 takes tokens 0..63 and owns O, the zero sums
-    // and the output; half 1 takes tokens 64..127.  As for the builders: the
-    // same barriers in every step, work skipped after an abort.  Thread 0 also
-    // issues every tcgen05.mma: the scores of step k + 1 right after the P.V
-    // of step k (the scores overwrite its P).
-    const int half = warp >> 2;
+    // A step (a group, or the window) is taken in two half-steps, one per
+    // 64-token half; half-step j = 2 k + h.  Warps w and w + 4 share rows
+    // 32 (w & 3) .. + 31 (their TMEM lanes) and split each half's tokens:
+    // warp group 0 takes the first 32 and owns O and the output, group 1 the
+    // other 32.  Each warp counts, for the issuer, when it has read the scores
+    // of a half-step and when it has written its P.  As for the builders: the
+    // same barriers in every half-step, work skipped after an abort.
+    const int grp = warp >> 2;
     const int r = 32 * (warp & 3) + lane;
     const int row = blockIdx.x * kTcRows + r;
     const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-    const bool issuer = tid == 0;
     const float fr = S.fexp[r];
-    float m_used = -INFINITY, l = 0.0f;   // l: this half's sum of p
-    float zacc[kVGroups] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float m_used = -INFINITY, l = 0.0f;   // l: this warp group's sum of p
     bool ok = true;
-    const uint32_t idS = idesc_f16(kNS, false), idO = idesc_f16(kHeadDim, false), idZ = idesc_f16(16, false);
-    const uint32_t idW = idesc_f16(kHeadDim, true);
-    const uint32_t sk1 = smem_u32(S.k1), sk2 = smem_u32(S.k2), sv1 = smem_u32(S.v1), sv2 = smem_u32(S.v2);
-    uint32_t n_sdone = 0, n_odone = 0;   // commits issued (issuer)
-    auto issue_scores = [&](int ks_step) {
-      if (!tc_wait_count(&S.kready, (uint32_t)ks_step, &S.abort_flag, p.err_word)) return;
-      tfence_after();
-      const bool w = ks_step == ng;
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint64_t dk1 = sdesc(sk1 + 2 * ks * kLboB, kLboB, kSbo);
-        if (w) {
-          mma_ts(tmem + kTS, tmem + kTQraw + 8 * ks, dk1, idW, ks > 0);
-        } else {
-          const uint64_t dk2 = sdesc(sk2 + 2 * ks * kLboB, kLboB, kSbo);
-          mma_ts(tmem + kTS, tmem + kTQ + 8 * ks, dk1, idS, ks > 0);
-          mma_ts(tmem + kTS, tmem + kTQ + 64 + 8 * ks, dk1, idS, true);
-          mma_ts(tmem + kTS, tmem + kTQ + 8 * ks, dk2, idS, true);
-        }
+    // wait for the P.V of half-step jp (bounded)
+    auto pv_done = [&](int jp) {
+      return tc_wait(&S.odone[jp & 1], (uint32_t)((jp >> 1) & 1), &S.abort_flag, p.err_word);
+    };
+    // this warp's TMEM accesses before are complete: count it for the issuer
+    auto count = [&](uint32_t* c) {
+      tfence_before();
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        atomicAdd(c, 1u);
       }
-      mma_commit(&S.sdone);
-      ++n_sdone;
     };
-    auto issue_pv = [&](int kp) {
-      if (!tc_wait_count(&S.vready, (uint32_t)kp, &S.abort_flag, p.err_word)) return;
-      tfence_after();
-      const bool w = kp == ng;
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t ah = tmem + p_col(ks, false), al = tmem + p_col(ks, true);
-        const uint64_t dv1 = sdesc(sv1 + 2 * ks * kLboB, kLboB, kSbo);
-        if (w) {
-          mma_ts(tmem + kTO, ah, dv1, idW, kp > 0 || ks > 0);
-          mma_ts(tmem + kTO, al, dv1, idW, true);
-        } else {
-          const uint64_t dv2 = sdesc(sv2 + 2 * ks * kLboV2, kLboV2, kSbo);
-          const uint64_t dvz = sdesc(sv1 + 2 * ks * kLboB + (kHeadDim / 8) * 128, kLboB, kSbo);
-          mma_ts(tmem + kTO, ah, dv1, idO, kp > 0 || ks > 0);
-          mma_ts(tmem + kTO, al, dv1, idO, true);
-          mma_ts(tmem + kTO, ah, dv2, idO, true);
-          mma_ts(tmem + kTZ, ah, dvz, idZ, ks > 0);
-          mma_ts(tmem + kTZ, al, dvz, idZ, true);
-        }
-      }
-      mma_commit(&S.odone);
-      ++n_odone;
-    };
-    // the value-zero term of step kz (after its P.V), folded into zacc (half 0)
-    auto take_z = [&](int kz) {
-      uint32_t zr[16];
-      tld16(lane_base + kTZ, zr);
-      tld_wait();
-      const float iz = tc_pow2(-S.gz[kz & 1]);
-#pragma unroll
-      for (int gr = 0; gr < 4; ++gr) zacc[gr] = fmaf(__uint_as_float(zr[gr]) + __uint_as_float(zr[4 + gr]), iz, zacc[gr]);
-    };
-    if (issuer && nsteps > 0) issue_scores(0);
-    const int t0 = 64 * half;   // this half's first token
-    for (int k = 0; k < nsteps; ++k) {
+    for (int jj = 0; jj < nh; ++jj) {
+      const int k = jj >> 1, h = jj & 1;
       const bool win = k == ng;
-      const uint32_t par = (uint32_t)(k & 1);
-      // the scores of step k are done, and with them the P.V of step k - 1
-      ok = ok && tc_wait(&S.sdone, par, &S.abort_flag, p.err_word);
-      ok = ok && (win || tc_wait_count(&S.kready, (uint32_t)k, &S.abort_flag, p.err_word));
-      ok = ok && (k == 0 || tc_wait_count(&S.vready, (uint32_t)(k - 1), &S.abort_flag, p.err_word));
+      const int c0 = 64 * h + 32 * grp;   // this warp group's 32 tokens of the step
+      // the scores of this half-step are done; norms and value zeros (groups)
+      // or 2^fw (the window) are in shared memory
+      ok = ok && tc_wait(&S.sdone[h], (uint32_t)((jj >> 1) & 1), &S.abort_flag, p.err_word);
+      ok = ok && tc_wait_count(&S.kready, (uint32_t)(2 * k), &S.abort_flag, p.err_word);
       ok = __all_sync(0xffffffffu, ok);   // TMEM loads and stores are warp-collective
-      float mx = -INFINITY;
-      float dz = 0.0f;
-      const float4* nrm4 = reinterpret_cast<const float4*>(S.nrm[k & 1]);
-      const float fs = win ? p.scale_log2 : 0.0f;
-      const float psc = win ? tc_pow2(Gv) : 1.0f;    // window P.V in the value pieces' units
-      // s - base for tokens c0 + i .. + 3 (log2 units): groups n_t (S_t + dz) fr,
-      // the window S_t scale (-inf past wlen)
-      auto shifted = [&](const uint32_t (&sr)[32], int c0, int i, float base, float2& w01, float2& w23) {
-        const float2 s01 = make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
-        const float2 s23 = make_float2(__uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
-        const float2 nb = make_float2(-base, -base);
-        if (win) {
-          const float2 f2 = make_float2(fs, fs);
-          w01 = __ffma2_rn(s01, f2, nb);
-          w23 = __ffma2_rn(s23, f2, nb);
-          if (c0 + i >= wlen) w01.x = -INFINITY;
-          if (c0 + i + 1 >= wlen) w01.y = -INFINITY;
-          if (c0 + i + 2 >= wlen) w23.x = -INFINITY;
-          if (c0 + i + 3 >= wlen) w23.y = -INFINITY;
-        } else {
-          const float4 n4 = nrm4[(c0 + i) >> 2];
-          const float2 d2 = make_float2(dz, dz), f2 = make_float2(fr, fr);
-          w01 = __ffma2_rn(__fadd2_rn(s01, d2), __fmul2_rn(make_float2(n4.x, n4.y), f2), nb);
-          w23 = __ffma2_rn(__fadd2_rn(s23, d2), __fmul2_rn(make_float2(n4.z, n4.w), f2), nb);
-        }
-      };
+      // w_t = s_t (log2 units) for this warp group's tokens: groups n_t (S1_t +
+      // S2_t + dz) fr, the window (S1_t + S2_t) fr 2^(2 - fw) (-inf past wlen)
+      float w[32];
       if (ok) {
         tfence_after();
-        if (half == 0 && k > 0) take_z(k - 1);   // before this step's rescale and P.V
-        if (!win) {
-          uint32_t zr[16];
-          tld16(lane_base + kTS + 128, zr);
+        uint32_t a[32], b2[32];
+        tld32(lane_base + kTS + 32 * grp, a);
+        tld32(lane_base + kTS + kN1 + 32 * grp, b2);
+        if (win) {
           tld_wait();
-          dz = __uint_as_float(zr[0]) + __uint_as_float(zr[1]);
-        }
-        // pass 1: this half's maximum (the scores stay in TMEM; pass 2 writes P over them)
-#pragma unroll 1
-        for (int c0 = t0; c0 < t0 + 64; c0 += 32) {
-          uint32_t sr[32];
-          tld32(lane_base + kTS + c0, sr);
+          const float fwin = fr * tc_pow2(2 - S.fw);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            w[i] = c0 + i < wlen ? (__uint_as_float(a[i]) + __uint_as_float(b2[i])) * fwin : -INFINITY;
+        } else {
+          uint32_t z2[2];
+          tld2(lane_base + kTS + 64, z2);
           tld_wait();
+          const float dz = __uint_as_float(z2[0]) + __uint_as_float(z2[1]);
+          const float4* nrm4 = reinterpret_cast<const float4*>(S.nrm[k % 3]) + (c0 >> 2);
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
-            float2 w01, w23;
-            shifted(sr, c0, i, 0.0f, w01, w23);
-            mx = fmaxf(mx, fmaxf(fmaxf(w01.x, w01.y), fmaxf(w23.x, w23.y)));
+            const float4 n4 = nrm4[i >> 2];
+            const float2 d2 = make_float2(dz, dz), f2 = make_float2(fr, fr);
+            const float2 s01 = __fadd2_rn(make_float2(__uint_as_float(a[i]), __uint_as_float(a[i + 1])),
+                                          make_float2(__uint_as_float(b2[i]), __uint_as_float(b2[i + 1])));
+            const float2 s23 = __fadd2_rn(make_float2(__uint_as_float(a[i + 2]), __uint_as_float(a[i + 3])),
+                                          make_float2(__uint_as_float(b2[i + 2]), __uint_as_float(b2[i + 3])));
+            const float2 w01 = __fmul2_rn(__fadd2_rn(s01, d2), __fmul2_rn(make_float2(n4.x, n4.y), f2));
+            const float2 w23 = __fmul2_rn(__fadd2_rn(s23, d2), __fmul2_rn(make_float2(n4.z, n4.w), f2));
+            w[i] = w01.x;
+            w[i + 1] = w01.y;
+            w[i + 2] = w23.x;
+            w[i + 3] = w23.y;
           }
         }
-        S.pmax[half][r] = mx;
+      }
+      count(&S.sread);   // the score buffer is free for the next half-step's scores
+      // pass 1: this warp group's maximum over its 32 tokens
+      float mx = -INFINITY;
+      if (ok) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, w[i]);
+        S.pmax[jj & 1][grp][r] = mx;
       }
       named_bar_sync(3, 256);
+      uint32_t pk[32];   // [hi pairs of the chunk (16) | lo pairs (16)]
       if (ok) {
-        mx = fmaxf(mx, S.pmax[half ^ 1][r]);
-        // running maximum: rescale O (TMEM, half 0), the zero sums and l only when
-        // it grows by > 8 (per row, the same decision in both halves; the TMEM
-        // pass runs for the whole warp when any of its rows needs it)
+        mx = fmaxf(mx, S.pmax[jj & 1][grp ^ 1][r]);
+        // running maximum: rescale [O | Z] (TMEM, group 0) and l only when it
+        // grows by > 8 (per row, the same decision in both groups; the TMEM
+        // pass runs for the whole warp when any of its rows needs it, once the
+        // P.V that writes O last has completed)
         const float m_new = fmaxf(m_used, mx);
         const bool need = m_new > m_used + kRescaleLog2 || m_used == -INFINITY;
         const float alpha = !need ? 1.0f : m_used == -INFINITY ? 0.0f : tc_exp2(m_used - m_new);
-        if (half == 0 && k > 0 && __any_sync(0xffffffffu, need)) {   // O is not being written (see above)
+        if (grp == 0 && jj > 0 && __any_sync(0xffffffffu, need)) {
+          const bool done = __all_sync(0xffffffffu, pv_done(jj - 1));
+          if (done) {
+            tfence_after();
 #pragma unroll 1
-          for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
-            uint32_t orr[32];
-            tld32(lane_base + kTO + c0, orr);
+            for (int o0 = 0; o0 < kHeadDim; o0 += 32) {
+              uint32_t orr[32];
+              tld32(lane_base + kTO + o0, orr);
+              tld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+              tst32(lane_base + kTO + o0, orr);
+            }
+            uint32_t zr[16];
+            tld16(lane_base + kTZ, zr);
             tld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-            tst32(lane_base + kTO + c0, orr);
+            for (int i = 0; i < 16; ++i) zr[i] = __float_as_uint(__uint_as_float(zr[i]) * alpha);
+            tst16(lane_base + kTZ, zr);
           }
         }
         if (need) {
-#pragma unroll
-          for (int gr = 0; gr < kVGroups; ++gr) zacc[gr] *= alpha;
           l *= alpha;
           m_used = m_new;
         }
-        // pass 2: P = 2^(s - m_used) <= 2^8 into TMEM over the 32 score
-        // columns just read (see p_col)
+        // pass 2: p = 2^(w - m_used) <= 2^8
         const float base = m_used == -INFINITY ? 0.0f : m_used;
+        const float psc = win ? tc_pow2(Gv) : 1.0f;    // window P.V in the value pieces' units
         float2 lsum = make_float2(0.0f, 0.0f);
-#pragma unroll 1
-        for (int c0 = t0; c0 < t0 + 64; c0 += 32) {
-          uint32_t sr[32];
-          tld32(lane_base + kTS + c0, sr);
-          tld_wait();
-          uint32_t pk[32];   // [hi pairs of the chunk (16) | lo pairs (16)]
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            float2 w01, w23;
-            shifted(sr, c0, i, base, w01, w23);
-            const float2 p01 = make_float2(tc_exp2(w01.x), tc_exp2(w01.y));
-            const float2 p23 = make_float2(tc_exp2(w23.x), tc_exp2(w23.y));
-            lsum = __fadd2_rn(lsum, __fadd2_rn(p01, p23));
-            split_p(p01.x * psc, p01.y * psc, win, pk[i >> 1], pk[16 + (i >> 1)]);
-            split_p(p23.x * psc, p23.y * psc, win, pk[(i >> 1) + 1], pk[16 + (i >> 1) + 1]);
-          }
-          tst32(lane_base + kTS + c0, pk);
+        for (int i = 0; i < 32; i += 2) {
+          const float2 p01 = make_float2(tc_exp2(w[i] - base), tc_exp2(w[i + 1] - base));
+          lsum = __fadd2_rn(lsum, p01);
+          split_p(p01.x * psc, p01.y * psc, win, pk[i >> 1], pk[16 + (i >> 1)]);
         }
         l += lsum.x + lsum.y;
       }
-      tst_wait();
-      tfence_before();
-      named_bar_sync(3, 256);
-      if (issuer && ok) {
-        issue_pv(k);
-        if (k + 1 < nsteps) issue_scores(k + 1);
+      // P goes over the P of half-step j - 2 once its P.V has read it
+      bool pv_ok = true;
+      if (ok && jj > 1) pv_ok = pv_done(jj - 2);
+      ok = __all_sync(0xffffffffu, ok && pv_ok);
+      if (ok) {
+        tfence_after();
+        tst32(lane_base + kTP + 64 * (jj & 1) + 32 * grp, pk);
       }
+      tst_wait();
+      count(&S.pcount);
     }
-    // ---- the last P.V, its value-zero term, then the rows out (half 0):
-    // o = (O 2^-Gv + z) / l, lse = (m + log2 l) ln 2 (the TMEM loads for the
-    // whole warp, the stores for rows that exist)
-    if (half == 1) S.lpart[r] = l;
-    ok = ok && (nsteps == 0 || tc_wait(&S.odone, (uint32_t)((nsteps - 1) & 1), &S.abort_flag, p.err_word));
+    // ---- the last P.V, then the rows out (group 0): o = (O 2^-Gv + Z
+    // 2^-gz) / l, lse = (m + log2 l) ln 2 (the TMEM loads for the whole warp,
+    // the stores for rows that exist)
+    if (grp == 1) S.lpart[r] = l;
+    ok = ok && (nh == 0 || pv_done(nh - 1));
     ok = __all_sync(0xffffffffu, ok);
     named_bar_sync(3, 256);
-    if (half == 0 && ok) {
+    if (grp == 0 && ok) {
       tfence_after();
-      if (nsteps > 0 && nsteps - 1 != ng) take_z(nsteps - 1);
       l += S.lpart[r];
+      float zs[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // sum p z^V per value group (no groups: none)
+      {
+        uint32_t zr[16];
+        tld16(lane_base + kTZ, zr);
+        tld_wait();
+        const float izf = tc_pow2(-S.gz);
+        if (ng > 0) {
+#pragma unroll
+          for (int gr = 0; gr < 4; ++gr) zs[gr] = (__uint_as_float(zr[gr]) + __uint_as_float(zr[4 + gr])) * izf;
+        }
+      }
       const bool live_row = row < p.rows;
       const float iv = tc_pow2(-Gv);
-      const int qi = row / p.gqa, h = j * p.gqa + row % p.gqa;
+      const int qi = row / p.gqa, hq = j * p.gqa + row % p.gqa;
       float* rec = p.n_parts > 1 ? p.parts + (((int64_t)part * p.hkv + j) * p.rows + row) * kPrefillRecFloats : nullptr;
       const float inv = 1.0f / l;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+      for (int o0 = 0; o0 < kHeadDim; o0 += 32) {
         uint32_t orr[32];
-        tld32(lane_base + kTO + c0, orr);
+        tld32(lane_base + kTO + o0, orr);
         tld_wait();
-        const float z = zacc[c0 >> 5];
+        const float z = zs[o0 >> 5];
         if (live_row && rec) {
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(rec + c0 + i) =
+            *reinterpret_cast<float4*>(rec + o0 + i) =
                 make_float4(fmaf(__uint_as_float(orr[i]), iv, z), fmaf(__uint_as_float(orr[i + 1]), iv, z),
                             fmaf(__uint_as_float(orr[i + 2]), iv, z), fmaf(__uint_as_float(orr[i + 3]), iv, z));
         } else if (live_row) {
-          uint32_t* orow = reinterpret_cast<uint32_t*>(p.out + ((int64_t)qi * p.hq + h) * kHeadDim + c0);
+          uint32_t* orow = reinterpret_cast<uint32_t*>(p.out + ((int64_t)qi * p.hq + hq) * kHeadDim + o0);
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             uint32_t u[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float o0 = fmaf(__uint_as_float(orr[i + 2 * e]), iv, z) * inv;
-              const float o1 = fmaf(__uint_as_float(orr[i + 2 * e + 1]), iv, z) * inv;
-              u[e] = f32_to_bf16_bits(o0) | (f32_to_bf16_bits(o1) << 16);
+              const float o_0 = fmaf(__uint_as_float(orr[i + 2 * e]), iv, z) * inv;
+              const float o_1 = fmaf(__uint_as_float(orr[i + 2 * e + 1]), iv, z) * inv;
+              u[e] = f32_to_bf16_bits(o_0) | (f32_to_bf16_bits(o_1) << 16);
             }
             *reinterpret_cast<uint4*>(orow + i / 2) = make_uint4(u[0], u[1], u[2], u[3]);
           }
@@ -812,17 +969,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       } else if (rec) {
         *reinterpret_cast<float2*>(rec + kHeadDim) = make_float2(m_used, l);
       } else if (p.lse != nullptr) {
-        p.lse[(int64_t)qi * p.hq + h] = (m_used + log2f(l)) * 0.69314718055994530942f;
-      }
-    }
-    if (issuer) {
-      // before TMEM is freed: the last committed MMAs have completed (bounded,
-      // whatever the abort state: MMAs always complete)
-      for (int q = 0; q < 2; ++q) {
-        const uint32_t n = q ? n_odone : n_sdone;
-        if (n == 0) continue;
-        for (uint32_t i = 0; i < kSpinLimit; ++i)
-          if (mbar_try_wait(q ? &S.odone : &S.sdone, (n - 1) & 1)) break;
+        p.lse[(int64_t)qi * p.hq + hq] = (m_used + log2f(l)) * 0.69314718055994530942f;
       }
     }
   }
