@@ -412,11 +412,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int c0 = 0; c0 < 64; c0 += 32) {
       uint32_t hi[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float x0 = qst[r * kHeadDim + 2 * (c0 + i)], x1 = qst[r * kHeadDim + 2 * (c0 + i) + 1];
-        uint32_t lo;
-        split2(x0, x1, false, hi[i], lo);
-        *reinterpret_cast<uint32_t*>(S.qlo + canon(r, 2 * (c0 + i), kTcRows)) = lo;
+      for (int i = 0; i < 32; i += 4) {
+        uint32_t lo[4];   // channels 2 (c0 + i) .. + 7: one 16-byte row of a core matrix
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float x0 = qst[r * kHeadDim + 2 * (c0 + i + e)], x1 = qst[r * kHeadDim + 2 * (c0 + i + e) + 1];
+          split2(x0, x1, false, hi[i + e], lo[e]);
+        }
+        *reinterpret_cast<uint4*>(S.qlo + canon(r, 2 * (c0 + i), kTcRows)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
       tst32(lane_base + kTQ + c0, hi);
     }
@@ -553,7 +556,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int gz = 0;
     {
       float zm = 0.0f;
-#pragma unroll 1
+#pragma unroll 8   // independent loads in flight
       for (int k = 0; k < ng; ++k) {
         const float4 z4 = MR::v4(blocks + (int64_t)k * B::kBytes + B::kVZero, b);
         zm = fmaxf(zm, fmaxf(fmaxf(fabsf(z4.x), fabsf(z4.y)), fmaxf(fabsf(z4.z), fabsf(z4.w))));
