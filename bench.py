@@ -542,7 +542,12 @@ def gpu_arm(args, rank, world):
                               "bound": "tensor", "peak_tflops": bf16_peak,
                               "frac_of_bf16_peak": round(tf / bf16_peak, 3) if bf16_peak else None,
                               "history_parts": parts, "method": "L2 flushed before each call; CUDA events",
-                              "note": "fp16 hi+lo operands: 2 mma per product term"}
+                              # tcgen05 work per 64-token half-step of 128 rows: scores 8 k-steps x
+                              # (N 144 + N 80), P.V 4 k-steps x (N 144 + N 144 + N 128), M 128, K 16
+                              "tensor_flops_per_flop": round((8 * (144 + 80) + 4 * (144 + 144 + 128)) * 2 * 128 * 16
+                                                             / (4.0 * 128 * 64 * 128), 3),
+                              "note": "tcgen05 on exact fp16 operand pieces (query and P hi + lo, scale pieces): "
+                                      "3 products per term plus the zero-term rows"}
             c.close()
             del c, ks, vs, qc, oc, lc, pws
             torch.cuda.empty_cache()
