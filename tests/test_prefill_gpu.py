@@ -20,13 +20,15 @@ pytestmark = pytest.mark.gpu
 LSE_TOL = 1e-3
 
 
-def _run(L, hkv, hq, n_q, seed, scale=0.0, split=False):
+def _run(L, hkv, hq, n_q, seed, scale=0.0, split=False, kvq=None):
     O_ = U.lib()
     gen = torch.Generator().manual_seed(seed)
     k, v = W.make_sequence_kv(L, hkv, W.LLAMA_RECIPE, gen)
+    q = torch.randn((n_q, hq, 128), generator=gen).to(torch.bfloat16)
+    if kvq is not None:
+        k, v, q = kvq(k, v, q)
     cache = O_.OscarCache(1, hkv, L + 128)
     U.append_all(cache, [0], [k], [v])
-    q = torch.randn((n_q, hq, 128), generator=gen).to(torch.bfloat16)
     out = torch.empty((n_q, hq, 128), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((n_q, hq), dtype=torch.float32, device="cuda")
     ws = None
@@ -125,3 +127,29 @@ def test_prefill_bad_args():
 def test_prefill_gqa8():
     """8 query heads per KV head (rows = queries x 8 per KV head)."""
     _run(2048 + 40, hkv=2, hq=16, n_q=11, seed=97)
+
+
+def _bf16(x):
+    return x.to(torch.bfloat16)
+
+
+# inputs that stretch the operand scalings: value zeros far above the value
+# scales, of both signs (the zero sums accumulate across groups in one
+# per-CTA unit); window keys up to ~1e4 (the rotated keys' fp16 pieces carry
+# 2^fw) and down to ~1e-4 (queries scaled the other way, so that scores stay
+# moderate); scores that grow along the sequence (the running maximum moves
+# by more than 8 in log2 units several times, so O and the zero sums are
+# rescaled in TMEM)
+_EXTREME = {
+    "value_offset": lambda k, v, q: (k, _bf16(v.float() * 0.02 + torch.where(
+        (torch.arange(v.shape[0]) // 128 % 2 == 0)[:, None, None], 40.0, -25.0)), q),
+    "large_window_keys": lambda k, v, q: (_bf16(k.float() * 700.0), v, _bf16(q.float() / 700.0)),
+    "small_window_keys": lambda k, v, q: (_bf16(k.float() * 1e-4), v, _bf16(q.float() * 1e4)),
+    "growing_scores": lambda k, v, q: (_bf16(k.float() * torch.linspace(0.05, 4.0, k.shape[0])[:, None, None]), v, q),
+}
+
+
+@pytest.mark.parametrize("case", sorted(_EXTREME))
+def test_prefill_extreme_magnitudes(case):
+    _run(2048 + 100, hkv=2, hq=8, n_q=33, seed=101, kvq=_EXTREME[case])
+    _run(2048 + 100, hkv=2, hq=8, n_q=33, seed=101, kvq=_EXTREME[case], split=True)
