@@ -16,6 +16,10 @@ by one:
   the window rolls over: decode of the last step and every group (those
   closed during the stream included), for two sampled sequences.
 
+* chunked prefill, 512 queries x 32 heads against a 32K-token history with
+  the library's workspace (the history split into parts, then the merge):
+  24 sampled queries of two KV heads.
+
 The error against unquantised attention of the sampled heads is printed.
 """
 import numpy as np
@@ -177,3 +181,39 @@ def test_ragged_stream_sampled():
         print(f"stream seq {i} (L {L0} + {steps}) head {head}: groups closed {closed}; decode max|gpu - oracle| = "
               f"{worst:.2e}, vs unquantised {exact:.2e}")
     _rate_ok(acc, "stream, 2 heads")
+
+
+def test_prefill_512x32k_sampled():
+    """Chunked prefill at the bench's size and launch configuration: 512
+    queries x 32 heads against a 32K-token history, with the workspace the
+    library asks for (the history split into parts, then the merge).  Every
+    row of two KV heads' sampled queries against the oracle over the GPU's
+    cache: the output by the decode rule, the log-sum-exp within 1e-3."""
+    O_ = U.lib()
+    L, C = 32768, 512
+    k, v = W.make_sequence_kv(L, HKV, W.LLAMA_RECIPE, _gen(5), "cuda")
+    cache = O_.OscarCache(1, HKV, L)
+    cache.append([0], [0, L], k, v)
+    q = torch.randn((C, HQ, 128), generator=_gen(55), device="cuda").to(torch.bfloat16)
+    out = torch.empty_like(q)
+    lse = torch.empty((C, HQ), dtype=torch.float32, device="cuda")
+    nb = O_.oscar_prefill_workspace_bytes(cache.handle, 0, C, HQ)
+    assert nb > 0, "the bench's configuration splits the history"
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    O_.oscar_prefill_attention(cache.handle, 0, q, HQ, 0.0, out, lse, workspace=ws)
+    torch.cuda.synchronize()
+    O_.oscar_cache_check(cache.handle)
+    arena = U.read_arena(cache)
+    gqa = HQ // HKV
+    qs = np.random.default_rng(7).choice(C, size=24, replace=False)      # sampled queries
+    got, gl, qn = U.f64(out), lse.cpu().numpy().astype(np.float64), U.f64(q)
+    for j in (2, 7):
+        head = U.gpu_head(cache, arena, 0, j)
+        rows = qn[qs, j * gqa:(j + 1) * gqa].reshape(-1, 128)
+        o_ref, l_ref = O.history_attention(rows, head)
+        o_gpu = got[qs, j * gqa:(j + 1) * gqa].reshape(-1, 128)
+        err = P.assert_decode(o_gpu, o_ref, f"prefill 512x32K head {j}")
+        e = float(np.abs(gl[qs, j * gqa:(j + 1) * gqa].reshape(-1) - l_ref).max())
+        assert e <= 1e-3, f"prefill 512x32K head {j}: lse error {e:.2e}"
+        print(f"prefill 512 x 32K head {j}: {len(qs) * gqa} rows, max|o err|={err:.2e} max|lse err|={e:.2e}")
+    cache.close()
