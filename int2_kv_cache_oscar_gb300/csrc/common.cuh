@@ -61,7 +61,8 @@ constexpr int kWindowBytes = 2 * kGroup * kHeadDim * 2;  // K rows then V rows, 
 constexpr int kMetaHeader = 256;                          // status words
 
 // Largest GQA group one pass of the INT2 / bf16 decode kernels serves.
-constexpr int kMaxGqa = 4;
+constexpr int kMaxGqa = 4;       // query heads per KV head in one launch of the BF16 reference decode
+constexpr int kMaxGqaInt2 = 8;   // ... of the INT2 decode (two head sets of 4, see decode.cu)
 
 // Bounded spin of every mbarrier wait (each try_wait may itself suspend).
 constexpr uint32_t kSpinLimit = 1u << 24;

@@ -64,12 +64,12 @@ template <bool M16>
 struct DecSmemT {
   static constexpr int kStages = Ring<M16>::kStages;
   alignas(128) uint8_t stage[kStages][Ring<M16>::kStageBytes];
-  alignas(16) float qrot[kMaxGqa][kHeadDim];              // float4 stores
-  alignas(16) float4 q2t[4][32];                          // per-lane scaled query values, [i/4][lane]
+  alignas(16) float qrot[kMaxGqaInt2][kHeadDim];          // float4 stores
+  alignas(16) float4 q2t[2][4][32];                       // per-lane scaled query values, [head set][i/4][lane]
   // consumer-private probabilities; at a segment end each warp's region holds
   // its output rows ([head][channel]) for the CTA merge instead
   alignas(16) float pbuf[kConsumers][kMaxGqa][kPbStride];
-  float qmax[kMaxGqa];
+  float qmax[kMaxGqaInt2];
   float mst[kConsumers][kMaxGqa];
   float lst[kConsumers][kMaxGqa];
   alignas(8) uint64_t full[kStages];
@@ -160,7 +160,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // programmatic dependency).
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-template <int MAXS, bool M16>
+template <int MAXS, bool M16, bool PAIRS>
 __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     decode_int2_kernel(const __grid_constant__ DecodeParams<MAXS> p, const uint8_t* __restrict__ arena) {
   using DecSmem = DecSmemT<M16>;
@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], 1);
+      mbar_init(&S.empty[s], PAIRS ? 2 : 1);   // the warps that read each block
       S.issued[s] = 0;
     }
     mbar_init(&S.qready, kConsumers);
@@ -263,6 +263,14 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
   const bool lo_lane = half != 0;
   const int gqa = p.h.gqa;
   const float scale_log2 = p.h.scale_log2;
+  // Up to 4 query heads: each warp takes every 4th block for all heads.  5 to
+  // 8 (PAIRS): warps 2 i and 2 i + 1 read the same blocks (every 2nd) for head
+  // sets 0-3 and 4-7, so the cache is streamed once for all of them.
+  constexpr bool pairs = PAIRS;
+  const int hs = pairs ? (warp & 1) : 0;          // head set of this warp
+  const int h0 = kMaxGqa * hs;                    // its first query head
+  const int cw = pairs ? (warp >> 1) : warp;      // block stream of this warp
+  const int ncw = pairs ? kConsumers / 2 : kConsumers;
 
   // The queries, the value-scale maxima and the workspace are outputs of the
   // kernels before this one: wait for them.  Every CTA of this persistent grid
@@ -312,15 +320,14 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     const int64_t k_end = k + (seg_end - u);
     const int slot = p.seq[b].slot;
 
-    // ---- segment setup: rotate the GQA queries (warp h < 4 rotates head h)
-    if (warp < kMaxGqa) {
-      const int h = warp;
+    // ---- segment setup: rotate the GQA queries (warp w rotates heads w and w + 4)
+    for (int h = warp; h < (pairs ? kMaxGqaInt2 : kMaxGqa); h += kConsumers) {
       float qv[4] = {0.f, 0.f, 0.f, 0.f};
       if (h < gqa) {
-        const uint2 raw = seg_idx == 0   ? qpre0
-                          : seg_idx == 1 ? qpre1
-                                         : *reinterpret_cast<const uint2*>(
-                                               p.h.q + ((int64_t)b * p.h.hq + j * p.h.q_group + p.h.q_head0 + h) * kHeadDim + 4 * lane);
+        const uint2 raw = h == warp && seg_idx == 0   ? qpre0
+                          : h == warp && seg_idx == 1 ? qpre1
+                                                       : *reinterpret_cast<const uint2*>(
+                                                             p.h.q + ((int64_t)b * p.h.hq + j * p.h.q_group + p.h.q_head0 + h) * kHeadDim + 4 * lane);
         qv[0] = bf16_lo(raw.x);
         qv[1] = bf16_hi(raw.x);
         qv[2] = bf16_lo(raw.y);
@@ -353,8 +360,8 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     named_bar_sync(1, kConsumers * 32);
 
     // per-lane constants of this segment
-    const int Fk_b = range_exponent(S.qmax[hb] * (2.0f / 3.0f));     // B-column head hb
-    const int Fk_s = range_exponent(S.qmax[tig] * (2.0f / 3.0f));    // score head tig
+    const int Fk_b = range_exponent(S.qmax[h0 + hb] * (2.0f / 3.0f));     // B-column head h0 + hb
+    const int Fk_s = range_exponent(S.qmax[h0 + tig] * (2.0f / 3.0f));    // score head h0 + tig
     const float kqs = pow2f(24 - Fk_s) * scale_log2;
     const float inv2Fk_b = pow2f(-Fk_b);
     const float vmax = __uint_as_float(
@@ -365,19 +372,20 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     const float fv = pow2f(Fv);
     const float kv = pow2f(24 - Fv);
     // q2 table: this lane's 16 query values (its half of each k-step's
-    // channel pairs) times 2^(F - p); the same for every warp, written by warp 0
-    if (warp == 0) {
+    // channel pairs) times 2^(F - p); the same for every warp of a head set,
+    // written by warp hs
+    if (warp == hs) {
       float q2[16];
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const int c = 16 * ks + 2 * tig + 8 * half;
         const int pp = half ? frag_p(2 * (ks & 3) + 1) : frag_p(2 * (ks & 3));
         const float f = pow2f(Fk_b - pp);
-        q2[2 * ks] = S.qrot[hb][c] * f;
-        q2[2 * ks + 1] = S.qrot[hb][c + 1] * f;
+        q2[2 * ks] = S.qrot[h0 + hb][c] * f;
+        q2[2 * ks + 1] = S.qrot[h0 + hb][c + 1] * f;
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) S.q2t[i][lane] = make_float4(q2[4 * i], q2[4 * i + 1], q2[4 * i + 2], q2[4 * i + 3]);
+      for (int i = 0; i < 4; ++i) S.q2t[hs][i][lane] = make_float4(q2[4 * i], q2[4 * i + 1], q2[4 * i + 2], q2[4 * i + 3]);
     }
     named_bar_sync(1, kConsumers * 32);
 
@@ -410,8 +418,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
 #pragma unroll
     for (int i = 0; i < kVGroups; ++i) zacc[i] = 0.0f;
 
-    for (int64_t kk = k_begin + ((warp - k_begin) % kConsumers + kConsumers) % kConsumers; kk < k_end;
-         kk += kConsumers) {
+    for (int64_t kk = k_begin + ((cw - k_begin) % ncw + ncw) % ncw; kk < k_end; kk += ncw) {
       const int s = (int)(kk % kStages);
       const uint32_t use = (uint32_t)(kk / kStages);
       if (!wait_issued(&S.issued[s], use, &S.abort_flag, p.h.err_word, p.h.spin_limit)) continue;
@@ -430,7 +437,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       for (int i = 0; i < 4; ++i) qzc[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float4 q4 = S.q2t[i][lane];
+        const float4 q4 = S.q2t[hs][i][lane];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int ks = 2 * i + e;
@@ -612,16 +619,16 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       for (int idx = threadIdx.x; idx < gqa * kHeadDim; idx += kConsumers * 32) {
         const int h = idx >> 7;
         const int c = idx & (kHeadDim - 1);
-        float M = S.mst[0][h];
-#pragma unroll
-        for (int w = 1; w < kConsumers; ++w) M = fmaxf(M, S.mst[w][h]);
+        const int hw = h & (kMaxGqa - 1);   // the head's row in its warps' state
+        const int w0 = pairs ? (h >> 2) : 0, dw = pairs ? 2 : 1;   // the warps of its head set
+        float M = -INFINITY;
+        for (int w = w0; w < kConsumers; w += dw) M = fmaxf(M, S.mst[w][hw]);
         float o = 0.0f, l = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kConsumers; ++w) {
-          const float mw = S.mst[w][h];
+        for (int w = w0; w < kConsumers; w += dw) {
+          const float mw = S.mst[w][hw];
           const float f = (mw == -INFINITY) ? 0.0f : exp2f(mw - M);
-          o = fmaf(f, S.pbuf[w][h][pb_col(h, c)], o);
-          l = fmaf(f, S.lst[w][h], l);
+          o = fmaf(f, S.pbuf[w][hw][pb_col(hw, c)], o);
+          l = fmaf(f, S.lst[w][hw], l);
         }
         part[h * kPartialFloats + c] = o;
         if (c == 0) {
@@ -651,7 +658,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
 //           (h, c) then sums p_t v_t;
 //   merge:  m* = max(m_window, m_i), o = (sum 2^(m_i - m*) o_i) /
 //           (sum 2^(m_i - m*) l_i), written as bf16.
-constexpr int kCombineThreads = 128 * kMaxGqa;
+constexpr int kCombineThreads = 128 * kMaxGqaInt2;   // launched with 128 x gqa
 constexpr int kCombinePartBytes = 96 * 1024;   // at most this many bytes of partial records per chunk
 constexpr int kCombineSmem = kWindowBytes + kCombinePartBytes;   // largest launch
 constexpr int kCombineMaxChunk = kCombinePartBytes / (kPartialFloats * 4);
@@ -666,11 +673,11 @@ __global__ void __launch_bounds__(kCombineThreads)
   uint16_t* wk = reinterpret_cast<uint16_t*>(smem_raw);
   uint16_t* wv = wk + wrows * kHeadDim;
   float* part = reinterpret_cast<float*>(smem_raw + 2 * wrows * kHeadDim * 2);
-  __shared__ __align__(16) float qs[kMaxGqa][kHeadDim];
-  __shared__ float pw[kMaxGqa][kGroup];                                 // window probabilities
-  __shared__ float wts[kMaxGqa][kCombineMaxChunk];
-  __shared__ float red[kMaxGqa][2][4];
-  __shared__ float win_m[kMaxGqa];
+  __shared__ __align__(16) float qs[kMaxGqaInt2][kHeadDim];
+  __shared__ float pw[kMaxGqaInt2][kGroup];                             // window probabilities
+  __shared__ float wts[kMaxGqaInt2][kCombineMaxChunk];
+  __shared__ float red[kMaxGqaInt2][2][4];
+  __shared__ float win_m[kMaxGqaInt2];
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
 
@@ -868,13 +875,13 @@ int num_sms(int device) {
   return n;
 }
 
-template <int MAXS, bool M16>
+template <int MAXS, bool M16, bool PAIRS>
 cudaError_t launch_decode_int2_t(const DecodeParams<MAXS>& p, const uint8_t* arena, cudaStream_t stream,
                                  cudaEvent_t ev_start, cudaEvent_t ev_stop) {
   if (p.h.n_units <= 0) return cudaSuccess;
   const int smem = (int)sizeof(DecSmemT<M16>);
   static bool attr_done[64] = {};
-  cudaError_t e = ensure_smem_attr(decode_int2_kernel<MAXS, M16>, smem, attr_done);
+  cudaError_t e = ensure_smem_attr(decode_int2_kernel<MAXS, M16, PAIRS>, smem, attr_done);
   if (e != cudaSuccess) return e;
   if (ev_start) cudaEventRecord(ev_start, stream);
   // programmatic dependent launch: the grid may start while the previous
@@ -889,7 +896,7 @@ cudaError_t launch_decode_int2_t(const DecodeParams<MAXS>& p, const uint8_t* are
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode_int2_kernel<MAXS, M16>, p, arena);
+  e = cudaLaunchKernelEx(&cfg, decode_int2_kernel<MAXS, M16, PAIRS>, p, arena);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (ev_stop) cudaEventRecord(ev_stop, stream);
   return e;
@@ -898,8 +905,12 @@ cudaError_t launch_decode_int2_t(const DecodeParams<MAXS>& p, const uint8_t* are
 template <int MAXS>
 cudaError_t launch_decode_int2(const DecodeParams<MAXS>& p, const uint8_t* arena, bool meta16, cudaStream_t stream,
                                cudaEvent_t ev_start, cudaEvent_t ev_stop) {
-  return meta16 ? launch_decode_int2_t<MAXS, true>(p, arena, stream, ev_start, ev_stop)
-                : launch_decode_int2_t<MAXS, false>(p, arena, stream, ev_start, ev_stop);
+  // more than kMaxGqa query heads per KV head: two head sets on the same blocks
+  if (p.h.gqa > kMaxGqa)
+    return meta16 ? launch_decode_int2_t<MAXS, true, true>(p, arena, stream, ev_start, ev_stop)
+                  : launch_decode_int2_t<MAXS, false, true>(p, arena, stream, ev_start, ev_stop);
+  return meta16 ? launch_decode_int2_t<MAXS, true, false>(p, arena, stream, ev_start, ev_stop)
+                : launch_decode_int2_t<MAXS, false, false>(p, arena, stream, ev_start, ev_stop);
 }
 
 template <int MAXS>
@@ -910,7 +921,7 @@ cudaError_t launch_combine(const DecodeParams<MAXS>& p, const uint8_t* arena, cu
   // programmatic dependent launch: may start while the main kernel drains
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.h.n_seqs * p.h.hkv);
-  cfg.blockDim = dim3(kCombineThreads);
+  cfg.blockDim = dim3(128 * p.h.gqa);
   cfg.dynamicSmemBytes = (size_t)2 * p.h.comb_wrows * kHeadDim * 2 + p.h.comb_part_bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

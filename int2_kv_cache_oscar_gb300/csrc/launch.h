@@ -96,7 +96,7 @@ struct DecodeSeq {
 struct DecodeHeader {
   int32_t n_seqs;
   int32_t hkv;
-  int32_t gqa;           // query heads of each KV head served by this launch (<= kMaxGqa)
+  int32_t gqa;           // query heads of each KV head served by this launch (<= kMaxGqa BF16, kMaxGqaInt2 INT2)
   int32_t hq;
   int32_t max_groups;    // INT2: groups per (slot, head); bf16: max_seq_len
   int32_t n_ctas;        // main-kernel CTAs (N)

@@ -216,7 +216,8 @@ oscar_status run_decode(int device, int sms, int ctas_per_sm, int32_t n, const i
   // no more than one unit per consumer warp (4 per CTA): fewer partial records
   // and CTA launches (8K-token batch-1 step 15.3 -> 14.0 us)
   const int64_t N = std::min(std::min(T, maxN), (T + 3) / 4);
-  const size_t need = partial_bytes(N + rows, q_group < kMaxGqa ? q_group : kMaxGqa);
+  const int max_gqa = bf16_mode ? kMaxGqa : kMaxGqaInt2;   // query heads per KV head in one launch
+  const size_t need = partial_bytes(N + rows, q_group < max_gqa ? q_group : max_gqa);
   if (ws_bytes < need)
     return fail(OSCAR_ERR_CAPACITY, "workspace too small: %zu < %zu bytes", ws_bytes, need);
   P.h.n_seqs = n;
@@ -243,9 +244,10 @@ oscar_status run_decode(int device, int sms, int ctas_per_sm, int32_t n, const i
     P.h.spin_limit = 1u << 14;
     P.h.fault_unit = 0;
   }
-  // The kernels serve at most kMaxGqa query heads of a KV head per launch (mma
-  // columns = heads x {hi, lo}); larger groups run as consecutive passes, each
-  // streaming the cache again.  A pass's main kernel writes the shared
+  // The kernels serve at most max_gqa query heads of a KV head per launch (mma
+  // columns = 4 heads x {hi, lo}; the INT2 kernel takes two such head sets on
+  // the same blocks); larger groups run as consecutive passes, each streaming
+  // the cache again.  A pass's main kernel writes the shared
   // workspace only after its grid dependency wait (the previous pass's
   // combine has completed), and a fused step's passes all store the same new
   // token.
@@ -270,8 +272,8 @@ oscar_status run_decode(int device, int sms, int ctas_per_sm, int32_t n, const i
   // (measured: sharing one slows short contexts, 8K 15.3 -> 16.4 us).
   const bool pack = (int64_t)n * hkv > sms;
   P.h.comb_wrows = pack ? (wrows + 7) & ~7 : kGroup;   // multiples of 8 rows keep 16-byte alignment
-  for (int head0 = 0; head0 < q_group; head0 += kMaxGqa) {
-    P.h.gqa = q_group - head0 < kMaxGqa ? q_group - head0 : kMaxGqa;
+  for (int head0 = 0; head0 < q_group; head0 += max_gqa) {
+    P.h.gqa = q_group - head0 < max_gqa ? q_group - head0 : max_gqa;
     P.h.q_head0 = head0;
     const int64_t rec_bytes = (int64_t)P.h.gqa * kPartialFloats * 4;
     const int64_t cap = (96 * 1024) / rec_bytes;          // records of one chunk at most
@@ -478,7 +480,7 @@ oscar_status oscar_decode_workspace_bytes(const oscar_cache* c, int32_t n_seqs, 
   const int hkv = c->cfg.num_kv_heads;
   if (num_q_heads % hkv != 0) return fail(OSCAR_ERR_INVALID_ARG, "num_q_heads must be a multiple of Hkv");
   const int64_t slots = (int64_t)c->sms * decode_int2_ctas_per_sm() + (int64_t)n_seqs * hkv;
-  const int per_pass = num_q_heads / hkv < kMaxGqa ? num_q_heads / hkv : kMaxGqa;   // heads per decode pass
+  const int per_pass = num_q_heads / hkv < kMaxGqaInt2 ? num_q_heads / hkv : kMaxGqaInt2;   // heads per decode pass
   *out_bytes = partial_bytes(slots, per_pass);
   return ok();
 }
