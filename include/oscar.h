@@ -182,9 +182,9 @@ oscar_status oscar_decode_workspace_bytes(const oscar_cache* cache, int32_t n_se
  *   seq_ids      host int32 [n_seqs]; every slot must have length >= 1
  *   q            bf16 [n_seqs, num_q_heads, 128] (unrotated queries), 16-byte
  *                aligned, in device memory or page-locked host memory
- *   num_q_heads  any multiple of Hkv; the kernels serve up to 4 query heads
- *                of a KV head per pass, so num_q_heads / Hkv = 5..8 takes two
- *                passes over the cache, 9..12 three, and so on
+ *   num_q_heads  any multiple of Hkv; the kernels serve up to 8 query heads
+ *                of a KV head per pass over the cache, so num_q_heads / Hkv
+ *                = 9..16 takes two passes, 17..24 three, and so on
  *   softmax_scale  0 means 1 / sqrt(128)
  *   out          bf16 [n_seqs, num_q_heads, 128], 16-byte aligned, in device
  *                memory or page-locked host memory
