@@ -121,8 +121,7 @@ __device__ __forceinline__ float3 value_coefficients(float range, float s, float
 // 0x4B400000 + code.  For float32 parameters P' lies in [-2 kappa, 3 (1 +
 // 2 lambda)], so the code is the low byte without a clamp.  The magic add
 // cannot merge with the multiply-add before it.
-__device__ __forceinline__ uint2 value_code_bits2(float2 x, float2 negz, float2 a, float2 b, float2 c) {
-  const float2 d = __fadd2_rn(x, negz);
+__device__ __forceinline__ uint2 value_code_bits2(float2 d, float2 a, float2 b, float2 c) {
   const float2 u = __ffma2_rn(a, d, b);
   const float2 p = __ffma2_rn(u, d, c);
   const float2 y = __fadd2_rn(p, make_float2(kMagic, kMagic));
@@ -172,7 +171,47 @@ __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
   return d;
 }
 
-__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) { return make_float2(bf16_lo(u), bf16_hi(u)); }
+// Mixed-precision adds and multiply-adds (sm_100 and later) take a bf16
+// operand, widen it exactly and round the float32 result once.
+// (lo + hi, lo - hi) of the two bf16 values of a word: the first Hadamard
+// stage straight from the packed input.
+__device__ __forceinline__ float2 bf16_pair_butterfly(uint32_t u) {
+  float s, d;
+  asm("{\n\t.reg .b16 lo, hi, m1;\n\t.reg .f32 lf;\n\tmov.b32 {lo, hi}, %2;\n\tmov.b16 m1, 0xBF80;\n\t"
+      "add.rn.f32.bf16 lf, lo, 0f80000000;\n\t"    // -0 + lo: lo widened
+      "add.rn.f32.bf16 %0, hi, lf;\n\t"
+      "fma.rn.f32.bf16 %1, hi, m1, lf;\n\t}"       // lo - hi
+      : "=f"(s), "=f"(d)
+      : "r"(u));
+  return make_float2(s, d);
+}
+// (lo + c, hi + c) of the two bf16 values of a word.
+__device__ __forceinline__ float2 bf16x2_add(uint32_t u, float c) {
+  float a, b;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tadd.rn.f32.bf16 %0, lo, %3;\n\t"
+      "add.rn.f32.bf16 %1, hi, %3;\n\t}"
+      : "=f"(a), "=f"(b)
+      : "r"(u), "f"(c));
+  return make_float2(a, b);
+}
+
+// Three-input float32 minimum / maximum (one instruction on sm_100 and later)
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float4 fmin3(float4 a, float4 b, float4 c) {
+  return make_float4(fmin3(a.x, b.x, c.x), fmin3(a.y, b.y, c.y), fmin3(a.z, b.z, c.z), fmin3(a.w, b.w, c.w));
+}
+__device__ __forceinline__ float4 fmax3(float4 a, float4 b, float4 c) {
+  return make_float4(fmax3(a.x, b.x, c.x), fmax3(a.y, b.y, c.y), fmax3(a.z, b.z, c.z), fmax3(a.w, b.w, c.w));
+}
 
 // a * m + c on the integer multiply-add path (m is opaque to the compiler, so
 // the packing below stays off the shift / logic pipe)
@@ -285,14 +324,13 @@ __global__ void __launch_bounds__(kQThreads, 2)
         const int gi = 2 * half + g2;
         const float3 co = value_coefficients(mx - mn, sc, inv, !M16);
         const float2 ca = make_float2(co.x, co.x), cb = make_float2(co.y, co.y), cc = make_float2(co.z, co.z);
-        const float2 negz2 = make_float2(-zq, -zq);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const uint32_t ws[4] = {w4[i].x, w4[i].y, w4[i].z, w4[i].w};
 #pragma unroll
           for (int qq = 0; qq < 2; ++qq) {   // channels gi*32 + 8i + 4qq .. + 3
-            const uint2 c01 = value_code_bits2(bf16x2_to_float2(ws[2 * qq]), negz2, ca, cb, cc);
-            const uint2 c23 = value_code_bits2(bf16x2_to_float2(ws[2 * qq + 1]), negz2, ca, cb, cc);
+            const uint2 c01 = value_code_bits2(bf16x2_add(ws[2 * qq], -zq), ca, cb, cc);
+            const uint2 c23 = value_code_bits2(bf16x2_add(ws[2 * qq + 1], -zq), ca, cb, cc);
             uint32_t b;
             if constexpr (M16) {
               b = clamped_code(c01.x) | (clamped_code(c01.y) << 2) | (clamped_code(c23.x) << 4) |
@@ -318,17 +356,15 @@ __global__ void __launch_bounds__(kQThreads, 2)
     // ---- keys: rotation (6 butterfly stages in registers + 1 across the
     // thread pair), norm, unit vector.  x[i] holds channels 64 half + 2 i',
     // + 1 with i' = i (thread 0) or i ^ 16 (thread 1: halves swapped).
+    // stage h = 1 (within each pair) as the words are widened
     float2 x[32];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      x[4 * i + 0] = bf16x2_to_float2(kr[i].x);
-      x[4 * i + 1] = bf16x2_to_float2(kr[i].y);
-      x[4 * i + 2] = bf16x2_to_float2(kr[i].z);
-      x[4 * i + 3] = bf16x2_to_float2(kr[i].w);
+      x[4 * i + 0] = bf16_pair_butterfly(kr[i].x);
+      x[4 * i + 1] = bf16_pair_butterfly(kr[i].y);
+      x[4 * i + 2] = bf16_pair_butterfly(kr[i].z);
+      x[4 * i + 3] = bf16_pair_butterfly(kr[i].w);
     }
-    // stage h = 1: within each pair
-#pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] = make_float2(x[i].x + x[i].y, x[i].x - x[i].y);
     // stages h = 2 .. 16: pairs (i, i + h/2) of float2, the same in both layouts
 #pragma unroll
     for (int hb = 0; hb < 4; ++hb) {
@@ -432,13 +468,20 @@ __global__ void __launch_bounds__(kQThreads, 2)
     {
       const int cq = tid & 31, ts = tid >> 5;
       const float4* rows = reinterpret_cast<const float4*>(&S.kh[(16 * ts) * kHeadDim]);
-      float4 mn = rows[kh_slot(0, cq)];
-      float4 mx = mn;
+      const float4 v0 = rows[kh_slot(0, cq)], v1 = rows[(kHeadDim / 4) + kh_slot(1, cq)];
+      float4 mn = fmin3(v0, v1, rows[2 * (kHeadDim / 4) + kh_slot(2, cq)]);
+      float4 mx = fmax3(v0, v1, rows[2 * (kHeadDim / 4) + kh_slot(2, cq)]);
 #pragma unroll
-      for (int r = 1; r < 16; ++r) {
-        const float4 v = rows[r * (kHeadDim / 4) + kh_slot(r, cq)];
-        mn.x = fminf(mn.x, v.x); mn.y = fminf(mn.y, v.y); mn.z = fminf(mn.z, v.z); mn.w = fminf(mn.w, v.w);
-        mx.x = fmaxf(mx.x, v.x); mx.y = fmaxf(mx.y, v.y); mx.z = fmaxf(mx.z, v.z); mx.w = fmaxf(mx.w, v.w);
+      for (int r = 3; r < 15; r += 2) {    // rows 3 .. 14 in pairs, then row 15
+        const float4 a = rows[r * (kHeadDim / 4) + kh_slot(r, cq)];
+        const float4 b = rows[(r + 1) * (kHeadDim / 4) + kh_slot(r + 1, cq)];
+        mn = fmin3(mn, a, b);
+        mx = fmax3(mx, a, b);
+      }
+      {
+        const float4 a = rows[15 * (kHeadDim / 4) + kh_slot(15, cq)];
+        mn = make_float4(fminf(mn.x, a.x), fminf(mn.y, a.y), fminf(mn.z, a.z), fminf(mn.w, a.w));
+        mx = make_float4(fmaxf(mx.x, a.x), fmaxf(mx.y, a.y), fmaxf(mx.z, a.z), fmaxf(mx.w, a.w));
       }
       S.rmin[ts][cq] = mn;
       S.rmax[ts][cq] = mx;
@@ -448,11 +491,11 @@ __global__ void __launch_bounds__(kQThreads, 2)
       const int c = tid;
       const float* rmn = reinterpret_cast<const float*>(S.rmin);
       const float* rmx = reinterpret_cast<const float*>(S.rmax);
-      float mn = rmn[c], mx = rmx[c];
+      float mn = fminf(rmn[c], rmn[kHeadDim + c]), mx = fmaxf(rmx[c], rmx[kHeadDim + c]);
 #pragma unroll
-      for (int ts = 1; ts < 8; ++ts) {
-        mn = fminf(mn, rmn[ts * kHeadDim + c]);
-        mx = fmaxf(mx, rmx[ts * kHeadDim + c]);
+      for (int ts = 2; ts < 8; ts += 2) {
+        mn = fmin3(mn, rmn[ts * kHeadDim + c], rmn[(ts + 1) * kHeadDim + c]);
+        mx = fmax3(mx, rmx[ts * kHeadDim + c], rmx[(ts + 1) * kHeadDim + c]);
       }
       float sc = (mx - mn) / 3.0f;
       if constexpr (M16) {     // decide against the stored (rounded) parameters
