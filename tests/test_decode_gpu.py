@@ -88,9 +88,11 @@ def test_ragged_batch_decode_and_split_invariance():
         assert np.abs(alone[0] - got[i]).max() <= 2 * 2.0 ** -8 * max(1.0, np.abs(got[i]).max())
 
 
-@pytest.mark.parametrize("gqa", [1, 2, 4, 5, 8])
+@pytest.mark.parametrize("gqa", [1, 2, 3, 4, 5, 6, 7, 8, 12, 16])
 def test_gqa_group_sizes(gqa):
-    """Ratios above 4 run as passes of up to 4 query heads per KV head."""
+    """One pass serves up to 8 query heads per KV head (5 to 8 as two head
+    sets reading each block once, the second one partial below 8); larger
+    ratios run as several passes (12 = 8 + 4, 16 = 8 + 8)."""
     hkv = 4
     hq = hkv * gqa
     gen = torch.Generator().manual_seed(30 + gqa)

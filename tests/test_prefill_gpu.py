@@ -96,7 +96,7 @@ def test_prefill_history_lengths(L):
     _run(L, hkv=2, hq=8, n_q=37, seed=61 + L % 7)
 
 
-@pytest.mark.parametrize("gqa", [1, 2, 4])
+@pytest.mark.parametrize("gqa", [1, 2, 3, 4, 6])
 def test_prefill_gqa(gqa):
     _run(2048 + 17, hkv=2, hq=2 * gqa, n_q=20, seed=70 + gqa)
 
