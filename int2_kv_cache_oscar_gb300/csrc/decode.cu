@@ -137,10 +137,16 @@ __device__ __forceinline__ void frag_a_dyn(int kk, uint32_t w0, uint32_t w1, uin
 // {2 tig, 2 tig + 1} (register b0) and {2 tig + 8, 2 tig + 9} (register b1).
 // The hi lane computes the b0 pair, the lo lane the b1 pair; each splits its
 // pair into hi + lo fp16 and they swap the half the other one needs.
+// The lo column holds the negated remainders, hi - x (exact in float32, one
+// mixed-precision subtraction each with the fp16 operand taken in place), so
+// a contraction's value is its hi column minus its lo column.
 __device__ __forceinline__ void split_exchange(float x0, float x1, bool lo_lane, uint32_t& b0, uint32_t& b1) {
   const uint32_t hi = pack_half2(x0, x1);
-  const float2 r = __fadd2_rn(make_float2(x0, x1), make_float2(-half_lo_to_float(hi), -half_hi_to_float(hi)));
-  const uint32_t lo = pack_half2(r.x, r.y);
+  float r0, r1;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tsub.rn.f32.f16 %0, l, %3;\n\tsub.rn.f32.f16 %1, h, %4;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "r"(hi), "f"(x0), "f"(x1));
+  const uint32_t lo = pack_half2(r0, r1);
   const uint32_t send = lo_lane ? hi : lo;
   const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 4);
   b0 = lo_lane ? recv : hi;
@@ -488,7 +494,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
           for (int m = 0; m < 4; ++m) {
             const int mt = 4 * mh + m;
             const int t0 = 16 * mt + g;
-            const float2 a = make_float2(acc[m][0] + acc[m][1], acc[m][2] + acc[m][3]);
+            const float2 a = make_float2(acc[m][0] - acc[m][1], acc[m][2] - acc[m][3]);
             sc[mt] = __fmul2_rn(__ffma2_rn(a, kq2, qz2), make_float2(MR::one(knm, t0), MR::one(knm, t0 + 8)));
           }
         }
@@ -580,7 +586,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
         const float2 al2 = make_float2(alpha, alpha);
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt)
-          o_acc[mt] = __ffma2_rn(o_acc[mt], al2, make_float2(pacc[mt][0] + pacc[mt][1], pacc[mt][2] + pacc[mt][3]));
+          o_acc[mt] = __ffma2_rn(o_acc[mt], al2, make_float2(pacc[mt][0] - pacc[mt][1], pacc[mt][2] - pacc[mt][3]));
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty[s]);
