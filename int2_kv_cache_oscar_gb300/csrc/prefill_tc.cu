@@ -301,6 +301,19 @@ __device__ __forceinline__ void split_p(float x0, float x1, bool bf16, uint32_t&
   }
 }
 
+// fp16 hi + lo of a pair of P values (x0 in the low half): hi rounded to
+// nearest, lo the remainder x - hi (exact in float: one mixed-precision
+// multiply-add per value with the fp16 hi taken in place) rounded to fp16.
+__device__ __forceinline__ void split_p16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(x1), "f"(x0));
+  float r0, r1;
+  asm("{\n\t.reg .b16 l, h, m1;\n\tmov.b32 {l, h}, %2;\n\tmov.b16 m1, 0xBC00;\n\t"
+      "fma.rn.f32.f16 %0, l, m1, %3;\n\tfma.rn.f32.f16 %1, h, m1, %4;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "r"(hi), "f"(x0), "f"(x1));
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(r1), "f"(r0));
+}
+
 // Normalised Walsh-Hadamard transform of a 128-vector held by one warp (lane
 // = elements 4 lane .. + 3): two stages in registers, five across lanes.
 __device__ __forceinline__ void fwht128_warp(float (&v)[4], int lane) {
@@ -894,13 +907,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         // pass 2: p = 2^(w - m_used) <= 2^8
         const float base = m_used == -INFINITY ? 0.0f : m_used;
-        const float psc = win ? tc_pow2(Gv) : 1.0f;    // window P.V in the value pieces' units
+        const float2 nb = make_float2(-base, -base);
         float2 lsum = make_float2(0.0f, 0.0f);
+        if (win) {
+          const float psc = tc_pow2(Gv);    // window P.V in the value pieces' units
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float2 p01 = make_float2(tc_exp2(w[i] - base), tc_exp2(w[i + 1] - base));
-          lsum = __fadd2_rn(lsum, p01);
-          split_p(p01.x * psc, p01.y * psc, win, pk[i >> 1], pk[16 + (i >> 1)]);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 d = __fadd2_rn(make_float2(w[i], w[i + 1]), nb);
+            const float2 p01 = make_float2(tc_exp2(d.x), tc_exp2(d.y));
+            lsum = __fadd2_rn(lsum, p01);
+            split_p(p01.x * psc, p01.y * psc, true, pk[i >> 1], pk[16 + (i >> 1)]);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float2 d = __fadd2_rn(make_float2(w[i], w[i + 1]), nb);
+            const float2 p01 = make_float2(tc_exp2(d.x), tc_exp2(d.y));
+            lsum = __fadd2_rn(lsum, p01);
+            split_p16(p01.x, p01.y, pk[i >> 1], pk[16 + (i >> 1)]);
+          }
         }
         l += lsum.x + lsum.y;
       }
