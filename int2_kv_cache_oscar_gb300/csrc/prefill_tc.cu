@@ -844,16 +844,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tld_wait();
           const float dz = __uint_as_float(z2[0]) + __uint_as_float(z2[1]);
           const float4* nrm4 = reinterpret_cast<const float4*>(S.nrm[k % 3]) + (c0 >> 2);
+          // w = ((s1 + s2) fr + dz fr) n
+          const float2 f2 = make_float2(fr, fr), dzf2 = make_float2(dz * fr, dz * fr);
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
             const float4 n4 = nrm4[i >> 2];
-            const float2 d2 = make_float2(dz, dz), f2 = make_float2(fr, fr);
             const float2 s01 = __fadd2_rn(make_float2(__uint_as_float(a[i]), __uint_as_float(a[i + 1])),
                                           make_float2(__uint_as_float(b2[i]), __uint_as_float(b2[i + 1])));
             const float2 s23 = __fadd2_rn(make_float2(__uint_as_float(a[i + 2]), __uint_as_float(a[i + 3])),
                                           make_float2(__uint_as_float(b2[i + 2]), __uint_as_float(b2[i + 3])));
-            const float2 w01 = __fmul2_rn(__fadd2_rn(s01, d2), __fmul2_rn(make_float2(n4.x, n4.y), f2));
-            const float2 w23 = __fmul2_rn(__fadd2_rn(s23, d2), __fmul2_rn(make_float2(n4.z, n4.w), f2));
+            const float2 w01 = __fmul2_rn(__ffma2_rn(s01, f2, dzf2), make_float2(n4.x, n4.y));
+            const float2 w23 = __fmul2_rn(__ffma2_rn(s23, f2, dzf2), make_float2(n4.z, n4.w));
             w[i] = w01.x;
             w[i + 1] = w01.y;
             w[i + 2] = w23.x;
@@ -866,7 +867,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float mx = -INFINITY;
       if (ok) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, w[i]);
+        for (int i = 0; i < 32; i += 2) {
+          asm("max.f32 %0, %0, %1, %2;" : "+f"(mx) : "f"(w[i]), "f"(w[i + 1]));
+        }
         S.pmax[jj & 1][grp][r] = mx;
       }
       named_bar_sync(3, 256);
