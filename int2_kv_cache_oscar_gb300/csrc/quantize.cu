@@ -16,8 +16,9 @@
 //      four channels per byte), s/z to the block.  The key row is already
 //      being loaded into registers.
 //   2. K: unnormalised fast Walsh-Hadamard transform, H_d = Hu / sqrt(128):
-//      6 butterfly stages in registers (packed f32x2), the 7th across the
-//      thread pair with shuffles of half the values (after it each thread
+//      6 butterfly stages in registers (the first as the bf16 words are
+//      widened, with mixed-precision adds; the others packed f32x2), the 7th
+//      across the thread pair with shuffles of half the values (after it each thread
 //      holds channels [32 half, + 32) and [64 + 32 half, + 32));
 //      n_t = sqrt(|Hu k|^2 / 128); k_hat = Hu k / |Hu k| (= H_d k / n_t).
 //   3. Per-channel min/max of k_hat over the 128 tokens (shared memory,
