@@ -411,9 +411,36 @@ __global__ void __launch_bounds__(kQThreads, 2)
       sq2b = __ffma2_rn(x[i + 1], x[i + 1], sq2b);
     }
     const float sq = (sq2.x + sq2.y) + (sq2b.x + sq2b.y);
-    const float ss = sq + __shfl_xor_sync(0xffffffffu, sq, 1);
-    const float norm = sqrtf(ss * (1.0f / kHeadDim));
-    const float rinv = ss > 0.0f ? 1.0f / sqrtf(ss) : 0.0f;
+    const float ss = sq + __shfl_xor_sync(0xffffffffu, sq, 1);   // the same sum in both threads
+    float norm, rinv;
+    if (ss >= 0x1p-100f && ss <= 0x1p+100f) {
+      norm = sqrtf(ss * (1.0f / kHeadDim));
+      rinv = 1.0f / sqrtf(ss);
+    } else {
+      // a zero token, or squares that under- or overflowed (both threads of
+      // the pair): the norm of Hu k from Hu k scaled by 2^-e, exact in two
+      // power-of-two steps, with m = max |Hu k| < 2^e
+      const unsigned pair = 3u << (tid & 30);
+      float m = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) m = fmaxf(m, fmaxf(fabsf(x[i].x), fabsf(x[i].y)));
+      m = fmaxf(m, __shfl_xor_sync(pair, m, 1));
+      int e = 0;
+      if (m > 0.0f) frexpf(m, &e);
+      const int e1 = -e / 2;
+      const float2 f1 = make_float2(ldexpf(1.0f, e1), ldexpf(1.0f, e1));
+      const float2 f2 = make_float2(ldexpf(1.0f, -e - e1), ldexpf(1.0f, -e - e1));
+      float2 a2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        x[i] = __fmul2_rn(__fmul2_rn(x[i], f1), f2);
+        a2 = __ffma2_rn(x[i], x[i], a2);
+      }
+      float s2 = a2.x + a2.y;
+      s2 += __shfl_xor_sync(pair, s2, 1);
+      norm = ldexpf(sqrtf(s2 * (1.0f / kHeadDim)), e);
+      rinv = s2 > 0.0f ? 1.0f / sqrtf(s2) : 0.0f;   // k_hat = (Hu k 2^-e) / |Hu k 2^-e|
+    }
     // scalar rounded products: the k_hat in registers (code decisions) is the
     // k_hat stored below (parameters), and its packed subtraction in
     // code_bits2 cannot be fused with this multiply

@@ -16,7 +16,8 @@ Canalized Rotation, then Omni-Token Scaling, then per-channel INT2).
 * Values on 4 dyadic levels z + s * code per token and 32-channel group, both
   extremes present: codes, s and z come back exactly.
 The first two tests use no oracle; the degenerate-input case (zero-norm
-tokens, an all-zero key group, an all-zero value group) is checked against it.
+tokens, an all-zero key group, an all-zero value group) and key tokens whose
+squares under- or overflow float32 are checked against it.
 """
 import numpy as np
 import pytest
@@ -145,3 +146,42 @@ def test_zero_norm_tokens_and_constant_channels():
     g1 = U.gpu_head(cache, arena, 0, 1)
     assert np.all(g1.values.scale[0][:, 1] == 0) and np.all(g1.values.zero[0][:, 1] == 0)
     assert np.all(g1.values.codes[0][:, 32:64] == 0)
+
+
+def test_extreme_key_norms():
+    """Key tokens whose squared channels under- or overflow float32: tokens
+    near 1e-24 and 1e-30, a token at the bf16 subnormal level, and tokens
+    near 1e22 (squares above 1e38).  Norms, scales, zeros and codes against
+    the oracle, and the decode over the GPU's cache (the huge tokens dominate
+    the softmax)."""
+    from int2_kv_cache_oscar_gb300 import workloads as W
+    from oracle import oscar_oracle as O
+    from tests import parity as P
+
+    gen = torch.Generator().manual_seed(17)
+    L, hkv, hq = 2 * G + 30, 2, 8
+    k, v = W.make_sequence_kv(L, hkv, W.LLAMA_RECIPE, gen)
+    k = k.double()
+    scale = {3: 1e-24, 40: 1e-30, 77: 1e-24, 90: 1e22, G + 5: 1e-40, G + 60: 1e22, G + 61: 1e-24}
+    for t, f in scale.items():
+        k[t] *= f
+    k = k.to(torch.bfloat16)
+    assert torch.isfinite(k.float()).all() and 0 < k[G + 5].float().abs().max() < 1.18e-38
+    cache = U.lib().OscarCache(1, hkv, L + 8)
+    U.append_all(cache, [0], [k], [v])
+    q = W.make_q(1, hq, seed=18)
+    out = torch.empty((1, hq, 128), dtype=torch.bfloat16, device="cuda")
+    cache.decode([0], q.cuda(), hq, out, cache.workspace(1, hq))
+    U.lib().oscar_cache_check(cache.handle)
+    arena = U.read_arena(cache)
+    got, qn = U.f64(out), U.f64(q)
+    for h in range(hkv):
+        g = U.gpu_head(cache, arena, 0, h)
+        r = U.oracle_head(k, v, h)
+        P.assert_codes(g.keys.codes, r.keys.codes, r.keys.pre, f"head {h} K codes")
+        for name in ("scale", "zero", "norm"):
+            P.assert_meta(getattr(g.keys, name), getattr(r.keys, name), f"head {h} K {name}")
+        norms = g.keys.norm.reshape(-1)
+        for t in scale:
+            assert norms[t] > 0.0 and np.isfinite(norms[t]), f"head {h}: token {t} norm {norms[t]}"
+        P.assert_decode(got[0, 4 * h:4 * h + 4], O.decode_head(qn[0, 4 * h:4 * h + 4], g), f"head {h} decode")
