@@ -57,7 +57,8 @@ struct Ring {
   static constexpr int kStageBytes = Blk<M16>::kBytes;
 };
 
-static_assert(kPreWaitStages <= Ring<false>::kStages && kPreWaitStages <= Ring<true>::kStages,
+static_assert(kPreWaitStages <= Ring<false>::kStages && kPreWaitStages <= Ring<true>::kStages &&
+                  kConsumers <= Ring<false>::kStages && kConsumers <= Ring<true>::kStages,
               "the pre-wait fill uses each stage once (no free-slot waits)");
 
 template <bool M16>
@@ -218,14 +219,16 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     // (no kernel that may still run can be writing them), kPreWaitStages at
     // most.  Launched as a programmatic dependent, this grid starts while the
     // previous kernel finishes, and these copies overlap its tail.
-    while (u < u1 && k < kPreWaitStages) {
+    // a CTA with at most one unit per consumer fills all of them
+    const int64_t pre = (u1 - u0) <= kConsumers ? kConsumers : kPreWaitStages;
+    while (u < u1 && k < pre) {
       int b, j, g, ng;
       locate_unit(p, u, b, j, g, ng);
       const int64_t row_end = p.seq[b].ubase + (int64_t)(j + 1) * ng;
       const int64_t seg_end = row_end < u1 ? row_end : u1;
       const int settled = p.seq[b].settled;
       const uint8_t* src = blocks + (((int64_t)p.seq[b].slot * hkv + j) * p.h.max_groups + g) * kStageBytes;
-      for (; u < seg_end && k < kPreWaitStages && g < settled; ++u, ++k, ++g, src += kStageBytes) issue(k, src);
+      for (; u < seg_end && k < pre && g < settled; ++u, ++k, ++g, src += kStageBytes) issue(k, src);
       if (u < seg_end) break;         // an unsettled group (or the ring is full)
     }
     grid_dependency_wait();
