@@ -89,9 +89,12 @@ enum {
  * must be 256-byte aligned):
  *
  *   [0, 256)                       status words; word 0 = device error flags
- *   [256, M)                       per (slot, kv head): float32 bit pattern of
+ *   [256, 256 + 4 S H)             per (slot, kv head): float32 bit pattern of
  *                                  the largest value scale s_v quantised so
- *                                  far (4 bytes each), M = 256-aligned end
+ *                                  far (4 bytes each; S = max_batch, H = Hkv)
+ *   [256 + 4 S H, M)               per (slot, kv head): float32 bit pattern of
+ *                                  the largest |value zero| z_v quantised so
+ *                                  far, M = 256-aligned end
  *   blocks  (base = M)             one block of B bytes per
  *                                  (slot, kv head, group g):
  *                                  base + ((slot*Hkv + head)*max_groups + g)*B,

@@ -69,7 +69,8 @@ constexpr uint32_t kSpinLimit = 1u << 24;
 constexpr uint32_t kErrTimeout = 1u;
 
 struct ArenaLayout {
-  int64_t meta_bytes;     // header + per (slot, head) s_v maxima, 256-aligned
+  int64_t meta_bytes;     // header + per (slot, head) s_v maxima + per (slot, head) |z_v| maxima, 256-aligned
+  int64_t zmax_off;       // the |z_v| maxima
   int64_t blocks_off;
   int64_t windows_off;
   int64_t total;
@@ -80,7 +81,8 @@ __host__ __device__ inline ArenaLayout arena_layout(int32_t max_batch, int32_t h
                                                     int32_t block_bytes = kBlockBytes) {
   ArenaLayout L;
   L.max_groups = (max_len + kGroup - 1) / kGroup;
-  int64_t meta = kMetaHeader + (int64_t)max_batch * hkv * 4;
+  L.zmax_off = kMetaHeader + (int64_t)max_batch * hkv * 4;
+  const int64_t meta = L.zmax_off + (int64_t)max_batch * hkv * 4;
   L.meta_bytes = (meta + 255) / 256 * 256;
   L.blocks_off = L.meta_bytes;
   int64_t blocks = (int64_t)max_batch * hkv * L.max_groups * block_bytes;

@@ -66,6 +66,7 @@ struct QuantPlan {
   int32_t wide;          // 1: k and v are 32-byte aligned (32-byte row loads)
   int64_t blocks_off;
   int64_t windows_off;
+  int64_t zmax_off;      // per (slot, head) largest |value zero| (float bits, atomicMax)
   PackedTask t[CAP];
 };
 static_assert(sizeof(QuantPlan<kQuantPlanLarge>) + 3 * sizeof(void*) <= 32764, "kernel parameter limit");
@@ -155,6 +156,7 @@ struct PrefillParams {
   int32_t max_groups;
   int64_t blocks_off;
   int64_t windows_off;
+  int64_t zmax_off;      // per (slot, head) largest |value zero| quantised so far (float bits)
   float scale_log2;      // softmax_scale * log2(e)
   int32_t n_parts;       // the groups are split into this many parts (grid.z); 1: no split
   const uint16_t* q;     // [n_q, hq, d] bf16

@@ -163,6 +163,7 @@ oscar_status run_quant_plan(oscar_cache* c, const std::vector<QuantTask>& tasks,
   plan.wide = (aligned(k, 32) && aligned(v, 32)) ? 1 : 0;   // the arena's window rows are 256-byte aligned
   plan.blocks_off = c->layout.blocks_off;
   plan.windows_off = c->layout.windows_off;
+  plan.zmax_off = c->layout.zmax_off;
   for (size_t i = begin; i < end; ++i) plan.t[i - begin] = pack_task(tasks[i]);
   cudaError_t e;
   if constexpr (CAP == kQuantPlanSmall)
@@ -356,12 +357,17 @@ oscar_status oscar_cache_reset(oscar_cache* c, int32_t seq, void* stream) {
   DeviceGuard dg(c->cfg.device);
   if (dg.err != cudaSuccess) return cuda_fail(dg.err, "cudaSetDevice");
   const int hkv = c->cfg.num_kv_heads;
+  // the slot's value-scale and |value zero| maxima
   uint8_t* meta = c->arena + kMetaHeader;
+  uint8_t* zmax = c->arena + c->layout.zmax_off;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (seq < 0)
-    e = cudaMemsetAsync(meta, 0, (size_t)c->cfg.max_batch * hkv * 4, static_cast<cudaStream_t>(stream));
-  else
-    e = cudaMemsetAsync(meta + (size_t)seq * hkv * 4, 0, (size_t)hkv * 4, static_cast<cudaStream_t>(stream));
+  if (seq < 0) {
+    e = cudaMemsetAsync(meta, 0, (size_t)c->cfg.max_batch * hkv * 4 * 2, st);   // both arrays, contiguous
+  } else {
+    e = cudaMemsetAsync(meta + (size_t)seq * hkv * 4, 0, (size_t)hkv * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(zmax + (size_t)seq * hkv * 4, 0, (size_t)hkv * 4, st);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(reset)");
   if (seq < 0) {
     std::fill(c->len.begin(), c->len.end(), 0);
@@ -738,6 +744,7 @@ oscar_status oscar_prefill_attention(oscar_cache* c, int32_t seq, int32_t n_q, c
   P.max_groups = c->layout.max_groups;
   P.blocks_off = c->layout.blocks_off;
   P.windows_off = c->layout.windows_off;
+  P.zmax_off = c->layout.zmax_off;
   const float scale = softmax_scale == 0.0f ? 1.0f / std::sqrt((float)kHeadDim) : softmax_scale;
   P.scale_log2 = scale * 1.4426950408889634f;
   P.q = static_cast<const uint16_t*>(q);

@@ -564,28 +564,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         S.nissued[k] = 1;
       }
     }
-    // 2^gz with max |z^V| 2^gz < 2^14 over this CTA's groups: the zero sums
-    // accumulate across groups in these units (token b's zeros of every group)
+    // 2^gz with max |z^V| 2^gz < 2^14 over the sequence's groups (the
+    // quantiser records each (slot, head)'s largest |value zero|): the zero
+    // sums accumulate across groups in these units
     int gz = 0;
     {
-      float zm = 0.0f;
-#pragma unroll 8   // independent loads in flight
-      for (int k = 0; k < ng; ++k) {
-        const float4 z4 = MR::v4(blocks + (int64_t)k * B::kBytes + B::kVZero, b);
-        zm = fmaxf(zm, fmaxf(fmaxf(fabsf(z4.x), fabsf(z4.y)), fmaxf(fabsf(z4.z), fabsf(z4.w))));
-      }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) zm = fmaxf(zm, __shfl_xor_sync(0xffffffffu, zm, o));
-      if (lane == 0) S.wmax[bw] = zm;
-      bar_sync_threads(2, 128);
-      zm = fmaxf(fmaxf(S.wmax[0], S.wmax[1]), fmaxf(S.wmax[2], S.wmax[3]));
+      const float zm = __uint_as_float(
+          reinterpret_cast<const uint32_t*>(arena + p.zmax_off)[(int64_t)p.slot * p.hkv + j]);
       if (zm > 0.0f && zm <= 3.0e38f) {
         int e;
         frexpf(zm, &e);   // zm < 2^e
         gz = max(-100, min(14 - e, 100));
       }
       if (lead) S.gz = gz;   // read by the rows after their last half-step
-      bar_sync_threads(2, 128);   // wmax is free again
     }
     const float gzf = tc_pow2(gz);
     uint32_t zk = 0u;            // key zero of channel b (x 4): fp16 hi | lo << 16

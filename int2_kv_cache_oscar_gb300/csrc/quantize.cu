@@ -56,7 +56,7 @@ struct QuantSmem {
   alignas(16) float4 rmin[8][kHeadDim / 4];          // per 16-token slice: channel minima
   alignas(16) float4 rmax[8][kHeadDim / 4];          // per 16-token slice: channel maxima
   alignas(16) float4 kq[kHeadDim / 2 + 4];           // per channel pair (1/s, 1/s', -z, -z'), see kq_index
-  float red[kQThreads / 32];
+  uint32_t red[2][kQThreads / 32];   // per warp: largest value scale, largest |value zero| (float bits)
 };
 static_assert(offsetof(QuantSmem, vb) % 16 == 0, "alignment");
 static_assert(offsetof(QuantSmem, kq) % 16 == 0, "alignment");
@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
     }
 
     // ---- values: per-token INT2 over this thread's two 32-channel groups
-    float smax = 0.0f;
+    float smax = 0.0f, zabs = 0.0f;   // largest value scale and |value zero| of this thread's groups
     {
       uint4 vr[8];
       const uint4* vs4 = reinterpret_cast<const uint4*>(vsrc);
@@ -322,6 +322,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
         sv[g2] = sc;
         zv[g2] = zq;
         smax = fmaxf(smax, sc);
+        zabs = fmaxf(zabs, fabsf(zq));
         const int gi = 2 * half + g2;
         const float3 co = value_coefficients(mx - mn, sc, inv, !M16);
         const float2 ca = make_float2(co.x, co.x), cb = make_float2(co.y, co.y), cc = make_float2(co.z, co.z);
@@ -461,8 +462,14 @@ __global__ void __launch_bounds__(kQThreads, 2)
       }
     }
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
-    if ((tid & 31) == 0) S.red[tid >> 5] = smax;
+    {   // non-negative floats order as their bit patterns
+      const uint32_t sm = __reduce_max_sync(0xffffffffu, __float_as_uint(smax));
+      const uint32_t zm = __reduce_max_sync(0xffffffffu, __float_as_uint(zabs));
+      if ((tid & 31) == 0) {
+        S.red[0][tid >> 5] = sm;
+        S.red[1][tid >> 5] = zm;
+      }
+    }
     __syncthreads();
 
     // ---- value code words, V order (the staged bytes are complete)
@@ -577,11 +584,11 @@ __global__ void __launch_bounds__(kQThreads, 2)
         kcodes[((mt * 32 + 4 * g + tig) * 4) + 2 * half + r] = w;
       }
     }
-    if (tid == 0) {
-      float m = S.red[0];
+    if (tid < 2) {   // the (slot, head)'s largest value scale (decode) and |value zero| (prefill)
+      uint32_t m = S.red[tid][0];
 #pragma unroll
-      for (int i = 1; i < kQThreads / 32; ++i) m = fmaxf(m, S.red[i]);
-      atomicMax(reinterpret_cast<unsigned int*>(arena + kMetaHeader) + sh, __float_as_uint(m));
+      for (int i = 1; i < kQThreads / 32; ++i) m = max(m, S.red[tid][i]);
+      atomicMax(reinterpret_cast<unsigned int*>(arena + (tid == 0 ? (int64_t)kMetaHeader : plan.zmax_off)) + sh, m);
     }
     if (T.tail_count() <= 0) return;
     // the window reads above completed before the first __syncthreads

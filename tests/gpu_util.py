@@ -73,13 +73,16 @@ def oracle_head(k: torch.Tensor, v: torch.Tensor, head: int, meta_bits: int = 32
 
 
 def live_bytes(cache, arena: np.ndarray, slot: int) -> np.ndarray:
-    """Concatenated bytes that hold state for `slot`: its value-scale maxima,
-    every closed group block and the occupied window rows of every head."""
+    """Concatenated bytes that hold state for `slot`: its value-scale and
+    |value zero| maxima, every closed group block and the occupied window rows
+    of every head."""
     O_ = lib()
     L = cache.length(slot)
     ng, w = L // 128, L % 128
     hkv = cache.num_kv_heads
-    parts = [arena[256 + slot * hkv * 4: 256 + (slot + 1) * hkv * 4]]
+    zoff = 256 + cache.cfg.max_batch * hkv * 4
+    parts = [arena[256 + slot * hkv * 4: 256 + (slot + 1) * hkv * 4],
+             arena[zoff + slot * hkv * 4: zoff + (slot + 1) * hkv * 4]]
     for h in range(hkv):
         for g in range(ng):
             off = O_.oscar_cache_block_offset(cache.handle, slot, h, g)

@@ -62,7 +62,7 @@ def test_every_declared_symbol_is_exported(O):
 def test_required_bytes_layout(O, meta_bits, block):
     cfg = O.make_config(3, 8, 1000, meta_bits=meta_bits)
     n = O.oscar_cache_required_bytes(cfg)
-    meta = -(-(256 + 3 * 8 * 4) // 256) * 256
+    meta = -(-(256 + 2 * 3 * 8 * 4) // 256) * 256   # status words, value-scale and |value zero| maxima
     groups = -(-1000 // 128)
     blocks = 3 * 8 * groups * block
     win_off = -(-(meta + blocks) // 256) * 256
