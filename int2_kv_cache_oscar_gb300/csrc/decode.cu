@@ -421,11 +421,11 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     float m_run = -INFINITY;   // running max (log2 units) of head tig
     float l_run = 0.0f;        // partial sum of p over this lane's tokens
     float2 o_acc[8];           // head tig, channels 16 mt + g (.x) and + 8 (.y), times 2^(Fv - 24)
-    float zacc[kVGroups];      // sum_t p_t z^V_t,gr over this lane's tokens
+    float2 zacc[kVGroups / 2]; // sum_t p_t z^V_t,gr over this lane's tokens, value groups (0, 1) and (2, 3)
 #pragma unroll
     for (int i = 0; i < 8; ++i) o_acc[i] = make_float2(0.0f, 0.0f);
 #pragma unroll
-    for (int i = 0; i < kVGroups; ++i) zacc[i] = 0.0f;
+    for (int i = 0; i < kVGroups / 2; ++i) zacc[i] = make_float2(0.0f, 0.0f);
 
     for (int64_t kk = k_begin + ((cw - k_begin) % ncw + ncw) % ncw; kk < k_end; kk += ncw) {
       const int s = (int)(kk % kStages);
@@ -506,7 +506,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       // ---- online softmax (head tig)
       float gm = fmaxf(sc[0].x, sc[0].y);
 #pragma unroll
-      for (int i = 1; i < 8; ++i) gm = fmaxf(gm, fmaxf(sc[i].x, sc[i].y));
+      for (int i = 1; i < 8; ++i) asm("max.f32 %0, %0, %1, %2;" : "+f"(gm) : "f"(sc[i].x), "f"(sc[i].y));
       gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 4));
       gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 8));
       gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 16));
@@ -523,7 +523,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       }
       l_run = fmaf(l_run, alpha, psum.x + psum.y);
 #pragma unroll
-      for (int gr = 0; gr < kVGroups; ++gr) zacc[gr] *= alpha;
+      for (int i = 0; i < kVGroups / 2; ++i) zacc[i] = __fmul2_rn(zacc[i], make_float2(alpha, alpha));
       float* pb = S.pbuf[warp][tig];
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
@@ -538,10 +538,9 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
           z0 = *reinterpret_cast<const float4*>(vze + 256 * mt + vzl0);
           z1 = *reinterpret_cast<const float4*>(vze + 256 * mt + vzl1);
         }
-        zacc[0] = fmaf(sc[mt].x, z0.x, fmaf(sc[mt].y, z1.x, zacc[0]));
-        zacc[1] = fmaf(sc[mt].x, z0.y, fmaf(sc[mt].y, z1.y, zacc[1]));
-        zacc[2] = fmaf(sc[mt].x, z0.z, fmaf(sc[mt].y, z1.z, zacc[2]));
-        zacc[3] = fmaf(sc[mt].x, z0.w, fmaf(sc[mt].y, z1.w, zacc[3]));
+        const float2 px = make_float2(sc[mt].x, sc[mt].x), py = make_float2(sc[mt].y, sc[mt].y);
+        zacc[0] = __ffma2_rn(px, make_float2(z0.x, z0.y), __ffma2_rn(py, make_float2(z1.x, z1.y), zacc[0]));
+        zacc[1] = __ffma2_rn(px, make_float2(z0.z, z0.w), __ffma2_rn(py, make_float2(z1.z, z1.w), zacc[1]));
       }
       __syncwarp();
 
@@ -604,7 +603,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       float zs[kVGroups];
 #pragma unroll
       for (int gr = 0; gr < kVGroups; ++gr) {
-        float z = zacc[gr];
+        float z = (gr & 1) ? zacc[gr >> 1].y : zacc[gr >> 1].x;
         z += __shfl_xor_sync(0xffffffffu, z, 4);
         z += __shfl_xor_sync(0xffffffffu, z, 8);
         z += __shfl_xor_sync(0xffffffffu, z, 16);
