@@ -57,6 +57,7 @@ struct Ring {
   static constexpr int kStageBytes = Blk<M16>::kBytes;
 };
 
+static_assert(kConsumers < Ring<false>::kStages && kConsumers < Ring<true>::kStages, "one stage step per block");
 static_assert(kPreWaitStages <= Ring<false>::kStages && kPreWaitStages <= Ring<true>::kStages &&
                   kConsumers <= Ring<false>::kStages && kConsumers <= Ring<true>::kStages,
               "the pre-wait fill uses each stage once (no free-slot waits)");
@@ -427,9 +428,17 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
 #pragma unroll
     for (int i = 0; i < kVGroups / 2; ++i) zacc[i] = make_float2(0.0f, 0.0f);
 
-    for (int64_t kk = k_begin + ((cw - k_begin) % ncw + ncw) % ncw; kk < k_end; kk += ncw) {
-      const int s = (int)(kk % kStages);
-      const uint32_t use = (uint32_t)(kk / kStages);
+    const int64_t kk0 = k_begin + ((cw - k_begin) % ncw + ncw) % ncw;
+    int s_next = (int)(kk0 % kStages);               // stage and use of the next block, kept
+    uint32_t use_next = (uint32_t)(kk0 / kStages);   // incrementally (ncw < kStages)
+    for (int64_t kk = kk0; kk < k_end; kk += ncw) {
+      const int s = s_next;
+      const uint32_t use = use_next;
+      s_next += ncw;
+      if (s_next >= kStages) {
+        s_next -= kStages;
+        ++use_next;
+      }
       if (!wait_issued(&S.issued[s], use, &S.abort_flag, p.h.err_word, p.h.spin_limit)) continue;
       if (!mbar_wait_bounded(&S.full[s], use & 1, &S.abort_flag, p.h.err_word, p.h.spin_limit)) continue;
       const uint8_t* blk = S.stage[s];
