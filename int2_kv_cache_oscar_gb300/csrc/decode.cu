@@ -205,16 +205,22 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
     if (lane != 0) return;
     int64_t k = 0;
     int64_t u = u0;
-    // Use k of the ring: stage k mod kStages, one block.  (Failure-path test:
-    // the copy of one unit of CTA 0 is never issued, so the phase its
-    // consumer waits for never completes.)
-    auto issue = [&](int64_t kk, const uint8_t* src) {
-      const int s = (int)(kk % kStages);
-      if (!(cta == 0 && kk == p.h.fault_unit)) {
-        mbar_arrive_expect_tx(&S.full[s], kStageBytes);
-        bulk_g2s(S.stage[s], src, kStageBytes, &S.full[s]);
+    // Use k of the ring: stage ks = k mod kStages, its use ku = k / kStages,
+    // both kept incrementally.  (Failure-path test: the copy of one unit of
+    // CTA 0 is never issued, so the phase its consumer waits for never
+    // completes.)
+    int ks = 0;
+    uint32_t ku = 0;
+    auto issue = [&](const uint8_t* src) {
+      if (!(cta == 0 && k == p.h.fault_unit)) {
+        mbar_arrive_expect_tx(&S.full[ks], kStageBytes);
+        bulk_g2s(S.stage[ks], src, kStageBytes, &S.full[ks]);
       }
-      reinterpret_cast<volatile uint32_t*>(S.issued)[s] = (uint32_t)(kk / kStages) + 1;
+      reinterpret_cast<volatile uint32_t*>(S.issued)[ks] = ku + 1;
+      if (++ks == kStages) {
+        ks = 0;
+        ++ku;
+      }
     };
     // Ring fill before the grid dependency wait: blocks of settled groups
     // (no kernel that may still run can be writing them), kPreWaitStages at
@@ -229,7 +235,7 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       const int64_t seg_end = row_end < u1 ? row_end : u1;
       const int settled = p.seq[b].settled;
       const uint8_t* src = blocks + (((int64_t)p.seq[b].slot * hkv + j) * p.h.max_groups + g) * kStageBytes;
-      for (; u < seg_end && k < pre && g < settled; ++u, ++k, ++g, src += kStageBytes) issue(k, src);
+      for (; u < seg_end && k < pre && g < settled; ++u, ++k, ++g, src += kStageBytes) issue(src);
       if (u < seg_end) break;         // an unsettled group (or the ring is full)
     }
     grid_dependency_wait();
@@ -242,14 +248,12 @@ __global__ void __launch_bounds__(kDecThreads, kCtasPerSm)
       const int64_t seg_end = row_end < u1 ? row_end : u1;
       const uint8_t* src = blocks + (((int64_t)p.seq[b].slot * hkv + j) * p.h.max_groups + g) * kStageBytes;
       for (; u < seg_end; ++u, ++k, src += kStageBytes) {
-        const int s = (int)(k % kStages);
-        if (k >= kStages) {
-          if (!mbar_wait_bounded(&S.empty[s], (uint32_t)(((k / kStages) - 1) & 1), &S.abort_flag, p.h.err_word,
-                                 p.h.spin_limit)) {
+        if (ku > 0) {   // the stage's previous use has been released
+          if (!mbar_wait_bounded(&S.empty[ks], (ku - 1) & 1, &S.abort_flag, p.h.err_word, p.h.spin_limit)) {
             goto drain;
           }
         }
-        issue(k, src);
+        issue(src);
       }
     }
   drain:
