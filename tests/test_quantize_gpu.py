@@ -163,3 +163,51 @@ def test_16_byte_aligned_inputs_match_32_byte_aligned():
     cache = O_.OscarCache(1, 8, 1024)
     U.append_all(cache, [0], ks, vs, chunk=100)
     _compare_cache(cache, [0], ks, vs, {})
+
+
+@pytest.mark.parametrize("meta_bits", [32, 16])
+def test_header_maxima(meta_bits):
+    """The arena header's per-(slot, head) maxima (include/oscar.h): the
+    largest stored value scale and the largest |stored value zero| over the
+    quantised groups, exactly; both equal the oracle's within its parameter
+    tolerance; a reset of the slot clears them, and appends after it start
+    over."""
+    gen = torch.Generator().manual_seed(71)
+    hkv, slots = 4, 3
+    lens = [1000, 300, 128 * 5]
+    ks, vs = [], []
+    for L in lens:
+        k, v = W.make_sequence_kv(L, hkv, W.LLAMA_RECIPE, gen)
+        ks.append(k)
+        vs.append(v)
+    cache = U.lib().OscarCache(slots, hkv, 1024, meta_bits=meta_bits)
+    U.append_all(cache, list(range(slots)), ks, vs, chunk=333)
+
+    def header(arena):
+        words = arena[256:256 + 2 * slots * hkv * 4].view(np.float32)
+        return words[:slots * hkv].reshape(slots, hkv), words[slots * hkv:].reshape(slots, hkv)
+
+    arena = U.read_arena(cache)
+    smax, zmax = header(arena)
+    for s in range(slots):
+        for h in range(hkv):
+            g = U.gpu_head(cache, arena, s, h)
+            r = U.oracle_head(ks[s], vs[s], h, meta_bits=meta_bits)
+            assert smax[s, h] == np.float32(np.max(g.values.scale)), f"slot {s} head {h}: value-scale maximum"
+            assert zmax[s, h] == np.float32(np.max(np.abs(g.values.zero))), f"slot {s} head {h}: |zero| maximum"
+            tol = 1e-6 if meta_bits == 32 else 2.0 ** -10
+            assert abs(smax[s, h] - np.max(r.values.scale)) <= tol * np.max(r.values.scale)
+            assert abs(zmax[s, h] - np.max(np.abs(r.values.zero))) <= tol * np.max(np.abs(r.values.zero))
+    # a reset clears the slot's maxima; the next append records its own
+    U.lib().oscar_cache_reset(cache.handle, 1)
+    k2, v2 = W.make_sequence_kv(256, hkv, W.LLAMA_RECIPE, gen)
+    v2 = (v2.float() * 0.01).to(torch.bfloat16)     # far smaller values: the new maxima must drop
+    arena_before = header(U.read_arena(cache))
+    assert np.all(arena_before[0][1] == 0) and np.all(arena_before[1][1] == 0)
+    U.append_all(cache, [1], [k2], [v2])
+    arena = U.read_arena(cache)
+    smax, zmax = header(arena)
+    for h in range(hkv):
+        g = U.gpu_head(cache, arena, 1, h)
+        assert smax[1, h] == np.float32(np.max(g.values.scale))
+        assert zmax[1, h] == np.float32(np.max(np.abs(g.values.zero)))
